@@ -1,0 +1,407 @@
+#!/usr/bin/env python3
+"""Throughput benchmark of the Cholesky forward + adjoint hot path on GB300.
+
+One step = ``chol_fwd`` then ``chol_adj`` over one batch of synthetic input
+(default workload: 65536 independent 16x16 float32 SPD matrices,
+``A = G G^T / 16 + I``, ``adj_L = tril(N(0, 1))``).  Inputs are resident in HBM
+when the timed region starts; each step reads 256 MiB of distinct buffers, more
+than the 129 MB L2, and steps alternate between two buffer sets.
+
+Prints ONE JSON line (rank 0).  ``value`` = matrices/s over all ranks,
+``e2e`` = the same metric through the public API with pinned host buffers and
+the host<->device copies inside the timed region, ``roofline`` = the dominant
+kernel's algorithmic bandwidth against the measured HBM copy peak,
+``cpu_baseline`` = the CPU oracle on the same workload.
+
+``--impl reference`` times the CPU oracle itself as the reference arm.
+Multi-GPU (torchrun): every rank factors its own batch (weak scaling, no
+collective on the data path; a barrier and a max-reduction of the time only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "Cholesky fwd+adjoint matrices/s and GFLOP/s (1 GB300), % of HBM/FP64 roofline"
+UNIT = "matrices/s"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ----------------------------------------------------------------------------
+# Workload description and algorithmic bytes / flops
+# ----------------------------------------------------------------------------
+
+WORKLOADS = {
+    # name: (batch, n, numpy dtype, description)
+    "batched_16": (65536, 16, np.float32,
+                   "65536 x 16x16 fp32, A = G G^T/16 + I (G ~ N(0,1), seed 0), adj_L = tril(N(0,1)) (seed 1)"),
+    "batched_64": (8192, 64, np.float32,
+                   "8192 x 64x64 fp32, A = G G^T/64 + 0.5 I, every 100th matrix non-PD (A[k,k] = -1)"),
+}
+
+
+def lower_sector_bytes(n: int, esize: int) -> int:
+    """Bytes of the 32-byte DRAM sectors that hold the lower triangle of one
+    row-major n x n matrix (row i needs ceil((i+1) * esize / 32) sectors)."""
+    return sum(math.ceil((i + 1) * esize / 32) * 32 for i in range(n))
+
+
+def algorithmic_bytes(n: int, esize: int):
+    low = lower_sector_bytes(n, esize)
+    fwd = low + n * n * esize + 4          # tril(A) in, full L out, status out
+    adj = 4 * low + 4                      # tril(L), tril(adj_L), tril(adj_A) in and out, status in
+    return fwd, adj
+
+
+def nominal_flops(n: int):
+    return n ** 3 / 3.0, float(n ** 3)     # forward n^3/3, adjoint ~n^3 (nominal)
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        for key in ("hbm_gbs", "hbm_GBs", "hbm_copy_gbs"):
+            if key in d:
+                return float(d[key]), "measured"
+        for k, v in d.items():
+            if "hbm" in k.lower() and isinstance(v, (int, float)):
+                return float(v), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# ----------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.samples = []  # (t, sm, smmax, reasons)
+        self.proc = None
+        self.thread = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if gpu_id:
+            cmd += ["-i", gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._reader, daemon=True)
+        self.thread.start()
+
+    def _reader(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.strip().split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm, smmax = float(parts[0]), float(parts[1])
+            except ValueError:
+                continue
+            reasons = [name for name, v in zip(self.REASONS, parts[4:8]) if v.lower() == "active"]
+            self.samples.append((time.monotonic(), sm, smmax, reasons))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        note = "sampled during the timed region"
+        if not inside:
+            # timed region shorter than the sampling period: nearest samples
+            inside = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:3]
+            note = "timed region shorter than the 100 ms sampling period; nearest samples"
+        reasons = sorted({r for s in inside for r in s[3]})
+        return {"sm_mhz": statistics.median(s[1] for s in inside),
+                "sm_max_mhz": max(s[2] for s in inside), "reasons": reasons,
+                "samples": len(inside), "note": note}
+
+
+def gpu_identifier(torch):
+    try:
+        u = torch.cuda.get_device_properties(0).uuid
+        s = str(u)
+        if s and not s.startswith("GPU-"):
+            s = "GPU-" + s
+        return s
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        first = vis.split(",")[0].strip() if vis else ""
+        return first or None
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline leg and the reference arm)
+# ----------------------------------------------------------------------------
+
+def time_oracle(w, count: int, threads: int = 1):
+    """Oracle fwd + adjoint over the first `count` matrices; returns seconds."""
+    import oracle
+    A = w.A[:count]
+    Lbar = w.adj_L[:count]
+    t0 = time.perf_counter()
+    L, st = oracle.potrf(A, threads=threads)
+    oracle.potrf_adj(L, Lbar, status=st, threads=threads)
+    return time.perf_counter() - t0
+
+
+def oracle_sample_size(w, budget_s: float = 2.0, cap: int | None = None):
+    """Matrices the oracle handles in about `budget_s` seconds (one thread)."""
+    probe = min(w.batch, 256)
+    t = max(time_oracle(w, probe), 1e-6)
+    count = int(min(w.batch, max(probe, probe * budget_s / t)))
+    if cap is not None:
+        count = min(count, cap)
+    return count
+
+
+def cpu_baseline(w):
+    count = oracle_sample_size(w, budget_s=3.0)
+    t = time_oracle(w, count)
+    return {"value": count / t, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"first {count} of {w.batch} matrices of the same workload, fwd + adjoint, "
+                      f"one thread, {t:.2f} s"}
+
+
+def run_reference(args, w, desc):
+    import oracle
+    oracle.build()
+    count = oracle_sample_size(w, budget_s=0.5)
+    for _ in range(args.warmup):
+        time_oracle(w, count)
+    times = [time_oracle(w, count) for _ in range(args.steps)]
+    total = sum(times)
+    value = args.steps * count / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32" if w.dtype == np.float32 else "f64", "data": "synthetic",
+        "config": {"workload": desc, "batch": w.batch, "n": w.n,
+                   "step": f"oracle fwd + adjoint over {count} matrices of the batch"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{count} of {w.batch} matrices per step, one thread"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+
+def make_workload(name):
+    from differentiable_cholesky_gb300 import workloads as W
+    return W.WORKLOADS[name]()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="batched_16")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    batch, n, np_dtype, desc = WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        run_reference(args, make_workload(args.workload), desc)
+        return
+
+    import torch
+    from differentiable_cholesky_gb300 import binding
+
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    binding.load_library()
+    dev = torch.device("cuda", local_rank)
+
+    w = make_workload(args.workload)
+    esize = np.dtype(np_dtype).itemsize
+    tdtype = torch.float32 if np_dtype == np.float32 else torch.float64
+
+    # two buffer sets, alternated between steps
+    sets = []
+    for _ in range(2):
+        A = torch.from_numpy(w.A).to(dev)
+        Lb = torch.from_numpy(w.adj_L).to(dev)
+        L = torch.empty_like(A)
+        G = torch.zeros_like(A)
+        st = torch.empty(batch, dtype=torch.int32, device=dev)
+        sets.append((A, Lb, L, G, st))
+    stream = torch.cuda.current_stream()
+
+    def step(k, ev=None):
+        A, Lb, L, G, st = sets[k & 1]
+        if ev is not None:
+            ev[0].record(stream)
+        binding.chol_fwd(A, L=L, status=st)
+        if ev is not None:
+            ev[1].record(stream)
+        binding.chol_adj(L, Lb, adj_A=G, status=st)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for k in range(args.warmup):
+        step(k)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(gpu_identifier(torch)) if rank == 0 else None
+    if sampler is not None:
+        time.sleep(0.3)
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.monotonic()
+    start.record(stream)
+    for k in range(args.steps):
+        step(k, events[k])
+    stop.record(stream)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall1 = time.monotonic()
+    elapsed_ms = start.elapsed_time(stop)
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in events)
+    adj_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in events)
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    clocks = sampler.summary(t_wall0, t_wall1) if sampler is not None else None
+
+    # end-to-end through the public API: pinned host in, pinned host out
+    hA = torch.from_numpy(w.A).pin_memory()
+    hLb = torch.from_numpy(w.adj_L).pin_memory()
+    hL = torch.empty_like(hA).pin_memory()
+    hG = torch.empty_like(hA).pin_memory()
+    hst = torch.empty(batch, dtype=torch.int32).pin_memory()
+    dA, dLb, dL, dG, dst = sets[0]
+
+    def e2e_step():
+        dA.copy_(hA, non_blocking=True)
+        dLb.copy_(hLb, non_blocking=True)
+        dG.zero_()
+        binding.chol_fwd(dA, L=dL, status=dst)
+        binding.chol_adj(dL, dLb, adj_A=dG, status=dst)
+        hL.copy_(dL, non_blocking=True)
+        hst.copy_(dst, non_blocking=True)
+        hG.copy_(dG, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    if sampler is not None:
+        sampler.stop()
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    matrices = args.steps * batch * world
+    value = matrices / (elapsed_ms / 1e3)
+    e2e_value = args.e2e_steps * batch * world / (e2e_ms / 1e3)
+    fwd_b, adj_b = algorithmic_bytes(n, esize)
+    fwd_f, adj_f = nominal_flops(n)
+    peak, peak_src = read_peaks()
+    fwd_gbs = fwd_b * batch / (fwd_ms / 1e3) / 1e9
+    adj_gbs = adj_b * batch / (adj_ms / 1e3) / 1e9
+    dominant = "adj" if adj_ms >= fwd_ms else "fwd"
+    achieved = adj_gbs if dominant == "adj" else fwd_gbs
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32" if np_dtype == np.float32 else "f64", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {desc}", "batch_per_gpu": batch, "n": n,
+                   "parallelism": f"independent batches per GPU x{world}" if world > 1 else "1 GPU",
+                   "l2": "inputs larger than L2 (256 MiB of distinct buffers per step, two sets alternated)"},
+        "gflops": value * (fwd_f + adj_f) / 1e9,
+        "kernels": {
+            "fwd": {"ms": fwd_ms, "algorithmic_GBps": fwd_gbs, "bytes_per_matrix": fwd_b},
+            "adj": {"ms": adj_ms, "algorithmic_GBps": adj_gbs, "bytes_per_matrix": adj_b},
+        },
+        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": f"{peak_src} HBM copy bandwidth",
+                     "traffic": None},
+        "gpu_launches": 2 * args.steps,
+        "e2e": {"value": e2e_value, "unit": UNIT,
+                "h2d_bytes_per_step": int(hA.numel() * esize + hLb.numel() * esize),
+                "d2h_bytes_per_step": int(hL.numel() * esize + hG.numel() * esize + hst.numel() * 4),
+                "steps": args.e2e_steps},
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        line["cpu_baseline"] = cpu_baseline(w)
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,175 @@
+"""ctypes binding of ``libchol_gb300.so`` (declared in ``include/chol.h``).
+
+Argument marshalling only: every step of the factorisation and of its adjoint
+runs in the library's CUDA kernels.  torch supplies device memory and the
+current stream.  There is no fallback: if the library is missing or a call
+fails, a ``RuntimeError`` says why.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+CHOL_F32 = 0
+CHOL_F64 = 1
+_DTYPES = {torch.float32: CHOL_F32, torch.float64: CHOL_F64}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class CholError(RuntimeError):
+    """A library call returned a negative code."""
+
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{msg} (code {code})")
+        self.code = code
+
+
+def load_library(path: str | None = None):
+    """Load (building first if needed) and return the ctypes library handle."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if path is None:
+            path = _build.LIB_PATH
+            if not _build.up_to_date():
+                path = _build.build()
+        if not os.path.exists(path):
+            raise RuntimeError(f"CUDA library not found at {path}; run the package build first")
+        lib = ctypes.CDLL(path)
+        i64, i32, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
+        lib.chol_fwd.argtypes = [i64, i32, i32, vp, vp, vp, vp]
+        lib.chol_fwd_ex.argtypes = [i64, i32, i32, vp, vp, vp, i32, vp]
+        lib.chol_adj.argtypes = [i64, i32, i32, vp, vp, vp, vp, vp]
+        lib.chol_adj_ex.argtypes = [i64, i32, i32, vp, vp, vp, vp, i32, vp]
+        for f in (lib.chol_fwd, lib.chol_fwd_ex, lib.chol_adj, lib.chol_adj_ex):
+            f.restype = ctypes.c_int
+        lib.chol_strerror.argtypes = [ctypes.c_int]
+        lib.chol_strerror.restype = ctypes.c_char_p
+        lib.chol_abi_version.argtypes = []
+        lib.chol_abi_version.restype = ctypes.c_int32
+        _lib = lib
+        return lib
+
+
+def _check(rc: int):
+    if rc != 0:
+        msg = load_library().chol_strerror(rc).decode()
+        raise CholError(rc, msg)
+
+
+def _shape(x: torch.Tensor):
+    if x.dim() < 2 or x.shape[-1] != x.shape[-2]:
+        raise ValueError(f"expected [..., n, n], got {tuple(x.shape)}")
+    n = int(x.shape[-1])
+    batch = 1
+    for s in x.shape[:-2]:
+        batch *= int(s)
+    return batch, n
+
+
+def _require(x: torch.Tensor, name: str, dtype=None):
+    if not isinstance(x, torch.Tensor) or not x.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not x.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and x.dtype != dtype:
+        raise ValueError(f"{name} must have dtype {dtype}, got {x.dtype}")
+
+
+def _stream_ptr(stream) -> int | None:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def chol_fwd(A: torch.Tensor, L: torch.Tensor | None = None, status: torch.Tensor | None = None,
+             tile: int = 0, stream=None):
+    """``L, status = chol_fwd(A)`` for ``A`` of shape ``[..., n, n]`` (fp32/fp64).
+
+    Only ``tril(A)`` is read.  ``status`` is int32 with the batch shape: 0, or
+    the 1-based first failing pivot column.  Pre-allocated ``L``/``status`` may
+    be passed to avoid allocation (they are fully overwritten).
+    """
+    _require(A, "A")
+    if A.dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {A.dtype}")
+    batch, n = _shape(A)
+    if L is None:
+        L = torch.empty_like(A)
+    if status is None:
+        status = torch.empty(A.shape[:-2], dtype=torch.int32, device=A.device)
+    _require(L, "L", A.dtype)
+    _require(status, "status", torch.int32)
+    if tuple(L.shape) != tuple(A.shape) or status.numel() != batch:
+        raise ValueError("L must match A's shape and status must have one entry per matrix")
+    lib = load_library()
+    rc = lib.chol_fwd_ex(batch, n, _DTYPES[A.dtype], A.data_ptr(), L.data_ptr(),
+                         status.data_ptr(), int(tile), _stream_ptr(stream))
+    _check(rc)
+    return L, status
+
+
+def chol_adj(L: torch.Tensor, adj_L: torch.Tensor, adj_A: torch.Tensor | None = None,
+             status: torch.Tensor | None = None, tile: int = 0, stream=None):
+    """Accumulate the Cholesky adjoint into ``adj_A`` (zeros if not given).
+
+    ``adj_A``'s lower triangle gains ``Phi(M + M^T)`` with
+    ``M = L^-T Phi(L^T tril(adj_L)) L^-1``; its upper triangle is not written.
+    Matrices with non-zero ``status`` are skipped.  Returns ``adj_A``.
+    """
+    _require(L, "L")
+    if L.dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {L.dtype}")
+    _require(adj_L, "adj_L", L.dtype)
+    if tuple(adj_L.shape) != tuple(L.shape):
+        raise ValueError("adj_L must match L's shape")
+    batch, n = _shape(L)
+    if adj_A is None:
+        adj_A = torch.zeros_like(L)
+    _require(adj_A, "adj_A", L.dtype)
+    if tuple(adj_A.shape) != tuple(L.shape):
+        raise ValueError("adj_A must match L's shape")
+    sp = None
+    if status is not None:
+        _require(status, "status", torch.int32)
+        if status.numel() != batch:
+            raise ValueError("status must have one entry per matrix")
+        sp = status.data_ptr()
+    lib = load_library()
+    rc = lib.chol_adj_ex(batch, n, _DTYPES[L.dtype], L.data_ptr(), adj_L.data_ptr(),
+                         adj_A.data_ptr(), sp, int(tile), _stream_ptr(stream))
+    _check(rc)
+    return adj_A
+
+
+class _Cholesky(torch.autograd.Function):
+    """Autograd wrapper: the gradient flows to the lower triangle of A only,
+    because the factorisation reads nothing else."""
+
+    @staticmethod
+    def forward(ctx, A, tile):
+        L, status = chol_fwd(A.contiguous(), tile=tile)
+        ctx.save_for_backward(L, status)
+        ctx.tile = tile
+        ctx.mark_non_differentiable(status)
+        return L, status
+
+    @staticmethod
+    def backward(ctx, gL, gstatus):
+        L, status = ctx.saved_tensors
+        if gL is None:
+            return None, None
+        gA = chol_adj(L, gL.contiguous(), status=status, tile=ctx.tile)
+        return gA, None
+
+
+def cholesky(A: torch.Tensor, tile: int = 0):
+    """Differentiable ``(L, status)``; ``A.grad`` gets the lower-triangle adjoint."""
+    return _Cholesky.apply(A, tile)

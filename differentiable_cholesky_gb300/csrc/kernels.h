@@ -1,0 +1,32 @@
+// Internal launch interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace chol {
+
+// Threads per matrix of the small path for order n (8, 16, 32 or 64).
+int small_nt(int n);
+
+// n <= 64.  `vec` selects 16-byte vector accesses (every pointer 16-byte
+// aligned and n a multiple of 16 / sizeof(T)).
+template <typename T>
+cudaError_t small_fwd(const T* A, T* L, int32_t* status, int64_t batch, int n, bool vec,
+                      cudaStream_t stream);
+template <typename T>
+cudaError_t small_adj(const T* L, const T* Lbar, T* Abar, const int32_t* status, int64_t batch,
+                      int n, bool vec, cudaStream_t stream);
+
+// n > 64, blocked with square tiles of `tile` (32, 64 or 128).
+template <typename T>
+cudaError_t blocked_fwd(const T* A, T* L, int32_t* status, int64_t batch, int n, int tile,
+                        cudaStream_t stream);
+// `work` holds batch * n * n elements of scratch.
+template <typename T>
+cudaError_t blocked_adj(const T* L, const T* Lbar, T* Abar, const int32_t* status,
+                        int64_t batch, int n, int tile, T* work, cudaStream_t stream);
+
+int blocked_default_tile(int n, int elem_size);
+
+}  // namespace chol

@@ -1,0 +1,128 @@
+/*
+ * chol.h -- C ABI of the GB300 (sm_103a) differentiable Cholesky library.
+ *
+ * Two calls make up the path:
+ *
+ *   chol_fwd  the Cholesky factorisation A = L L^T of symmetric positive-
+ *             definite matrices, lower factor, out of place, with a per-matrix
+ *             status.  Defined by the jaxmg docs "Cholesky factorization"
+ *             (intro: potrf returns the lower-triangular factor without a
+ *             solve; "Advanced: control the outer jax.jit": the call returns
+ *             `factor, status`) and by NVIDIA/warp issue #1316's closing
+ *             comment (wp.tile_cholesky, the out-of-place variant).
+ *
+ *   chol_adj  its reverse-mode adjoint, the symmetric-matrix derivative of
+ *             Cholesky (Murray 2016) as NVIDIA/warp issue #1316's closing
+ *             comment states it: S = Phi(L^T adj_L), two triangular solves
+ *             against L^T and L, accumulation into the lower triangle of A's
+ *             gradient.  Phi keeps the lower triangle and halves the diagonal.
+ *
+ * Conventions shared by every call
+ *   - Matrices are dense, row-major, contiguous: element (i, j) of matrix b
+ *     lives at offset (b * n + i) * n + j.  dtype selects float32 or float64.
+ *   - Every pointer is a DEVICE pointer (cudaMalloc'd, stream-ordered or
+ *     managed memory) owned by the caller; the library keeps no state and
+ *     never frees or retains caller memory.  Element pointers must be aligned
+ *     to their element size; 16-byte alignment (with n a multiple of 16 / the
+ *     element size) selects vectorised loads.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *     only enqueue work on it and return without synchronising; results are
+ *     stream-ordered.  No kernel traps, asserts or waits without bound.
+ *   - Invalid arguments are reported synchronously by a negative return code
+ *     (chol_strerror gives the text) and nothing is enqueued.  A matrix that
+ *     is not positive definite is data, not an error: it sets its status.
+ *   - batch == 0 is a no-op that returns CHOL_OK.
+ */
+#ifndef CHOL_GB300_H
+#define CHOL_GB300_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define CHOL_API __attribute__((visibility("default")))
+#else
+#define CHOL_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { CHOL_F32 = 0, CHOL_F64 = 1 } chol_dtype_t;
+
+enum {
+    CHOL_OK = 0,
+    CHOL_EINVAL = -1,  /* null/misaligned/host pointer, n <= 0, batch < 0, bad tile, size overflow */
+    CHOL_EDTYPE = -2,  /* dtype is neither CHOL_F32 nor CHOL_F64                                     */
+    CHOL_EALIAS = -3,  /* an output overlaps an input it must not overlap                            */
+    CHOL_ENOMEM = -4,  /* workspace allocation failed                                                */
+    CHOL_ECUDA = -5    /* a CUDA call or kernel launch failed (see cudaGetLastError)                 */
+};
+
+/*
+ * chol_fwd -- L_b = chol(A_b) for b in [0, batch).
+ *   A       in : dtype[batch][n][n].  Only the lower triangle (j <= i) is
+ *                read; the upper triangle may hold anything.  Never written.
+ *   L       out: dtype[batch][n][n].  Fully written: the factor on and below
+ *                the diagonal, exact zeros above it.  Must not overlap A or
+ *                status (CHOL_EALIAS).
+ *   status  out: int32[batch].  0 if A_b is positive definite; otherwise
+ *                j + 1 for the first column j (0-based) whose pivot
+ *                a_jj - sum_k l_jk^2 is not > 0 (zero, negative or NaN), the
+ *                LAPACK `info` convention.  For such a matrix the part of L_b
+ *                from column j on is unspecified.
+ * n <= 64 runs one fused register/shared-memory kernel per batch; larger n
+ * runs the blocked right-looking algorithm (diagonal-tile factor, panel
+ * triangular solve, trailing update) with the default tile.
+ */
+CHOL_API int chol_fwd(int64_t batch, int32_t n, int32_t dtype, const void* A, void* L,
+             int32_t* status, void* stream);
+
+/*
+ * chol_fwd_ex -- chol_fwd with an explicit tile for the blocked path
+ * (n > 64): tile in {32, 64, 128}, or 0 for the default.  Results are
+ * tile-independent up to rounding.  Ignored for n <= 64.
+ */
+CHOL_API int chol_fwd_ex(int64_t batch, int32_t n, int32_t dtype, const void* A, void* L,
+                int32_t* status, int32_t tile, void* stream);
+
+/*
+ * chol_adj -- adj_A_b += dA for the loss gradient adj_L_b, b in [0, batch).
+ *   L       in : dtype[batch][n][n], the factor from chol_fwd.  Only its lower
+ *                triangle is read.
+ *   adj_L   in : dtype[batch][n][n], the gradient of the loss with respect to
+ *                L.  Only its lower triangle is read (the upper is taken as 0).
+ *   adj_A   in/out: dtype[batch][n][n].  On the lower triangle, adds the
+ *                partial derivatives of the loss with respect to the entries
+ *                a_ij (i >= j) that chol_fwd reads:
+ *                  M = L^-T Phi(L^T tril(adj_L)) L^-1,
+ *                  adj_A_ij += M_ij + M_ji (i > j),  adj_A_ii += M_ii.
+ *                The upper triangle is never written.  Must not overlap L,
+ *                adj_L or status (CHOL_EALIAS).
+ *   status  in : int32[batch] from chol_fwd, or NULL.  Matrices with a non-zero
+ *                status are skipped (their adj_A is left unchanged).
+ * The gradient of torch.linalg.cholesky (a symmetric matrix G) relates to this
+ * one by adj_A = tril(G + G^T) - diag(G).
+ * n > 64 needs batch * n * n elements of device workspace, taken with
+ * cudaMallocAsync/cudaFreeAsync on `stream` (CHOL_ENOMEM on failure).
+ */
+CHOL_API int chol_adj(int64_t batch, int32_t n, int32_t dtype, const void* L, const void* adj_L,
+             void* adj_A, const int32_t* status, void* stream);
+
+/* chol_adj with an explicit blocked-path tile (as chol_fwd_ex). */
+CHOL_API int chol_adj_ex(int64_t batch, int32_t n, int32_t dtype, const void* L, const void* adj_L,
+                void* adj_A, const int32_t* status, int32_t tile, void* stream);
+
+/* Static text for a return code (never NULL). */
+CHOL_API const char* chol_strerror(int code);
+
+/* ABI version of this header: (major << 16) | minor. */
+CHOL_API int32_t chol_abi_version(void);
+
+#define CHOL_ABI_VERSION ((1 << 16) | 0)
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CHOL_GB300_H */

@@ -1,0 +1,84 @@
+"""The C-ABI library loads and exports every symbol include/chol.h declares;
+argument checks that need no GPU return the documented codes (CPU only)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from differentiable_cholesky_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "chol.h")
+
+CHOL_OK, CHOL_EINVAL, CHOL_EDTYPE = 0, -1, -2
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"CHOL_API\s+[\w\s\*]+?\b(chol_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_path():
+    syms = declared_symbols()
+    for s in ("chol_fwd", "chol_adj", "chol_fwd_ex", "chol_adj_ex", "chol_strerror",
+              "chol_abi_version"):
+        assert s in syms
+
+
+def test_library_exports_every_declared_symbol():
+    lib = binding.load_library()
+    for s in declared_symbols():
+        assert hasattr(lib, s), f"{s} not exported"
+    assert lib.chol_abi_version() == (1 << 16) | 0
+
+
+def test_strerror_covers_every_code():
+    lib = binding.load_library()
+    for code in (0, -1, -2, -3, -4, -5):
+        txt = lib.chol_strerror(code).decode()
+        assert txt and "unknown" not in txt
+    assert "unknown" in lib.chol_strerror(-99).decode()
+
+
+def test_argument_checks_without_gpu():
+    lib = binding.load_library()
+    buf = (ctypes.c_double * 16)()
+    st = (ctypes.c_int32 * 4)()
+    p, s = ctypes.addressof(buf), ctypes.addressof(st)
+    # bad dtype, bad n, bad batch, bad tile
+    assert lib.chol_fwd(1, 4, 7, p, p, s, None) == CHOL_EDTYPE
+    assert lib.chol_fwd(1, 0, 1, p, p, s, None) == CHOL_EINVAL
+    assert lib.chol_fwd(-1, 4, 1, p, p, s, None) == CHOL_EINVAL
+    assert lib.chol_fwd_ex(1, 100, 1, p, p, s, 48, None) == CHOL_EINVAL
+    assert lib.chol_adj(1, -3, 0, p, p, p, None, None) == CHOL_EINVAL
+    assert lib.chol_adj(1, 4, 5, p, p, p, None, None) == CHOL_EDTYPE
+    # batch == 0 is a no-op, even with null pointers
+    assert lib.chol_fwd(0, 4, 1, None, None, None, None) == CHOL_OK
+    assert lib.chol_adj(0, 4, 1, None, None, None, None, None) == CHOL_OK
+    # null pointers
+    assert lib.chol_fwd(1, 4, 1, None, p, s, None) == CHOL_EINVAL
+    assert lib.chol_adj(1, 4, 1, p, None, p, None, None) == CHOL_EINVAL
+    # misaligned element pointer
+    assert lib.chol_fwd(1, 2, 1, p + 4, p + 64, s, None) == CHOL_EINVAL
+    # host memory is rejected (not a device pointer)
+    big = (ctypes.c_double * 64)()
+    q = ctypes.addressof(big)
+    assert lib.chol_fwd(1, 2, 1, q, q + 256, s, None) == CHOL_EINVAL
+
+
+def test_size_overflow_rejected():
+    lib = binding.load_library()
+    buf = (ctypes.c_double * 4)()
+    p = ctypes.addressof(buf)
+    assert lib.chol_fwd(1 << 40, 1 << 20, 1, p, p, p, None) == CHOL_EINVAL
+
+
+def test_binding_rejects_cpu_tensors():
+    torch = pytest.importorskip("torch")
+    A = torch.eye(4, dtype=torch.float64)
+    with pytest.raises(ValueError):
+        binding.chol_fwd(A)
+    with pytest.raises(ValueError):
+        binding.chol_adj(A, A)
