@@ -55,6 +55,8 @@ def load_library(path: str | None = None):
         lib.chol_strerror.restype = ctypes.c_char_p
         lib.chol_abi_version.argtypes = []
         lib.chol_abi_version.restype = ctypes.c_int32
+        lib.chol_probe_fma_peak.argtypes = [i32, i64, vp, ctypes.POINTER(ctypes.c_double), vp]
+        lib.chol_probe_fma_peak.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -147,6 +149,18 @@ def chol_adj(L: torch.Tensor, adj_L: torch.Tensor, adj_A: torch.Tensor | None = 
                          adj_A.data_ptr(), sp, int(tile), _stream_ptr(stream))
     _check(rc)
     return adj_A
+
+
+def probe_fma_peak(dtype=torch.float64, iters: int = 1 << 16, stream=None) -> float:
+    """Measured FMA throughput of the current device in FLOP/s (2 per FMA)."""
+    if dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {dtype}")
+    sink = torch.zeros(1, dtype=dtype, device="cuda")
+    out = ctypes.c_double(0.0)
+    rc = load_library().chol_probe_fma_peak(_DTYPES[dtype], int(iters), sink.data_ptr(),
+                                            ctypes.byref(out), _stream_ptr(stream))
+    _check(rc)
+    return out.value
 
 
 class _Cholesky(torch.autograd.Function):

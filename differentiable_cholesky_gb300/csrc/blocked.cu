@@ -1,25 +1,547 @@
-// Blocked Cholesky forward and adjoint for n > 64 (placeholder: not built yet).
+// Blocked Cholesky forward and adjoint for n > 64 (square tiles of T = 32, 64
+// or 128; the last tile of a row/column is ragged when T does not divide n).
+//
+// Forward: right-looking blocked potrf with L as the work buffer (A is only
+// read, by the first kernel).  Per tile step k (jaxmg docs "Cholesky
+// factorization", tile size T_A; the pages' own prior art is a distributed
+// tiled factorisation, here the tiles stay on one GPU):
+//   1. potrf_diag : factor the diagonal tile L_kk in shared memory (status on
+//                   the first non-positive pivot, column k*T + j + 1);
+//   2. trsm       : panel L_ik <- L_ik L_kk^-T for the rows below the tile;
+//   3. gemm       : trailing update L_ij -= L_ik L_jk^T on the lower tiles.
+// Only step 3 is a dense contraction.
+//
+// Adjoint (Murray 2016 as NVIDIA/warp issue #1316's closing comment states it:
+// S = Phi(L^T adj_L), two triangular solves, accumulation into the lower
+// triangle of adj_A; that comment's accelerated path is GEMM + TRSM with
+// element-wise steps in shared memory, and so is this one), on a workspace W
+// of one n x n matrix per batch entry:
+//   1. gemm (P)   : W_IJ = Phi(sum_{K>=I} L_KI^T tril(adj_L)_KJ), I >= J,
+//                   Phi fused in the epilogue of the diagonal tiles, W_IJ = 0
+//                   for I < J;
+//   2. X = L^-T S : for tile rows I = nt-1 .. 0: trsm solves L_II^T X_I = W_I,
+//                   then gemm W_I' -= L_II'^T X_I for I' < I;
+//   3. M = X L^-1 : for tile columns J = nt-1 .. 0: trsm solves M_J L_JJ = W_J,
+//                   then gemm W_J' -= M_J L_JJ' for J' < J;
+//   4. phi_acc    : adj_A_ij += M_ij + M_ji (i > j), adj_A_ii += M_ii.
+// Matrices whose status is non-zero are skipped by every kernel.
+//
+// The FP64 path is bound by the FP64 FMA pipe; every kernel keeps each SM's
+// pipe fed with independent FMAs and does nothing else of consequence.
+
 #include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
 
 #include "common.cuh"
 #include "kernels.h"
 
 namespace chol {
+namespace {
 
-int blocked_default_tile(int n, int elem_size) { return 128; }
+constexpr int kThreads = 256;
+
+inline unsigned grid_y(int64_t batch) { return (unsigned)std::min<int64_t>(batch, 65535); }
+
+__device__ __forceinline__ bool skip_matrix(const int32_t* status, int64_t b) {
+    return status != nullptr && status[b] != 0;
+}
+
+// ---------------------------------------------------------------------------
+// L = tril(A), status = 0
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+tril_copy_kernel(const T* __restrict__ A, T* __restrict__ L, int32_t* __restrict__ status,
+                 int64_t batch, int n) {
+    const int64_t nn = (int64_t)n * n;
+    const int64_t total = batch * nn;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t w = e % nn;
+        const int i = (int)(w / n), j = (int)(w % n);
+        L[e] = (j <= i) ? A[e] : T(0);
+    }
+    for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < batch;
+         b += (int64_t)gridDim.x * blockDim.x)
+        status[b] = 0;
+}
+
+// ---------------------------------------------------------------------------
+// Diagonal tile factor (one block per matrix), in shared memory.
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+potrf_diag_kernel(T* __restrict__ L, int32_t* __restrict__ status, int64_t batch, int n,
+                  int k0, int kb) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    T* S = reinterpret_cast<T*>(smem_raw);
+    const int P = kb + 1;
+    for (int64_t b = blockIdx.y; b < batch; b += gridDim.y) {
+        if (skip_matrix(status, b)) continue;
+        T* Lb = L + b * (int64_t)n * n;
+        __syncthreads();
+        for (int e = threadIdx.x; e < kb * kb; e += blockDim.x) {
+            const int r = e / kb, c = e % kb;
+            S[r * P + c] = (c <= r) ? Lb[(int64_t)(k0 + r) * n + k0 + c] : T(0);
+        }
+        __syncthreads();
+        bool failed = false;
+        for (int j = 0; j < kb; ++j) {
+            const T d = S[j * P + j];
+            if (!(d > T(0))) {  // same value in every thread: uniform exit
+                if (threadIdx.x == 0) status[b] = k0 + j + 1;
+                failed = true;
+                break;
+            }
+            const T ljj = sqrt_t(d);
+            __syncthreads();  // every thread has read the pivot
+            for (int i = j + 1 + threadIdx.x; i < kb; i += blockDim.x) S[i * P + j] = S[i * P + j] / ljj;
+            if (threadIdx.x == 0) S[j * P + j] = ljj;
+            __syncthreads();
+            const int m = kb - j - 1;
+            for (int e = threadIdx.x; e < m * m; e += blockDim.x) {
+                const int i = j + 1 + e / m, c = j + 1 + e % m;
+                if (c <= i) S[i * P + c] = fma(-S[i * P + j], S[c * P + j], S[i * P + c]);
+            }
+            __syncthreads();
+        }
+        if (failed) continue;
+        for (int e = threadIdx.x; e < kb * kb; e += blockDim.x) {
+            const int r = e / kb, c = e % kb;
+            if (c <= r) Lb[(int64_t)(k0 + r) * n + k0 + c] = S[r * P + c];
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Triangular solves with a diagonal tile G of L, many right-hand sides.
+// Each right-hand side ("vector") is solved by 4 consecutive lanes that split
+// every dot product and combine it with two shuffles.
+// ---------------------------------------------------------------------------
+enum TrsmMode {
+    TRSM_FWD_PANEL = 0,  // rows of L below tile k:  x L_kk^T = b  (G = L_kk, forward)
+    TRSM_ADJ_X = 1,      // columns of W tile row I:  L_II^T x = b  (G = L_II^T, backward)
+    TRSM_ADJ_M = 2       // rows of W tile column J:  m L_JJ = b    (G = L_JJ^T, backward)
+};
+
+constexpr int kVecPerBlock = kThreads / 4;
+
+template <typename T, int MODE>
+__global__ void __launch_bounds__(kThreads)
+trsm_kernel(const T* L, T* W, const int32_t* __restrict__ status,
+            int64_t batch, int n, int t0, int kb, int v_begin, int v_count) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const int P = kb + 1;
+    T* G = reinterpret_cast<T*>(smem_raw);          // kb x P
+    T* V = G + (size_t)kb * P;                      // kVecPerBlock x P
+    const int vloc = threadIdx.x >> 2;
+    const int q = threadIdx.x & 3;
+    const int v0 = v_begin + blockIdx.x * kVecPerBlock;
+    const int nv = min(kVecPerBlock, v_begin + v_count - v0);
+    for (int64_t b = blockIdx.y; b < batch; b += gridDim.y) {
+        if (skip_matrix(status, b)) continue;
+        const T* Lb = L + b * (int64_t)n * n;
+        T* Wb = W + b * (int64_t)n * n;
+        __syncthreads();
+        // G: lower tile (forward) or the transposed tile (backward)
+        for (int e = threadIdx.x; e < kb * kb; e += blockDim.x) {
+            const int r = e / kb, c = e % kb;  // coalesced over c in global memory
+            const T x = (c <= r) ? Lb[(int64_t)(t0 + r) * n + t0 + c] : T(0);
+            if (MODE == TRSM_FWD_PANEL) G[r * P + c] = x;
+            else G[c * P + r] = x;
+        }
+        // right-hand sides
+        if (MODE == TRSM_ADJ_X) {
+            // vectors are columns v0.. of rows [t0, t0 + kb)
+            for (int e = threadIdx.x; e < kb * kVecPerBlock; e += blockDim.x) {
+                const int m = e / kVecPerBlock, v = e % kVecPerBlock;
+                V[v * P + m] = (v < nv) ? Wb[(int64_t)(t0 + m) * n + v0 + v] : T(0);
+            }
+        } else {
+            // vectors are rows v0.. of columns [t0, t0 + kb) (of L itself in
+            // the forward panel, where W == L)
+            for (int e = threadIdx.x; e < kb * kVecPerBlock; e += blockDim.x) {
+                const int v = e / kb, m = e % kb;
+                V[v * P + m] = (v < nv) ? Wb[(int64_t)(v0 + v) * n + t0 + m] : T(0);
+            }
+        }
+        __syncthreads();
+        {
+            // every group runs the same sweep (idle groups on zero vectors
+            // that are not stored), so the warp's shuffles stay convergent
+            T* x = V + vloc * P;
+            if (MODE == TRSM_FWD_PANEL) {
+                for (int c = 0; c < kb; ++c) {
+                    const T* g = G + c * P;
+                    T s = T(0);
+                    for (int m = q; m < c; m += 4) s = fma(g[m], x[m], s);
+                    s += __shfl_xor_sync(0xffffffffu, s, 1);
+                    s += __shfl_xor_sync(0xffffffffu, s, 2);
+                    if (q == 0) x[c] = (x[c] - s) / g[c];
+                    __syncwarp();
+                }
+            } else {
+                for (int c = kb - 1; c >= 0; --c) {
+                    const T* g = G + c * P;
+                    T s = T(0);
+                    for (int m = c + 1 + q; m < kb; m += 4) s = fma(g[m], x[m], s);
+                    s += __shfl_xor_sync(0xffffffffu, s, 1);
+                    s += __shfl_xor_sync(0xffffffffu, s, 2);
+                    if (q == 0) x[c] = (x[c] - s) / g[c];
+                    __syncwarp();
+                }
+            }
+        }
+        __syncthreads();
+        if (MODE == TRSM_ADJ_X) {
+            for (int e = threadIdx.x; e < kb * kVecPerBlock; e += blockDim.x) {
+                const int m = e / kVecPerBlock, v = e % kVecPerBlock;
+                if (v < nv) Wb[(int64_t)(t0 + m) * n + v0 + v] = V[v * P + m];
+            }
+        } else {
+            for (int e = threadIdx.x; e < kb * kVecPerBlock; e += blockDim.x) {
+                const int v = e / kb, m = e % kb;
+                if (v < nv) Wb[(int64_t)(v0 + v) * n + t0 + m] = V[v * P + m];
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Tile GEMM: C_sub (BM x BM) = alpha * sum_kk opA(r, kk) opB(kk, c) + beta * C_sub
+// over the tile schedules of the forward trailing update and the adjoint.
+// ---------------------------------------------------------------------------
+enum GemmMode {
+    GEMM_FWD_TRAIL = 0,  // L_ij -= L_ik L_jk^T, k < j <= i
+    GEMM_ADJ_P = 1,      // W_IJ = Phi(sum_{K>=I} L_KI^T tril(adj_L)_KJ) (I >= J); 0 for I < J
+    GEMM_ADJ_XUPD = 2,   // W_I'J -= L_II'^T W_IJ, I' < I, all J
+    GEMM_ADJ_MUPD = 3    // W_IJ' -= W_IJ L_JJ', all I, J' < J
+};
 
 template <typename T>
-cudaError_t blocked_fwd(const T*, T*, int32_t*, int64_t, int, int, cudaStream_t) {
-    return cudaErrorNotSupported;
+struct GemmArgs {
+    const T* A;   // operand matrices (batch-strided by n*n)
+    const T* B;
+    T* C;
+    const int32_t* status;
+    int64_t batch;
+    int n;
+    int tile;     // T
+    int nt;       // tiles per side
+    int step;     // k, I or J
+};
+
+struct TileJob {
+    int ci, cj;           // C tile (row, col) in tiles
+    int a_row0, a_col0;   // global origin of op(A)
+    int b_row0, b_col0;   // global origin of op(B)
+    int klen;             // length of the reduction
+    bool a_trans, b_trans, a_lower, b_lower;
+    bool zero_only;       // write zeros (upper tiles of P)
+    bool phi;             // apply Phi (diagonal tile of P)
+    float alpha, beta;
+};
+
+// (i, j) of the t-th entry of a row-major enumeration of a lower triangle.
+__device__ __forceinline__ void lower_index(int t, int& i, int& j) {
+    int r = (int)((sqrt(8.0 * t + 1.0) - 1.0) * 0.5);
+    while ((r + 1) * (r + 2) / 2 <= t) ++r;
+    while (r * (r + 1) / 2 > t) --r;
+    i = r;
+    j = t - r * (r + 1) / 2;
 }
+
+template <typename T, int MODE>
+__device__ __forceinline__ TileJob make_job(const GemmArgs<T>& g, int tile_id) {
+    TileJob job{};
+    const int Tt = g.tile;
+    const int s = g.step;
+    if (MODE == GEMM_FWD_TRAIL) {
+        int i, j;
+        lower_index(tile_id, i, j);
+        i += s + 1;
+        j += s + 1;
+        job.ci = i; job.cj = j;
+        job.a_row0 = i * Tt; job.a_col0 = s * Tt; job.a_trans = false;
+        job.b_row0 = j * Tt; job.b_col0 = s * Tt; job.b_trans = true;
+        job.klen = min(Tt, g.n - s * Tt);
+        job.alpha = -1.f; job.beta = 1.f;
+    } else if (MODE == GEMM_ADJ_P) {
+        const int I = tile_id / g.nt, J = tile_id % g.nt;
+        job.ci = I; job.cj = J;
+        job.zero_only = I < J;
+        job.phi = I == J;
+        job.a_row0 = I * Tt; job.a_col0 = I * Tt; job.a_trans = true;  job.a_lower = true;
+        job.b_row0 = I * Tt; job.b_col0 = J * Tt; job.b_trans = false; job.b_lower = true;
+        job.klen = g.n - I * Tt;
+        job.alpha = 1.f; job.beta = 0.f;
+    } else if (MODE == GEMM_ADJ_XUPD) {
+        const int Ip = tile_id / g.nt, J = tile_id % g.nt;  // Ip < I = s
+        job.ci = Ip; job.cj = J;
+        job.a_row0 = s * Tt; job.a_col0 = Ip * Tt; job.a_trans = true;
+        job.b_row0 = s * Tt; job.b_col0 = J * Tt;  job.b_trans = false;
+        job.klen = min(Tt, g.n - s * Tt);
+        job.alpha = -1.f; job.beta = 1.f;
+    } else {  // GEMM_ADJ_MUPD
+        const int I = tile_id / s, Jp = tile_id % s;  // Jp < J = s
+        job.ci = I; job.cj = Jp;
+        job.a_row0 = I * Tt; job.a_col0 = s * Tt;  job.a_trans = false;
+        job.b_row0 = s * Tt; job.b_col0 = Jp * Tt; job.b_trans = false;
+        job.klen = min(Tt, g.n - s * Tt);
+        job.alpha = -1.f; job.beta = 1.f;
+    }
+    return job;
+}
+
+template <typename T, int BM, int MODE>
+__global__ void __launch_bounds__(kThreads)
+gemm_kernel(GemmArgs<T> g) {
+    constexpr int BK = 16;
+    constexpr int MT = BM / 16;  // micro-tile per thread (MT x MT)
+    constexpr int PAD = 16 / sizeof(T);
+    __shared__ __align__(16) T As[BK][BM + PAD];
+    __shared__ __align__(16) T Bs[BK][BM + PAD];
+    const int subs_per_side = g.tile / BM;
+    const int sub = blockIdx.x % (subs_per_side * subs_per_side);
+    const int tile_id = blockIdx.x / (subs_per_side * subs_per_side);
+    const TileJob job = make_job<T, MODE>(g, tile_id);
+    const int r_off = (sub / subs_per_side) * BM;  // sub-block origin inside the tile
+    const int c_off = (sub % subs_per_side) * BM;
+    const int crow0 = job.ci * g.tile + r_off;
+    const int ccol0 = job.cj * g.tile + c_off;
+    if (crow0 >= g.n || ccol0 >= g.n) return;
+    const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+    const int64_t nn = (int64_t)g.n * g.n;
+
+    for (int64_t b = blockIdx.y; b < g.batch; b += gridDim.y) {
+        if (skip_matrix(g.status, b)) continue;
+        T* Cb = g.C + b * nn;
+        if (job.zero_only) {
+            for (int e = threadIdx.x; e < BM * BM; e += blockDim.x) {
+                const int r = crow0 + e / BM, c = ccol0 + e % BM;
+                if (r < g.n && c < g.n) Cb[(int64_t)r * g.n + c] = T(0);
+            }
+            continue;
+        }
+        const T* Ab = g.A + b * nn;
+        const T* Bb = g.B + b * nn;
+        T acc[MT][MT];
+#pragma unroll
+        for (int i = 0; i < MT; ++i)
+#pragma unroll
+            for (int j = 0; j < MT; ++j) acc[i][j] = T(0);
+
+        for (int k0 = 0; k0 < job.klen; k0 += BK) {
+            __syncthreads();
+            // op(A)(r, kk) for r in the sub-block rows, kk in [k0, k0 + BK)
+            for (int e = threadIdx.x; e < BK * BM; e += blockDim.x) {
+                int r, kk;
+                if (job.a_trans) { kk = e / BM; r = e % BM; }   // contiguous over r
+                else             { r = e / BK;  kk = e % BK; }  // contiguous over kk
+                const int gr = job.a_trans ? job.a_row0 + k0 + kk : job.a_row0 + r_off + r;
+                const int gc = job.a_trans ? job.a_col0 + r_off + r : job.a_col0 + k0 + kk;
+                T x = T(0);
+                if (k0 + kk < job.klen && gr < g.n && gc < g.n && (!job.a_lower || gc <= gr))
+                    x = Ab[(int64_t)gr * g.n + gc];
+                As[kk][r] = x;
+            }
+            // op(B)(kk, c)
+            for (int e = threadIdx.x; e < BK * BM; e += blockDim.x) {
+                int c, kk;
+                if (job.b_trans) { c = e / BK;  kk = e % BK; }  // contiguous over kk
+                else             { kk = e / BM; c = e % BM; }   // contiguous over c
+                const int gr = job.b_trans ? job.b_row0 + c_off + c : job.b_row0 + k0 + kk;
+                const int gc = job.b_trans ? job.b_col0 + k0 + kk : job.b_col0 + c_off + c;
+                T x = T(0);
+                if (k0 + kk < job.klen && gr < g.n && gc < g.n && (!job.b_lower || gc <= gr))
+                    x = Bb[(int64_t)gr * g.n + gc];
+                Bs[kk][c] = x;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int kk = 0; kk < BK; ++kk) {
+                T a[MT], bv[MT];
+#pragma unroll
+                for (int i = 0; i < MT; ++i) a[i] = As[kk][ty * MT + i];
+#pragma unroll
+                for (int j = 0; j < MT; ++j) bv[j] = Bs[kk][tx * MT + j];
+#pragma unroll
+                for (int i = 0; i < MT; ++i)
+#pragma unroll
+                    for (int j = 0; j < MT; ++j) acc[i][j] = fma(a[i], bv[j], acc[i][j]);
+            }
+        }
+        // epilogue
+#pragma unroll
+        for (int i = 0; i < MT; ++i) {
+            const int r = crow0 + ty * MT + i;
+            if (r >= g.n) continue;
+#pragma unroll
+            for (int j = 0; j < MT; ++j) {
+                const int c = ccol0 + tx * MT + j;
+                if (c >= g.n) continue;
+                if (MODE == GEMM_FWD_TRAIL && c > r) continue;  // L stays zero above the diagonal
+                T* cp = Cb + (int64_t)r * g.n + c;
+                T v = T(job.alpha) * acc[i][j];
+                if (job.beta != 0.f) v += *cp;
+                if (job.phi) v = (c < r) ? v : (c == r ? v * T(0.5) : T(0));
+                *cp = v;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// adj_A_ij += M_ij + M_ji (i > j), adj_A_ii += M_ii, through 32x32 blocks.
+// ---------------------------------------------------------------------------
 template <typename T>
-cudaError_t blocked_adj(const T*, const T*, T*, const int32_t*, int64_t, int, int, T*,
-                        cudaStream_t) {
-    return cudaErrorNotSupported;
+__global__ void __launch_bounds__(kThreads)
+phi_acc_kernel(const T* __restrict__ W, T* __restrict__ Abar, const int32_t* __restrict__ status,
+               int64_t batch, int n) {
+    __shared__ T Wt[32][33];
+    const int nb = (n + 31) / 32;
+    int bi, bj;
+    lower_index(blockIdx.x, bi, bj);  // bi >= bj
+    if (bi >= nb) return;
+    const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;
+    for (int64_t b = blockIdx.y; b < batch; b += gridDim.y) {
+        if (skip_matrix(status, b)) continue;
+        const T* Wb = W + b * (int64_t)n * n;
+        T* Ab = Abar + b * (int64_t)n * n;
+        __syncthreads();
+        // W block (bj, bi), transposed into Wt[c][r] = W[bj*32 + r][bi*32 + c]
+        for (int r = ty; r < 32; r += kThreads / 32) {
+            const int gr = bj * 32 + r, gc = bi * 32 + tx;
+            Wt[tx][r] = (gr < n && gc < n) ? Wb[(int64_t)gr * n + gc] : T(0);
+        }
+        __syncthreads();
+        for (int r = ty; r < 32; r += kThreads / 32) {
+            const int gi = bi * 32 + r, gj = bj * 32 + tx;
+            if (gi < n && gj < n && gj <= gi) {
+                const int64_t o = (int64_t)gi * n + gj;
+                const T m_ij = Wb[o];
+                const T m_ji = Wt[r][tx];  // = W[gj][gi]
+                Ab[o] += (gj < gi) ? (m_ij + m_ji) : m_ij;
+            }
+        }
+    }
 }
-template cudaError_t blocked_fwd<float>(const float*, float*, int32_t*, int64_t, int, int, cudaStream_t);
-template cudaError_t blocked_fwd<double>(const double*, double*, int32_t*, int64_t, int, int, cudaStream_t);
-template cudaError_t blocked_adj<float>(const float*, const float*, float*, const int32_t*, int64_t, int, int, float*, cudaStream_t);
-template cudaError_t blocked_adj<double>(const double*, const double*, double*, const int32_t*, int64_t, int, int, double*, cudaStream_t);
+
+size_t trsm_smem(int kb, int esize) {
+    return (size_t)(kb + kVecPerBlock) * (kb + 1) * esize;
+}
+
+template <typename T, int MODE>
+cudaError_t launch_trsm(const T* L, T* W, const int32_t* status, int64_t batch, int n, int t0,
+                        int kb, int v_begin, int v_count, cudaStream_t stream) {
+    if (v_count <= 0) return cudaSuccess;
+    const size_t smem = trsm_smem(kb, sizeof(T));
+    auto kern = trsm_kernel<T, MODE>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)((v_count + kVecPerBlock - 1) / kVecPerBlock), grid_y(batch));
+    kern<<<grid, kThreads, smem, stream>>>(L, W, status, batch, n, t0, kb, v_begin, v_count);
+    return cudaGetLastError();
+}
+
+template <typename T, int MODE>
+cudaError_t launch_gemm(const GemmArgs<T>& g, int tiles, cudaStream_t stream) {
+    if (tiles <= 0) return cudaSuccess;
+    const int bm = g.tile >= 64 ? 64 : 32;
+    const int subs = (g.tile / bm) * (g.tile / bm);
+    dim3 grid((unsigned)(tiles * subs), grid_y(g.batch));
+    if (bm == 64) gemm_kernel<T, 64, MODE><<<grid, kThreads, 0, stream>>>(g);
+    else gemm_kernel<T, 32, MODE><<<grid, kThreads, 0, stream>>>(g);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int blocked_default_tile(int n, int elem_size) {
+    (void)elem_size;
+    return n <= 256 ? 32 : (n <= 1024 ? 64 : 128);
+}
+
+#define CHOL_TRY(x)                              \
+    do {                                         \
+        cudaError_t e_ = (x);                    \
+        if (e_ != cudaSuccess) return e_;        \
+    } while (0)
+
+template <typename T>
+cudaError_t blocked_fwd(const T* A, T* L, int32_t* status, int64_t batch, int n, int tile,
+                        cudaStream_t stream) {
+    const int nt = (n + tile - 1) / tile;
+    {
+        const int64_t total = batch * (int64_t)n * n;
+        const int64_t blocks = std::min<int64_t>((total + kThreads - 1) / kThreads, 152 * 32);
+        tril_copy_kernel<T><<<(unsigned)std::max<int64_t>(blocks, 1), kThreads, 0, stream>>>(
+            A, L, status, batch, n);
+        CHOL_TRY(cudaGetLastError());
+    }
+    const size_t diag_smem = (size_t)tile * (tile + 1) * sizeof(T);
+    CHOL_TRY(cudaFuncSetAttribute(potrf_diag_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)diag_smem));
+    for (int k = 0; k < nt; ++k) {
+        const int k0 = k * tile;
+        const int kb = std::min(tile, n - k0);
+        potrf_diag_kernel<T><<<dim3(1, grid_y(batch)), kThreads, (size_t)kb * (kb + 1) * sizeof(T),
+                               stream>>>(L, status, batch, n, k0, kb);
+        CHOL_TRY(cudaGetLastError());
+        if (k == nt - 1) break;
+        CHOL_TRY((launch_trsm<T, TRSM_FWD_PANEL>(L, L, status, batch, n, k0, kb, k0 + kb,
+                                                 n - k0 - kb, stream)));
+        const int m = nt - k - 1;
+        GemmArgs<T> g{L, L, L, status, batch, n, tile, nt, k};
+        CHOL_TRY((launch_gemm<T, GEMM_FWD_TRAIL>(g, m * (m + 1) / 2, stream)));
+    }
+    return cudaSuccess;
+}
+
+template <typename T>
+cudaError_t blocked_adj(const T* L, const T* Lbar, T* Abar, const int32_t* status,
+                        int64_t batch, int n, int tile, T* W, cudaStream_t stream) {
+    const int nt = (n + tile - 1) / tile;
+    {
+        GemmArgs<T> g{L, Lbar, W, status, batch, n, tile, nt, 0};
+        CHOL_TRY((launch_gemm<T, GEMM_ADJ_P>(g, nt * nt, stream)));
+    }
+    // X = L^-T S, tile rows from the bottom
+    for (int I = nt - 1; I >= 0; --I) {
+        const int t0 = I * tile, kb = std::min(tile, n - t0);
+        CHOL_TRY((launch_trsm<T, TRSM_ADJ_X>(L, W, status, batch, n, t0, kb, 0, n, stream)));
+        if (I > 0) {
+            GemmArgs<T> g{L, W, W, status, batch, n, tile, nt, I};
+            CHOL_TRY((launch_gemm<T, GEMM_ADJ_XUPD>(g, I * nt, stream)));
+        }
+    }
+    // M = X L^-1, tile columns from the right
+    for (int J = nt - 1; J >= 0; --J) {
+        const int t0 = J * tile, kb = std::min(tile, n - t0);
+        CHOL_TRY((launch_trsm<T, TRSM_ADJ_M>(L, W, status, batch, n, t0, kb, 0, n, stream)));
+        if (J > 0) {
+            GemmArgs<T> g{W, L, W, status, batch, n, tile, nt, J};
+            CHOL_TRY((launch_gemm<T, GEMM_ADJ_MUPD>(g, nt * J, stream)));
+        }
+    }
+    {
+        const int nb = (n + 31) / 32;
+        phi_acc_kernel<T><<<dim3((unsigned)(nb * (nb + 1) / 2), grid_y(batch)), kThreads, 0,
+                            stream>>>(W, Abar, status, batch, n);
+        CHOL_TRY(cudaGetLastError());
+    }
+    return cudaSuccess;
+}
+
+template cudaError_t blocked_fwd<float>(const float*, float*, int32_t*, int64_t, int, int,
+                                        cudaStream_t);
+template cudaError_t blocked_fwd<double>(const double*, double*, int32_t*, int64_t, int, int,
+                                         cudaStream_t);
+template cudaError_t blocked_adj<float>(const float*, const float*, float*, const int32_t*,
+                                        int64_t, int, int, float*, cudaStream_t);
+template cudaError_t blocked_adj<double>(const double*, const double*, double*, const int32_t*,
+                                         int64_t, int, int, double*, cudaStream_t);
 
 }  // namespace chol

@@ -10,20 +10,21 @@ import pytest
 from differentiable_cholesky_gb300 import binding
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "chol.h")
+HEADERS = [os.path.join(ROOT, "include", h) for h in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if h.endswith(".h")]
 
 CHOL_OK, CHOL_EINVAL, CHOL_EDTYPE = 0, -1, -2
 
 
 def declared_symbols():
-    text = open(HEADER).read()
+    text = "".join(open(h).read() for h in HEADERS)
     return sorted(set(re.findall(r"CHOL_API\s+[\w\s\*]+?\b(chol_\w+)\s*\(", text)))
 
 
 def test_header_declares_the_path():
     syms = declared_symbols()
     for s in ("chol_fwd", "chol_adj", "chol_fwd_ex", "chol_adj_ex", "chol_strerror",
-              "chol_abi_version"):
+              "chol_abi_version", "chol_probe_fma_peak"):
         assert s in syms
 
 

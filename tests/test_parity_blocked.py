@@ -1,0 +1,150 @@
+"""GPU parity of the blocked path (n > 64) against the oracle, through the C ABI."""
+import numpy as np
+import pytest
+
+import oracle
+from differentiable_cholesky_gb300 import workloads as W
+from parity_util import TOL_ADJ, TOL_L, gpu_fwd_adj, max_rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+def check(A, Lbar, dtype, tile=0, adj_A0=None, expect_L=None):
+    dtype = np.dtype(dtype)
+    L, st, G = gpu_fwd_adj(A, Lbar, tile=tile, adj_A0=adj_A0)
+    _, st_ref = oracle.potrf(A, dtype=dtype)
+    assert np.array_equal(st.reshape(-1), st_ref.reshape(-1))
+    ok = st.reshape(-1) == 0
+    L_ref, _ = oracle.potrf(A.astype(np.float64))
+    G_ref = oracle.potrf_adj(L_ref, Lbar.astype(np.float64),
+                             Abar=None if adj_A0 is None else adj_A0.astype(np.float64),
+                             status=st_ref)
+    assert np.all(np.triu(L[ok], 1) == 0)
+    assert max_rel_err(L, L_ref, mask=ok) <= TOL_L[dtype]
+    assert max_rel_err(G, G_ref, mask=ok, lower=True) <= TOL_ADJ[dtype]
+    if expect_L is not None:
+        assert max_rel_err(L, expect_L) <= TOL_L[dtype]
+    return L, st, G
+
+
+@pytest.mark.parametrize("dtype", [np.float64, np.float32])
+@pytest.mark.parametrize("n", [65, 96, 127, 128, 129, 200, 257, 300])
+def test_sizes_default_tile(n, dtype):
+    A = W.gram_spd(3, n, 21 + n, 1.0, dtype)
+    Lbar = W.tril_normal(3, n, 22 + n, dtype)
+    check(A, Lbar, dtype)
+
+
+@pytest.mark.parametrize("tile", [32, 64, 128])
+@pytest.mark.parametrize("n", [65, 190, 300])
+def test_explicit_tiles(n, tile):
+    A = W.gram_spd(2, n, 23, 1.0, np.float64)
+    Lbar = W.tril_normal(2, n, 24, np.float64)
+    check(A, Lbar, np.float64, tile=tile)
+
+
+def test_tile_independence():
+    n = 300
+    A = W.gram_spd(2, n, 25, 1.0, np.float64)
+    Lbar = W.tril_normal(2, n, 26, np.float64)
+    outs = [gpu_fwd_adj(A, Lbar, tile=t) for t in (32, 64, 128)]
+    for L, st, G in outs[1:]:
+        assert max_rel_err(L, outs[0][0]) <= 1e-13
+        assert max_rel_err(G, outs[0][2], lower=True) <= 1e-12
+
+
+def test_bidiagonal_512_closed_form():
+    """jaxmg docs worked example: the factor of E E^T is E (N = 512, T_A = 128)."""
+    w = W.bidiagonal_512()
+    check(w.A, w.adj_L, np.float64, tile=128, expect_L=w.expected_L)
+
+
+def test_batched_512_full_size_sampled():
+    w = W.batched_512()
+    L, st, G = gpu_fwd_adj(w.A, w.adj_L, tile=128)
+    assert np.all(st == 0)
+    assert np.all(np.triu(L, 1) == 0)
+    for b in (0, 85, 170, 255):
+        L_ref, s = oracle.potrf(w.A[b])
+        assert int(s) == 0
+        G_ref = oracle.potrf_adj(L_ref, w.adj_L[b])
+        assert max_rel_err(L[b:b + 1], L_ref[None]) <= 1e-12
+        assert max_rel_err(G[b:b + 1], G_ref[None], lower=True) <= 1e-10
+
+
+def test_banded_8192_full_size():
+    """L equals the banded E (closed form); the adjoint satisfies
+    L^T Z L = S + S^T with Z = adj_A + adj_A^T, S = Phi(L^T tril(adj_L)),
+    checked on sampled columns (the relation determines Z uniquely)."""
+    w = W.banded_8192()
+    L, st, G = gpu_fwd_adj(w.A, w.adj_L, tile=128)
+    assert int(st[0]) == 0
+    E = w.expected_L[0]
+    assert max_rel_err(L, E[None]) <= 1e-12
+    Gl = np.tril(G[0])
+    Lb = w.adj_L[0]
+    n = E.shape[0]
+    rng = np.random.default_rng(7)
+    for j in [0, 1, n // 2, n - 2, n - 1] + list(rng.integers(0, n, 3)):
+        j = int(j)
+        zcol = Gl @ E[:, j] + Gl.T @ E[:, j]     # Z L e_j
+        lhs = E.T @ zcol                          # L^T Z L e_j
+        col_p = E.T @ Lb[:, j]                    # (L^T Lbar)_{:, j}
+        row_p = E[:, j] @ Lb                      # (L^T Lbar)_{j, :}
+        rhs = np.zeros(n)
+        rhs[j + 1:] = col_p[j + 1:]               # S_ij, i > j
+        rhs[:j] = row_p[:j]                       # S_ji, i < j
+        rhs[j] = col_p[j]                         # 2 * S_jj = P_jj
+        assert np.linalg.norm(lhs - rhs) <= 1e-10 * np.linalg.norm(rhs)
+
+
+@pytest.mark.parametrize("tile", [32, 64])
+def test_status_global_column_and_skip(tile):
+    n, batch = 200, 4
+    A = W.gram_spd(batch, n, 27, 1.0, np.float64)
+    A[1, 150, 150] = -1.0
+    A[2, 0, 0] = 0.0
+    A[3, 199, 199] = np.nan
+    Lbar = W.tril_normal(batch, n, 28, np.float64)
+    G0 = np.full_like(A, 2.0)
+    L, st, G = check(A, Lbar, np.float64, tile=tile, adj_A0=G0)
+    assert list(st) == [0, 151, 1, 200]
+    assert np.all(G[1:] == 2.0)
+
+
+def test_upper_triangles_ignored_and_untouched():
+    import torch
+    from differentiable_cholesky_gb300 import binding
+    n, batch = 150, 2
+    A = W.gram_spd(batch, n, 29, 1.0, np.float64)
+    Lbar = W.tril_normal(batch, n, 30, np.float64)
+    iu = np.triu_indices(n, 1)
+    Ag = A.copy(); Ag[:, iu[0], iu[1]] = np.nan
+    Lbg = Lbar.copy(); Lbg[:, iu[0], iu[1]] = 1e30
+    G0 = np.full_like(A, -1.5)
+    L1, s1, G1 = gpu_fwd_adj(A, Lbar, adj_A0=G0, tile=64)
+    dev = torch.device("cuda:0")
+    Lt, st = binding.chol_fwd(torch.from_numpy(Ag).to(dev), tile=64)
+    Lt2 = Lt.clone()
+    Lt2[:, iu[0], iu[1]] = 3.0
+    Gt = binding.chol_adj(Lt2, torch.from_numpy(Lbg).to(dev), adj_A=torch.from_numpy(G0).to(dev),
+                          status=st, tile=64)
+    torch.cuda.synchronize()
+    assert np.array_equal(Lt.cpu().numpy(), L1)
+    assert np.array_equal(Gt.cpu().numpy(), G1)
+    assert np.all(G1[:, iu[0], iu[1]] == -1.5)
+
+
+def test_autograd_wrapper_matches_the_adjoint():
+    import torch
+    from differentiable_cholesky_gb300 import binding
+    dev = torch.device("cuda:0")
+    for n in (12, 100):
+        A = W.gram_spd(2, n, 31, 1.0, np.float64)
+        Lbar = W.tril_normal(2, n, 32, np.float64)
+        At = torch.from_numpy(A).to(dev).requires_grad_(True)
+        L, st = binding.cholesky(At)
+        (L * torch.from_numpy(Lbar).to(dev)).sum().backward()
+        L_ref, _ = oracle.potrf(A)
+        G_ref = oracle.potrf_adj(L_ref, Lbar)
+        assert max_rel_err(At.grad.cpu().numpy(), G_ref) <= 1e-10
