@@ -1,0 +1,325 @@
+// Thread-per-matrix Cholesky forward and adjoint for float32 matrices of order
+// N = 8 or 16 (the batched 65536 x 16x16 workload).
+//
+// One warp handles 32 matrices per round, one per lane, with no communication
+// between lanes: every lane keeps the lower triangle of its own matrix in
+// registers.  Matrices move between HBM and shared memory by TMA bulk copies
+// (cp.async.bulk, one per matrix, completion on an mbarrier) into per-lane
+// slots that are skewed by 16 bytes, so each lane's 16-byte row reads and
+// writes fall in distinct bank groups; results leave by bulk stores.  A block
+// is one warp; blocks are persistent (resident blocks per SM x SMs).
+//
+// Forward (jaxmg docs "Cholesky factorization": lower factor and status):
+// right-looking column recurrence with IEEE square root and a correctly
+// rounded reciprocal of the pivot.
+//
+// Adjoint: the symmetric-matrix derivative of Murray (2016) -- the one
+// NVIDIA/warp issue #1316's closing comment implements with S = Phi(L^T adj_L)
+// and two triangular solves -- evaluated here by the same paper's in-place
+// reverse sweep over the factorisation (columns j = N-1 .. 0), which reaches
+// the same lower-triangle gradient Phi(M + M^T) with one triangle of
+// registers and N^3/3 multiply-adds instead of 7N^3/6.  The gradient is added
+// to the old adj_A in shared memory and written back as a whole matrix: the
+// upper triangle is rewritten with the values that were read.
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace chol {
+namespace {
+
+template <int N>
+struct Tpm {
+    static constexpr uint32_t kBytes = N * N * 4;   // one matrix
+    static constexpr int kSlot = N * N + 4;         // floats per lane slot (16-byte skew)
+    static constexpr size_t kSlotsBytes = 32 * (size_t)kSlot * 4;
+    static_assert(kBytes % 16 == 0, "bulk copies move multiples of 16 bytes");
+};
+
+constexpr int kBarBytes = 128;  // mbarrier area in front of the slots
+
+// Lower triangle of row i of the slot into registers.
+template <int N>
+__device__ __forceinline__ void slot_load_lower(const float* slot, float (&a)[N][N]) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+#pragma unroll
+        for (int c = 0; c < N / 4; ++c) {
+            if (4 * c > i) continue;
+            const float4 v = reinterpret_cast<const float4*>(slot + i * N)[c];
+            a[i][4 * c + 0] = v.x;
+            if (4 * c + 1 <= i) a[i][4 * c + 1] = v.y;
+            if (4 * c + 2 <= i) a[i][4 * c + 2] = v.z;
+            if (4 * c + 3 <= i) a[i][4 * c + 3] = v.w;
+        }
+    }
+}
+
+template <int N>
+__global__ void __launch_bounds__(32)
+tpm_potrf_kernel(const float* __restrict__ A, float* __restrict__ L, int32_t* __restrict__ status,
+                 int64_t batch) {
+    using C = Tpm<N>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
+    const int lane = threadIdx.x;
+    float* slot = reinterpret_cast<float*>(smem + kBarBytes) + lane * C::kSlot;
+    if (lane == 0) mbar_init(bar, 1);
+    fence_mbar_init();
+    __syncwarp();
+
+    uint32_t phase = 0;
+#pragma unroll 1
+    for (int64_t w = blockIdx.x; w * 32 < batch; w += gridDim.x) {
+        const int64_t m0 = w * 32;
+        const int nvalid = batch - m0 < 32 ? (int)(batch - m0) : 32;
+        const int64_t m = m0 + lane;
+        fence_proxy_async_smem();
+        if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)nvalid * C::kBytes);
+        __syncwarp();
+        if (lane < nvalid) bulk_load(slot, A + m * (N * N), C::kBytes, bar);
+        if (!__all_sync(0xffffffffu, mbar_wait(bar, phase, kMbarPolls))) {
+            // The copies did not complete: mark this round's matrices and stop
+            // (after one more bounded wait for the copies in flight).
+            if (lane < nvalid) status[m] = -1;
+            mbar_wait(bar, phase, kMbarPolls);
+            break;
+        }
+        phase ^= 1u;
+
+        float a[N][N];
+        if (lane < nvalid) {
+            slot_load_lower<N>(slot, a);
+        } else {
+#pragma unroll
+            for (int i = 0; i < N; ++i)
+#pragma unroll
+                for (int k = 0; k <= i; ++k) a[i][k] = (i == k) ? 1.f : 0.f;
+        }
+
+        int st = 0;
+#pragma unroll
+        for (int j = 0; j < N; ++j) {
+            float d = a[j][j];
+            if (!(d > 0.f)) {
+                if (st == 0) st = j + 1;
+                d = 1.f;
+            }
+            const float ljj = __fsqrt_rn(d);
+            const float inv = __frcp_rn(ljj);
+            a[j][j] = ljj;
+#pragma unroll
+            for (int i = j + 1; i < N; ++i) a[i][j] *= inv;
+#pragma unroll
+            for (int k = j + 1; k < N; ++k)
+#pragma unroll
+                for (int i = k; i < N; ++i) a[i][k] = fmaf(-a[i][j], a[k][j], a[i][k]);
+        }
+
+        if (lane < nvalid) {
+#pragma unroll
+            for (int i = 0; i < N; ++i) {
+#pragma unroll
+                for (int c = 0; c < N / 4; ++c) {
+                    float4 v;
+                    v.x = (4 * c + 0 <= i) ? a[i][4 * c + 0] : 0.f;
+                    v.y = (4 * c + 1 <= i) ? a[i][4 * c + 1] : 0.f;
+                    v.z = (4 * c + 2 <= i) ? a[i][4 * c + 2] : 0.f;
+                    v.w = (4 * c + 3 <= i) ? a[i][4 * c + 3] : 0.f;
+                    reinterpret_cast<float4*>(slot + i * N)[c] = v;
+                }
+            }
+            fence_proxy_async_smem();
+            bulk_store(L + m * (N * N), slot, C::kBytes);
+            bulk_commit();
+            status[m] = st;
+        }
+        bulk_wait_read_all();  // the slot is free for the next round's load
+        __syncwarp();
+    }
+    bulk_wait_all();
+}
+
+template <int N>
+__global__ void __launch_bounds__(32)
+tpm_potrf_adj_kernel(const float* __restrict__ Lg, const float* __restrict__ Lbar,
+                     float* __restrict__ Abar, const int32_t* __restrict__ status, int64_t batch) {
+    using C = Tpm<N>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t* bar_in = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* bar_ab = bar_in + 1;
+    const int lane = threadIdx.x;
+    const float* lslot = reinterpret_cast<float*>(smem + kBarBytes) + lane * C::kSlot;
+    float* bslot = reinterpret_cast<float*>(smem + kBarBytes + C::kSlotsBytes) + lane * C::kSlot;
+    if (lane == 0) {
+        mbar_init(bar_in, 1);
+        mbar_init(bar_ab, 1);
+    }
+    fence_mbar_init();
+    __syncwarp();
+
+    uint32_t phase = 0;
+#pragma unroll 1
+    for (int64_t w = blockIdx.x; w * 32 < batch; w += gridDim.x) {
+        const int64_t m0 = w * 32;
+        const int nvalid = batch - m0 < 32 ? (int)(batch - m0) : 32;
+        const int64_t m = m0 + lane;
+        bool active = lane < nvalid;
+        if (active && status != nullptr) active = (__ldg(status + m) == 0);
+
+        // L and adj_L in
+        fence_proxy_async_smem();
+        if (lane == 0) mbar_arrive_expect_tx(bar_in, (uint32_t)nvalid * 2u * C::kBytes);
+        __syncwarp();
+        if (lane < nvalid) {
+            bulk_load(const_cast<float*>(lslot), Lg + m * (N * N), C::kBytes, bar_in);
+            bulk_load(bslot, Lbar + m * (N * N), C::kBytes, bar_in);
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_in, phase, kMbarPolls))) {
+            mbar_wait(bar_in, phase, kMbarPolls);
+            break;  // the copies did not complete: adj_A of this round is left unchanged
+        }
+
+        float g[N][N];
+        slot_load_lower<N>(bslot, g);
+
+        // old adj_A into the adj_L slot while the sweep runs
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_expect_tx(bar_ab, (uint32_t)nvalid * C::kBytes);
+        __syncwarp();
+        if (lane < nvalid) bulk_load(bslot, Abar + m * (N * N), C::kBytes, bar_ab);
+
+        // Reverse sweep.  Column j of g holds the gradient w.r.t. column j of
+        // L on entry and w.r.t. column j of A (lower part) on exit.
+#pragma unroll
+        for (int j = N - 1; j >= 0; --j) {
+            const float ljj = lslot[j * N + j];
+            const float inv = __frcp_rn(ljj);
+            float s = 0.f;
+            // rows below j: prefix [0, j] of row i of L
+#pragma unroll
+            for (int i = N - 1; i > j; --i) {
+                float lrow[N];
+#pragma unroll
+                for (int c = 0; c < N / 4; ++c) {
+                    if (4 * c > j) continue;
+                    const float4 v = reinterpret_cast<const float4*>(lslot + i * N)[c];
+                    lrow[4 * c + 0] = v.x;
+                    lrow[4 * c + 1] = v.y;
+                    lrow[4 * c + 2] = v.z;
+                    lrow[4 * c + 3] = v.w;
+                }
+                s = fmaf(lrow[j], g[i][j], s);
+                g[i][j] *= inv;
+#pragma unroll
+                for (int k = 0; k < j; ++k) g[j][k] = fmaf(-g[i][j], lrow[k], g[j][k]);
+            }
+            g[j][j] = (g[j][j] - s * inv) * inv;
+            float lj[N];
+#pragma unroll
+            for (int c = 0; c < N / 4; ++c) {
+                if (4 * c > j) continue;
+                const float4 v = reinterpret_cast<const float4*>(lslot + j * N)[c];
+                lj[4 * c + 0] = v.x;
+                lj[4 * c + 1] = v.y;
+                lj[4 * c + 2] = v.z;
+                lj[4 * c + 3] = v.w;
+            }
+#pragma unroll
+            for (int k = 0; k < j; ++k) g[j][k] = fmaf(-g[j][j], lj[k], g[j][k]);
+#pragma unroll
+            for (int i = j + 1; i < N; ++i)
+#pragma unroll
+                for (int k = 0; k < j; ++k) g[i][k] = fmaf(-g[i][j], lj[k], g[i][k]);
+            g[j][j] *= 0.5f;
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_ab, phase, kMbarPolls))) {
+            mbar_wait(bar_ab, phase, kMbarPolls);
+            break;
+        }
+        phase ^= 1u;  // both barriers complete one phase per round
+        if (active) {
+#pragma unroll
+            for (int i = 0; i < N; ++i) {
+#pragma unroll
+                for (int c = 0; c < N / 4; ++c) {
+                    if (4 * c > i) continue;
+                    float4 v = reinterpret_cast<const float4*>(bslot + i * N)[c];
+                    v.x += g[i][4 * c + 0];
+                    if (4 * c + 1 <= i) v.y += g[i][4 * c + 1];
+                    if (4 * c + 2 <= i) v.z += g[i][4 * c + 2];
+                    if (4 * c + 3 <= i) v.w += g[i][4 * c + 3];
+                    reinterpret_cast<float4*>(bslot + i * N)[c] = v;
+                }
+            }
+            fence_proxy_async_smem();
+            bulk_store(Abar + m * (N * N), bslot, C::kBytes);
+            bulk_commit();
+        }
+        bulk_wait_read_all();
+        __syncwarp();
+    }
+    bulk_wait_all();
+}
+
+template <typename K>
+int tpm_grid(K kern, size_t smem, int64_t rounds) {
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32, smem) != cudaSuccess ||
+        per_sm < 1) {
+        cudaGetLastError();
+        per_sm = 1;
+    }
+    return (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)std::max(sms, 1) * per_sm, rounds));
+}
+
+template <int N>
+cudaError_t tpm_fwd_n(const float* A, float* L, int32_t* status, int64_t batch,
+                      cudaStream_t stream) {
+    const size_t smem = kBarBytes + Tpm<N>::kSlotsBytes;
+    auto kern = tpm_potrf_kernel<N>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int grid = tpm_grid(kern, smem, (batch + 31) / 32);
+    kern<<<grid, 32, smem, stream>>>(A, L, status, batch);
+    return cudaGetLastError();
+}
+
+template <int N>
+cudaError_t tpm_adj_n(const float* L, const float* Lbar, float* Abar, const int32_t* status,
+                      int64_t batch, cudaStream_t stream) {
+    const size_t smem = kBarBytes + 2 * Tpm<N>::kSlotsBytes;
+    auto kern = tpm_potrf_adj_kernel<N>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int grid = tpm_grid(kern, smem, (batch + 31) / 32);
+    kern<<<grid, 32, smem, stream>>>(L, Lbar, Abar, status, batch);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tpm_supported(int n) { return n == 8 || n == 16; }
+
+cudaError_t tpm_fwd(const float* A, float* L, int32_t* status, int64_t batch, int n,
+                    cudaStream_t stream) {
+    if (n == 16) return tpm_fwd_n<16>(A, L, status, batch, stream);
+    if (n == 8) return tpm_fwd_n<8>(A, L, status, batch, stream);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t tpm_adj(const float* L, const float* Lbar, float* Abar, const int32_t* status,
+                    int64_t batch, int n, cudaStream_t stream) {
+    if (n == 16) return tpm_adj_n<16>(L, Lbar, Abar, status, batch, stream);
+    if (n == 8) return tpm_adj_n<8>(L, Lbar, Abar, status, batch, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace chol
