@@ -6,8 +6,9 @@
 // registers.  Matrices move between HBM and shared memory by TMA bulk copies
 // (cp.async.bulk, one per matrix, completion on an mbarrier) into per-lane
 // slots that are skewed by 16 bytes, so each lane's 16-byte row reads and
-// writes fall in distinct bank groups; results leave by bulk stores.  A block
-// is one warp; blocks are persistent (resident blocks per SM x SMs).
+// writes fall in distinct bank groups.  Each warp owns two slot sets, so the
+// copy for its next round is in flight while it computes the current one.  A
+// block is one warp; blocks are persistent (resident blocks per SM x SMs).
 //
 // Forward (jaxmg docs "Cholesky factorization": lower factor and status):
 // right-looking column recurrence with IEEE square root and a correctly
@@ -18,9 +19,10 @@
 // and two triangular solves -- evaluated here by the same paper's in-place
 // reverse sweep over the factorisation (columns j = N-1 .. 0), which reaches
 // the same lower-triangle gradient Phi(M + M^T) with one triangle of
-// registers and N^3/3 multiply-adds instead of 7N^3/6.  The gradient is added
-// to the old adj_A in shared memory and written back as a whole matrix: the
-// upper triangle is rewritten with the values that were read.
+// registers and N^3/3 multiply-adds instead of 7N^3/6.  adj_L and adj_A are
+// read (and adj_A written) by each lane directly, in 16-byte chunks of its
+// matrix's lower triangle; the chunk that straddles the diagonal is written
+// back with the upper values that were read.
 
 #include <cuda_runtime.h>
 
@@ -59,37 +61,68 @@ __device__ __forceinline__ void slot_load_lower(const float* slot, float (&a)[N]
     }
 }
 
+// Issue the bulk loads of matrices [m0, m0 + nvalid) into the lanes' slots,
+// completion on `bar`.  Every lane of the warp calls this.
+template <int N>
+__device__ __forceinline__ void issue_round_load(const float* __restrict__ src, int64_t m0,
+                                                 int nvalid, float* slot, uint64_t* bar,
+                                                 int lane) {
+    fence_proxy_async_smem();  // earlier generic accesses to the slot come first
+    __syncwarp();
+    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)nvalid * Tpm<N>::kBytes);
+    __syncwarp();
+    if (lane < nvalid) bulk_load(slot, src + (m0 + lane) * (N * N), Tpm<N>::kBytes, bar);
+}
+
+__device__ __forceinline__ int round_count(int64_t batch, int64_t w) {
+    return batch - w * 32 < 32 ? (int)(batch - w * 32) : 32;
+}
+
+// Forward.  Two slot sets per warp: the copy of round r + 1 is in flight
+// while round r is factored; L leaves through the slot it arrived in.
 template <int N>
 __global__ void __launch_bounds__(32)
 tpm_potrf_kernel(const float* __restrict__ A, float* __restrict__ L, int32_t* __restrict__ status,
                  int64_t batch) {
     using C = Tpm<N>;
     extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);  // bar[0], bar[1]
     const int lane = threadIdx.x;
-    float* slot = reinterpret_cast<float*>(smem + kBarBytes) + lane * C::kSlot;
-    if (lane == 0) mbar_init(bar, 1);
+    float* slots = reinterpret_cast<float*>(smem + kBarBytes);
+    float* slot_of[2] = {slots + lane * C::kSlot, slots + (32 + lane) * C::kSlot};
+    if (lane == 0) {
+        mbar_init(bar + 0, 1);
+        mbar_init(bar + 1, 1);
+    }
     fence_mbar_init();
     __syncwarp();
 
-    uint32_t phase = 0;
+    int64_t w = blockIdx.x;
+    if (w * 32 >= batch) return;
+    issue_round_load<N>(A, w * 32, round_count(batch, w), slot_of[0], bar + 0, lane);
+    uint32_t phase[2] = {0u, 0u};
 #pragma unroll 1
-    for (int64_t w = blockIdx.x; w * 32 < batch; w += gridDim.x) {
+    for (int r = 0; w * 32 < batch; ++r, w += gridDim.x) {
+        const int b = r & 1;
         const int64_t m0 = w * 32;
-        const int nvalid = batch - m0 < 32 ? (int)(batch - m0) : 32;
+        const int nvalid = round_count(batch, w);
         const int64_t m = m0 + lane;
-        fence_proxy_async_smem();
-        if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)nvalid * C::kBytes);
-        __syncwarp();
-        if (lane < nvalid) bulk_load(slot, A + m * (N * N), C::kBytes, bar);
-        if (!__all_sync(0xffffffffu, mbar_wait(bar, phase, kMbarPolls))) {
+        const int64_t wn = w + gridDim.x;
+        if (wn * 32 < batch) {
+            bulk_wait_read_all();  // the other slot's last store has left shared memory
+            issue_round_load<N>(A, wn * 32, round_count(batch, wn), slot_of[b ^ 1], bar + (b ^ 1),
+                                lane);
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(bar + b, phase[b], kMbarPolls))) {
             // The copies did not complete: mark this round's matrices and stop
             // (after one more bounded wait for the copies in flight).
             if (lane < nvalid) status[m] = -1;
-            mbar_wait(bar, phase, kMbarPolls);
+            mbar_wait(bar + b, phase[b], kMbarPolls);
+            mbar_wait(bar + (b ^ 1), phase[b ^ 1], kMbarPolls);
             break;
         }
-        phase ^= 1u;
+        phase[b] ^= 1u;
+        float* slot = slot_of[b];
 
         float a[N][N];
         if (lane < nvalid) {
@@ -138,61 +171,81 @@ tpm_potrf_kernel(const float* __restrict__ A, float* __restrict__ L, int32_t* __
             bulk_commit();
             status[m] = st;
         }
-        bulk_wait_read_all();  // the slot is free for the next round's load
-        __syncwarp();
     }
     bulk_wait_all();
 }
 
+// Lower 16-byte chunks of matrix row i from global memory into r.
+template <int N>
+__device__ __forceinline__ void ldg_lower(const float* __restrict__ mat, float (&r)[N][N]) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+#pragma unroll
+        for (int c = 0; c < N / 4; ++c) {
+            if (4 * c > i) continue;
+            const float4 v = __ldg(reinterpret_cast<const float4*>(mat + i * N) + c);
+            r[i][4 * c + 0] = v.x;
+            if (4 * c + 1 <= i) r[i][4 * c + 1] = v.y;
+            if (4 * c + 2 <= i) r[i][4 * c + 2] = v.z;
+            if (4 * c + 3 <= i) r[i][4 * c + 3] = v.w;
+        }
+    }
+}
+
+// Adjoint.  L arrives by bulk copy into two slot sets (round r + 1 in flight
+// while round r runs); adj_L and adj_A are read and written by each lane
+// directly, in 16-byte chunks of its own matrix's lower triangle (the chunk
+// that straddles the diagonal is written back with the upper values it read).
 template <int N>
 __global__ void __launch_bounds__(32)
 tpm_potrf_adj_kernel(const float* __restrict__ Lg, const float* __restrict__ Lbar,
                      float* __restrict__ Abar, const int32_t* __restrict__ status, int64_t batch) {
     using C = Tpm<N>;
     extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t* bar_in = reinterpret_cast<uint64_t*>(smem);
-    uint64_t* bar_ab = bar_in + 1;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
     const int lane = threadIdx.x;
-    const float* lslot = reinterpret_cast<float*>(smem + kBarBytes) + lane * C::kSlot;
-    float* bslot = reinterpret_cast<float*>(smem + kBarBytes + C::kSlotsBytes) + lane * C::kSlot;
+    float* slots = reinterpret_cast<float*>(smem + kBarBytes);
+    float* slot_of[2] = {slots + lane * C::kSlot, slots + (32 + lane) * C::kSlot};
     if (lane == 0) {
-        mbar_init(bar_in, 1);
-        mbar_init(bar_ab, 1);
+        mbar_init(bar + 0, 1);
+        mbar_init(bar + 1, 1);
     }
     fence_mbar_init();
     __syncwarp();
 
-    uint32_t phase = 0;
+    int64_t w = blockIdx.x;
+    if (w * 32 >= batch) return;
+    issue_round_load<N>(Lg, w * 32, round_count(batch, w), slot_of[0], bar + 0, lane);
+    uint32_t phase[2] = {0u, 0u};
 #pragma unroll 1
-    for (int64_t w = blockIdx.x; w * 32 < batch; w += gridDim.x) {
+    for (int r = 0; w * 32 < batch; ++r, w += gridDim.x) {
+        const int b = r & 1;
         const int64_t m0 = w * 32;
-        const int nvalid = batch - m0 < 32 ? (int)(batch - m0) : 32;
+        const int nvalid = round_count(batch, w);
         const int64_t m = m0 + lane;
+        const int64_t wn = w + gridDim.x;
+        if (wn * 32 < batch)
+            issue_round_load<N>(Lg, wn * 32, round_count(batch, wn), slot_of[b ^ 1], bar + (b ^ 1),
+                                lane);
         bool active = lane < nvalid;
         if (active && status != nullptr) active = (__ldg(status + m) == 0);
 
-        // L and adj_L in
-        fence_proxy_async_smem();
-        if (lane == 0) mbar_arrive_expect_tx(bar_in, (uint32_t)nvalid * 2u * C::kBytes);
-        __syncwarp();
-        if (lane < nvalid) {
-            bulk_load(const_cast<float*>(lslot), Lg + m * (N * N), C::kBytes, bar_in);
-            bulk_load(bslot, Lbar + m * (N * N), C::kBytes, bar_in);
+        float g[N][N];
+        if (active) {
+            ldg_lower<N>(Lbar + m * (N * N), g);
+        } else {
+#pragma unroll
+            for (int i = 0; i < N; ++i)
+#pragma unroll
+                for (int k = 0; k <= i; ++k) g[i][k] = 0.f;
         }
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_in, phase, kMbarPolls))) {
-            mbar_wait(bar_in, phase, kMbarPolls);
+        if (!__all_sync(0xffffffffu, mbar_wait(bar + b, phase[b], kMbarPolls))) {
+            mbar_wait(bar + b, phase[b], kMbarPolls);
+            mbar_wait(bar + (b ^ 1), phase[b ^ 1], kMbarPolls);
             break;  // the copies did not complete: adj_A of this round is left unchanged
         }
-
-        float g[N][N];
-        slot_load_lower<N>(bslot, g);
-
-        // old adj_A into the adj_L slot while the sweep runs
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_expect_tx(bar_ab, (uint32_t)nvalid * C::kBytes);
-        __syncwarp();
-        if (lane < nvalid) bulk_load(bslot, Abar + m * (N * N), C::kBytes, bar_ab);
+        phase[b] ^= 1u;
+        const float* lslot = slot_of[b];  // inactive lanes sweep zeros
 
         // Reverse sweep.  Column j of g holds the gradient w.r.t. column j of
         // L on entry and w.r.t. column j of A (lower part) on exit.
@@ -238,33 +291,25 @@ tpm_potrf_adj_kernel(const float* __restrict__ Lg, const float* __restrict__ Lba
                 for (int k = 0; k < j; ++k) g[i][k] = fmaf(-g[i][j], lj[k], g[i][k]);
             g[j][j] *= 0.5f;
         }
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_ab, phase, kMbarPolls))) {
-            mbar_wait(bar_ab, phase, kMbarPolls);
-            break;
-        }
-        phase ^= 1u;  // both barriers complete one phase per round
+
         if (active) {
+            float* dst = Abar + m * (N * N);
 #pragma unroll
             for (int i = 0; i < N; ++i) {
 #pragma unroll
                 for (int c = 0; c < N / 4; ++c) {
                     if (4 * c > i) continue;
-                    float4 v = reinterpret_cast<const float4*>(bslot + i * N)[c];
+                    float4* p = reinterpret_cast<float4*>(dst + i * N) + c;
+                    float4 v = *p;
                     v.x += g[i][4 * c + 0];
                     if (4 * c + 1 <= i) v.y += g[i][4 * c + 1];
                     if (4 * c + 2 <= i) v.z += g[i][4 * c + 2];
                     if (4 * c + 3 <= i) v.w += g[i][4 * c + 3];
-                    reinterpret_cast<float4*>(bslot + i * N)[c] = v;
+                    *p = v;
                 }
             }
-            fence_proxy_async_smem();
-            bulk_store(Abar + m * (N * N), bslot, C::kBytes);
-            bulk_commit();
         }
-        bulk_wait_read_all();
-        __syncwarp();
     }
-    bulk_wait_all();
 }
 
 template <typename K>
@@ -283,7 +328,7 @@ int tpm_grid(K kern, size_t smem, int64_t rounds) {
 template <int N>
 cudaError_t tpm_fwd_n(const float* A, float* L, int32_t* status, int64_t batch,
                       cudaStream_t stream) {
-    const size_t smem = kBarBytes + Tpm<N>::kSlotsBytes;
+    const size_t smem = kBarBytes + 2 * Tpm<N>::kSlotsBytes;
     auto kern = tpm_potrf_kernel<N>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
