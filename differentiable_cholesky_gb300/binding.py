@@ -55,6 +55,8 @@ def load_library(path: str | None = None):
         lib.chol_strerror.restype = ctypes.c_char_p
         lib.chol_abi_version.argtypes = []
         lib.chol_abi_version.restype = ctypes.c_int32
+        lib.chol_adj_noalloc.argtypes = [i64, i32, i32, vp, vp, vp, vp, i32, vp]
+        lib.chol_adj_noalloc.restype = ctypes.c_int
         lib.chol_probe_fma_peak.argtypes = [i32, i64, vp, ctypes.POINTER(ctypes.c_double), vp]
         lib.chol_probe_fma_peak.restype = ctypes.c_int
         _lib = lib

@@ -115,6 +115,28 @@ CHOL_API int chol_adj(int64_t batch, int32_t n, int32_t dtype, const void* L, co
 CHOL_API int chol_adj_ex(int64_t batch, int32_t n, int32_t dtype, const void* L, const void* adj_L,
                 void* adj_A, const int32_t* status, int32_t tile, void* stream);
 
+/*
+ * chol_adj_noalloc -- chol_adj_ex for callers that cannot allocate device
+ * memory while they run (inside a CUDA-graph capture that must not grow its
+ * memory pool, hosts that forbid device allocation after start-up, plug-ins
+ * whose host application owns every allocation).  It has no counterpart in the
+ * pages: it exists for those callers only.
+ *   Same arguments, results and error codes as chol_adj_ex, but it calls no
+ *   allocator: for n > 64 the blocked path's workspace is a fixed 16 MiB
+ *   scratch array inside the library (held by every GPU that loads the library
+ *   until the process exits), so batch * n * n * element size must be at most
+ *   16 MiB, else CHOL_ENOMEM and nothing is enqueued.  n <= 64 needs no
+ *   scratch and has no limit.
+ *   The first call on a device looks the scratch array's address up; make it
+ *   before any stream capture begins.  All calls on a device share the array
+ *   and leave their last contents in it (nothing needs clearing: every scratch
+ *   element read is first written by the same call), so calls that overlap on
+ *   the GPU race and corrupt each other: order them on one stream.
+ */
+CHOL_API int chol_adj_noalloc(int64_t batch, int32_t n, int32_t dtype, const void* L,
+                              const void* adj_L, void* adj_A, const int32_t* status,
+                              int32_t tile, void* stream);
+
 /* Static text for a return code (never NULL). */
 CHOL_API const char* chol_strerror(int code);
 
