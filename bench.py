@@ -46,13 +46,18 @@ L2_BYTES = 129 * 1024 * 1024
 # ----------------------------------------------------------------------------
 
 WORKLOADS = {
-    # name: (batch, n, numpy dtype, description)
+    # name: (batch, n, numpy dtype, description, tile)
     "batched_16": (65536, 16, np.float32,
-                   "65536 x 16x16 fp32, A = G G^T/16 + I (G ~ N(0,1), seed 0), adj_L = tril(N(0,1)) (seed 1)"),
+                   "65536 x 16x16 fp32, A = G G^T/16 + I (G ~ N(0,1), seed 0), adj_L = tril(N(0,1)) (seed 1)", 0),
     "batched_64": (8192, 64, np.float32,
-                   "8192 x 64x64 fp32, A = G G^T/64 + 0.5 I, every 100th matrix non-PD (A[k,k] = -1)"),
+                   "8192 x 64x64 fp32, A = G G^T/64 + 0.5 I, every 100th matrix non-PD (A[k,k] = -1)", 0),
+    "bidiagonal_512": (1, 512, np.float64,
+                       "1 x 512x512 fp64, A = E E^T with E lower bidiagonal (diag linspace(1,2), subdiag 0.5), tile 128", 128),
+    "batched_512": (256, 512, np.float64,
+                    "256 x 512x512 fp64, A = G G^T/512 + I, tile 128", 128),
+    "banded_8192": (1, 8192, np.float64,
+                    "1 x 8192x8192 fp64, A = E E^T with E lower banded (bandwidth 32), tile 128", 128),
 }
-
 
 def lower_sector_bytes(n: int, esize: int) -> int:
     """Bytes of the 32-byte DRAM sectors that hold the lower triangle of one
@@ -69,6 +74,22 @@ def algorithmic_bytes(n: int, esize: int):
 
 def nominal_flops(n: int):
     return n ** 3 / 3.0, float(n ** 3)     # forward n^3/3, adjoint ~n^3 (nominal)
+
+
+def executed_flops(n: int):
+    """Flops the kernels execute: forward n^3/3; the blocked adjoint's
+    Phi(L^T tril(adj_L)) and two solves, 7 n^3 / 3."""
+    return n ** 3 / 3.0, 7.0 * n ** 3 / 3.0
+
+
+def launches_per_step(n: int, tile: int) -> int:
+    """Kernels the library launches for one chol_fwd + chol_adj."""
+    if n <= 64:
+        return 2
+    nt = (n + tile - 1) // tile
+    fwd = 1 + nt + 2 * (nt - 1)              # copy, diagonal factors, panel solves + updates
+    adj = 1 + 2 * nt + 2 * (nt - 1) + 1      # P, solves and updates for X and M, accumulate
+    return fwd + adj
 
 
 def read_peaks():
@@ -231,19 +252,28 @@ def make_workload(name):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: 2000 for n <= 64, else 3)")
+    ap.add_argument("--warmup", type=int, default=None,
+                    help="warm-up steps (default: 20 for n <= 64, else 3)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="batched_16")
-    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--e2e-steps", type=int, default=None,
+                    help="end-to-end steps (default: 20 for n <= 64, else 1)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    batch, n, np_dtype, desc, tile = WORKLOADS[args.workload]
+    if args.steps is None:
+        args.steps = 2000 if n <= 64 else 3
+    if args.warmup is None:
+        args.warmup = 20 if n <= 64 else 3
+    if args.e2e_steps is None:
+        args.e2e_steps = 20 if n <= 64 else 1
     args.warmup = max(args.warmup, 3)
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    batch, n, np_dtype, desc = WORKLOADS[args.workload]
 
     if args.impl == "reference":
         if rank != 0:
@@ -281,10 +311,10 @@ def main():
         A, Lb, L, G, st = sets[k & 1]
         if ev is not None:
             ev[0].record(stream)
-        binding.chol_fwd(A, L=L, status=st)
+        binding.chol_fwd(A, L=L, status=st, tile=tile)
         if ev is not None:
             ev[1].record(stream)
-        binding.chol_adj(L, Lb, adj_A=G, status=st)
+        binding.chol_adj(L, Lb, adj_A=G, status=st, tile=tile)
         if ev is not None:
             ev[2].record(stream)
 
@@ -330,13 +360,13 @@ def main():
         dA.copy_(hA, non_blocking=True)
         dLb.copy_(hLb, non_blocking=True)
         dG.zero_()
-        binding.chol_fwd(dA, L=dL, status=dst)
-        binding.chol_adj(dL, dLb, adj_A=dG, status=dst)
+        binding.chol_fwd(dA, L=dL, status=dst, tile=tile)
+        binding.chol_adj(dL, dLb, adj_A=dG, status=dst, tile=tile)
         hL.copy_(dL, non_blocking=True)
         hst.copy_(dst, non_blocking=True)
         hG.copy_(dG, non_blocking=True)
 
-    for _ in range(3):
+    for _ in range(3 if n <= 64 else 1):
         e2e_step()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -365,29 +395,49 @@ def main():
     e2e_value = args.e2e_steps * batch * world / (e2e_ms / 1e3)
     fwd_b, adj_b = algorithmic_bytes(n, esize)
     fwd_f, adj_f = nominal_flops(n)
-    peak, peak_src = read_peaks()
+    hbm_peak, peak_src = read_peaks()
     fwd_gbs = fwd_b * batch / (fwd_ms / 1e3) / 1e9
     adj_gbs = adj_b * batch / (adj_ms / 1e3) / 1e9
     dominant = "adj" if adj_ms >= fwd_ms else "fwd"
-    achieved = adj_gbs if dominant == "adj" else fwd_gbs
+    kernels = {
+        "fwd": {"ms": fwd_ms, "algorithmic_GBps": fwd_gbs, "bytes_per_matrix": fwd_b},
+        "adj": {"ms": adj_ms, "algorithmic_GBps": adj_gbs, "bytes_per_matrix": adj_b},
+    }
+    if n <= 64:
+        achieved = adj_gbs if dominant == "adj" else fwd_gbs
+        roofline = {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": hbm_peak,
+                    "unit": "GB/s", "frac": achieved / hbm_peak,
+                    "peak_source": f"{peak_src} HBM copy bandwidth", "traffic": None}
+    else:
+        # FP64 FMA-pipe bound: executed flops per call against the FMA peak
+        # measured by the library's probe on this GPU.
+        ex_f, ex_a = executed_flops(n)
+        fp64_peak = binding.probe_fma_peak(tdtype, iters=1 << 15) / 1e12
+        tf_f = ex_f * batch / (fwd_ms / 1e3) / 1e12
+        tf_a = ex_a * batch / (adj_ms / 1e3) / 1e12
+        kernels["fwd"]["executed_TFLOPs"] = tf_f
+        kernels["adj"]["executed_TFLOPs"] = tf_a
+        achieved = tf_a if dominant == "adj" else tf_f
+        roofline = {"bound": "fp64" if np_dtype == np.float64 else "fp32", "kernel": dominant,
+                    "achieved": achieved, "peak": fp64_peak, "unit": "TFLOP/s",
+                    "frac": achieved / fp64_peak,
+                    "peak_source": "measured by chol_probe_fma_peak (independent FMA chains on every SM)",
+                    "traffic": None}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32" if np_dtype == np.float32 else "f64", "data": "synthetic",
         "config": {"workload": f"{args.workload}: {desc}", "batch_per_gpu": batch, "n": n,
+                   "tile": tile if n > 64 else None,
                    "parallelism": f"independent batches per GPU x{world}" if world > 1 else "1 GPU",
-                   "l2": "inputs larger than L2 (256 MiB of distinct buffers per step, two sets alternated)"},
+                   "l2": "inputs larger than L2 (256 MiB of distinct buffers per step, two sets alternated)"
+                   if batch * n * n * esize * 4 > L2_BYTES else
+                   "working set below L2 size: steps run back to back on two buffer sets"},
         "gflops": value * (fwd_f + adj_f) / 1e9,
-        "kernels": {
-            "fwd": {"ms": fwd_ms, "algorithmic_GBps": fwd_gbs, "bytes_per_matrix": fwd_b},
-            "adj": {"ms": adj_ms, "algorithmic_GBps": adj_gbs, "bytes_per_matrix": adj_b},
-        },
-        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": peak,
-                     "unit": "GB/s", "frac": achieved / peak,
-                     "peak_source": f"{peak_src} HBM copy bandwidth",
-                     "traffic": None},
-        "gpu_launches": 2 * args.steps,
+        "kernels": kernels,
+        "roofline": roofline,
+        "gpu_launches": launches_per_step(n, tile if n > 64 else 0) * args.steps,
         "e2e": {"value": e2e_value, "unit": UNIT,
                 "h2d_bytes_per_step": int(hA.numel() * esize + hLb.numel() * esize),
                 "d2h_bytes_per_step": int(hL.numel() * esize + hG.numel() * esize + hst.numel() * 4),

@@ -89,10 +89,6 @@ int adj_impl(int64_t batch, int32_t n, const void* L, const void* Lbar, void* Ab
     T* ab = static_cast<T*>(Abar);
     if (n <= kSmallMax) {
         const bool vec = vec_ok(n, sizeof(T), {L, Lbar, Abar});
-        if constexpr (sizeof(T) == 4) {
-            if (vec && chol::tpm_supported(n))
-                return to_code(chol::tpm_adj(l, lb, ab, status, batch, n, stream));
-        }
         return to_code(chol::small_adj<T>(l, lb, ab, status, batch, n, vec, stream));
     }
     if (tile == 0) tile = chol::blocked_default_tile(n, (int)sizeof(T));

@@ -4,9 +4,22 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "chol.h"
 
 namespace chol {
+
+// Compile-time loop: f(std::integral_constant<int, I>) for I in [B, E).  Used
+// where every index must be a constant so that arrays stay in registers,
+// whatever the unroller decides about large loop nests.
+template <int B, int E, typename F>
+__device__ __forceinline__ void static_for(F&& f) {
+    if constexpr (B < E) {
+        f(std::integral_constant<int, B>{});
+        static_for<B + 1, E>(f);
+    }
+}
 
 // 16-byte vector of the element type: the unit of every vectorised global or
 // shared-memory access in these kernels.

@@ -18,13 +18,10 @@ template <typename T>
 cudaError_t small_adj(const T* L, const T* Lbar, T* Abar, const int32_t* status, int64_t batch,
                       int n, bool vec, cudaStream_t stream);
 
-// Thread-per-matrix float32 kernels for n in {8, 16}; every pointer 16-byte
-// aligned.
+// Thread-per-matrix float32 forward for n in {8, 16}; A and L 16-byte aligned.
 bool tpm_supported(int n);
 cudaError_t tpm_fwd(const float* A, float* L, int32_t* status, int64_t batch, int n,
                     cudaStream_t stream);
-cudaError_t tpm_adj(const float* L, const float* Lbar, float* Abar, const int32_t* status,
-                    int64_t batch, int n, cudaStream_t stream);
 
 // n > 64, blocked with square tiles of `tile` (32, 64 or 128).
 template <typename T>

@@ -88,11 +88,7 @@ int run(int64_t batch, int32_t n, const void* L, const void* Lbar, void* Abar,
     if (n <= 64) {
         const bool vec = (n * (int)sizeof(T)) % 16 == 0 && aligned16(L) && aligned16(Lbar) &&
                          aligned16(Abar);
-        if (sizeof(T) == 4 && vec && chol::tpm_supported(n))
-            e = chol::tpm_adj(reinterpret_cast<const float*>(l), reinterpret_cast<const float*>(lb),
-                              reinterpret_cast<float*>(ab), status, batch, n, stream);
-        else
-            e = chol::small_adj<T>(l, lb, ab, status, batch, n, vec, stream);
+        e = chol::small_adj<T>(l, lb, ab, status, batch, n, vec, stream);
         return e == cudaSuccess ? CHOL_OK : CHOL_ECUDA;
     }
     const unsigned __int128 need =

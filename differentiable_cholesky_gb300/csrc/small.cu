@@ -1,39 +1,40 @@
 // Batched Cholesky forward and adjoint for small matrices (n <= 64).
 //
-// One group of NT threads (NT = 8, 16, 32 or 64, the next size >= n) owns one
-// matrix; a 128-thread block holds 128 / NT groups.  A matrix of order n < NT
-// is padded to blockdiag(A, I), whose factor is blockdiag(L, I) and whose
-// adjoint (with a zero-padded adj_L) is blockdiag(adj_A, 0): the padding
-// changes no result.  Every loop over matrix indices is fully unrolled, so each
-// thread keeps its row (or column) of the matrix in registers.
+// A group of LPG lanes owns one matrix of padded order NT = 8, 16, 32 or 64
+// (the next size >= n); each lane owns two rows (or columns) of it, t and
+// NT-1-t, where registers allow (LPG = NT / 2), else one.  A 128-thread block
+// holds 128 / LPG groups.  A matrix of order n < NT is padded to
+// blockdiag(A, I), whose factor is blockdiag(L, I) and whose adjoint (with a
+// zero-padded adj_L) is blockdiag(adj_A, 0): the padding changes no result.
+// Every loop over matrix indices is fully unrolled, so each lane keeps its
+// rows (or columns) in registers.
 //
 // Forward (jaxmg docs "Cholesky factorization": lower factor and status;
 // NVIDIA/warp issue #1316: out-of-place tile factor, one block per tile).
-//   Thread i holds row i.  Right-looking column recurrence, one group barrier
-//   per column: at step j every thread publishes its current a_ij to a
-//   double-buffered shared column, then reads the pivot d = a_jj, computes
-//   r = 1/sqrt(d) itself (no second broadcast), sets l_ij = a_ij * r and
-//   updates its trailing entries a_ik -= (l_ij r) a_kj.  A pivot that is not
-//   > 0 records status j + 1 (first failure only) and is replaced by 1 so the
-//   rest of the (unspecified) factor stays finite and the group stays
-//   convergent.
+//   Right-looking column recurrence, one group barrier per column: at step j
+//   every lane publishes its current a_ij to a double-buffered shared column,
+//   then reads the pivot d = a_jj, computes r = 1/sqrt(d) itself (no second
+//   broadcast), sets l_ij = a_ij * r and updates its trailing entries
+//   a_ik -= (l_ij r) a_kj.  A pivot that is not > 0 records status j + 1
+//   (first failure only) and is replaced by 1 so the rest of the (unspecified)
+//   factor stays finite and the group stays convergent.
 //
 // Adjoint (Murray 2016 as NVIDIA/warp issue #1316's closing comment states it:
 // S = Phi(L^T adj_L), then solves against L^T and L, accumulated into the lower
 // triangle of adj_A).  L is staged in shared memory and read by broadcast.
-//   1. thread t takes column t of tril(adj_L) and forms column t of
-//      P = L^T tril(adj_L) in place (outer-product order over the rows of L);
-//   2. S = Phi(P) on that column;
-//   3. X = L^-T S: back substitution on the column (rows of L broadcast);
-//   4. transpose through shared memory: thread t takes row t of X;
-//   5. M = X L^-1: back substitution on the row (rows of L broadcast);
-//   6. transpose once more and add M_tk + M_kt (k < t) and M_tt into row t of
-//      adj_A's lower triangle.  Matrices with status != 0 are skipped.
+//   1. each lane takes its columns of tril(adj_L) and forms the same columns
+//      of P = L^T tril(adj_L) in place (outer-product order over rows of L);
+//   2. S = Phi(P) on those columns;
+//   3. X = L^-T S: back substitution on the columns (rows of L broadcast);
+//   4. transpose through shared memory: the lane takes the same rows of X;
+//   5. M = X L^-1: back substitution on the rows (rows of L broadcast);
+//   6. transpose once more and add M_tk + M_kt (k < t) and M_tt into the
+//      lane's rows of adj_A's lower triangle.  Matrices with status != 0 are
+//      skipped.
 
 #include <cuda_runtime.h>
 
 #include <algorithm>
-#include <type_traits>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -42,16 +43,6 @@ namespace chol {
 namespace {
 
 constexpr int kBlock = 128;
-
-template <int NT>
-__device__ __forceinline__ void group_sync(int group) {
-    if constexpr (NT <= 32) {
-        __syncwarp();
-    } else {
-        // Named barrier per 64-thread group (id 0 is __syncthreads).
-        asm volatile("bar.sync %0, %1;" ::"r"(1 + group), "r"(NT) : "memory");
-    }
-}
 
 // Load the lower part of row `row` (row < n) into r[0..NT): zeros above the
 // diagonal.  Only the 16-byte chunks that hold lower-triangle elements are read.
@@ -104,108 +95,123 @@ __device__ __forceinline__ void fetch_fwd_row(const T* __restrict__ A, int64_t b
     }
 }
 
-// Persistent kernel: block c handles groups of G matrices c, c + gridDim.x, ...
-// and fetches the next group's rows while it factors the current one.
-template <typename T, int NT, bool VEC>
+// Lanes per matrix LPG = NT / RPL: each lane owns RPL rows, t and NT-1-t for
+// RPL = 2 (balanced triangle rows).  Every broadcast read of the published
+// column then feeds RPL rows.
+__host__ __device__ constexpr int owned_index(int t, int q, int lpg) {
+    return (q & 1) ? (q + 1) * lpg - 1 - t : q * lpg + t;
+}
+
+template <int LPG>
+__device__ __forceinline__ void lanes_sync(int group) {
+    if constexpr (LPG <= 32) {
+        __syncwarp();
+    } else {
+        // Named barrier per group of LPG (a multiple of 32) threads; id 0 is
+        // __syncthreads.
+        asm volatile("bar.sync %0, %1;" ::"r"(1 + group), "r"(LPG) : "memory");
+    }
+}
+
+template <typename T, int NT, int RPL, bool VEC>
 __global__ void __launch_bounds__(kBlock)
 small_potrf_kernel(const T* __restrict__ A, T* __restrict__ L, int32_t* __restrict__ status,
                    int64_t batch, int n) {
-    constexpr int G = kBlock / NT;
-    constexpr int CS = group_stride<T, NT>(2 * NT);
+    constexpr int LPG = NT / RPL;
+    constexpr int G = kBlock / LPG;
+    constexpr int CS = group_stride<T, LPG>(2 * NT);
     __shared__ __align__(16) T colbuf[G * CS];
     using V = typename Vec16<T>::type;
     constexpr int W = Vec16<T>::N;
 
-    const int g = threadIdx.x / NT;
-    const int i = threadIdx.x % NT;
-    const int64_t ntasks = (batch + G - 1) / G;
-    int64_t task = blockIdx.x;
-    if (task >= ntasks) return;  // uniform for the whole block
-
-    // the next group's row is held in registers while the current one is
-    // factored, when that costs few registers
-    constexpr bool kPrefetch = NT * sizeof(T) <= 64;
-    T nxt[kPrefetch ? NT : 1];
-    if constexpr (kPrefetch) fetch_fwd_row<T, NT, VEC>(A, task * G + g, batch, i, n, nxt);
-
-#pragma unroll 1
-    for (; task < ntasks; task = kPrefetch ? task + gridDim.x : ntasks) {
-        const int64_t b = task * G + g;
-        T a[NT];
-        if constexpr (kPrefetch) {
+    const int g = threadIdx.x / LPG;
+    const int t = threadIdx.x % LPG;
+    const int64_t b = (int64_t)blockIdx.x * G + g;
+    int rows[RPL];
 #pragma unroll
-            for (int k = 0; k < NT; ++k) a[k] = nxt[k];
-            if (task + gridDim.x < ntasks)
-                fetch_fwd_row<T, NT, VEC>(A, (task + gridDim.x) * G + g, batch, i, n, nxt);
-        } else {
-            fetch_fwd_row<T, NT, VEC>(A, b, batch, i, n, a);
+    for (int q = 0; q < RPL; ++q) rows[q] = owned_index(t, q, LPG);
+
+    T a[RPL][NT];
+#pragma unroll
+    for (int q = 0; q < RPL; ++q) fetch_fwd_row<T, NT, VEC>(A, b, batch, rows[q], n, a[q]);
+
+    int st = 0;
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+        T* buf = colbuf + g * CS + (j & 1) * NT;
+#pragma unroll
+        for (int q = 0; q < RPL; ++q) buf[rows[q]] = a[q][j];
+        lanes_sync<LPG>(g);
+        T d = buf[j];
+        if (!(d > T(0))) {
+            if (st == 0) st = j + 1;
+            d = T(1);
         }
-
-        int st = 0;
+        const T r = rsqrt_t(d);
+        T coef[RPL];
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-            T* buf = colbuf + g * CS + (j & 1) * NT;
-            buf[i] = a[j];
-            group_sync<NT>(g);
-            T d = buf[j];
-            if (!(d > T(0))) {
-                if (st == 0) st = j + 1;
-                d = T(1);
+        for (int q = 0; q < RPL; ++q) {
+            const T lij = a[q][j] * r;
+            coef[q] = (rows[q] > j) ? lij * r : T(0);
+            a[q][j] = lij;
+        }
+        // trailing update with the published column, read as aligned vectors
+        // (constant trip counts: inner loops unroll first)
+#pragma unroll
+        for (int c = 0; c < NT / W; ++c) {
+            if (c < (j + 1) / W) continue;
+            const V v = reinterpret_cast<const V*>(buf)[c];
+#pragma unroll
+            for (int e = 0; e < W; ++e) {
+                const int k = c * W + e;
+#pragma unroll
+                for (int q = 0; q < RPL; ++q)
+                    if (k > j) a[q][k] = fma(-coef[q], vget<T>(v, e), a[q][k]);
             }
-            const T r = rsqrt_t(d);
-            const T lij = a[j] * r;
-            const T coef = (i > j) ? lij * r : T(0);
-            a[j] = lij;
-            // trailing update with the published column, read as aligned
-            // vectors (constant trip counts: inner loops unroll first)
+        }
+    }
+
+    if (b >= batch) return;
+#pragma unroll
+    for (int q = 0; q < RPL; ++q) {
+        const int i = rows[q];
+        if (i >= n) continue;
+        T* rowp = L + (size_t)b * n * n + (size_t)i * n;
+        if constexpr (VEC) {
+            V* vp = reinterpret_cast<V*>(rowp);
 #pragma unroll
             for (int c = 0; c < NT / W; ++c) {
-                if (c < (j + 1) / W) continue;
-                const V v = reinterpret_cast<const V*>(buf)[c];
+                if (c * W < n) {
+                    V v;
 #pragma unroll
-                for (int e = 0; e < W; ++e) {
-                    const int k = c * W + e;
-                    if (k > j) a[k] = fma(-coef, vget<T>(v, e), a[k]);
+                    for (int e = 0; e < W; ++e)
+                        vset<T>(v, e, (c * W + e <= i) ? a[q][c * W + e] : T(0));
+                    vp[c] = v;
                 }
             }
+        } else {
+#pragma unroll
+            for (int k = 0; k < NT; ++k)
+                if (k < n) rowp[k] = (k <= i) ? a[q][k] : T(0);
         }
-
-        if (b < batch && i < n) {
-            T* rowp = L + (size_t)b * n * n + (size_t)i * n;
-            if constexpr (VEC) {
-                V* vp = reinterpret_cast<V*>(rowp);
-#pragma unroll
-                for (int c = 0; c < NT / W; ++c) {
-                    if (c * W < n) {
-                        V v;
-#pragma unroll
-                        for (int e = 0; e < W; ++e)
-                            vset<T>(v, e, (c * W + e <= i) ? a[c * W + e] : T(0));
-                        vp[c] = v;
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int k = 0; k < NT; ++k)
-                    if (k < n) rowp[k] = (k <= i) ? a[k] : T(0);
-            }
-        }
-        if (b < batch && i == 0) status[b] = st;
     }
+    if (t == 0) status[b] = st;
 }
 
-template <typename T, int NT>
-struct AdjSmem {
-    static constexpr int G = kBlock / NT;
-    static constexpr int LP = NT + 16 / (int)sizeof(T);  // L row pitch: 16-byte skew per row
-    static constexpr int RP = NT + 1;                     // transpose pitch
-    static constexpr int per_group =
-        group_stride<T, NT>(NT * LP + NT * RP + ((NT + 3) / 4) * 4);
+// Adjoint layout: a group of LPG = NT / CPL lanes per matrix, each lane owning
+// CPL columns (and, after the transpose, CPL rows): columns t and NT-1-t for
+// CPL = 2, which balances the triangular work.  Every broadcast read of a row
+// of L then feeds CPL columns.
+template <typename T, int NT, int CPL>
+struct AdjCfg {
+    static constexpr int LPG = NT / CPL;                   // lanes per matrix
+    static constexpr int G = kBlock / LPG;                 // matrices per block
+    static constexpr int LP = NT + 16 / (int)sizeof(T);    // L row pitch: 16-byte skew per row
+    static constexpr int RP = NT + 1;                      // transpose pitch
+    static constexpr int per_group = group_stride<T, LPG>(NT * LP + NT * RP + ((NT + 3) / 4) * 4);
     static constexpr size_t bytes = (size_t)G * per_group * sizeof(T);
-    // rows of L, adj_L and adj_A for the next group are held in registers
-    // while the current group is processed, when that costs few registers
-    static constexpr bool prefetch = NT * sizeof(T) <= 64;
 };
+
 
 // Whether matrix b takes part in the adjoint (in the batch, status == 0).
 __device__ __forceinline__ bool adj_active(const int32_t* __restrict__ status, int64_t b,
@@ -216,7 +222,7 @@ __device__ __forceinline__ bool adj_active(const int32_t* __restrict__ status, i
 }
 
 // Row `row` of one of the adjoint's inputs, or its padding: identity rows of
-// L, zero rows of adj_L / adj_A.
+// L, zero rows of adj_L.
 template <typename T, int NT, bool VEC>
 __device__ __forceinline__ void fetch_adj_row(const T* __restrict__ src, bool active, int64_t b,
                                               int row, int n, T pad_diag, T (&r)[NT]) {
@@ -228,255 +234,224 @@ __device__ __forceinline__ void fetch_adj_row(const T* __restrict__ src, bool ac
     }
 }
 
-// The three rows of the next matrix, held in registers while the current
-// matrix is processed (used when rows are short).
-template <typename T, int NT, bool VEC>
-struct AdjRows {
-    T l[NT], lb[NT], ab[NT];
-    bool active;
-
-    __device__ __forceinline__ void fetch(const T* __restrict__ Lg, const T* __restrict__ Lbar,
-                                          const T* __restrict__ Abar,
-                                          const int32_t* __restrict__ status, int64_t b,
-                                          int64_t batch, int row, int n) {
-        active = adj_active(status, b, batch);
-        fetch_adj_row<T, NT, VEC>(Lg, active, b, row, n, T(1), l);
-        fetch_adj_row<T, NT, VEC>(Lbar, active, b, row, n, T(0), lb);
-        fetch_adj_row<T, NT, VEC>(Abar, active, b, row, n, T(0), ab);
-    }
-};
-
-template <typename T, int NT, bool VEC>
+template <typename T, int NT, int CPL, bool VEC>
 __global__ void __launch_bounds__(kBlock)
 small_potrf_adj_kernel(const T* __restrict__ Lg, const T* __restrict__ Lbar,
                        T* __restrict__ Abar, const int32_t* __restrict__ status,
                        int64_t batch, int n) {
-    using S = AdjSmem<T, NT>;
+    using S = AdjCfg<T, NT, CPL>;
     using V = typename Vec16<T>::type;
     constexpr int W = Vec16<T>::N;
     constexpr int LP = S::LP;
     constexpr int RP = S::RP;
-    constexpr int G = S::G;
+    constexpr int LPG = S::LPG;
     extern __shared__ __align__(16) unsigned char smem_raw[];
 
-    const int g = threadIdx.x / NT;
-    const int t = threadIdx.x % NT;
-    const int64_t ntasks = (batch + G - 1) / G;
-    int64_t task = blockIdx.x;
-    if (task >= ntasks) return;  // uniform for the whole block
+    const int g = threadIdx.x / LPG;
+    const int t = threadIdx.x % LPG;
+    const int64_t b = (int64_t)blockIdx.x * S::G + g;
+    const bool active = adj_active(status, b, batch);
 
     T* Ls = reinterpret_cast<T*>(smem_raw) + (size_t)g * S::per_group;
     T* R = Ls + (size_t)NT * LP;
     T* rinv = R + (size_t)NT * RP;
+    int col[CPL];
+#pragma unroll
+    for (int q = 0; q < CPL; ++q) col[q] = owned_index(t, q, LPG);
 
-    struct Empty {};
-    using Pf = typename std::conditional<S::prefetch, AdjRows<T, NT, VEC>, Empty>::type;
-    Pf pf;
-    if constexpr (S::prefetch) pf.fetch(Lg, Lbar, Abar, status, task * G + g, batch, t, n);
-
-#pragma unroll 1
-    for (; task < ntasks; task = S::prefetch ? task + gridDim.x : ntasks) {
-        const int64_t b = task * G + g;
-        T c[NT];
-        T ab[S::prefetch ? NT : 1];
-        bool active;
-        group_sync<NT>(g);  // the previous matrix's readers are done with Ls, R, rinv
-        if constexpr (S::prefetch) {
-            const AdjRows<T, NT, VEC> cur = pf;
-            if (task + gridDim.x < ntasks)
-                pf.fetch(Lg, Lbar, Abar, status, (task + gridDim.x) * G + g, batch, t, n);
-            active = cur.active;
+    // Rows col[q] of L into shared memory (identity rows for padding or
+    // skipped matrices) and rows col[q] of tril(adj_L) into the transpose buffer.
 #pragma unroll
-            for (int q = 0; q < NT / W; ++q) {
-                V v;
+    for (int q = 0; q < CPL; ++q) {
+        T r[NT];
+        fetch_adj_row<T, NT, VEC>(Lg, active, b, col[q], n, T(1), r);
 #pragma unroll
-                for (int e = 0; e < W; ++e) vset<T>(v, e, cur.l[q * W + e]);
-                reinterpret_cast<V*>(Ls + (size_t)t * LP)[q] = v;
-            }
+        for (int u = 0; u < NT / W; ++u) {
+            V v;
 #pragma unroll
-            for (int k = 0; k < NT; ++k) R[t * RP + k] = cur.lb[k];
-#pragma unroll
-            for (int k = 0; k < NT; ++k) ab[k] = cur.ab[k];
-        } else {
-            active = adj_active(status, b, batch);
-            // Row t of L into shared memory (identity rows for padding / skipped).
-            fetch_adj_row<T, NT, VEC>(Lg, active, b, t, n, T(1), c);
-#pragma unroll
-            for (int q = 0; q < NT / W; ++q) {
-                V v;
-#pragma unroll
-                for (int e = 0; e < W; ++e) vset<T>(v, e, c[q * W + e]);
-                reinterpret_cast<V*>(Ls + (size_t)t * LP)[q] = v;
-            }
-            // Row t of tril(adj_L) into the transpose buffer.
-            fetch_adj_row<T, NT, VEC>(Lbar, active, b, t, n, T(0), c);
-#pragma unroll
-            for (int k = 0; k < NT; ++k) R[t * RP + k] = c[k];
+            for (int e = 0; e < W; ++e) vset<T>(v, e, r[u * W + e]);
+            reinterpret_cast<V*>(Ls + (size_t)col[q] * LP)[u] = v;
         }
-        group_sync<NT>(g);
-        rinv[t] = rcp_t(Ls[t * LP + t]);
-        // Column t of tril(adj_L).
+        fetch_adj_row<T, NT, VEC>(Lbar, active, b, col[q], n, T(0), r);
 #pragma unroll
-        for (int k = 0; k < NT; ++k) c[k] = R[k * RP + t];
+        for (int k = 0; k < NT; ++k) R[col[q] * RP + k] = r[k];
+    }
+    lanes_sync<LPG>(g);
+#pragma unroll
+    for (int q = 0; q < CPL; ++q) rinv[col[q]] = rcp_t(Ls[col[q] * LP + col[q]]);
 
-        // 1. column t of P = L^T tril(adj_L), in place: slot k is finished
-        //    once row k of L has been applied, so it can take p_k's first term.
+    // Columns col[q] of tril(adj_L).
+    T c[CPL][NT];
 #pragma unroll
-        for (int k = 0; k < NT; ++k) {
-            const T ck = c[k];
-            const T* lrow = Ls + k * LP;
+    for (int q = 0; q < CPL; ++q)
 #pragma unroll
-            for (int q = 0; q < NT / W; ++q) {
-                if (q > k / W) continue;
-                const V v = reinterpret_cast<const V*>(lrow)[q];
+        for (int k = 0; k < NT; ++k) c[q][k] = R[k * RP + col[q]];
+
+    // 1. columns of P = L^T tril(adj_L), in place: slot k is finished once
+    //    row k of L has been applied, so it can take p_k's first term.
+    static_for<0, NT>([&](auto kc) {
+        constexpr int k = decltype(kc)::value;
+        T ck[CPL];
 #pragma unroll
-                for (int e = 0; e < W; ++e) {
-                    const int i = q * W + e;
-                    if (i < k) c[i] = fma(vget<T>(v, e), ck, c[i]);
-                    else if (i == k) c[i] = vget<T>(v, e) * ck;
+        for (int q = 0; q < CPL; ++q) ck[q] = c[q][k];
+        const T* lrow = Ls + k * LP;
+        static_for<0, k / W + 1>([&](auto uc) {
+            constexpr int u = decltype(uc)::value;
+            const V v = reinterpret_cast<const V*>(lrow)[u];
+            static_for<0, W>([&](auto ec) {
+                constexpr int i = u * W + decltype(ec)::value;
+#pragma unroll
+                for (int q = 0; q < CPL; ++q) {
+                    if constexpr (i < k) c[q][i] = fma(vget<T>(v, i - u * W), ck[q], c[q][i]);
+                    else if constexpr (i == k) c[q][i] = vget<T>(v, i - u * W) * ck[q];
                 }
-            }
-        }
-        // 2. S = Phi(P): keep rows below t, halve row t, clear rows above.
+            });
+        });
+    });
+    // 2. S = Phi(P): keep rows below the column, halve the diagonal, clear above.
+    // (a factor rather than a select: a select chain on a lane-dependent index
+    //  is turned into an indexed store, which moves c out of registers)
 #pragma unroll
-        for (int i = 0; i < NT; ++i) c[i] = (i > t) ? c[i] : ((i == t) ? c[i] * T(0.5) : T(0));
-        group_sync<NT>(g);  // rinv visible to the group
+    for (int q = 0; q < CPL; ++q)
+#pragma unroll
+        for (int i = 0; i < NT; ++i) c[q][i] *= T(0.5) * (T(i > col[q]) + T(i >= col[q]));
+    lanes_sync<LPG>(g);  // rinv visible to the group
 
-        // 3. X = L^-T S (back substitution, rows of L broadcast).
+    // 3. X = L^-T S (back substitution, rows of L broadcast).
+    static_for<0, NT>([&](auto ic) {
+        constexpr int i = NT - 1 - decltype(ic)::value;
+        const T ri = rinv[i];
+        T xi[CPL];
 #pragma unroll
-        for (int i = NT - 1; i >= 0; --i) {
-            const T xi = c[i] * rinv[i];
-            c[i] = xi;
-            const T* lrow = Ls + i * LP;
+        for (int q = 0; q < CPL; ++q) {
+            xi[q] = c[q][i] * ri;
+            c[q][i] = xi[q];
+        }
+        const T* lrow = Ls + i * LP;
+        static_for<0, (i + W - 1) / W>([&](auto uc) {
+            constexpr int u = decltype(uc)::value;
+            const V v = reinterpret_cast<const V*>(lrow)[u];
+            static_for<0, W>([&](auto ec) {
+                constexpr int k = u * W + decltype(ec)::value;
+                if constexpr (k < i) {
 #pragma unroll
-            for (int q = 0; q < NT / W; ++q) {
-                if (q * W >= i) continue;
-                const V v = reinterpret_cast<const V*>(lrow)[q];
-#pragma unroll
-                for (int e = 0; e < W; ++e) {
-                    const int k = q * W + e;
-                    if (k < i) c[k] = fma(-vget<T>(v, e), xi, c[k]);
+                    for (int q = 0; q < CPL; ++q)
+                        c[q][k] = fma(-vget<T>(v, k - u * W), xi[q], c[q][k]);
                 }
-            }
-        }
-        // 4. transpose: thread t writes column t of X and reads row t.
+            });
+        });
+    });
+    // 4. transpose: columns col[q] of X out, rows col[q] in.
 #pragma unroll
-        for (int i = 0; i < NT; ++i) R[i * RP + t] = c[i];
-        group_sync<NT>(g);
+    for (int q = 0; q < CPL; ++q)
 #pragma unroll
-        for (int k = 0; k < NT; ++k) c[k] = R[t * RP + k];
+        for (int i = 0; i < NT; ++i) R[i * RP + col[q]] = c[q][i];
+    lanes_sync<LPG>(g);
+#pragma unroll
+    for (int q = 0; q < CPL; ++q)
+#pragma unroll
+        for (int k = 0; k < NT; ++k) c[q][k] = R[col[q] * RP + k];
 
-        // 5. M = X L^-1 (back substitution on row t).
+    // 5. M = X L^-1 (back substitution on the rows).
+    static_for<0, NT>([&](auto jc) {
+        constexpr int j = NT - 1 - decltype(jc)::value;
+        const T rj = rinv[j];
+        T mj[CPL];
 #pragma unroll
-        for (int j = NT - 1; j >= 0; --j) {
-            const T mj = c[j] * rinv[j];
-            c[j] = mj;
-            const T* lrow = Ls + j * LP;
+        for (int q = 0; q < CPL; ++q) {
+            mj[q] = c[q][j] * rj;
+            c[q][j] = mj[q];
+        }
+        const T* lrow = Ls + j * LP;
+        static_for<0, (j + W - 1) / W>([&](auto uc) {
+            constexpr int u = decltype(uc)::value;
+            const V v = reinterpret_cast<const V*>(lrow)[u];
+            static_for<0, W>([&](auto ec) {
+                constexpr int k = u * W + decltype(ec)::value;
+                if constexpr (k < j) {
 #pragma unroll
-            for (int q = 0; q < NT / W; ++q) {
-                if (q * W >= j) continue;
-                const V v = reinterpret_cast<const V*>(lrow)[q];
-#pragma unroll
-                for (int e = 0; e < W; ++e) {
-                    const int k = q * W + e;
-                    if (k < j) c[k] = fma(-vget<T>(v, e), mj, c[k]);
+                    for (int q = 0; q < CPL; ++q)
+                        c[q][k] = fma(-vget<T>(v, k - u * W), mj[q], c[q][k]);
                 }
-            }
-        }
-        // 6. Phi(M + M^T) into row t of adj_A's lower triangle.  Thread t only
-        //    rewrites row t, which only it has read.
+            });
+        });
+    });
+    // 6. Phi(M + M^T) into rows col[q] of adj_A's lower triangle.  Each lane
+    //    only rewrites the rows it has read.
 #pragma unroll
-        for (int k = 0; k < NT; ++k) R[t * RP + k] = c[k];
-        group_sync<NT>(g);
+    for (int q = 0; q < CPL; ++q)
 #pragma unroll
-        for (int k = 0; k < NT; ++k) c[k] += (k < t) ? R[k * RP + t] : T(0);
+        for (int k = 0; k < NT; ++k) R[col[q] * RP + k] = c[q][k];
+    lanes_sync<LPG>(g);
+#pragma unroll
+    for (int q = 0; q < CPL; ++q)
+#pragma unroll
+        for (int k = 0; k < NT; ++k) c[q][k] += T(k < col[q]) * R[k * RP + col[q]];
 
-        if (active && t < n) {
-            T* rowp = Abar + (size_t)b * n * n + (size_t)t * n;
-            if constexpr (!S::prefetch) {
-                // add the old values in place (no row held across the solve)
-                T old[NT];
-                load_lower_row<T, NT, VEC>(rowp, t, n, old);
+    if (!active) return;
+    static_for<0, CPL>([&](auto qc) {
+        constexpr int q = decltype(qc)::value;
+        const int row = col[q];
+        if (row >= n) return;
+        T* rowp = Abar + (size_t)b * n * n + (size_t)row * n;
+        T old[NT];
+        load_lower_row<T, NT, VEC>(rowp, row, n, old);
+        if constexpr (VEC) {
+            V* vp = reinterpret_cast<V*>(rowp);
+            static_for<0, NT / W>([&](auto uc) {
+                constexpr int u = decltype(uc)::value;
+                if (u * W + W - 1 <= row) {
+                    V v;
 #pragma unroll
-                for (int k = 0; k < NT; ++k) c[k] += old[k];
-            } else {
+                    for (int e = 0; e < W; ++e) vset<T>(v, e, old[u * W + e] + c[q][u * W + e]);
+                    vp[u] = v;
+                } else if (u * W <= row) {
+                    // chunk straddling the diagonal: write only k <= row
 #pragma unroll
-                for (int k = 0; k < NT; ++k) c[k] += ab[k];
-            }
-            if constexpr (VEC) {
-                V* vp = reinterpret_cast<V*>(rowp);
-#pragma unroll
-                for (int q = 0; q < NT / W; ++q) {
-                    if (q * W + W - 1 <= t) {
-                        V v;
-#pragma unroll
-                        for (int e = 0; e < W; ++e) vset<T>(v, e, c[q * W + e]);
-                        vp[q] = v;
-                    } else if (q * W <= t) {
-                        // chunk straddling the diagonal: write only k <= t
-#pragma unroll
-                        for (int e = 0; e < W; ++e) {
-                            const int k = q * W + e;
-                            if (k <= t) rowp[k] = c[k];
-                        }
+                    for (int e = 0; e < W; ++e) {
+                        const int k = u * W + e;
+                        if (k <= row) rowp[k] = old[k] + c[q][k];
                     }
                 }
-            } else {
+            });
+        } else {
 #pragma unroll
-                for (int k = 0; k < NT; ++k)
-                    if (k <= t && k < n) rowp[k] = c[k];
-            }
+            for (int k = 0; k < NT; ++k)
+                if (k <= row && k < n) rowp[k] = old[k] + c[q][k];
         }
-    }
+    });
 }
 
-// Persistent grid: resident blocks per SM (queried once per kernel) times the
-// SM count of the current device, capped by the number of tasks.
-template <typename K>
-int persistent_grid(K kern, size_t smem, int64_t tasks, int* per_sm_cache) {
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (*per_sm_cache <= 0) {
-        int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kBlock, smem) !=
-                cudaSuccess || per_sm < 1) {
-            cudaGetLastError();
-            per_sm = 1;
-        }
-        *per_sm_cache = per_sm;
-    }
-    const int64_t full = (int64_t)std::max(sms, 1) * *per_sm_cache;
-    return (int)std::max<int64_t>(1, std::min<int64_t>(full, tasks));
+// Rows (forward) / columns (adjoint) per lane: two where the registers allow.
+template <typename T, int NT>
+constexpr int per_lane() {
+    return (NT * (int)sizeof(T) <= 128) ? 2 : 1;
 }
 
 template <typename T, int NT, bool VEC>
 cudaError_t launch_fwd_nt(const T* A, T* L, int32_t* status, int64_t batch, int n,
                           cudaStream_t stream) {
-    constexpr int G = kBlock / NT;
-    const int64_t tasks = (batch + G - 1) / G;
-    auto kern = small_potrf_kernel<T, NT, VEC>;
-    // persistent blocks when the kernel prefetches, else one block per group
-    static int per_sm = 0;
-    const int64_t grid = NT * sizeof(T) <= 64 ? persistent_grid(kern, 0, tasks, &per_sm) : tasks;
-    kern<<<(unsigned)grid, kBlock, 0, stream>>>(A, L, status, batch, n);
+    constexpr int RPL = per_lane<T, NT>();
+    constexpr int G = kBlock / (NT / RPL);
+    const int64_t blocks = (batch + G - 1) / G;
+    small_potrf_kernel<T, NT, RPL, VEC><<<(unsigned)blocks, kBlock, 0, stream>>>(A, L, status,
+                                                                                 batch, n);
     return cudaGetLastError();
 }
 
 template <typename T, int NT, bool VEC>
 cudaError_t launch_adj_nt(const T* L, const T* Lbar, T* Abar, const int32_t* status,
                           int64_t batch, int n, cudaStream_t stream) {
-    using S = AdjSmem<T, NT>;
-    const int64_t tasks = (batch + S::G - 1) / S::G;
-    auto kern = small_potrf_adj_kernel<T, NT, VEC>;
-    static int per_sm = 0;
+    constexpr int CPL = per_lane<T, NT>();
+    using S = AdjCfg<T, NT, CPL>;
+    const int64_t blocks = (batch + S::G - 1) / S::G;
+    auto kern = small_potrf_adj_kernel<T, NT, CPL, VEC>;
     if (S::bytes > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)S::bytes);
         if (e != cudaSuccess) return e;
     }
-    const int64_t grid = S::prefetch ? persistent_grid(kern, S::bytes, tasks, &per_sm) : tasks;
-    kern<<<(unsigned)grid, kBlock, S::bytes, stream>>>(L, Lbar, Abar, status, batch, n);
+    kern<<<(unsigned)blocks, kBlock, S::bytes, stream>>>(L, Lbar, Abar, status, batch, n);
     return cudaGetLastError();
 }
 

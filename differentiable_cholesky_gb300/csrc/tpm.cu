@@ -1,28 +1,18 @@
-// Thread-per-matrix Cholesky forward and adjoint for float32 matrices of order
-// N = 8 or 16 (the batched 65536 x 16x16 workload).
+// Thread-per-matrix Cholesky forward for float32 matrices of order N = 8 or
+// 16 (the batched 65536 x 16x16 workload).  jaxmg docs "Cholesky
+// factorization": lower factor and status.
 //
 // One warp handles 32 matrices per round, one per lane, with no communication
 // between lanes: every lane keeps the lower triangle of its own matrix in
-// registers.  Matrices move between HBM and shared memory by TMA bulk copies
-// (cp.async.bulk, one per matrix, completion on an mbarrier) into per-lane
-// slots that are skewed by 16 bytes, so each lane's 16-byte row reads and
-// writes fall in distinct bank groups.  Each warp owns two slot sets, so the
-// copy for its next round is in flight while it computes the current one.  A
-// block is one warp; blocks are persistent (resident blocks per SM x SMs).
-//
-// Forward (jaxmg docs "Cholesky factorization": lower factor and status):
-// right-looking column recurrence with IEEE square root and a correctly
-// rounded reciprocal of the pivot.
-//
-// Adjoint: the symmetric-matrix derivative of Murray (2016) -- the one
-// NVIDIA/warp issue #1316's closing comment implements with S = Phi(L^T adj_L)
-// and two triangular solves -- evaluated here by the same paper's in-place
-// reverse sweep over the factorisation (columns j = N-1 .. 0), which reaches
-// the same lower-triangle gradient Phi(M + M^T) with one triangle of
-// registers and N^3/3 multiply-adds instead of 7N^3/6.  adj_L and adj_A are
-// read (and adj_A written) by each lane directly, in 16-byte chunks of its
-// matrix's lower triangle; the chunk that straddles the diagonal is written
-// back with the upper values that were read.
+// registers and runs the right-looking column recurrence on it
+// (l_jj = d * rsqrt(d), column scaled by rsqrt(d), which keeps the per-column
+// latency chain short).  Matrices move between HBM and shared memory by TMA
+// bulk copies (cp.async.bulk, one per matrix, completion on an mbarrier) into
+// per-lane slots skewed by 16 bytes, so each lane's 16-byte row reads and
+// writes fall in distinct bank groups, and L leaves by bulk stores from the
+// same slots.  Each warp owns two slot sets, so the copy for its next round is
+// in flight while it factors the current one.  A block is one warp; blocks are
+// persistent (resident blocks per SM x SMs).
 
 #include <cuda_runtime.h>
 
@@ -78,8 +68,6 @@ __device__ __forceinline__ int round_count(int64_t batch, int64_t w) {
     return batch - w * 32 < 32 ? (int)(batch - w * 32) : 32;
 }
 
-// Forward.  Two slot sets per warp: the copy of round r + 1 is in flight
-// while round r is factored; L leaves through the slot it arrived in.
 template <int N>
 __global__ void __launch_bounds__(32)
 tpm_potrf_kernel(const float* __restrict__ A, float* __restrict__ L, int32_t* __restrict__ status,
@@ -142,9 +130,8 @@ tpm_potrf_kernel(const float* __restrict__ A, float* __restrict__ L, int32_t* __
                 if (st == 0) st = j + 1;
                 d = 1.f;
             }
-            const float ljj = __fsqrt_rn(d);
-            const float inv = __frcp_rn(ljj);
-            a[j][j] = ljj;
+            const float inv = rsqrtf(d);  // 1 / l_jj
+            a[j][j] = d * inv;
 #pragma unroll
             for (int i = j + 1; i < N; ++i) a[i][j] *= inv;
 #pragma unroll
@@ -175,143 +162,6 @@ tpm_potrf_kernel(const float* __restrict__ A, float* __restrict__ L, int32_t* __
     bulk_wait_all();
 }
 
-// Lower 16-byte chunks of matrix row i from global memory into r.
-template <int N>
-__device__ __forceinline__ void ldg_lower(const float* __restrict__ mat, float (&r)[N][N]) {
-#pragma unroll
-    for (int i = 0; i < N; ++i) {
-#pragma unroll
-        for (int c = 0; c < N / 4; ++c) {
-            if (4 * c > i) continue;
-            const float4 v = __ldg(reinterpret_cast<const float4*>(mat + i * N) + c);
-            r[i][4 * c + 0] = v.x;
-            if (4 * c + 1 <= i) r[i][4 * c + 1] = v.y;
-            if (4 * c + 2 <= i) r[i][4 * c + 2] = v.z;
-            if (4 * c + 3 <= i) r[i][4 * c + 3] = v.w;
-        }
-    }
-}
-
-// Adjoint.  L arrives by bulk copy into two slot sets (round r + 1 in flight
-// while round r runs); adj_L and adj_A are read and written by each lane
-// directly, in 16-byte chunks of its own matrix's lower triangle (the chunk
-// that straddles the diagonal is written back with the upper values it read).
-template <int N>
-__global__ void __launch_bounds__(32)
-tpm_potrf_adj_kernel(const float* __restrict__ Lg, const float* __restrict__ Lbar,
-                     float* __restrict__ Abar, const int32_t* __restrict__ status, int64_t batch) {
-    using C = Tpm<N>;
-    extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
-    const int lane = threadIdx.x;
-    float* slots = reinterpret_cast<float*>(smem + kBarBytes);
-    float* slot_of[2] = {slots + lane * C::kSlot, slots + (32 + lane) * C::kSlot};
-    if (lane == 0) {
-        mbar_init(bar + 0, 1);
-        mbar_init(bar + 1, 1);
-    }
-    fence_mbar_init();
-    __syncwarp();
-
-    int64_t w = blockIdx.x;
-    if (w * 32 >= batch) return;
-    issue_round_load<N>(Lg, w * 32, round_count(batch, w), slot_of[0], bar + 0, lane);
-    uint32_t phase[2] = {0u, 0u};
-#pragma unroll 1
-    for (int r = 0; w * 32 < batch; ++r, w += gridDim.x) {
-        const int b = r & 1;
-        const int64_t m0 = w * 32;
-        const int nvalid = round_count(batch, w);
-        const int64_t m = m0 + lane;
-        const int64_t wn = w + gridDim.x;
-        if (wn * 32 < batch)
-            issue_round_load<N>(Lg, wn * 32, round_count(batch, wn), slot_of[b ^ 1], bar + (b ^ 1),
-                                lane);
-        bool active = lane < nvalid;
-        if (active && status != nullptr) active = (__ldg(status + m) == 0);
-
-        float g[N][N];
-        if (active) {
-            ldg_lower<N>(Lbar + m * (N * N), g);
-        } else {
-#pragma unroll
-            for (int i = 0; i < N; ++i)
-#pragma unroll
-                for (int k = 0; k <= i; ++k) g[i][k] = 0.f;
-        }
-        if (!__all_sync(0xffffffffu, mbar_wait(bar + b, phase[b], kMbarPolls))) {
-            mbar_wait(bar + b, phase[b], kMbarPolls);
-            mbar_wait(bar + (b ^ 1), phase[b ^ 1], kMbarPolls);
-            break;  // the copies did not complete: adj_A of this round is left unchanged
-        }
-        phase[b] ^= 1u;
-        const float* lslot = slot_of[b];  // inactive lanes sweep zeros
-
-        // Reverse sweep.  Column j of g holds the gradient w.r.t. column j of
-        // L on entry and w.r.t. column j of A (lower part) on exit.
-#pragma unroll
-        for (int j = N - 1; j >= 0; --j) {
-            const float ljj = lslot[j * N + j];
-            const float inv = __frcp_rn(ljj);
-            float s = 0.f;
-            // rows below j: prefix [0, j] of row i of L
-#pragma unroll
-            for (int i = N - 1; i > j; --i) {
-                float lrow[N];
-#pragma unroll
-                for (int c = 0; c < N / 4; ++c) {
-                    if (4 * c > j) continue;
-                    const float4 v = reinterpret_cast<const float4*>(lslot + i * N)[c];
-                    lrow[4 * c + 0] = v.x;
-                    lrow[4 * c + 1] = v.y;
-                    lrow[4 * c + 2] = v.z;
-                    lrow[4 * c + 3] = v.w;
-                }
-                s = fmaf(lrow[j], g[i][j], s);
-                g[i][j] *= inv;
-#pragma unroll
-                for (int k = 0; k < j; ++k) g[j][k] = fmaf(-g[i][j], lrow[k], g[j][k]);
-            }
-            g[j][j] = (g[j][j] - s * inv) * inv;
-            float lj[N];
-#pragma unroll
-            for (int c = 0; c < N / 4; ++c) {
-                if (4 * c > j) continue;
-                const float4 v = reinterpret_cast<const float4*>(lslot + j * N)[c];
-                lj[4 * c + 0] = v.x;
-                lj[4 * c + 1] = v.y;
-                lj[4 * c + 2] = v.z;
-                lj[4 * c + 3] = v.w;
-            }
-#pragma unroll
-            for (int k = 0; k < j; ++k) g[j][k] = fmaf(-g[j][j], lj[k], g[j][k]);
-#pragma unroll
-            for (int i = j + 1; i < N; ++i)
-#pragma unroll
-                for (int k = 0; k < j; ++k) g[i][k] = fmaf(-g[i][j], lj[k], g[i][k]);
-            g[j][j] *= 0.5f;
-        }
-
-        if (active) {
-            float* dst = Abar + m * (N * N);
-#pragma unroll
-            for (int i = 0; i < N; ++i) {
-#pragma unroll
-                for (int c = 0; c < N / 4; ++c) {
-                    if (4 * c > i) continue;
-                    float4* p = reinterpret_cast<float4*>(dst + i * N) + c;
-                    float4 v = *p;
-                    v.x += g[i][4 * c + 0];
-                    if (4 * c + 1 <= i) v.y += g[i][4 * c + 1];
-                    if (4 * c + 2 <= i) v.z += g[i][4 * c + 2];
-                    if (4 * c + 3 <= i) v.w += g[i][4 * c + 3];
-                    *p = v;
-                }
-            }
-        }
-    }
-}
-
 template <typename K>
 int tpm_grid(K kern, size_t smem, int64_t rounds) {
     int dev = 0, sms = 0, per_sm = 0;
@@ -337,18 +187,6 @@ cudaError_t tpm_fwd_n(const float* A, float* L, int32_t* status, int64_t batch,
     return cudaGetLastError();
 }
 
-template <int N>
-cudaError_t tpm_adj_n(const float* L, const float* Lbar, float* Abar, const int32_t* status,
-                      int64_t batch, cudaStream_t stream) {
-    const size_t smem = kBarBytes + 2 * Tpm<N>::kSlotsBytes;
-    auto kern = tpm_potrf_adj_kernel<N>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    const int grid = tpm_grid(kern, smem, (batch + 31) / 32);
-    kern<<<grid, 32, smem, stream>>>(L, Lbar, Abar, status, batch);
-    return cudaGetLastError();
-}
-
 }  // namespace
 
 bool tpm_supported(int n) { return n == 8 || n == 16; }
@@ -357,13 +195,6 @@ cudaError_t tpm_fwd(const float* A, float* L, int32_t* status, int64_t batch, in
                     cudaStream_t stream) {
     if (n == 16) return tpm_fwd_n<16>(A, L, status, batch, stream);
     if (n == 8) return tpm_fwd_n<8>(A, L, status, batch, stream);
-    return cudaErrorInvalidValue;
-}
-
-cudaError_t tpm_adj(const float* L, const float* Lbar, float* Abar, const int32_t* status,
-                    int64_t batch, int n, cudaStream_t stream) {
-    if (n == 16) return tpm_adj_n<16>(L, Lbar, Abar, status, batch, stream);
-    if (n == 8) return tpm_adj_n<8>(L, Lbar, Abar, status, batch, stream);
     return cudaErrorInvalidValue;
 }
 

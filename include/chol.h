@@ -97,9 +97,7 @@ CHOL_API int chol_fwd_ex(int64_t batch, int32_t n, int32_t dtype, const void* A,
  *                a_ij (i >= j) that chol_fwd reads:
  *                  M = L^-T Phi(L^T tril(adj_L)) L^-1,
  *                  adj_A_ij += M_ij + M_ji (i > j),  adj_A_ii += M_ii.
- *                The upper triangle keeps its values (the float32 n = 8 / 16
- *                path stores whole matrices and rewrites it with the values it
- *                read; the other paths never write it).  Must not overlap L,
+ *                The upper triangle is never written.  Must not overlap L,
  *                adj_L or status (CHOL_EALIAS).
  *   status  in : int32[batch] from chol_fwd, or NULL.  Matrices with a non-zero
  *                status are skipped (their adj_A is left unchanged).
