@@ -171,6 +171,21 @@ class ClockSampler:
                 "samples": len(inside), "note": note}
 
 
+def max_over_ranks(value_ms: float, dist, device) -> float:
+    """The slowest rank's time (the job's time), or the value itself on one rank."""
+    if dist is None:
+        return value_ms
+    import torch
+    t = torch.tensor([value_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: int, world: int, slowest_ms: float) -> float:
+    """Whole-job units per second: every rank's units over the slowest rank's time."""
+    return units_per_rank * world / (slowest_ms / 1e3)
+
+
 def gpu_identifier(torch):
     try:
         u = torch.cuda.get_device_properties(0).uuid
@@ -342,10 +357,7 @@ def main():
     elapsed_ms = start.elapsed_time(stop)
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in events)
     adj_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in events)
-    if dist is not None:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dist, dev)
     clocks = sampler.summary(t_wall0, t_wall1) if sampler is not None else None
 
     # end-to-end through the public API: pinned host in, pinned host out
@@ -378,10 +390,7 @@ def main():
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
     if sampler is not None:
         sampler.stop()
 
@@ -390,9 +399,8 @@ def main():
             dist.destroy_process_group()
         return
 
-    matrices = args.steps * batch * world
-    value = matrices / (elapsed_ms / 1e3)
-    e2e_value = args.e2e_steps * batch * world / (e2e_ms / 1e3)
+    value = job_throughput(args.steps * batch, world, elapsed_ms)
+    e2e_value = job_throughput(args.e2e_steps * batch, world, e2e_ms)
     fwd_b, adj_b = algorithmic_bytes(n, esize)
     fwd_f, adj_f = nominal_flops(n)
     hbm_peak, peak_src = read_peaks()

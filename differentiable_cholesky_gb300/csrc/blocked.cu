@@ -217,7 +217,11 @@ enum GemmMode {
     GEMM_FWD_TRAIL = 0,  // L_ij -= L_ik L_jk^T, k < j <= i
     GEMM_ADJ_P = 1,      // W_IJ = Phi(sum_{K>=I} L_KI^T tril(adj_L)_KJ) (I >= J); 0 for I < J
     GEMM_ADJ_XUPD = 2,   // W_I'J -= L_II'^T W_IJ, I' < I, all J
-    GEMM_ADJ_MUPD = 3    // W_IJ' -= W_IJ L_JJ', all I, J' < J
+    GEMM_ADJ_MUPD = 3,   // W_IJ' -= W_IJ L_JJ', all I, J' < J
+    // reverse sweep over tile column J = step (see blocked_adj):
+    GEMM_REV_ROW = 4,    // W_JK -= Wbar_panel^T L_panel,K  (K <= J; split over the rows below)
+    GEMM_REV_UPD = 5,    // W_IK -= W_IJ L_JK  (I > J, K < J)
+    GEMM_REV_SYM = 6     // W_JK -= (W_JJ + W_JJ^T) L_JK  (K < J; W_JJ lower)
 };
 
 template <typename T>
@@ -231,6 +235,8 @@ struct GemmArgs {
     int tile;     // T
     int nt;       // tiles per side
     int step;     // k, I or J
+    int kchunk;   // reduction length per blockIdx.z (split reduction)
+    int atomic;   // 1: the epilogue adds with atomics (split reduction)
 };
 
 struct TileJob {
@@ -239,6 +245,7 @@ struct TileJob {
     int b_row0, b_col0;   // global origin of op(B)
     int klen;             // length of the reduction
     bool a_trans, b_trans, a_lower, b_lower;
+    bool a_sym;           // op(A) is the symmetric matrix A + A^T of a lower tile
     bool zero_only;       // write zeros (upper tiles of P)
     bool phi;             // apply Phi (diagonal tile of P)
     float alpha, beta;
@@ -284,11 +291,33 @@ __device__ __forceinline__ TileJob make_job(const GemmArgs<T>& g, int tile_id) {
         job.b_row0 = s * Tt; job.b_col0 = J * Tt;  job.b_trans = false;
         job.klen = min(Tt, g.n - s * Tt);
         job.alpha = -1.f; job.beta = 1.f;
-    } else {  // GEMM_ADJ_MUPD
+    } else if (MODE == GEMM_ADJ_MUPD) {
         const int I = tile_id / s, Jp = tile_id % s;  // Jp < J = s
         job.ci = I; job.cj = Jp;
         job.a_row0 = I * Tt; job.a_col0 = s * Tt;  job.a_trans = false;
         job.b_row0 = s * Tt; job.b_col0 = Jp * Tt; job.b_trans = false;
+        job.klen = min(Tt, g.n - s * Tt);
+        job.alpha = -1.f; job.beta = 1.f;
+    } else if (MODE == GEMM_REV_ROW) {
+        const int K = tile_id;  // K <= J = s
+        const int r0 = s * Tt + min(Tt, g.n - s * Tt);
+        job.ci = s; job.cj = K;
+        job.a_row0 = r0; job.a_col0 = s * Tt; job.a_trans = true;
+        job.b_row0 = r0; job.b_col0 = K * Tt; job.b_trans = false;
+        job.klen = g.n - r0;
+        job.alpha = -1.f; job.beta = 1.f;
+    } else if (MODE == GEMM_REV_UPD) {
+        const int I = s + 1 + tile_id / s, K = tile_id % s;
+        job.ci = I; job.cj = K;
+        job.a_row0 = I * Tt; job.a_col0 = s * Tt; job.a_trans = false;
+        job.b_row0 = s * Tt; job.b_col0 = K * Tt; job.b_trans = false;
+        job.klen = min(Tt, g.n - s * Tt);
+        job.alpha = -1.f; job.beta = 1.f;
+    } else {  // GEMM_REV_SYM
+        const int K = tile_id;  // K < J = s
+        job.ci = s; job.cj = K;
+        job.a_row0 = s * Tt; job.a_col0 = s * Tt; job.a_trans = false; job.a_sym = true;
+        job.b_row0 = s * Tt; job.b_col0 = K * Tt; job.b_trans = false;
         job.klen = min(Tt, g.n - s * Tt);
         job.alpha = -1.f; job.beta = 1.f;
     }
@@ -333,18 +362,30 @@ gemm_kernel(GemmArgs<T> g) {
 #pragma unroll
             for (int j = 0; j < MT; ++j) acc[i][j] = T(0);
 
-        for (int k0 = 0; k0 < job.klen; k0 += BK) {
+        const int kbeg = blockIdx.z * g.kchunk;
+        const int kend = min(job.klen, kbeg + g.kchunk);
+        for (int k0 = kbeg; k0 < kend; k0 += BK) {
             __syncthreads();
             // op(A)(r, kk) for r in the sub-block rows, kk in [k0, k0 + BK)
             for (int e = threadIdx.x; e < BK * BM; e += blockDim.x) {
                 int r, kk;
                 if (job.a_trans) { kk = e / BM; r = e % BM; }   // contiguous over r
                 else             { r = e / BK;  kk = e % BK; }  // contiguous over kk
-                const int gr = job.a_trans ? job.a_row0 + k0 + kk : job.a_row0 + r_off + r;
-                const int gc = job.a_trans ? job.a_col0 + r_off + r : job.a_col0 + k0 + kk;
+                int gr = job.a_trans ? job.a_row0 + k0 + kk : job.a_row0 + r_off + r;
+                int gc = job.a_trans ? job.a_col0 + r_off + r : job.a_col0 + k0 + kk;
                 T x = T(0);
-                if (k0 + kk < job.klen && gr < g.n && gc < g.n && (!job.a_lower || gc <= gr))
-                    x = Ab[(int64_t)gr * g.n + gc];
+                if (k0 + kk < kend && gr < g.n && gc < g.n) {
+                    if (job.a_sym) {
+                        // (A + A^T) of a lower tile: the upper half mirrors the lower
+                        // one and the diagonal is doubled
+                        const bool diag = gc == gr;
+                        if (gc > gr) { const int t = gr; gr = gc; gc = t; }
+                        x = Ab[(int64_t)gr * g.n + gc];
+                        if (diag) x += x;
+                    } else if (!job.a_lower || gc <= gr) {
+                        x = Ab[(int64_t)gr * g.n + gc];
+                    }
+                }
                 As[kk][r] = x;
             }
             // op(B)(kk, c)
@@ -355,7 +396,7 @@ gemm_kernel(GemmArgs<T> g) {
                 const int gr = job.b_trans ? job.b_row0 + c_off + c : job.b_row0 + k0 + kk;
                 const int gc = job.b_trans ? job.b_col0 + k0 + kk : job.b_col0 + c_off + c;
                 T x = T(0);
-                if (k0 + kk < job.klen && gr < g.n && gc < g.n && (!job.b_lower || gc <= gr))
+                if (k0 + kk < kend && gr < g.n && gc < g.n && (!job.b_lower || gc <= gr))
                     x = Bb[(int64_t)gr * g.n + gc];
                 Bs[kk][c] = x;
             }
@@ -385,6 +426,10 @@ gemm_kernel(GemmArgs<T> g) {
                 if (MODE == GEMM_FWD_TRAIL && c > r) continue;  // L stays zero above the diagonal
                 T* cp = Cb + (int64_t)r * g.n + c;
                 T v = T(job.alpha) * acc[i][j];
+                if (g.atomic) {
+                    atomicAdd(cp, v);
+                    continue;
+                }
                 if (job.beta != 0.f) v += *cp;
                 if (job.phi) v = (c < r) ? v : (c == r ? v * T(0.5) : T(0));
                 *cp = v;
@@ -433,13 +478,24 @@ size_t trsm_smem(int kb, int esize) {
     return (size_t)(kb + kVecPerBlock) * (kb + 1) * esize;
 }
 
+// Raise a kernel's dynamic shared-memory limit once, to the largest size any
+// tile needs (attribute calls are host-synchronous, so not one per launch).
+template <typename K>
+cudaError_t allow_smem(K kern, size_t bytes, int* done) {
+    if (*done) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) *done = 1;
+    return e;
+}
+
 template <typename T, int MODE>
 cudaError_t launch_trsm(const T* L, T* W, const int32_t* status, int64_t batch, int n, int t0,
                         int kb, int v_begin, int v_count, cudaStream_t stream) {
     if (v_count <= 0) return cudaSuccess;
     const size_t smem = trsm_smem(kb, sizeof(T));
     auto kern = trsm_kernel<T, MODE>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static int smem_set = 0;
+    cudaError_t e = allow_smem(kern, trsm_smem(128, sizeof(T)), &smem_set);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((v_count + kVecPerBlock - 1) / kVecPerBlock), grid_y(batch));
     kern<<<grid, kThreads, smem, stream>>>(L, W, status, batch, n, t0, kb, v_begin, v_count);
@@ -447,14 +503,136 @@ cudaError_t launch_trsm(const T* L, T* W, const int32_t* status, int64_t batch, 
 }
 
 template <typename T, int MODE>
-cudaError_t launch_gemm(const GemmArgs<T>& g, int tiles, cudaStream_t stream) {
+cudaError_t launch_gemm(GemmArgs<T> g, int tiles, cudaStream_t stream, int ksplits = 1,
+                        int klen = 0) {
     if (tiles <= 0) return cudaSuccess;
     const int bm = g.tile >= 64 ? 64 : 32;
     const int subs = (g.tile / bm) * (g.tile / bm);
-    dim3 grid((unsigned)(tiles * subs), grid_y(g.batch));
+    unsigned zdim = 1;
+    if (ksplits > 1 && klen > 0) {
+        // split the reduction over blockIdx.z; partial sums meet by atomics
+        const int per = (klen + ksplits - 1) / ksplits;
+        g.kchunk = (per + 15) / 16 * 16;
+        zdim = (unsigned)((klen + g.kchunk - 1) / g.kchunk);
+        g.atomic = zdim > 1;
+    } else {
+        g.kchunk = 1 << 30;
+        g.atomic = 0;
+    }
+    dim3 grid((unsigned)(tiles * subs), grid_y(g.batch), zdim);
     if (bm == 64) gemm_kernel<T, 64, MODE><<<grid, kThreads, 0, stream>>>(g);
     else gemm_kernel<T, 32, MODE><<<grid, kThreads, 0, stream>>>(g);
     return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Reverse sweep over one diagonal tile (Murray 2016, unblocked form): on entry
+// W_JJ holds the gradient w.r.t. the tile's factor L_JJ (lower), on exit the
+// gradient w.r.t. the lower entries of the tile D = A_JJ - R R^T it factored.
+// Columns j = kb-1 .. 0 in shared memory, one block per matrix.
+// ---------------------------------------------------------------------------
+// Packed lower-triangle index (i >= j).
+__device__ __forceinline__ int tri(int i, int j) { return i * (i + 1) / 2 + j; }
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+diag_rev_kernel(const T* __restrict__ L, T* __restrict__ W, const int32_t* __restrict__ status,
+                int64_t batch, int n, int j0, int kb) {
+    // both tiles packed as lower triangles: kb (kb + 1) elements in all
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    T* Ls = reinterpret_cast<T*>(smem_raw);
+    T* Ws = Ls + (size_t)kb * (kb + 1) / 2;
+    __shared__ T red[kThreads / 32];
+    const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
+    for (int64_t b = blockIdx.y; b < batch; b += gridDim.y) {
+        if (skip_matrix(status, b)) continue;
+        const T* Lb = L + b * (int64_t)n * n;
+        T* Wb = W + b * (int64_t)n * n;
+        __syncthreads();
+        for (int e = tid; e < kb * kb; e += blockDim.x) {
+            const int r = e / kb, c = e % kb;
+            if (c > r) continue;
+            const int64_t o = (int64_t)(j0 + r) * n + j0 + c;
+            Ls[tri(r, c)] = Lb[o];
+            Ws[tri(r, c)] = Wb[o];
+        }
+        __syncthreads();
+        for (int j = kb - 1; j >= 0; --j) {
+            // s = sum_{i > j} L_ij W_ij
+            T part = T(0);
+            for (int i = j + 1 + tid; i < kb; i += blockDim.x)
+                part = fma(Ls[tri(i, j)], Ws[tri(i, j)], part);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+            if (lane == 0) red[warp] = part;
+            __syncthreads();
+            T sum = T(0);
+#pragma unroll
+            for (int w = 0; w < kThreads / 32; ++w) sum += red[w];
+            const T inv = T(1) / Ls[tri(j, j)];
+            // column j: diagonal from the sum, the rest scaled
+            for (int i = j + 1 + tid; i < kb; i += blockDim.x) Ws[tri(i, j)] *= inv;
+            if (tid == 0) Ws[tri(j, j)] = (Ws[tri(j, j)] - sum * inv) * inv;
+            __syncthreads();
+            // row j left of the diagonal: W_jk -= sum_{i >= j} W_ij L_ik
+            for (int k = tid; k < j; k += blockDim.x) {
+                T acc = T(0);
+                for (int i = j; i < kb; ++i) acc = fma(Ws[tri(i, j)], Ls[tri(i, k)], acc);
+                Ws[tri(j, k)] -= acc;
+            }
+            // rows below, left of column j: W_ik -= W_ij L_jk
+            if (j > 0) {
+                const int m = kb - 1 - j;
+                for (int e = tid; e < m * j; e += blockDim.x) {
+                    const int i = j + 1 + e / j, k = e % j;
+                    Ws[tri(i, k)] = fma(-Ws[tri(i, j)], Ls[tri(j, k)], Ws[tri(i, k)]);
+                }
+            }
+            __syncthreads();
+            if (tid == 0) Ws[tri(j, j)] *= T(0.5);
+            // (the next column's first barrier orders this write)
+        }
+        __syncthreads();
+        for (int e = tid; e < kb * kb; e += blockDim.x) {
+            const int r = e / kb, c = e % kb;
+            if (c <= r) Wb[(int64_t)(j0 + r) * n + j0 + c] = Ws[tri(r, c)];
+        }
+    }
+}
+
+// dst = tril(src) (zeros above the diagonal), matrices with status != 0 skipped.
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+lower_copy_kernel(const T* __restrict__ src, T* __restrict__ dst,
+                  const int32_t* __restrict__ status, int64_t batch, int n) {
+    const int64_t nn = (int64_t)n * n;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < batch * nn;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t b = e / nn, w = e % nn;
+        if (skip_matrix(status, b)) continue;
+        const int i = (int)(w / n), j = (int)(w % n);
+        dst[e] = (j <= i) ? src[e] : T(0);
+    }
+}
+
+// dst_ij += src_ij on the lower triangle (j <= i), matrices with status != 0 skipped.
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+lower_add_kernel(const T* __restrict__ src, T* __restrict__ dst,
+                 const int32_t* __restrict__ status, int64_t batch, int n) {
+    const int64_t nn = (int64_t)n * n;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < batch * nn;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t b = e / nn, w = e % nn;
+        const int i = (int)(w / n), j = (int)(w % n);
+        if (j > i || skip_matrix(status, b)) continue;
+        dst[e] += src[e];
+    }
+}
+
+inline unsigned elementwise_blocks(int64_t total) {
+    return (unsigned)std::max<int64_t>(1, std::min<int64_t>((total + kThreads - 1) / kThreads,
+                                                            152 * 16));
 }
 
 }  // namespace
@@ -481,9 +659,8 @@ cudaError_t blocked_fwd(const T* A, T* L, int32_t* status, int64_t batch, int n,
             A, L, status, batch, n);
         CHOL_TRY(cudaGetLastError());
     }
-    const size_t diag_smem = (size_t)tile * (tile + 1) * sizeof(T);
-    CHOL_TRY(cudaFuncSetAttribute(potrf_diag_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)diag_smem));
+    static int diag_smem_set = 0;
+    CHOL_TRY(allow_smem(potrf_diag_kernel<T>, (size_t)128 * 129 * sizeof(T), &diag_smem_set));
     for (int k = 0; k < nt; ++k) {
         const int k0 = k * tile;
         const int kb = std::min(tile, n - k0);
@@ -494,45 +671,65 @@ cudaError_t blocked_fwd(const T* A, T* L, int32_t* status, int64_t batch, int n,
         CHOL_TRY((launch_trsm<T, TRSM_FWD_PANEL>(L, L, status, batch, n, k0, kb, k0 + kb,
                                                  n - k0 - kb, stream)));
         const int m = nt - k - 1;
-        GemmArgs<T> g{L, L, L, status, batch, n, tile, nt, k};
+        GemmArgs<T> g{L, L, L, status, batch, n, tile, nt, k, 0, 0};
         CHOL_TRY((launch_gemm<T, GEMM_FWD_TRAIL>(g, m * (m + 1) / 2, stream)));
     }
     return cudaSuccess;
 }
 
+// Adjoint by the blocked reverse sweep of Murray (2016) over a left-looking
+// blocked factorisation, in place on W (= tril(adj_L) on entry):
+// for tile columns J = nt-1 .. 0, with C = W's panel below the diagonal tile,
+//   C      <- C L_JJ^-1                 (triangular solve, rows of the panel)
+//   W_JK   -= C^T L_panel,K   (K <= J)  (reduction over the rows below J)
+//   W_IK   -= C L_JK          (I > J, K < J)
+//   W_JJ   <- reverse sweep of the tile's own factorisation
+//   W_JK   -= (W_JJ + W_JJ^T) L_JK      (K < J)
+// and finally adj_A += tril(W).  This is the same lower-triangle gradient as
+// Phi(M + M^T), M = L^-T Phi(L^T adj_L) L^-1, in 2 n^3 / 3 flops instead of
+// the 7 n^3 / 3 of forming P and solving twice.
 template <typename T>
 cudaError_t blocked_adj(const T* L, const T* Lbar, T* Abar, const int32_t* status,
                         int64_t batch, int n, int tile, T* W, cudaStream_t stream) {
     const int nt = (n + tile - 1) / tile;
+    const int64_t total = batch * (int64_t)n * n;
+    lower_copy_kernel<T><<<elementwise_blocks(total), kThreads, 0, stream>>>(Lbar, W, status,
+                                                                            batch, n);
+    CHOL_TRY(cudaGetLastError());
+    static int diag_smem_set = 0;
+    CHOL_TRY(allow_smem(diag_rev_kernel<T>, (size_t)128 * 129 * sizeof(T), &diag_smem_set));
+    int sms = 152;
     {
-        GemmArgs<T> g{L, Lbar, W, status, batch, n, tile, nt, 0};
-        CHOL_TRY((launch_gemm<T, GEMM_ADJ_P>(g, nt * nt, stream)));
+        int dev = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess)
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     }
-    // X = L^-T S, tile rows from the bottom
-    for (int I = nt - 1; I >= 0; --I) {
-        const int t0 = I * tile, kb = std::min(tile, n - t0);
-        CHOL_TRY((launch_trsm<T, TRSM_ADJ_X>(L, W, status, batch, n, t0, kb, 0, n, stream)));
-        if (I > 0) {
-            GemmArgs<T> g{L, W, W, status, batch, n, tile, nt, I};
-            CHOL_TRY((launch_gemm<T, GEMM_ADJ_XUPD>(g, I * nt, stream)));
-        }
-    }
-    // M = X L^-1, tile columns from the right
+    const int bm = tile >= 64 ? 64 : 32;
+    const int subs = (tile / bm) * (tile / bm);
+    const int64_t bmat = std::min<int64_t>(batch, 65535);
     for (int J = nt - 1; J >= 0; --J) {
-        const int t0 = J * tile, kb = std::min(tile, n - t0);
-        CHOL_TRY((launch_trsm<T, TRSM_ADJ_M>(L, W, status, batch, n, t0, kb, 0, n, stream)));
+        const int j0 = J * tile, kb = std::min(tile, n - j0), r0 = j0 + kb, nb = n - r0;
+        if (nb > 0) {
+            CHOL_TRY((launch_trsm<T, TRSM_ADJ_M>(L, W, status, batch, n, j0, kb, r0, nb, stream)));
+            GemmArgs<T> g{W, L, W, status, batch, n, tile, nt, J, 0, 0};
+            // enough blocks to fill the GPU twice over, splitting the long reduction
+            const int64_t blocks = (int64_t)(J + 1) * subs * bmat;
+            const int ks = (int)std::max<int64_t>(
+                1, std::min<int64_t>((2 * sms + blocks - 1) / blocks, (nb + 127) / 128));
+            CHOL_TRY((launch_gemm<T, GEMM_REV_ROW>(g, J + 1, stream, ks, nb)));
+            if (J > 0) CHOL_TRY((launch_gemm<T, GEMM_REV_UPD>(g, (nt - J - 1) * J, stream)));
+        }
+        diag_rev_kernel<T><<<dim3(1, grid_y(batch)), kThreads, (size_t)kb * (kb + 1) * sizeof(T),
+                             stream>>>(L, W, status, batch, n, j0, kb);
+        CHOL_TRY(cudaGetLastError());
         if (J > 0) {
-            GemmArgs<T> g{W, L, W, status, batch, n, tile, nt, J};
-            CHOL_TRY((launch_gemm<T, GEMM_ADJ_MUPD>(g, nt * J, stream)));
+            GemmArgs<T> g{W, L, W, status, batch, n, tile, nt, J, 0, 0};
+            CHOL_TRY((launch_gemm<T, GEMM_REV_SYM>(g, J, stream)));
         }
     }
-    {
-        const int nb = (n + 31) / 32;
-        phi_acc_kernel<T><<<dim3((unsigned)(nb * (nb + 1) / 2), grid_y(batch)), kThreads, 0,
-                            stream>>>(W, Abar, status, batch, n);
-        CHOL_TRY(cudaGetLastError());
-    }
-    return cudaSuccess;
+    lower_add_kernel<T><<<elementwise_blocks(total), kThreads, 0, stream>>>(W, Abar, status,
+                                                                           batch, n);
+    return cudaGetLastError();
 }
 
 template cudaError_t blocked_fwd<float>(const float*, float*, int32_t*, int64_t, int, int,

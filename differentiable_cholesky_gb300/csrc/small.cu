@@ -136,8 +136,8 @@ small_potrf_kernel(const T* __restrict__ A, T* __restrict__ L, int32_t* __restri
     for (int q = 0; q < RPL; ++q) fetch_fwd_row<T, NT, VEC>(A, b, batch, rows[q], n, a[q]);
 
     int st = 0;
-#pragma unroll
-    for (int j = 0; j < NT; ++j) {
+    static_for<0, NT>([&](auto jc) {
+        constexpr int j = decltype(jc)::value;
         T* buf = colbuf + g * CS + (j & 1) * NT;
 #pragma unroll
         for (int q = 0; q < RPL; ++q) buf[rows[q]] = a[q][j];
@@ -152,24 +152,23 @@ small_potrf_kernel(const T* __restrict__ A, T* __restrict__ L, int32_t* __restri
 #pragma unroll
         for (int q = 0; q < RPL; ++q) {
             const T lij = a[q][j] * r;
-            coef[q] = (rows[q] > j) ? lij * r : T(0);
+            coef[q] = T(rows[q] > j) * (lij * r);
             a[q][j] = lij;
         }
         // trailing update with the published column, read as aligned vectors
-        // (constant trip counts: inner loops unroll first)
-#pragma unroll
-        for (int c = 0; c < NT / W; ++c) {
-            if (c < (j + 1) / W) continue;
+        static_for<(j + 1) / W, NT / W>([&](auto cc) {
+            constexpr int c = decltype(cc)::value;
             const V v = reinterpret_cast<const V*>(buf)[c];
+            static_for<0, W>([&](auto ec) {
+                constexpr int e = decltype(ec)::value;
+                constexpr int k = c * W + e;
+                if constexpr (k > j) {
 #pragma unroll
-            for (int e = 0; e < W; ++e) {
-                const int k = c * W + e;
-#pragma unroll
-                for (int q = 0; q < RPL; ++q)
-                    if (k > j) a[q][k] = fma(-coef[q], vget<T>(v, e), a[q][k]);
-            }
-        }
-    }
+                    for (int q = 0; q < RPL; ++q) a[q][k] = fma(-coef[q], vget<T>(v, e), a[q][k]);
+                }
+            });
+        });
+    });
 
     if (b >= batch) return;
 #pragma unroll
@@ -206,7 +205,7 @@ template <typename T, int NT, int CPL>
 struct AdjCfg {
     static constexpr int LPG = NT / CPL;                   // lanes per matrix
     static constexpr int G = kBlock / LPG;                 // matrices per block
-    static constexpr int LP = NT + 16 / (int)sizeof(T);    // L row pitch: 16-byte skew per row
+    static constexpr int LP = NT;                          // L row pitch (rows are read by broadcast)
     static constexpr int RP = NT + 1;                      // transpose pitch
     static constexpr int per_group = group_stride<T, LPG>(NT * LP + NT * RP + ((NT + 3) / 4) * 4);
     static constexpr size_t bytes = (size_t)G * per_group * sizeof(T);
@@ -258,6 +257,22 @@ small_potrf_adj_kernel(const T* __restrict__ Lg, const T* __restrict__ Lbar,
     int col[CPL];
 #pragma unroll
     for (int q = 0; q < CPL; ++q) col[q] = owned_index(t, q, LPG);
+
+    // When they are short, the lane's rows of adj_A are read now, so their
+    // latency overlaps the solves; otherwise just before they are updated.
+    constexpr bool kEarly = NT * CPL * sizeof(T) <= 64;
+    T old[CPL][NT];
+#pragma unroll
+    for (int q = 0; q < CPL; ++q) {
+        if (!kEarly) break;
+        if (active && col[q] < n) {
+            load_lower_row<T, NT, VEC>(Abar + (size_t)b * n * n + (size_t)col[q] * n, col[q], n,
+                                       old[q]);
+        } else {
+#pragma unroll
+            for (int k = 0; k < NT; ++k) old[q][k] = T(0);
+        }
+    }
 
     // Rows col[q] of L into shared memory (identity rows for padding or
     // skipped matrices) and rows col[q] of tril(adj_L) into the transpose buffer.
@@ -394,8 +409,7 @@ small_potrf_adj_kernel(const T* __restrict__ Lg, const T* __restrict__ Lbar,
         const int row = col[q];
         if (row >= n) return;
         T* rowp = Abar + (size_t)b * n * n + (size_t)row * n;
-        T old[NT];
-        load_lower_row<T, NT, VEC>(rowp, row, n, old);
+        if constexpr (!kEarly) load_lower_row<T, NT, VEC>(rowp, row, n, old[q]);
         if constexpr (VEC) {
             V* vp = reinterpret_cast<V*>(rowp);
             static_for<0, NT / W>([&](auto uc) {
@@ -403,21 +417,22 @@ small_potrf_adj_kernel(const T* __restrict__ Lg, const T* __restrict__ Lbar,
                 if (u * W + W - 1 <= row) {
                     V v;
 #pragma unroll
-                    for (int e = 0; e < W; ++e) vset<T>(v, e, old[u * W + e] + c[q][u * W + e]);
+                    for (int e = 0; e < W; ++e)
+                        vset<T>(v, e, old[q][u * W + e] + c[q][u * W + e]);
                     vp[u] = v;
                 } else if (u * W <= row) {
                     // chunk straddling the diagonal: write only k <= row
 #pragma unroll
                     for (int e = 0; e < W; ++e) {
                         const int k = u * W + e;
-                        if (k <= row) rowp[k] = old[k] + c[q][k];
+                        if (k <= row) rowp[k] = old[q][k] + c[q][k];
                     }
                 }
             });
         } else {
 #pragma unroll
             for (int k = 0; k < NT; ++k)
-                if (k <= row && k < n) rowp[k] = old[k] + c[q][k];
+                if (k <= row && k < n) rowp[k] = old[q][k] + c[q][k];
         }
     });
 }
@@ -431,7 +446,7 @@ constexpr int per_lane() {
 template <typename T, int NT, bool VEC>
 cudaError_t launch_fwd_nt(const T* A, T* L, int32_t* status, int64_t batch, int n,
                           cudaStream_t stream) {
-    constexpr int RPL = per_lane<T, NT>();
+    constexpr int RPL = (NT * (int)sizeof(T) <= 256) ? 2 : 1;
     constexpr int G = kBlock / (NT / RPL);
     const int64_t blocks = (batch + G - 1) / G;
     small_potrf_kernel<T, NT, RPL, VEC><<<(unsigned)blocks, kBlock, 0, stream>>>(A, L, status,
@@ -446,10 +461,12 @@ cudaError_t launch_adj_nt(const T* L, const T* Lbar, T* Abar, const int32_t* sta
     using S = AdjCfg<T, NT, CPL>;
     const int64_t blocks = (batch + S::G - 1) / S::G;
     auto kern = small_potrf_adj_kernel<T, NT, CPL, VEC>;
-    if (S::bytes > 48 * 1024) {
+    static int smem_set = 0;
+    if (S::bytes > 48 * 1024 && !smem_set) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)S::bytes);
         if (e != cudaSuccess) return e;
+        smem_set = 1;
     }
     kern<<<(unsigned)blocks, kBlock, S::bytes, stream>>>(L, Lbar, Abar, status, batch, n);
     return cudaGetLastError();

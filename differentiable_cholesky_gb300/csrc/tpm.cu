@@ -162,17 +162,24 @@ tpm_potrf_kernel(const float* __restrict__ A, float* __restrict__ L, int32_t* __
     bulk_wait_all();
 }
 
+// Persistent grid: resident blocks per SM (queried once per kernel) times the
+// SM count of the current device, capped by the number of rounds.
 template <typename K>
-int tpm_grid(K kern, size_t smem, int64_t rounds) {
-    int dev = 0, sms = 0, per_sm = 0;
+int tpm_grid(K kern, size_t smem, int64_t rounds, int* per_sm_cache) {
+    int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32, smem) != cudaSuccess ||
-        per_sm < 1) {
-        cudaGetLastError();
-        per_sm = 1;
+    if (*per_sm_cache <= 0) {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32, smem) !=
+                cudaSuccess || per_sm < 1) {
+            cudaGetLastError();
+            per_sm = 1;
+        }
+        *per_sm_cache = per_sm;
     }
-    return (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)std::max(sms, 1) * per_sm, rounds));
+    return (int)std::max<int64_t>(
+        1, std::min<int64_t>((int64_t)std::max(sms, 1) * *per_sm_cache, rounds));
 }
 
 template <int N>
@@ -180,9 +187,14 @@ cudaError_t tpm_fwd_n(const float* A, float* L, int32_t* status, int64_t batch,
                       cudaStream_t stream) {
     const size_t smem = kBarBytes + 2 * Tpm<N>::kSlotsBytes;
     auto kern = tpm_potrf_kernel<N>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    const int grid = tpm_grid(kern, smem, (batch + 31) / 32);
+    static int smem_set = 0, per_sm = 0;
+    if (!smem_set) {
+        cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        smem_set = 1;
+    }
+    const int grid = tpm_grid(kern, smem, (batch + 31) / 32, &per_sm);
     kern<<<grid, 32, smem, stream>>>(A, L, status, batch);
     return cudaGetLastError();
 }
