@@ -52,7 +52,7 @@ WORKLOADS = {
     "batched_64": (8192, 64, np.float32,
                    "8192 x 64x64 fp32, A = G G^T/64 + 0.5 I, every 100th matrix non-PD (A[k,k] = -1)", 0),
     "bidiagonal_512": (1, 512, np.float64,
-                       "1 x 512x512 fp64, A = E E^T with E lower bidiagonal (diag linspace(1,2), subdiag 0.5), tile 128", 128),
+                       "1 x 512x512 fp64, A = E E^T with E lower bidiagonal (diag linspace(1,2), subdiag 0.5), default tile", 0),
     "batched_512": (256, 512, np.float64,
                     "256 x 512x512 fp64, A = G G^T/512 + I, tile 128", 128),
     "banded_8192": (1, 8192, np.float64,
@@ -77,9 +77,17 @@ def nominal_flops(n: int):
 
 
 def executed_flops(n: int):
-    """Flops the kernels execute: forward n^3/3; the blocked adjoint's
-    Phi(L^T tril(adj_L)) and two solves, 7 n^3 / 3."""
-    return n ** 3 / 3.0, 7.0 * n ** 3 / 3.0
+    """Flops the blocked kernels execute: forward n^3/3; the adjoint's blocked
+    reverse sweep 2 n^3 / 3 (lower-order terms left out)."""
+    return n ** 3 / 3.0, 2.0 * n ** 3 / 3.0
+
+
+def default_tile(n: int, batch: int) -> int:
+    """The library's default blocked tile (mirrors blocked_default_tile)."""
+    if n >= 2048:
+        return 128
+    per_side = (n + 63) // 64
+    return 64 if batch * per_side * per_side >= 4 * 152 else 32
 
 
 def launches_per_step(n: int, tile: int) -> int:
@@ -88,8 +96,34 @@ def launches_per_step(n: int, tile: int) -> int:
         return 2
     nt = (n + tile - 1) // tile
     fwd = 1 + nt + 2 * (nt - 1)              # copy, diagonal factors, panel solves + updates
-    adj = 1 + 2 * nt + 2 * (nt - 1) + 1      # P, solves and updates for X and M, accumulate
+    # copy, per tile column: solve, row update, panel update, diagonal sweep,
+    # symmetric update (the first and last columns skip some), accumulate
+    adj = 3 if nt == 1 else 5 * nt - 3
     return fwd + adj
+
+
+# DRAM bytes (read + write) per launch of the dominant kernel, from the ncu
+# capture summarised in profiles/batched_16_kernels.md.  Reported only while
+# the kernel source still hashes to what was captured; otherwise null.
+MEASURED_TRAFFIC = {
+    "batched_16": {"kernel": "adj", "bytes": (201.661952 + 24.349184) * 1e6,
+                   "source": "differentiable_cholesky_gb300/csrc/small.cu",
+                   "sha256": "6ee74de0d5e19766100d933e1aa70829d5604cc5ed202579fa6da2dfa0906f5c"},
+}
+
+
+def measured_traffic(workload: str, kernel: str):
+    import hashlib
+    rec = MEASURED_TRAFFIC.get(workload)
+    if rec is None or rec["kernel"] != kernel:
+        return None
+    try:
+        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != rec["sha256"]:
+                return None
+    except OSError:
+        return None
+    return rec["bytes"]
 
 
 def read_peaks():
@@ -235,7 +269,9 @@ def cpu_baseline(w):
 def run_reference(args, w, desc):
     import oracle
     oracle.build()
-    count = oracle_sample_size(w, budget_s=0.5)
+    # a bounded sample per step, sized so the whole run stays within ~2 minutes
+    per_step = max(0.02, min(0.5, 120.0 / max(1, args.steps + args.warmup)))
+    count = oracle_sample_size(w, budget_s=per_step)
     for _ in range(args.warmup):
         time_oracle(w, count)
     times = [time_oracle(w, count) for _ in range(args.steps)]
@@ -415,7 +451,8 @@ def main():
         achieved = adj_gbs if dominant == "adj" else fwd_gbs
         roofline = {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": hbm_peak,
                     "unit": "GB/s", "frac": achieved / hbm_peak,
-                    "peak_source": f"{peak_src} HBM copy bandwidth", "traffic": None}
+                    "peak_source": f"{peak_src} HBM copy bandwidth",
+                    "traffic": measured_traffic(args.workload, dominant)}
     else:
         # FP64 FMA-pipe bound: executed flops per call against the FMA peak
         # measured by the library's probe on this GPU.
@@ -437,7 +474,7 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32" if np_dtype == np.float32 else "f64", "data": "synthetic",
         "config": {"workload": f"{args.workload}: {desc}", "batch_per_gpu": batch, "n": n,
-                   "tile": tile if n > 64 else None,
+                   "tile": (tile or "default") if n > 64 else None,
                    "parallelism": f"independent batches per GPU x{world}" if world > 1 else "1 GPU",
                    "l2": "inputs larger than L2 (256 MiB of distinct buffers per step, two sets alternated)"
                    if batch * n * n * esize * 4 > L2_BYTES else
@@ -445,7 +482,7 @@ def main():
         "gflops": value * (fwd_f + adj_f) / 1e9,
         "kernels": kernels,
         "roofline": roofline,
-        "gpu_launches": launches_per_step(n, tile if n > 64 else 0) * args.steps,
+        "gpu_launches": launches_per_step(n, (tile or default_tile(n, batch)) if n > 64 else 0) * args.steps,
         "e2e": {"value": e2e_value, "unit": UNIT,
                 "h2d_bytes_per_step": int(hA.numel() * esize + hLb.numel() * esize),
                 "d2h_bytes_per_step": int(hL.numel() * esize + hG.numel() * esize + hst.numel() * 4),

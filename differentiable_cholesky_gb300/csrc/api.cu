@@ -77,7 +77,7 @@ int fwd_impl(int64_t batch, int32_t n, const void* A, void* L, int32_t* status, 
         }
         return to_code(chol::small_fwd<T>(a, l, status, batch, n, vec, stream));
     }
-    if (tile == 0) tile = chol::blocked_default_tile(n, (int)sizeof(T));
+    if (tile == 0) tile = chol::blocked_default_tile(n, batch);
     return to_code(chol::blocked_fwd<T>(a, l, status, batch, n, tile, stream));
 }
 
@@ -91,7 +91,7 @@ int adj_impl(int64_t batch, int32_t n, const void* L, const void* Lbar, void* Ab
         const bool vec = vec_ok(n, sizeof(T), {L, Lbar, Abar});
         return to_code(chol::small_adj<T>(l, lb, ab, status, batch, n, vec, stream));
     }
-    if (tile == 0) tile = chol::blocked_default_tile(n, (int)sizeof(T));
+    if (tile == 0) tile = chol::blocked_default_tile(n, batch);
     void* work = nullptr;
     if (cudaMallocAsync(&work, bytes, stream) != cudaSuccess) {
         cudaGetLastError();

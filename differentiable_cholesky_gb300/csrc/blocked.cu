@@ -11,19 +11,12 @@
 //   3. gemm       : trailing update L_ij -= L_ik L_jk^T on the lower tiles.
 // Only step 3 is a dense contraction.
 //
-// Adjoint (Murray 2016 as NVIDIA/warp issue #1316's closing comment states it:
-// S = Phi(L^T adj_L), two triangular solves, accumulation into the lower
-// triangle of adj_A; that comment's accelerated path is GEMM + TRSM with
-// element-wise steps in shared memory, and so is this one), on a workspace W
-// of one n x n matrix per batch entry:
-//   1. gemm (P)   : W_IJ = Phi(sum_{K>=I} L_KI^T tril(adj_L)_KJ), I >= J,
-//                   Phi fused in the epilogue of the diagonal tiles, W_IJ = 0
-//                   for I < J;
-//   2. X = L^-T S : for tile rows I = nt-1 .. 0: trsm solves L_II^T X_I = W_I,
-//                   then gemm W_I' -= L_II'^T X_I for I' < I;
-//   3. M = X L^-1 : for tile columns J = nt-1 .. 0: trsm solves M_J L_JJ = W_J,
-//                   then gemm W_J' -= M_J L_JJ' for J' < J;
-//   4. phi_acc    : adj_A_ij += M_ij + M_ji (i > j), adj_A_ii += M_ii.
+// Adjoint: the symmetric-matrix derivative of Murray (2016) that NVIDIA/warp
+// issue #1316's closing comment states as S = Phi(L^T adj_L) followed by two
+// triangular solves, evaluated here by the same paper's blocked reverse sweep
+// over a left-looking blocked factorisation (see blocked_adj): per tile column
+// a triangular solve, three GEMM-shaped updates and a shared-memory reverse
+// sweep of the diagonal tile, 2 n^3 / 3 flops in all instead of 7 n^3 / 3.
 // Matrices whose status is non-zero are skipped by every kernel.
 //
 // The FP64 path is bound by the FP64 FMA pipe; every kernel keeps each SM's
@@ -121,9 +114,8 @@ potrf_diag_kernel(T* __restrict__ L, int32_t* __restrict__ status, int64_t batch
 // every dot product and combine it with two shuffles.
 // ---------------------------------------------------------------------------
 enum TrsmMode {
-    TRSM_FWD_PANEL = 0,  // rows of L below tile k:  x L_kk^T = b  (G = L_kk, forward)
-    TRSM_ADJ_X = 1,      // columns of W tile row I:  L_II^T x = b  (G = L_II^T, backward)
-    TRSM_ADJ_M = 2       // rows of W tile column J:  m L_JJ = b    (G = L_JJ^T, backward)
+    TRSM_FWD_PANEL = 0,  // rows of L below tile k:        x L_kk^T = b  (G = L_kk, forward)
+    TRSM_ADJ_M = 2       // rows of W below tile column J: m L_JJ = b    (G = L_JJ^T, backward)
 };
 
 constexpr int kVecPerBlock = kThreads / 4;
@@ -153,19 +145,11 @@ trsm_kernel(const T* L, T* W, const int32_t* __restrict__ status,
             else G[c * P + r] = x;
         }
         // right-hand sides
-        if (MODE == TRSM_ADJ_X) {
-            // vectors are columns v0.. of rows [t0, t0 + kb)
-            for (int e = threadIdx.x; e < kb * kVecPerBlock; e += blockDim.x) {
-                const int m = e / kVecPerBlock, v = e % kVecPerBlock;
-                V[v * P + m] = (v < nv) ? Wb[(int64_t)(t0 + m) * n + v0 + v] : T(0);
-            }
-        } else {
-            // vectors are rows v0.. of columns [t0, t0 + kb) (of L itself in
-            // the forward panel, where W == L)
-            for (int e = threadIdx.x; e < kb * kVecPerBlock; e += blockDim.x) {
-                const int v = e / kb, m = e % kb;
-                V[v * P + m] = (v < nv) ? Wb[(int64_t)(v0 + v) * n + t0 + m] : T(0);
-            }
+        // vectors are rows v0.. of columns [t0, t0 + kb) (of L itself in the
+        // forward panel, where W == L)
+        for (int e = threadIdx.x; e < kb * kVecPerBlock; e += blockDim.x) {
+            const int v = e / kb, m = e % kb;
+            V[v * P + m] = (v < nv) ? Wb[(int64_t)(v0 + v) * n + t0 + m] : T(0);
         }
         __syncthreads();
         {
@@ -195,16 +179,9 @@ trsm_kernel(const T* L, T* W, const int32_t* __restrict__ status,
             }
         }
         __syncthreads();
-        if (MODE == TRSM_ADJ_X) {
-            for (int e = threadIdx.x; e < kb * kVecPerBlock; e += blockDim.x) {
-                const int m = e / kVecPerBlock, v = e % kVecPerBlock;
-                if (v < nv) Wb[(int64_t)(t0 + m) * n + v0 + v] = V[v * P + m];
-            }
-        } else {
-            for (int e = threadIdx.x; e < kb * kVecPerBlock; e += blockDim.x) {
-                const int v = e / kb, m = e % kb;
-                if (v < nv) Wb[(int64_t)(v0 + v) * n + t0 + m] = V[v * P + m];
-            }
+        for (int e = threadIdx.x; e < kb * kVecPerBlock; e += blockDim.x) {
+            const int v = e / kb, m = e % kb;
+            if (v < nv) Wb[(int64_t)(v0 + v) * n + t0 + m] = V[v * P + m];
         }
     }
 }
@@ -215,9 +192,6 @@ trsm_kernel(const T* L, T* W, const int32_t* __restrict__ status,
 // ---------------------------------------------------------------------------
 enum GemmMode {
     GEMM_FWD_TRAIL = 0,  // L_ij -= L_ik L_jk^T, k < j <= i
-    GEMM_ADJ_P = 1,      // W_IJ = Phi(sum_{K>=I} L_KI^T tril(adj_L)_KJ) (I >= J); 0 for I < J
-    GEMM_ADJ_XUPD = 2,   // W_I'J -= L_II'^T W_IJ, I' < I, all J
-    GEMM_ADJ_MUPD = 3,   // W_IJ' -= W_IJ L_JJ', all I, J' < J
     // reverse sweep over tile column J = step (see blocked_adj):
     GEMM_REV_ROW = 4,    // W_JK -= Wbar_panel^T L_panel,K  (K <= J; split over the rows below)
     GEMM_REV_UPD = 5,    // W_IK -= W_IJ L_JK  (I > J, K < J)
@@ -246,8 +220,6 @@ struct TileJob {
     int klen;             // length of the reduction
     bool a_trans, b_trans, a_lower, b_lower;
     bool a_sym;           // op(A) is the symmetric matrix A + A^T of a lower tile
-    bool zero_only;       // write zeros (upper tiles of P)
-    bool phi;             // apply Phi (diagonal tile of P)
     float alpha, beta;
 };
 
@@ -273,29 +245,6 @@ __device__ __forceinline__ TileJob make_job(const GemmArgs<T>& g, int tile_id) {
         job.ci = i; job.cj = j;
         job.a_row0 = i * Tt; job.a_col0 = s * Tt; job.a_trans = false;
         job.b_row0 = j * Tt; job.b_col0 = s * Tt; job.b_trans = true;
-        job.klen = min(Tt, g.n - s * Tt);
-        job.alpha = -1.f; job.beta = 1.f;
-    } else if (MODE == GEMM_ADJ_P) {
-        const int I = tile_id / g.nt, J = tile_id % g.nt;
-        job.ci = I; job.cj = J;
-        job.zero_only = I < J;
-        job.phi = I == J;
-        job.a_row0 = I * Tt; job.a_col0 = I * Tt; job.a_trans = true;  job.a_lower = true;
-        job.b_row0 = I * Tt; job.b_col0 = J * Tt; job.b_trans = false; job.b_lower = true;
-        job.klen = g.n - I * Tt;
-        job.alpha = 1.f; job.beta = 0.f;
-    } else if (MODE == GEMM_ADJ_XUPD) {
-        const int Ip = tile_id / g.nt, J = tile_id % g.nt;  // Ip < I = s
-        job.ci = Ip; job.cj = J;
-        job.a_row0 = s * Tt; job.a_col0 = Ip * Tt; job.a_trans = true;
-        job.b_row0 = s * Tt; job.b_col0 = J * Tt;  job.b_trans = false;
-        job.klen = min(Tt, g.n - s * Tt);
-        job.alpha = -1.f; job.beta = 1.f;
-    } else if (MODE == GEMM_ADJ_MUPD) {
-        const int I = tile_id / s, Jp = tile_id % s;  // Jp < J = s
-        job.ci = I; job.cj = Jp;
-        job.a_row0 = I * Tt; job.a_col0 = s * Tt;  job.a_trans = false;
-        job.b_row0 = s * Tt; job.b_col0 = Jp * Tt; job.b_trans = false;
         job.klen = min(Tt, g.n - s * Tt);
         job.alpha = -1.f; job.beta = 1.f;
     } else if (MODE == GEMM_REV_ROW) {
@@ -347,13 +296,6 @@ gemm_kernel(GemmArgs<T> g) {
     for (int64_t b = blockIdx.y; b < g.batch; b += gridDim.y) {
         if (skip_matrix(g.status, b)) continue;
         T* Cb = g.C + b * nn;
-        if (job.zero_only) {
-            for (int e = threadIdx.x; e < BM * BM; e += blockDim.x) {
-                const int r = crow0 + e / BM, c = ccol0 + e % BM;
-                if (r < g.n && c < g.n) Cb[(int64_t)r * g.n + c] = T(0);
-            }
-            continue;
-        }
         const T* Ab = g.A + b * nn;
         const T* Bb = g.B + b * nn;
         T acc[MT][MT];
@@ -431,44 +373,7 @@ gemm_kernel(GemmArgs<T> g) {
                     continue;
                 }
                 if (job.beta != 0.f) v += *cp;
-                if (job.phi) v = (c < r) ? v : (c == r ? v * T(0.5) : T(0));
                 *cp = v;
-            }
-        }
-    }
-}
-
-// ---------------------------------------------------------------------------
-// adj_A_ij += M_ij + M_ji (i > j), adj_A_ii += M_ii, through 32x32 blocks.
-// ---------------------------------------------------------------------------
-template <typename T>
-__global__ void __launch_bounds__(kThreads)
-phi_acc_kernel(const T* __restrict__ W, T* __restrict__ Abar, const int32_t* __restrict__ status,
-               int64_t batch, int n) {
-    __shared__ T Wt[32][33];
-    const int nb = (n + 31) / 32;
-    int bi, bj;
-    lower_index(blockIdx.x, bi, bj);  // bi >= bj
-    if (bi >= nb) return;
-    const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;
-    for (int64_t b = blockIdx.y; b < batch; b += gridDim.y) {
-        if (skip_matrix(status, b)) continue;
-        const T* Wb = W + b * (int64_t)n * n;
-        T* Ab = Abar + b * (int64_t)n * n;
-        __syncthreads();
-        // W block (bj, bi), transposed into Wt[c][r] = W[bj*32 + r][bi*32 + c]
-        for (int r = ty; r < 32; r += kThreads / 32) {
-            const int gr = bj * 32 + r, gc = bi * 32 + tx;
-            Wt[tx][r] = (gr < n && gc < n) ? Wb[(int64_t)gr * n + gc] : T(0);
-        }
-        __syncthreads();
-        for (int r = ty; r < 32; r += kThreads / 32) {
-            const int gi = bi * 32 + r, gj = bj * 32 + tx;
-            if (gi < n && gj < n && gj <= gi) {
-                const int64_t o = (int64_t)gi * n + gj;
-                const T m_ij = Wb[o];
-                const T m_ji = Wt[r][tx];  // = W[gj][gi]
-                Ab[o] += (gj < gi) ? (m_ij + m_ji) : m_ij;
             }
         }
     }
@@ -637,9 +542,13 @@ inline unsigned elementwise_blocks(int64_t total) {
 
 }  // namespace
 
-int blocked_default_tile(int n, int elem_size) {
-    (void)elem_size;
-    return n <= 256 ? 32 : (n <= 1024 ? 64 : 128);
+// Large matrices take 128-wide tiles (fewer, longer GEMMs); below that, 64
+// when the batch alone gives every SM several 64-wide tiles to work on, else
+// 32 so that a few matrices still spread over the GPU.
+int blocked_default_tile(int n, int64_t batch) {
+    if (n >= 2048) return 128;
+    const int64_t per_side = (n + 63) / 64;
+    return batch * per_side * per_side >= 4 * 152 ? 64 : 32;
 }
 
 #define CHOL_TRY(x)                              \

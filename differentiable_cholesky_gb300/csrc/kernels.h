@@ -32,6 +32,6 @@ template <typename T>
 cudaError_t blocked_adj(const T* L, const T* Lbar, T* Abar, const int32_t* status,
                         int64_t batch, int n, int tile, T* work, cudaStream_t stream);
 
-int blocked_default_tile(int n, int elem_size);
+int blocked_default_tile(int n, int64_t batch);
 
 }  // namespace chol

@@ -96,7 +96,7 @@ int run(int64_t batch, int32_t n, const void* L, const void* Lbar, void* Abar,
     if (need > kScratchBytes) return CHOL_ENOMEM;
     void* work = scratch_on_current_device();
     if (work == nullptr) return CHOL_ECUDA;
-    if (tile == 0) tile = chol::blocked_default_tile(n, (int)sizeof(T));
+    if (tile == 0) tile = chol::blocked_default_tile(n, batch);
     e = chol::blocked_adj<T>(l, lb, ab, status, batch, n, tile, static_cast<T*>(work), stream);
     return e == cudaSuccess ? CHOL_OK : CHOL_ECUDA;
 }

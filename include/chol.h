@@ -73,7 +73,8 @@ enum {
  *                from column j on is unspecified.
  * n <= 64 runs one fused register/shared-memory kernel per batch; larger n
  * runs the blocked right-looking algorithm (diagonal-tile factor, panel
- * triangular solve, trailing update) with the default tile.
+ * triangular solve, trailing update) with the default tile: 128 for
+ * n >= 2048, else 64 when batch * ceil(n/64)^2 >= 608, else 32.
  */
 CHOL_API int chol_fwd(int64_t batch, int32_t n, int32_t dtype, const void* A, void* L,
              int32_t* status, void* stream);
