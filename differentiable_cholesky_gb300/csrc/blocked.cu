@@ -89,14 +89,19 @@ potrf_diag_kernel(T* __restrict__ L, int32_t* __restrict__ status, int64_t batch
                 break;
             }
             const T ljj = sqrt_t(d);
-            __syncthreads();  // every thread has read the pivot
-            for (int i = j + 1 + threadIdx.x; i < kb; i += blockDim.x) S[i * P + j] = S[i * P + j] / ljj;
+            const T inv = rcp_t(ljj);  // one reciprocal per column, then products
+            __syncthreads();           // every thread has read the pivot
+            for (int i = j + 1 + threadIdx.x; i < kb; i += blockDim.x) S[i * P + j] *= inv;
             if (threadIdx.x == 0) S[j * P + j] = ljj;
             __syncthreads();
-            const int m = kb - j - 1;
-            for (int e = threadIdx.x; e < m * m; e += blockDim.x) {
-                const int i = j + 1 + e / m, c = j + 1 + e % m;
-                if (c <= i) S[i * P + c] = fma(-S[i * P + j], S[c * P + j], S[i * P + c]);
+            // trailing update of the lower part, 16 x 16 threads over (i, c)
+            {
+                const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
+                for (int i = j + 1 + ty; i < kb; i += kThreads / 16) {
+                    const T lij = S[i * P + j];
+                    for (int c = j + 1 + tx; c <= i; c += 16)
+                        S[i * P + c] = fma(-lij, S[c * P + j], S[i * P + c]);
+                }
             }
             __syncthreads();
         }
@@ -128,6 +133,7 @@ trsm_kernel(const T* L, T* W, const int32_t* __restrict__ status,
     const int P = kb + 1;
     T* G = reinterpret_cast<T*>(smem_raw);          // kb x P
     T* V = G + (size_t)kb * P;                      // kVecPerBlock x P
+    T* ginv = V + (size_t)kVecPerBlock * P;         // kb reciprocals of G's diagonal
     const int vloc = threadIdx.x >> 2;
     const int q = threadIdx.x & 3;
     const int v0 = v_begin + blockIdx.x * kVecPerBlock;
@@ -152,6 +158,8 @@ trsm_kernel(const T* L, T* W, const int32_t* __restrict__ status,
             V[v * P + m] = (v < nv) ? Wb[(int64_t)(v0 + v) * n + t0 + m] : T(0);
         }
         __syncthreads();
+        for (int c = threadIdx.x; c < kb; c += blockDim.x) ginv[c] = rcp_t(G[c * P + c]);
+        __syncthreads();
         {
             // every group runs the same sweep (idle groups on zero vectors
             // that are not stored), so the warp's shuffles stay convergent
@@ -163,7 +171,7 @@ trsm_kernel(const T* L, T* W, const int32_t* __restrict__ status,
                     for (int m = q; m < c; m += 4) s = fma(g[m], x[m], s);
                     s += __shfl_xor_sync(0xffffffffu, s, 1);
                     s += __shfl_xor_sync(0xffffffffu, s, 2);
-                    if (q == 0) x[c] = (x[c] - s) / g[c];
+                    if (q == 0) x[c] = (x[c] - s) * ginv[c];
                     __syncwarp();
                 }
             } else {
@@ -173,7 +181,7 @@ trsm_kernel(const T* L, T* W, const int32_t* __restrict__ status,
                     for (int m = c + 1 + q; m < kb; m += 4) s = fma(g[m], x[m], s);
                     s += __shfl_xor_sync(0xffffffffu, s, 1);
                     s += __shfl_xor_sync(0xffffffffu, s, 2);
-                    if (q == 0) x[c] = (x[c] - s) / g[c];
+                    if (q == 0) x[c] = (x[c] - s) * ginv[c];
                     __syncwarp();
                 }
             }
@@ -380,7 +388,7 @@ gemm_kernel(GemmArgs<T> g) {
 }
 
 size_t trsm_smem(int kb, int esize) {
-    return (size_t)(kb + kVecPerBlock) * (kb + 1) * esize;
+    return ((size_t)(kb + kVecPerBlock) * (kb + 1) + kb) * esize;
 }
 
 // Raise a kernel's dynamic shared-memory limit once, to the largest size any
@@ -486,11 +494,12 @@ diag_rev_kernel(const T* __restrict__ L, T* __restrict__ W, const int32_t* __res
                 Ws[tri(j, k)] -= acc;
             }
             // rows below, left of column j: W_ik -= W_ij L_jk
-            if (j > 0) {
-                const int m = kb - 1 - j;
-                for (int e = tid; e < m * j; e += blockDim.x) {
-                    const int i = j + 1 + e / j, k = e % j;
-                    Ws[tri(i, k)] = fma(-Ws[tri(i, j)], Ls[tri(j, k)], Ws[tri(i, k)]);
+            {
+                const int ty = tid / 16, tx = tid % 16;
+                for (int i = j + 1 + ty; i < kb; i += kThreads / 16) {
+                    const T wij = Ws[tri(i, j)];
+                    for (int k = tx; k < j; k += 16)
+                        Ws[tri(i, k)] = fma(-wij, Ls[tri(j, k)], Ws[tri(i, k)]);
                 }
             }
             __syncthreads();
