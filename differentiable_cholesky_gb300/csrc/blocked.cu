@@ -64,8 +64,8 @@ tril_copy_kernel(const T* __restrict__ A, T* __restrict__ L, int32_t* __restrict
 // ---------------------------------------------------------------------------
 // Diagonal tile factor (one block per matrix), in shared memory.
 // ---------------------------------------------------------------------------
-template <typename T>
-__global__ void __launch_bounds__(kThreads)
+template <typename T, int THREADS>
+__global__ void __launch_bounds__(THREADS)
 potrf_diag_kernel(T* __restrict__ L, int32_t* __restrict__ status, int64_t batch, int n,
                   int k0, int kb) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -97,7 +97,7 @@ potrf_diag_kernel(T* __restrict__ L, int32_t* __restrict__ status, int64_t batch
             // trailing update of the lower part, 16 x 16 threads over (i, c)
             {
                 const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
-                for (int i = j + 1 + ty; i < kb; i += kThreads / 16) {
+                for (int i = j + 1 + ty; i < kb; i += THREADS / 16) {
                     const T lij = S[i * P + j];
                     for (int c = j + 1 + tx; c <= i; c += 16)
                         S[i * P + c] = fma(-lij, S[c * P + j], S[i * P + c]);
@@ -447,15 +447,15 @@ cudaError_t launch_gemm(GemmArgs<T> g, int tiles, cudaStream_t stream, int kspli
 // Packed lower-triangle index (i >= j).
 __device__ __forceinline__ int tri(int i, int j) { return i * (i + 1) / 2 + j; }
 
-template <typename T>
-__global__ void __launch_bounds__(kThreads)
+template <typename T, int THREADS>
+__global__ void __launch_bounds__(THREADS)
 diag_rev_kernel(const T* __restrict__ L, T* __restrict__ W, const int32_t* __restrict__ status,
                 int64_t batch, int n, int j0, int kb) {
     // both tiles packed as lower triangles: kb (kb + 1) elements in all
     extern __shared__ __align__(16) unsigned char smem_raw[];
     T* Ls = reinterpret_cast<T*>(smem_raw);
     T* Ws = Ls + (size_t)kb * (kb + 1) / 2;
-    __shared__ T red[kThreads / 32];
+    __shared__ T red[THREADS / 32];
     const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
     for (int64_t b = blockIdx.y; b < batch; b += gridDim.y) {
         if (skip_matrix(status, b)) continue;
@@ -481,7 +481,7 @@ diag_rev_kernel(const T* __restrict__ L, T* __restrict__ W, const int32_t* __res
             __syncthreads();
             T sum = T(0);
 #pragma unroll
-            for (int w = 0; w < kThreads / 32; ++w) sum += red[w];
+            for (int w = 0; w < THREADS / 32; ++w) sum += red[w];
             const T inv = T(1) / Ls[tri(j, j)];
             // column j: diagonal from the sum, the rest scaled
             for (int i = j + 1 + tid; i < kb; i += blockDim.x) Ws[tri(i, j)] *= inv;
@@ -496,7 +496,7 @@ diag_rev_kernel(const T* __restrict__ L, T* __restrict__ W, const int32_t* __res
             // rows below, left of column j: W_ik -= W_ij L_jk
             {
                 const int ty = tid / 16, tx = tid % 16;
-                for (int i = j + 1 + ty; i < kb; i += kThreads / 16) {
+                for (int i = j + 1 + ty; i < kb; i += THREADS / 16) {
                     const T wij = Ws[tri(i, j)];
                     for (int k = tx; k < j; k += 16)
                         Ws[tri(i, k)] = fma(-wij, Ls[tri(j, k)], Ws[tri(i, k)]);
@@ -578,12 +578,19 @@ cudaError_t blocked_fwd(const T* A, T* L, int32_t* status, int64_t batch, int n,
         CHOL_TRY(cudaGetLastError());
     }
     static int diag_smem_set = 0;
-    CHOL_TRY(allow_smem(potrf_diag_kernel<T>, (size_t)128 * 129 * sizeof(T), &diag_smem_set));
+    CHOL_TRY(allow_smem(potrf_diag_kernel<T, kThreads>, (size_t)128 * 129 * sizeof(T),
+                        &diag_smem_set));
     for (int k = 0; k < nt; ++k) {
         const int k0 = k * tile;
         const int kb = std::min(tile, n - k0);
-        potrf_diag_kernel<T><<<dim3(1, grid_y(batch)), kThreads, (size_t)kb * (kb + 1) * sizeof(T),
-                               stream>>>(L, status, batch, n, k0, kb);
+        // small tiles: two warps, so the per-column barriers stay cheap
+        const size_t dsm = (size_t)kb * (kb + 1) * sizeof(T);
+        if (kb <= 32)
+            potrf_diag_kernel<T, 64><<<dim3(1, grid_y(batch)), 64, dsm, stream>>>(L, status, batch,
+                                                                                 n, k0, kb);
+        else
+            potrf_diag_kernel<T, kThreads><<<dim3(1, grid_y(batch)), kThreads, dsm, stream>>>(
+                L, status, batch, n, k0, kb);
         CHOL_TRY(cudaGetLastError());
         if (k == nt - 1) break;
         CHOL_TRY((launch_trsm<T, TRSM_FWD_PANEL>(L, L, status, batch, n, k0, kb, k0 + kb,
@@ -615,7 +622,8 @@ cudaError_t blocked_adj(const T* L, const T* Lbar, T* Abar, const int32_t* statu
                                                                             batch, n);
     CHOL_TRY(cudaGetLastError());
     static int diag_smem_set = 0;
-    CHOL_TRY(allow_smem(diag_rev_kernel<T>, (size_t)128 * 129 * sizeof(T), &diag_smem_set));
+    CHOL_TRY(allow_smem(diag_rev_kernel<T, kThreads>, (size_t)128 * 129 * sizeof(T),
+                        &diag_smem_set));
     int sms = 152;
     {
         int dev = 0;
@@ -637,8 +645,13 @@ cudaError_t blocked_adj(const T* L, const T* Lbar, T* Abar, const int32_t* statu
             CHOL_TRY((launch_gemm<T, GEMM_REV_ROW>(g, J + 1, stream, ks, nb)));
             if (J > 0) CHOL_TRY((launch_gemm<T, GEMM_REV_UPD>(g, (nt - J - 1) * J, stream)));
         }
-        diag_rev_kernel<T><<<dim3(1, grid_y(batch)), kThreads, (size_t)kb * (kb + 1) * sizeof(T),
-                             stream>>>(L, W, status, batch, n, j0, kb);
+        const size_t dsm = (size_t)kb * (kb + 1) * sizeof(T);
+        if (kb <= 32)
+            diag_rev_kernel<T, 64><<<dim3(1, grid_y(batch)), 64, dsm, stream>>>(L, W, status, batch,
+                                                                              n, j0, kb);
+        else
+            diag_rev_kernel<T, kThreads><<<dim3(1, grid_y(batch)), kThreads, dsm, stream>>>(
+                L, W, status, batch, n, j0, kb);
         CHOL_TRY(cudaGetLastError());
         if (J > 0) {
             GemmArgs<T> g{W, L, W, status, batch, n, tile, nt, J, 0, 0};

@@ -201,12 +201,49 @@ small_potrf_kernel(const T* __restrict__ A, T* __restrict__ L, int32_t* __restri
 // CPL columns (and, after the transpose, CPL rows): columns t and NT-1-t for
 // CPL = 2, which balances the triangular work.  Every broadcast read of a row
 // of L then feeds CPL columns.
+
+// Row r[0..NT) to / from a 16-byte aligned shared-memory row, as vectors.
+template <typename T, int NT>
+__device__ __forceinline__ void store_row(T* dst, const T (&r)[NT]) {
+    using V = typename Vec16<T>::type;
+    constexpr int W = Vec16<T>::N;
+#pragma unroll
+    for (int u = 0; u < NT / W; ++u) {
+        V v;
+#pragma unroll
+        for (int e = 0; e < W; ++e) vset<T>(v, e, r[u * W + e]);
+        reinterpret_cast<V*>(dst)[u] = v;
+    }
+}
+template <typename T, int NT>
+__device__ __forceinline__ void load_row(const T* src, T (&r)[NT]) {
+    using V = typename Vec16<T>::type;
+    constexpr int W = Vec16<T>::N;
+#pragma unroll
+    for (int u = 0; u < NT / W; ++u) {
+        const V v = reinterpret_cast<const V*>(src)[u];
+#pragma unroll
+        for (int e = 0; e < W; ++e) r[u * W + e] = vget<T>(v, e);
+    }
+}
+
+// Phi's factor for row i of column col: 1 below the diagonal, 1/2 on it,
+// 0 above; and the strict-lower indicator k < col.  float uses one saturated
+// add each; double compares.
+__device__ __forceinline__ float phi_factor(int i, float colf) {
+    return __saturatef((float(i) + 0.5f) - colf);
+}
+__device__ __forceinline__ float below(int k, float colf) { return __saturatef(colf - float(k)); }
+
+template <typename T, int NT, int CPL>
+struct AdjCfg;
+
 template <typename T, int NT, int CPL>
 struct AdjCfg {
     static constexpr int LPG = NT / CPL;                   // lanes per matrix
     static constexpr int G = kBlock / LPG;                 // matrices per block
     static constexpr int LP = NT;                          // L row pitch (rows are read by broadcast)
-    static constexpr int RP = NT + 1;                      // transpose pitch
+    static constexpr int RP = NT + 16 / (int)sizeof(T);    // transpose pitch (16-byte rows)
     static constexpr int per_group = group_stride<T, LPG>(NT * LP + NT * RP + ((NT + 3) / 4) * 4);
     static constexpr size_t bytes = (size_t)G * per_group * sizeof(T);
 };
@@ -288,8 +325,7 @@ small_potrf_adj_kernel(const T* __restrict__ Lg, const T* __restrict__ Lbar,
             reinterpret_cast<V*>(Ls + (size_t)col[q] * LP)[u] = v;
         }
         fetch_adj_row<T, NT, VEC>(Lbar, active, b, col[q], n, T(0), r);
-#pragma unroll
-        for (int k = 0; k < NT; ++k) R[col[q] * RP + k] = r[k];
+        store_row<T, NT>(R + col[q] * RP, r);
     }
     lanes_sync<LPG>(g);
 #pragma unroll
@@ -327,15 +363,22 @@ small_potrf_adj_kernel(const T* __restrict__ Lg, const T* __restrict__ Lbar,
     // (a factor rather than a select: a select chain on a lane-dependent index
     //  is turned into an indexed store, which moves c out of registers)
 #pragma unroll
-    for (int q = 0; q < CPL; ++q)
+    for (int q = 0; q < CPL; ++q) {
+        const float colf = float(col[q]);
 #pragma unroll
-        for (int i = 0; i < NT; ++i) c[q][i] *= T(0.5) * (T(i > col[q]) + T(i >= col[q]));
+        for (int i = 0; i < NT; ++i) c[q][i] *= T(phi_factor(i, colf));
+    }
     lanes_sync<LPG>(g);  // rinv visible to the group
+    // the reciprocals in registers when they are few, else read as used
+    constexpr bool kRv = NT * sizeof(T) <= 64;
+    T rv[kRv ? NT : 1];
+    if constexpr (kRv) load_row<T, NT>(rinv, rv);
 
     // 3. X = L^-T S (back substitution, rows of L broadcast).
     static_for<0, NT>([&](auto ic) {
         constexpr int i = NT - 1 - decltype(ic)::value;
-        const T ri = rinv[i];
+        T ri;
+        if constexpr (kRv) ri = rv[i]; else ri = rinv[i];
         T xi[CPL];
 #pragma unroll
         for (int q = 0; q < CPL; ++q) {
@@ -363,14 +406,13 @@ small_potrf_adj_kernel(const T* __restrict__ Lg, const T* __restrict__ Lbar,
         for (int i = 0; i < NT; ++i) R[i * RP + col[q]] = c[q][i];
     lanes_sync<LPG>(g);
 #pragma unroll
-    for (int q = 0; q < CPL; ++q)
-#pragma unroll
-        for (int k = 0; k < NT; ++k) c[q][k] = R[col[q] * RP + k];
+    for (int q = 0; q < CPL; ++q) load_row<T, NT>(R + col[q] * RP, c[q]);
 
     // 5. M = X L^-1 (back substitution on the rows).
     static_for<0, NT>([&](auto jc) {
         constexpr int j = NT - 1 - decltype(jc)::value;
-        const T rj = rinv[j];
+        T rj;
+        if constexpr (kRv) rj = rv[j]; else rj = rinv[j];
         T mj[CPL];
 #pragma unroll
         for (int q = 0; q < CPL; ++q) {
@@ -394,14 +436,14 @@ small_potrf_adj_kernel(const T* __restrict__ Lg, const T* __restrict__ Lbar,
     // 6. Phi(M + M^T) into rows col[q] of adj_A's lower triangle.  Each lane
     //    only rewrites the rows it has read.
 #pragma unroll
-    for (int q = 0; q < CPL; ++q)
-#pragma unroll
-        for (int k = 0; k < NT; ++k) R[col[q] * RP + k] = c[q][k];
+    for (int q = 0; q < CPL; ++q) store_row<T, NT>(R + col[q] * RP, c[q]);
     lanes_sync<LPG>(g);
 #pragma unroll
-    for (int q = 0; q < CPL; ++q)
+    for (int q = 0; q < CPL; ++q) {
+        const float colf = float(col[q]);
 #pragma unroll
-        for (int k = 0; k < NT; ++k) c[q][k] += T(k < col[q]) * R[k * RP + col[q]];
+        for (int k = 0; k < NT; ++k) c[q][k] = fma(T(below(k, colf)), R[k * RP + col[q]], c[q][k]);
+    }
 
     if (!active) return;
     static_for<0, CPL>([&](auto qc) {
