@@ -240,8 +240,11 @@ struct AdjCfg;
 
 template <typename T, int NT, int CPL>
 struct AdjCfg {
+    // short matrices run in 64-thread blocks: more, smaller blocks per SM hide
+    // the global-load latency at their start and end better
+    static constexpr int BLOCK = NT <= 16 ? 64 : kBlock;
     static constexpr int LPG = NT / CPL;                   // lanes per matrix
-    static constexpr int G = kBlock / LPG;                 // matrices per block
+    static constexpr int G = BLOCK / LPG;                  // matrices per block
     static constexpr int LP = NT;                          // L row pitch (rows are read by broadcast)
     static constexpr int RP = NT + 16 / (int)sizeof(T);    // transpose pitch (16-byte rows)
     static constexpr int per_group = group_stride<T, LPG>(NT * LP + NT * RP + ((NT + 3) / 4) * 4);
@@ -271,7 +274,7 @@ __device__ __forceinline__ void fetch_adj_row(const T* __restrict__ src, bool ac
 }
 
 template <typename T, int NT, int CPL, bool VEC>
-__global__ void __launch_bounds__(kBlock)
+__global__ void __launch_bounds__(AdjCfg<T, NT, CPL>::BLOCK)
 small_potrf_adj_kernel(const T* __restrict__ Lg, const T* __restrict__ Lbar,
                        T* __restrict__ Abar, const int32_t* __restrict__ status,
                        int64_t batch, int n) {
@@ -313,19 +316,28 @@ small_potrf_adj_kernel(const T* __restrict__ Lg, const T* __restrict__ Lbar,
 
     // Rows col[q] of L into shared memory (identity rows for padding or
     // skipped matrices) and rows col[q] of tril(adj_L) into the transpose buffer.
+    if constexpr (NT * CPL * sizeof(T) <= 128) {
+        // short rows: all of the lane's row loads are issued before any store
+        T lr[CPL][NT], br[CPL][NT];
 #pragma unroll
-    for (int q = 0; q < CPL; ++q) {
-        T r[NT];
-        fetch_adj_row<T, NT, VEC>(Lg, active, b, col[q], n, T(1), r);
-#pragma unroll
-        for (int u = 0; u < NT / W; ++u) {
-            V v;
-#pragma unroll
-            for (int e = 0; e < W; ++e) vset<T>(v, e, r[u * W + e]);
-            reinterpret_cast<V*>(Ls + (size_t)col[q] * LP)[u] = v;
+        for (int q = 0; q < CPL; ++q) {
+            fetch_adj_row<T, NT, VEC>(Lg, active, b, col[q], n, T(1), lr[q]);
+            fetch_adj_row<T, NT, VEC>(Lbar, active, b, col[q], n, T(0), br[q]);
         }
-        fetch_adj_row<T, NT, VEC>(Lbar, active, b, col[q], n, T(0), r);
-        store_row<T, NT>(R + col[q] * RP, r);
+#pragma unroll
+        for (int q = 0; q < CPL; ++q) {
+            store_row<T, NT>(Ls + (size_t)col[q] * LP, lr[q]);
+            store_row<T, NT>(R + col[q] * RP, br[q]);
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < CPL; ++q) {
+            T r[NT];
+            fetch_adj_row<T, NT, VEC>(Lg, active, b, col[q], n, T(1), r);
+            store_row<T, NT>(Ls + (size_t)col[q] * LP, r);
+            fetch_adj_row<T, NT, VEC>(Lbar, active, b, col[q], n, T(0), r);
+            store_row<T, NT>(R + col[q] * RP, r);
+        }
     }
     lanes_sync<LPG>(g);
 #pragma unroll
@@ -503,6 +515,7 @@ cudaError_t launch_adj_nt(const T* L, const T* Lbar, T* Abar, const int32_t* sta
     using S = AdjCfg<T, NT, CPL>;
     const int64_t blocks = (batch + S::G - 1) / S::G;
     auto kern = small_potrf_adj_kernel<T, NT, CPL, VEC>;
+    constexpr int kThreadsPerBlock = S::BLOCK;
     static int smem_set = 0;
     if (S::bytes > 48 * 1024 && !smem_set) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -510,7 +523,7 @@ cudaError_t launch_adj_nt(const T* L, const T* Lbar, T* Abar, const int32_t* sta
         if (e != cudaSuccess) return e;
         smem_set = 1;
     }
-    kern<<<(unsigned)blocks, kBlock, S::bytes, stream>>>(L, Lbar, Abar, status, batch, n);
+    kern<<<(unsigned)blocks, kThreadsPerBlock, S::bytes, stream>>>(L, Lbar, Abar, status, batch, n);
     return cudaGetLastError();
 }
 

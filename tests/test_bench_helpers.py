@@ -1,0 +1,53 @@
+"""bench.py's accounting (CPU only): algorithmic bytes, launch counts, the
+reported-traffic gate, and the oracle reference arm's JSON line."""
+import json
+import subprocess
+import sys
+import os
+
+import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_lower_sector_bytes_and_algorithmic_bytes():
+    # 16x16 fp32: rows 0-7 need one 32-byte sector, rows 8-15 two
+    assert bench.lower_sector_bytes(16, 4) == 8 * 32 + 8 * 64
+    fwd, adj = bench.algorithmic_bytes(16, 4)
+    assert fwd == 768 + 1024 + 4 and adj == 4 * 768 + 4
+    assert bench.algorithmic_bytes(64, 4) == (25604, 36868)
+    assert bench.lower_sector_bytes(512, 8) == 1056768
+
+
+def test_launch_counts():
+    assert bench.launches_per_step(16, 0) == 2
+    # nt = 4: forward 1 + 4 + 6, adjoint 5 * 4 - 3
+    assert bench.launches_per_step(512, 128) == 11 + 17
+    assert bench.launches_per_step(100, 128) == 1 + 1 + 0 + 3
+
+
+def test_default_tile_mirrors_the_library_rule():
+    assert bench.default_tile(8192, 1) == 128
+    assert bench.default_tile(512, 1) == 32
+    assert bench.default_tile(512, 256) == 64
+
+
+def test_traffic_is_reported_only_for_the_captured_kernel_source():
+    rec = bench.MEASURED_TRAFFIC["batched_16"]
+    got = bench.measured_traffic("batched_16", rec["kernel"])
+    assert got is None or got == rec["bytes"]
+    assert bench.measured_traffic("batched_16", "fwd" if rec["kernel"] == "adj" else "adj") is None
+    assert bench.measured_traffic("banded_8192", "adj") is None
+
+
+def test_reference_arm_prints_one_json_line():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--steps", "2", "--warmup", "3"], capture_output=True, text=True,
+                         timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr
+    lines = [l for l in out.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "matrices/s" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle"
+    assert d["e2e"]["h2d_bytes_per_step"] == 0
