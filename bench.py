@@ -107,7 +107,7 @@ def launches_per_step(n: int, tile: int) -> int:
 # the kernel source still hashes to what was captured; otherwise null.
 MEASURED_TRAFFIC = {
     "batched_16": {"kernel": "adj", "bytes": (201.631744 + 24.965376) * 1e6,
-                   "source": "differentiable_cholesky_gb300/csrc/small.cu",
+                   "source": "differentiable_cholesky_gb300/csrc/small_kernels.cuh",
                    "sha256": "43ae7516aa3060fddd7d3f10732ba508d6cb3f1c153859baab48d3926d06470c"},
 }
 

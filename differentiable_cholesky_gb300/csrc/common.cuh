@@ -146,6 +146,13 @@ __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Bring `bytes` of global memory into L2 without waiting for them (a hint:
+// nothing is written and no completion is tracked).  Address 16-byte aligned,
+// bytes a multiple of 16.
+__device__ __forceinline__ void l2_prefetch(const void* gmem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gmem), "r"(bytes) : "memory");
+}
+
 // Order generic-proxy shared-memory accesses before later async-proxy ones.
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

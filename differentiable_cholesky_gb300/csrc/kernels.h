@@ -18,6 +18,15 @@ template <typename T>
 cudaError_t small_adj(const T* L, const T* Lbar, T* Abar, const int32_t* status, int64_t batch,
                       int n, bool vec, cudaStream_t stream);
 
+// The same for one padded order NT (8, 16, 32 or 64, n <= NT) and access mode
+// (VEC: 16-byte vectors).
+template <typename T, int NT, bool VEC>
+cudaError_t small_fwd_nt(const T* A, T* L, int32_t* status, int64_t batch, int n,
+                         cudaStream_t stream);
+template <typename T, int NT, bool VEC>
+cudaError_t small_adj_nt(const T* L, const T* Lbar, T* Abar, const int32_t* status,
+                         int64_t batch, int n, cudaStream_t stream);
+
 // Thread-per-matrix float32 forward for n in {8, 16}; A and L 16-byte aligned.
 bool tpm_supported(int n);
 cudaError_t tpm_fwd(const float* A, float* L, int32_t* status, int64_t batch, int n,

@@ -1,0 +1,9 @@
+// Small-path adjoint kernel for double matrices of padded order 64,
+// scalar accesses.
+#include "small_kernels.cuh"
+
+namespace chol {
+
+CHOL_SMALL_ADJ(double, 64, false)
+
+}  // namespace chol

@@ -1,0 +1,589 @@
+// Kernels of the small path (n <= 64): included by the translation units
+// that instantiate them, one per element type and padded order, so that
+// they compile in parallel.
+//
+// Batched Cholesky forward and adjoint for small matrices (n <= 64).
+//
+// A group of LPG lanes owns one matrix of padded order NT = 8, 16, 32 or 64
+// (the next size >= n); each lane owns two rows (or columns) of it, t and
+// NT-1-t, where registers allow (LPG = NT / 2), else one.  A 128-thread block
+// holds 128 / LPG groups.  A matrix of order n < NT is padded to
+// blockdiag(A, I), whose factor is blockdiag(L, I) and whose adjoint (with a
+// zero-padded adj_L) is blockdiag(adj_A, 0): the padding changes no result.
+// Every loop over matrix indices is fully unrolled, so each lane keeps its
+// rows (or columns) in registers.
+//
+// Forward (jaxmg docs "Cholesky factorization": lower factor and status;
+// NVIDIA/warp issue #1316: out-of-place tile factor, one block per tile).
+//   Right-looking column recurrence, one group barrier per column: at step j
+//   every lane publishes its current a_ij to a double-buffered shared column,
+//   then reads the pivot d = a_jj, computes r = 1/sqrt(d) itself (no second
+//   broadcast), sets l_ij = a_ij * r and updates its trailing entries
+//   a_ik -= (l_ij r) a_kj.  A pivot that is not > 0 records status j + 1
+//   (first failure only) and is replaced by 1 so the rest of the (unspecified)
+//   factor stays finite and the group stays convergent.
+//
+// Adjoint (Murray 2016 as NVIDIA/warp issue #1316's closing comment states it:
+// S = Phi(L^T adj_L), then solves against L^T and L, accumulated into the lower
+// triangle of adj_A).  L is staged in shared memory and read by broadcast.
+//   1. each lane takes its columns of tril(adj_L) and forms the same columns
+//      of P = L^T tril(adj_L) in place (outer-product order over rows of L);
+//   2. S = Phi(P) on those columns;
+//   3. X = L^-T S: back substitution on the columns (rows of L broadcast);
+//   4. transpose through shared memory: the lane takes the same rows of X;
+//   5. M = X L^-1: back substitution on the rows (rows of L broadcast);
+//   6. transpose once more and add M_tk + M_kt (k < t) and M_tt into the
+//      lane's rows of adj_A's lower triangle.  Matrices with status != 0 are
+//      skipped.
+
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace chol {
+namespace {
+
+constexpr int kBlock = 128;
+
+// Load the lower part of row `row` (row < n) into r[0..NT): zeros above the
+// diagonal.  Only the 16-byte chunks that hold lower-triangle elements are read.
+template <typename T, int NT, bool VEC>
+__device__ __forceinline__ void load_lower_row(const T* __restrict__ rowp, int row, int n,
+                                               T (&r)[NT]) {
+    if constexpr (VEC) {
+        using V = typename Vec16<T>::type;
+        constexpr int W = Vec16<T>::N;
+        const V* vp = reinterpret_cast<const V*>(rowp);
+#pragma unroll
+        for (int c = 0; c < NT / W; ++c) {
+            V v;
+            if (c * W <= row) {
+                v = __ldg(vp + c);
+            } else {
+                v = V{};
+            }
+#pragma unroll
+            for (int e = 0; e < W; ++e) r[c * W + e] = (c * W + e <= row) ? vget<T>(v, e) : T(0);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < NT; ++k) r[k] = (k <= row && k < n) ? __ldg(rowp + k) : T(0);
+    }
+}
+
+// Element offset that shifts a group's shared-memory region by NT 4-byte
+// words modulo 32 banks, so the groups that share a warp (NT < 32) never hit
+// the same bank with their broadcast reads.
+template <typename T, int NT>
+__host__ __device__ constexpr int group_stride(int base_elems) {
+    constexpr int wpe = (int)sizeof(T) / 4;  // words per element
+    const int words = base_elems * wpe;
+    const int target = NT < 32 ? NT : 0;
+    const int pad_words = ((target - words % 32) % 32 + 32) % 32;
+    return base_elems + pad_words / wpe;
+}
+
+// Row `row` of matrix b for the forward: lower part of A, or an identity row
+// for padding rows and for slots past the end of the batch.
+template <typename T, int NT, bool VEC>
+__device__ __forceinline__ void fetch_fwd_row(const T* __restrict__ A, int64_t b, int64_t batch,
+                                              int row, int n, T (&r)[NT]) {
+    if (b < batch && row < n) {
+        load_lower_row<T, NT, VEC>(A + (size_t)b * n * n + (size_t)row * n, row, n, r);
+    } else {
+#pragma unroll
+        for (int k = 0; k < NT; ++k) r[k] = (k == row) ? T(1) : T(0);
+    }
+}
+
+// Lanes per matrix LPG = NT / RPL: each lane owns RPL rows, t and NT-1-t for
+// RPL = 2 (balanced triangle rows).  Every broadcast read of the published
+// column then feeds RPL rows.
+__host__ __device__ constexpr int owned_index(int t, int q, int lpg) {
+    return (q & 1) ? (q + 1) * lpg - 1 - t : q * lpg + t;
+}
+
+template <int LPG>
+__device__ __forceinline__ void lanes_sync(int group) {
+    if constexpr (LPG <= 32) {
+        __syncwarp();
+    } else {
+        // Named barrier per group of LPG (a multiple of 32) threads; id 0 is
+        // __syncthreads.
+        asm volatile("bar.sync %0, %1;" ::"r"(1 + group), "r"(LPG) : "memory");
+    }
+}
+
+template <typename T, int NT, int RPL, bool VEC>
+__global__ void __launch_bounds__(kBlock)
+small_potrf_kernel(const T* __restrict__ A, T* __restrict__ L, int32_t* __restrict__ status,
+                   int64_t batch, int n) {
+    constexpr int LPG = NT / RPL;
+    constexpr int G = kBlock / LPG;
+    constexpr int CS = group_stride<T, LPG>(2 * NT);
+    __shared__ __align__(16) T colbuf[G * CS];
+    using V = typename Vec16<T>::type;
+    constexpr int W = Vec16<T>::N;
+
+    const int g = threadIdx.x / LPG;
+    const int t = threadIdx.x % LPG;
+    const int64_t b = (int64_t)blockIdx.x * G + g;
+    int rows[RPL];
+#pragma unroll
+    for (int q = 0; q < RPL; ++q) rows[q] = owned_index(t, q, LPG);
+
+    T a[RPL][NT];
+#pragma unroll
+    for (int q = 0; q < RPL; ++q) fetch_fwd_row<T, NT, VEC>(A, b, batch, rows[q], n, a[q]);
+
+    int st = 0;
+    static_for<0, NT>([&](auto jc) {
+        constexpr int j = decltype(jc)::value;
+        T* buf = colbuf + g * CS + (j & 1) * NT;
+#pragma unroll
+        for (int q = 0; q < RPL; ++q) buf[rows[q]] = a[q][j];
+        lanes_sync<LPG>(g);
+        T d = buf[j];
+        if (!(d > T(0))) {
+            if (st == 0) st = j + 1;
+            d = T(1);
+        }
+        const T r = rsqrt_t(d);
+        T coef[RPL];
+#pragma unroll
+        for (int q = 0; q < RPL; ++q) {
+            const T lij = a[q][j] * r;
+            coef[q] = T(rows[q] > j) * (lij * r);
+            a[q][j] = lij;
+        }
+        // trailing update with the published column, read as aligned vectors.
+        // Row q = 0 of a lane (t < LPG) only ever needs columns k <= t < LPG:
+        // its entries at k >= LPG lie above the diagonal and are left stale.
+        static_for<(j + 1) / W, NT / W>([&](auto cc) {
+            constexpr int c = decltype(cc)::value;
+            const V v = reinterpret_cast<const V*>(buf)[c];
+            static_for<0, W>([&](auto ec) {
+                constexpr int e = decltype(ec)::value;
+                constexpr int k = c * W + e;
+                if constexpr (k > j) {
+                    static_for<0, RPL>([&](auto qc) {
+                        constexpr int q = decltype(qc)::value;
+                        if constexpr (!(RPL == 2 && q == 0 && k >= LPG))
+                            a[q][k] = fma(-coef[q], vget<T>(v, e), a[q][k]);
+                    });
+                }
+            });
+        });
+    });
+
+    if (b >= batch) return;
+#pragma unroll
+    for (int q = 0; q < RPL; ++q) {
+        const int i = rows[q];
+        if (i >= n) continue;
+        T* rowp = L + (size_t)b * n * n + (size_t)i * n;
+        if constexpr (VEC) {
+            V* vp = reinterpret_cast<V*>(rowp);
+#pragma unroll
+            for (int c = 0; c < NT / W; ++c) {
+                if (c * W < n) {
+                    V v;
+#pragma unroll
+                    for (int e = 0; e < W; ++e)
+                        vset<T>(v, e, (c * W + e <= i) ? a[q][c * W + e] : T(0));
+                    vp[c] = v;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < NT; ++k)
+                if (k < n) rowp[k] = (k <= i) ? a[q][k] : T(0);
+        }
+    }
+    if (t == 0) status[b] = st;
+}
+
+// Adjoint layout: a group of LPG = NT / CPL lanes per matrix, each lane owning
+// CPL columns (and, after the transpose, CPL rows): columns t and NT-1-t for
+// CPL = 2, which balances the triangular work.  Every broadcast read of a row
+// of L then feeds CPL columns.
+
+// Row r[0..NT) to / from a 16-byte aligned shared-memory row, as vectors.
+template <typename T, int NT>
+__device__ __forceinline__ void store_row(T* dst, const T (&r)[NT]) {
+    using V = typename Vec16<T>::type;
+    constexpr int W = Vec16<T>::N;
+#pragma unroll
+    for (int u = 0; u < NT / W; ++u) {
+        V v;
+#pragma unroll
+        for (int e = 0; e < W; ++e) vset<T>(v, e, r[u * W + e]);
+        reinterpret_cast<V*>(dst)[u] = v;
+    }
+}
+template <typename T, int NT>
+__device__ __forceinline__ void load_row(const T* src, T (&r)[NT]) {
+    using V = typename Vec16<T>::type;
+    constexpr int W = Vec16<T>::N;
+#pragma unroll
+    for (int u = 0; u < NT / W; ++u) {
+        const V v = reinterpret_cast<const V*>(src)[u];
+#pragma unroll
+        for (int e = 0; e < W; ++e) r[u * W + e] = vget<T>(v, e);
+    }
+}
+
+// Phi's factor for row i of column col: 1 below the diagonal, 1/2 on it,
+// 0 above; and the strict-lower indicator k < col.  float uses one saturated
+// add each; double compares.
+__device__ __forceinline__ float phi_factor(int i, float colf) {
+    return __saturatef((float(i) + 0.5f) - colf);
+}
+__device__ __forceinline__ float below(int k, float colf) { return __saturatef(colf - float(k)); }
+
+template <typename T, int NT, int CPL>
+struct AdjCfg;
+
+template <typename T, int NT, int CPL>
+struct AdjCfg {
+    // short matrices run in 64-thread blocks: more, smaller blocks per SM hide
+    // the global-load latency at their start and end better
+    static constexpr int BLOCK = NT <= 16 ? 64 : kBlock;
+    static constexpr int LPG = NT / CPL;                   // lanes per matrix
+    static constexpr int G = BLOCK / LPG;                  // matrices per block
+    static constexpr int LP = NT;                          // L row pitch (rows are read by broadcast)
+    static constexpr int RP = NT + 16 / (int)sizeof(T);    // transpose pitch (16-byte rows)
+    static constexpr int per_group = group_stride<T, LPG>(NT * LP + NT * RP + ((NT + 3) / 4) * 4);
+    static constexpr size_t bytes = (size_t)G * per_group * sizeof(T);
+};
+
+
+// Row `row` of one of the adjoint's inputs, or its padding: identity rows of
+// L, zero rows of adj_L.
+template <typename T, int NT, bool VEC>
+__device__ __forceinline__ void fetch_adj_row(const T* __restrict__ src, bool active, int64_t b,
+                                              int row, int n, T pad_diag, T (&r)[NT]) {
+    if (active && row < n) {
+        load_lower_row<T, NT, VEC>(src + (size_t)b * n * n + (size_t)row * n, row, n, r);
+    } else {
+#pragma unroll
+        for (int k = 0; k < NT; ++k) r[k] = (k == row) ? pad_diag : T(0);
+    }
+}
+
+// Padding rows in place of rows that were read: identity rows of L, zero
+// rows of adj_L (for matrices whose status turned out non-zero).
+template <typename T, int NT>
+__device__ __forceinline__ void pad_row(int row, T pad_diag, T (&r)[NT]) {
+#pragma unroll
+    for (int k = 0; k < NT; ++k) r[k] = (k == row) ? pad_diag : T(0);
+}
+
+// adj_A is read only at the adjoint's end: one lane per matrix starts bringing
+// it into L2 at the start, so that read finds it there (orders up to 32; at 64
+// the extra L2 traffic cost more than it saved).
+template <typename T, int NT, bool VEC>
+__device__ __forceinline__ void prefetch_abar(const T* Abar, int64_t b, int n, bool issue) {
+    if constexpr (VEC && NT <= 32) {
+        if (issue) l2_prefetch(Abar + (size_t)b * n * n, (uint32_t)((size_t)n * n * sizeof(T)));
+    }
+}
+
+template <typename T, int NT, int CPL, bool VEC>
+__global__ void __launch_bounds__(AdjCfg<T, NT, CPL>::BLOCK)
+small_potrf_adj_kernel(const T* __restrict__ Lg, const T* __restrict__ Lbar,
+                       T* __restrict__ Abar, const int32_t* __restrict__ status,
+                       int64_t batch, int n) {
+    using S = AdjCfg<T, NT, CPL>;
+    using V = typename Vec16<T>::type;
+    constexpr int W = Vec16<T>::N;
+    constexpr int LP = S::LP;
+    constexpr int RP = S::RP;
+    constexpr int LPG = S::LPG;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+
+    const int g = threadIdx.x / LPG;
+    const int t = threadIdx.x % LPG;
+    const int64_t b = (int64_t)blockIdx.x * S::G + g;
+    // The status word is read beside the rows, not before them, so the row
+    // loads never wait for it; a matrix with status != 0 (skipped) has its
+    // rows replaced by padding once they arrive.
+    const bool in_batch = b < batch;
+    const int32_t st = (in_batch && status != nullptr) ? __ldg(status + b) : 0;
+
+    T* Ls = reinterpret_cast<T*>(smem_raw) + (size_t)g * S::per_group;
+    T* R = Ls + (size_t)NT * LP;
+    T* rinv = R + (size_t)NT * RP;
+    int col[CPL];
+#pragma unroll
+    for (int q = 0; q < CPL; ++q) col[q] = owned_index(t, q, LPG);
+
+    // When they are short, the lane's rows of adj_A are read now, so their
+    // latency overlaps the solves; otherwise just before they are updated.
+    constexpr bool kEarly = NT * CPL * sizeof(T) <= 64;
+    T old[CPL][NT];
+#pragma unroll
+    for (int q = 0; q < CPL; ++q) {
+        if (!kEarly) break;
+        if (in_batch && col[q] < n) {
+            load_lower_row<T, NT, VEC>(Abar + (size_t)b * n * n + (size_t)col[q] * n, col[q], n,
+                                       old[q]);
+        } else {
+#pragma unroll
+            for (int k = 0; k < NT; ++k) old[q][k] = T(0);
+        }
+    }
+
+    // Rows col[q] of L into shared memory (identity rows for padding or
+    // skipped matrices) and rows col[q] of tril(adj_L) into the transpose buffer.
+    if constexpr (NT * CPL * sizeof(T) <= 128) {
+        // short rows: all of the lane's row loads are issued before any store
+        T lr[CPL][NT], br[CPL][NT];
+#pragma unroll
+        for (int q = 0; q < CPL; ++q) {
+            fetch_adj_row<T, NT, VEC>(Lg, in_batch, b, col[q], n, T(1), lr[q]);
+            fetch_adj_row<T, NT, VEC>(Lbar, in_batch, b, col[q], n, T(0), br[q]);
+        }
+        prefetch_abar<T, NT, VEC>(Abar, b, n, t == 0 && in_batch);
+        if (st != 0) {
+#pragma unroll
+            for (int q = 0; q < CPL; ++q) {
+                pad_row<T, NT>(col[q], T(1), lr[q]);
+                pad_row<T, NT>(col[q], T(0), br[q]);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < CPL; ++q) {
+            store_row<T, NT>(Ls + (size_t)col[q] * LP, lr[q]);
+            store_row<T, NT>(R + col[q] * RP, br[q]);
+        }
+    } else {
+        prefetch_abar<T, NT, VEC>(Abar, b, n, t == 0 && in_batch);
+#pragma unroll
+        for (int q = 0; q < CPL; ++q) {
+            T r[NT];
+            fetch_adj_row<T, NT, VEC>(Lg, in_batch, b, col[q], n, T(1), r);
+            if (st != 0) pad_row<T, NT>(col[q], T(1), r);
+            store_row<T, NT>(Ls + (size_t)col[q] * LP, r);
+            fetch_adj_row<T, NT, VEC>(Lbar, in_batch, b, col[q], n, T(0), r);
+            if (st != 0) pad_row<T, NT>(col[q], T(0), r);
+            store_row<T, NT>(R + col[q] * RP, r);
+        }
+    }
+    const bool active = in_batch && st == 0;
+    lanes_sync<LPG>(g);
+#pragma unroll
+    for (int q = 0; q < CPL; ++q) rinv[col[q]] = rcp_t(Ls[col[q] * LP + col[q]]);
+
+    // Columns col[q] of tril(adj_L).
+    T c[CPL][NT];
+#pragma unroll
+    for (int q = 0; q < CPL; ++q)
+#pragma unroll
+        for (int k = 0; k < NT; ++k) c[q][k] = R[k * RP + col[q]];
+
+    // 1. columns of P = L^T tril(adj_L), in place: slot k is finished once
+    //    row k of L has been applied, so it can take p_k's first term.
+    static_for<0, NT>([&](auto kc) {
+        constexpr int k = decltype(kc)::value;
+        T ck[CPL];
+#pragma unroll
+        for (int q = 0; q < CPL; ++q) ck[q] = c[q][k];
+        const T* lrow = Ls + k * LP;
+        static_for<0, k / W + 1>([&](auto uc) {
+            constexpr int u = decltype(uc)::value;
+            const V v = reinterpret_cast<const V*>(lrow)[u];
+            static_for<0, W>([&](auto ec) {
+                constexpr int i = u * W + decltype(ec)::value;
+#pragma unroll
+                for (int q = 0; q < CPL; ++q) {
+                    if constexpr (i < k) c[q][i] = fma(vget<T>(v, i - u * W), ck[q], c[q][i]);
+                    else if constexpr (i == k) c[q][i] = vget<T>(v, i - u * W) * ck[q];
+                }
+            });
+        });
+    });
+    // 2. S = Phi(P): keep rows below the column, halve the diagonal, clear above.
+    // (a factor rather than a select: a select chain on a lane-dependent index
+    //  is turned into an indexed store, which moves c out of registers)
+#pragma unroll
+    for (int q = 0; q < CPL; ++q) {
+        const float colf = float(col[q]);
+#pragma unroll
+        for (int i = 0; i < NT; ++i) c[q][i] *= T(phi_factor(i, colf));
+    }
+    lanes_sync<LPG>(g);  // rinv visible to the group
+    // the reciprocals in registers when they are few, else read as used
+    constexpr bool kRv = NT * sizeof(T) <= 64;
+    T rv[kRv ? NT : 1];
+    if constexpr (kRv) load_row<T, NT>(rinv, rv);
+
+    // 3. X = L^-T S (back substitution, rows of L broadcast).
+    static_for<0, NT>([&](auto ic) {
+        constexpr int i = NT - 1 - decltype(ic)::value;
+        T ri;
+        if constexpr (kRv) ri = rv[i]; else ri = rinv[i];
+        T xi[CPL];
+#pragma unroll
+        for (int q = 0; q < CPL; ++q) {
+            xi[q] = c[q][i] * ri;
+            c[q][i] = xi[q];
+        }
+        const T* lrow = Ls + i * LP;
+        static_for<0, (i + W - 1) / W>([&](auto uc) {
+            constexpr int u = decltype(uc)::value;
+            const V v = reinterpret_cast<const V*>(lrow)[u];
+            static_for<0, W>([&](auto ec) {
+                constexpr int k = u * W + decltype(ec)::value;
+                if constexpr (k < i) {
+#pragma unroll
+                    for (int q = 0; q < CPL; ++q)
+                        c[q][k] = fma(-vget<T>(v, k - u * W), xi[q], c[q][k]);
+                }
+            });
+        });
+    });
+    // 4. transpose: columns col[q] of X out, rows col[q] in.
+#pragma unroll
+    for (int q = 0; q < CPL; ++q)
+#pragma unroll
+        for (int i = 0; i < NT; ++i) R[i * RP + col[q]] = c[q][i];
+    lanes_sync<LPG>(g);
+#pragma unroll
+    for (int q = 0; q < CPL; ++q) load_row<T, NT>(R + col[q] * RP, c[q]);
+
+    // 5. M = X L^-1 (back substitution on the rows).
+    static_for<0, NT>([&](auto jc) {
+        constexpr int j = NT - 1 - decltype(jc)::value;
+        T rj;
+        if constexpr (kRv) rj = rv[j]; else rj = rinv[j];
+        T mj[CPL];
+#pragma unroll
+        for (int q = 0; q < CPL; ++q) {
+            mj[q] = c[q][j] * rj;
+            c[q][j] = mj[q];
+        }
+        const T* lrow = Ls + j * LP;
+        static_for<0, (j + W - 1) / W>([&](auto uc) {
+            constexpr int u = decltype(uc)::value;
+            const V v = reinterpret_cast<const V*>(lrow)[u];
+            static_for<0, W>([&](auto ec) {
+                constexpr int k = u * W + decltype(ec)::value;
+                if constexpr (k < j) {
+#pragma unroll
+                    for (int q = 0; q < CPL; ++q)
+                        c[q][k] = fma(-vget<T>(v, k - u * W), mj[q], c[q][k]);
+                }
+            });
+        });
+    });
+    // 6. Phi(M + M^T) into rows col[q] of adj_A's lower triangle.  Each lane
+    //    only rewrites the rows it has read.
+#pragma unroll
+    for (int q = 0; q < CPL; ++q) store_row<T, NT>(R + col[q] * RP, c[q]);
+    lanes_sync<LPG>(g);
+#pragma unroll
+    for (int q = 0; q < CPL; ++q) {
+        const float colf = float(col[q]);
+#pragma unroll
+        for (int k = 0; k < NT; ++k) c[q][k] = fma(T(below(k, colf)), R[k * RP + col[q]], c[q][k]);
+    }
+
+    if (!active) return;
+    static_for<0, CPL>([&](auto qc) {
+        constexpr int q = decltype(qc)::value;
+        const int row = col[q];
+        if (row >= n) return;
+        T* rowp = Abar + (size_t)b * n * n + (size_t)row * n;
+        if constexpr (!kEarly) load_lower_row<T, NT, VEC>(rowp, row, n, old[q]);
+        if constexpr (VEC) {
+            V* vp = reinterpret_cast<V*>(rowp);
+            static_for<0, NT / W>([&](auto uc) {
+                constexpr int u = decltype(uc)::value;
+                if (u * W + W - 1 <= row) {
+                    V v;
+#pragma unroll
+                    for (int e = 0; e < W; ++e)
+                        vset<T>(v, e, old[q][u * W + e] + c[q][u * W + e]);
+                    vp[u] = v;
+                } else if (u * W <= row) {
+                    // chunk straddling the diagonal: write only k <= row
+#pragma unroll
+                    for (int e = 0; e < W; ++e) {
+                        const int k = u * W + e;
+                        if (k <= row) rowp[k] = old[q][k] + c[q][k];
+                    }
+                }
+            });
+        } else {
+#pragma unroll
+            for (int k = 0; k < NT; ++k)
+                if (k <= row && k < n) rowp[k] = old[q][k] + c[q][k];
+        }
+    });
+}
+
+// Rows (forward) / columns (adjoint) per lane: two where the registers allow.
+template <typename T, int NT>
+constexpr int per_lane() {
+    return (NT * (int)sizeof(T) <= 128) ? 2 : 1;
+}
+
+template <typename T, int NT, bool VEC>
+cudaError_t launch_fwd_nt(const T* A, T* L, int32_t* status, int64_t batch, int n,
+                          cudaStream_t stream) {
+    constexpr int RPL = (NT * (int)sizeof(T) <= 256) ? 2 : 1;
+    constexpr int G = kBlock / (NT / RPL);
+    const int64_t blocks = (batch + G - 1) / G;
+    small_potrf_kernel<T, NT, RPL, VEC><<<(unsigned)blocks, kBlock, 0, stream>>>(A, L, status,
+                                                                                 batch, n);
+    return cudaGetLastError();
+}
+
+template <typename T, int NT, bool VEC>
+cudaError_t launch_adj_nt(const T* L, const T* Lbar, T* Abar, const int32_t* status,
+                          int64_t batch, int n, cudaStream_t stream) {
+    constexpr int CPL = per_lane<T, NT>();
+    using S = AdjCfg<T, NT, CPL>;
+    const int64_t blocks = (batch + S::G - 1) / S::G;
+    auto kern = small_potrf_adj_kernel<T, NT, CPL, VEC>;
+    constexpr int kThreadsPerBlock = S::BLOCK;
+    static int smem_set = 0;
+    if (S::bytes > 48 * 1024 && !smem_set) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)S::bytes);
+        if (e != cudaSuccess) return e;
+        smem_set = 1;
+    }
+    kern<<<(unsigned)blocks, kThreadsPerBlock, S::bytes, stream>>>(L, Lbar, Abar, status, batch, n);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+template <typename T, int NT, bool VEC>
+cudaError_t small_fwd_nt(const T* A, T* L, int32_t* status, int64_t batch, int n,
+                         cudaStream_t stream) {
+    return launch_fwd_nt<T, NT, VEC>(A, L, status, batch, n, stream);
+}
+
+template <typename T, int NT, bool VEC>
+cudaError_t small_adj_nt(const T* L, const T* Lbar, T* Abar, const int32_t* status,
+                         int64_t batch, int n, cudaStream_t stream) {
+    return launch_adj_nt<T, NT, VEC>(L, Lbar, Abar, status, batch, n, stream);
+}
+
+// Explicit instantiations, one macro per kernel kind.
+#define CHOL_SMALL_FWD(T, NT, VEC)                                                   \
+    template cudaError_t small_fwd_nt<T, NT, VEC>(const T*, T*, int32_t*, int64_t, int, \
+                                                  cudaStream_t);
+#define CHOL_SMALL_ADJ(T, NT, VEC)                                                  \
+    template cudaError_t small_adj_nt<T, NT, VEC>(const T*, const T*, T*, const int32_t*, \
+                                                  int64_t, int, cudaStream_t);
+
+}  // namespace chol
