@@ -246,8 +246,32 @@ __device__ __forceinline__ float phi_factor(int i, float colf) {
 }
 __device__ __forceinline__ float below(int k, float colf) { return __saturatef(colf - float(k)); }
 
-template <typename T, int NT, int CPL>
-struct AdjCfg;
+// L is staged with its rows packed: row r keeps only the 16-byte vectors that
+// hold its lower part, W * (r / W + 1) elements (W per vector), and starts
+// where row r - 1 ends.  Every read of a row has a compile-time r.
+template <typename T>
+__host__ __device__ constexpr int lrow_off(int r) {
+    constexpr int W = 16 / (int)sizeof(T);
+    const int a = r / W, b = r % W;
+    return W * (W * a * (a + 1) / 2 + b * (a + 1));
+}
+
+// Row `row` (runtime) of L into its packed place: the vectors up to the diagonal.
+template <typename T, int NT>
+__device__ __forceinline__ void store_lrow(T* Ls, int row, const T (&r)[NT]) {
+    using V = typename Vec16<T>::type;
+    constexpr int W = Vec16<T>::N;
+    V* dst = reinterpret_cast<V*>(Ls + lrow_off<T>(row));
+#pragma unroll
+    for (int u = 0; u < NT / W; ++u) {
+        if (u * W <= row) {
+            V v;
+#pragma unroll
+            for (int e = 0; e < W; ++e) vset<T>(v, e, r[u * W + e]);
+            dst[u] = v;
+        }
+    }
+}
 
 template <typename T, int NT, int CPL>
 struct AdjCfg {
@@ -256,9 +280,13 @@ struct AdjCfg {
     static constexpr int BLOCK = NT <= 16 ? 64 : kBlock;
     static constexpr int LPG = NT / CPL;                   // lanes per matrix
     static constexpr int G = BLOCK / LPG;                  // matrices per block
-    static constexpr int LP = NT;                          // L row pitch (rows are read by broadcast)
+    static constexpr int LSIZE = lrow_off<T>(NT);          // packed L (rows read by broadcast)
     static constexpr int RP = NT + 16 / (int)sizeof(T);    // transpose pitch (16-byte rows)
-    static constexpr int per_group = group_stride<T, LPG>(NT * LP + NT * RP + ((NT + 3) / 4) * 4);
+    // The reciprocals of L's diagonal live in R's padding columns (NT .. RP-1,
+    // never touched by the transposes): 1/l_ii at row i / W, column NT + i % W.
+    // They are read into registers when they are few, else as used.
+    static constexpr bool RV = NT * sizeof(T) <= 64;
+    static constexpr int per_group = group_stride<T, LPG>(LSIZE + NT * RP);
     static constexpr size_t bytes = (size_t)G * per_group * sizeof(T);
 };
 
@@ -302,7 +330,6 @@ small_potrf_adj_kernel(const T* __restrict__ Lg, const T* __restrict__ Lbar,
     using S = AdjCfg<T, NT, CPL>;
     using V = typename Vec16<T>::type;
     constexpr int W = Vec16<T>::N;
-    constexpr int LP = S::LP;
     constexpr int RP = S::RP;
     constexpr int LPG = S::LPG;
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -317,8 +344,8 @@ small_potrf_adj_kernel(const T* __restrict__ Lg, const T* __restrict__ Lbar,
     const int32_t st = (in_batch && status != nullptr) ? __ldg(status + b) : 0;
 
     T* Ls = reinterpret_cast<T*>(smem_raw) + (size_t)g * S::per_group;
-    T* R = Ls + (size_t)NT * LP;
-    T* rinv = R + (size_t)NT * RP;
+    T* R = Ls + S::LSIZE;
+    auto rinv = [&](int i) -> T& { return R[(i / W) * RP + NT + i % W]; };
     int col[CPL];
 #pragma unroll
     for (int q = 0; q < CPL; ++q) col[q] = owned_index(t, q, LPG);
@@ -359,7 +386,7 @@ small_potrf_adj_kernel(const T* __restrict__ Lg, const T* __restrict__ Lbar,
         }
 #pragma unroll
         for (int q = 0; q < CPL; ++q) {
-            store_row<T, NT>(Ls + (size_t)col[q] * LP, lr[q]);
+            store_lrow<T, NT>(Ls, col[q], lr[q]);
             store_row<T, NT>(R + col[q] * RP, br[q]);
         }
     } else {
@@ -369,7 +396,7 @@ small_potrf_adj_kernel(const T* __restrict__ Lg, const T* __restrict__ Lbar,
             T r[NT];
             fetch_adj_row<T, NT, VEC>(Lg, in_batch, b, col[q], n, T(1), r);
             if (st != 0) pad_row<T, NT>(col[q], T(1), r);
-            store_row<T, NT>(Ls + (size_t)col[q] * LP, r);
+            store_lrow<T, NT>(Ls, col[q], r);
             fetch_adj_row<T, NT, VEC>(Lbar, in_batch, b, col[q], n, T(0), r);
             if (st != 0) pad_row<T, NT>(col[q], T(0), r);
             store_row<T, NT>(R + col[q] * RP, r);
@@ -378,7 +405,7 @@ small_potrf_adj_kernel(const T* __restrict__ Lg, const T* __restrict__ Lbar,
     const bool active = in_batch && st == 0;
     lanes_sync<LPG>(g);
 #pragma unroll
-    for (int q = 0; q < CPL; ++q) rinv[col[q]] = rcp_t(Ls[col[q] * LP + col[q]]);
+    for (int q = 0; q < CPL; ++q) rinv(col[q]) = rcp_t(Ls[lrow_off<T>(col[q]) + col[q]]);
 
     // Columns col[q] of tril(adj_L).
     T c[CPL][NT];
@@ -394,7 +421,7 @@ small_potrf_adj_kernel(const T* __restrict__ Lg, const T* __restrict__ Lbar,
         T ck[CPL];
 #pragma unroll
         for (int q = 0; q < CPL; ++q) ck[q] = c[q][k];
-        const T* lrow = Ls + k * LP;
+        const T* lrow = Ls + lrow_off<T>(k);
         static_for<0, k / W + 1>([&](auto uc) {
             constexpr int u = decltype(uc)::value;
             const V v = reinterpret_cast<const V*>(lrow)[u];
@@ -418,23 +445,29 @@ small_potrf_adj_kernel(const T* __restrict__ Lg, const T* __restrict__ Lbar,
         for (int i = 0; i < NT; ++i) c[q][i] *= T(phi_factor(i, colf));
     }
     lanes_sync<LPG>(g);  // rinv visible to the group
-    // the reciprocals in registers when they are few, else read as used
-    constexpr bool kRv = NT * sizeof(T) <= 64;
+    constexpr bool kRv = S::RV;
     T rv[kRv ? NT : 1];
-    if constexpr (kRv) load_row<T, NT>(rinv, rv);
+    if constexpr (kRv) {
+#pragma unroll
+        for (int u = 0; u < NT / W; ++u) {
+            const V v = *reinterpret_cast<const V*>(R + u * RP + NT);
+#pragma unroll
+            for (int e = 0; e < W; ++e) rv[u * W + e] = vget<T>(v, e);
+        }
+    }
 
     // 3. X = L^-T S (back substitution, rows of L broadcast).
     static_for<0, NT>([&](auto ic) {
         constexpr int i = NT - 1 - decltype(ic)::value;
         T ri;
-        if constexpr (kRv) ri = rv[i]; else ri = rinv[i];
+        if constexpr (kRv) ri = rv[i]; else ri = rinv(i);
         T xi[CPL];
 #pragma unroll
         for (int q = 0; q < CPL; ++q) {
             xi[q] = c[q][i] * ri;
             c[q][i] = xi[q];
         }
-        const T* lrow = Ls + i * LP;
+        const T* lrow = Ls + lrow_off<T>(i);
         static_for<0, (i + W - 1) / W>([&](auto uc) {
             constexpr int u = decltype(uc)::value;
             const V v = reinterpret_cast<const V*>(lrow)[u];
@@ -461,14 +494,14 @@ small_potrf_adj_kernel(const T* __restrict__ Lg, const T* __restrict__ Lbar,
     static_for<0, NT>([&](auto jc) {
         constexpr int j = NT - 1 - decltype(jc)::value;
         T rj;
-        if constexpr (kRv) rj = rv[j]; else rj = rinv[j];
+        if constexpr (kRv) rj = rv[j]; else rj = rinv(j);
         T mj[CPL];
 #pragma unroll
         for (int q = 0; q < CPL; ++q) {
             mj[q] = c[q][j] * rj;
             c[q][j] = mj[q];
         }
-        const T* lrow = Ls + j * LP;
+        const T* lrow = Ls + lrow_off<T>(j);
         static_for<0, (j + W - 1) / W>([&](auto uc) {
             constexpr int u = decltype(uc)::value;
             const V v = reinterpret_cast<const V*>(lrow)[u];

@@ -2,7 +2,7 @@
 // 16 (the batched 65536 x 16x16 workload).  jaxmg docs "Cholesky
 // factorization": lower factor and status.
 //
-// One warp handles 32 matrices per round, one per lane, with no communication
+// One warp handles up to 32 matrices per round, one per lane, with no communication
 // between lanes: every lane keeps the lower triangle of its own matrix in
 // registers and runs the right-looking column recurrence on it
 // (l_jj = d * rsqrt(d), column scaled by rsqrt(d), which keeps the per-column
@@ -12,7 +12,8 @@
 // writes fall in distinct bank groups, and L leaves by bulk stores from the
 // same slots.  Each warp owns two slot sets, so the copy for its next round is
 // in flight while it factors the current one.  A block is one warp; blocks are
-// persistent (resident blocks per SM x SMs).
+// persistent (resident blocks per SM x SMs).  At n = 16 a round takes 27
+// matrices, so that four blocks (one per SM scheduler) fit in shared memory.
 
 #include <cuda_runtime.h>
 
@@ -24,15 +25,18 @@
 namespace chol {
 namespace {
 
-template <int N>
+// M matrices per round (lanes 0..M-1 of the warp; the others idle), NSETS
+// slot sets: up to NSETS - 1 rounds' loads are in flight while one round is
+// factored.
+template <int N, int M, int NSETS>
 struct Tpm {
     static constexpr uint32_t kBytes = N * N * 4;   // one matrix
     static constexpr int kSlot = N * N + 4;         // floats per lane slot (16-byte skew)
-    static constexpr size_t kSlotsBytes = 32 * (size_t)kSlot * 4;
+    static constexpr size_t kSetBytes = (size_t)M * kSlot * 4;
+    static constexpr size_t kSmem = 128 + NSETS * kSetBytes;
     static_assert(kBytes % 16 == 0, "bulk copies move multiples of 16 bytes");
+    static_assert(M >= 1 && M <= 32 && NSETS >= 2 && NSETS <= 8, "one warp, 2..8 slot sets");
 };
-
-constexpr int kBarBytes = 128;  // mbarrier area in front of the slots
 
 // Lower triangle of row i of the slot into registers.
 template <int N>
@@ -59,58 +63,75 @@ __device__ __forceinline__ void issue_round_load(const float* __restrict__ src, 
                                                  int lane) {
     fence_proxy_async_smem();  // earlier generic accesses to the slot come first
     __syncwarp();
-    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)nvalid * Tpm<N>::kBytes);
+    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)nvalid * (N * N * 4));
     __syncwarp();
-    if (lane < nvalid) bulk_load(slot, src + (m0 + lane) * (N * N), Tpm<N>::kBytes, bar);
+    if (lane < nvalid) bulk_load(slot, src + (m0 + lane) * (N * N), N * N * 4, bar);
 }
 
+template <int M>
 __device__ __forceinline__ int round_count(int64_t batch, int64_t w) {
-    return batch - w * 32 < 32 ? (int)(batch - w * 32) : 32;
+    return batch - w * M < M ? (int)(batch - w * M) : M;
 }
 
-template <int N>
+template <int N, int M, int NSETS>
 __global__ void __launch_bounds__(32)
 tpm_potrf_kernel(const float* __restrict__ A, float* __restrict__ L, int32_t* __restrict__ status,
                  int64_t batch) {
-    using C = Tpm<N>;
+    using C = Tpm<N, M, NSETS>;
     extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);  // bar[0], bar[1]
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);  // one per slot set
     const int lane = threadIdx.x;
-    float* slots = reinterpret_cast<float*>(smem + kBarBytes);
-    float* slot_of[2] = {slots + lane * C::kSlot, slots + (32 + lane) * C::kSlot};
+    float* slots = reinterpret_cast<float*>(smem + 128);
+    // this lane's slot in set s (lanes >= M have none)
+    auto slot_of = [&](int s) { return slots + ((size_t)s * M + (lane < M ? lane : 0)) * C::kSlot; };
     if (lane == 0) {
-        mbar_init(bar + 0, 1);
-        mbar_init(bar + 1, 1);
+#pragma unroll
+        for (int s = 0; s < NSETS; ++s) mbar_init(bar + s, 1);
     }
     fence_mbar_init();
     __syncwarp();
 
-    int64_t w = blockIdx.x;
-    if (w * 32 >= batch) return;
-    issue_round_load<N>(A, w * 32, round_count(batch, w), slot_of[0], bar + 0, lane);
-    uint32_t phase[2] = {0u, 0u};
-#pragma unroll 1
-    for (int r = 0; w * 32 < batch; ++r, w += gridDim.x) {
-        const int b = r & 1;
-        const int64_t m0 = w * 32;
-        const int nvalid = round_count(batch, w);
-        const int64_t m = m0 + lane;
-        const int64_t wn = w + gridDim.x;
-        if (wn * 32 < batch) {
-            bulk_wait_read_all();  // the other slot's last store has left shared memory
-            issue_round_load<N>(A, wn * 32, round_count(batch, wn), slot_of[b ^ 1], bar + (b ^ 1),
-                                lane);
+    const int64_t rounds = (batch + M - 1) / M;
+    const int64_t w0 = blockIdx.x;
+    if (w0 >= rounds) return;
+    uint32_t phase_bits = 0u;  // bit s: parity of set s's next completion
+    uint32_t inflight = 0u;    // bit s: set s has a load in flight
+    // the first NSETS - 1 rounds of this warp go out at once
+#pragma unroll
+    for (int s = 0; s < NSETS - 1; ++s) {
+        const int64_t w = w0 + (int64_t)s * gridDim.x;
+        if (w < rounds) {
+            issue_round_load<N>(A, w * M, round_count<M>(batch, w), slot_of(s), bar + s, lane);
+            inflight |= 1u << s;
         }
-        if (!__all_sync(0xffffffffu, mbar_wait(bar + b, phase[b], kMbarPolls))) {
+    }
+#pragma unroll 1
+    for (int64_t r = 0, w = w0; w < rounds; ++r, w += gridDim.x) {
+        const int b = (int)(r % NSETS);
+        const int64_t m0 = w * M;
+        const int nvalid = round_count<M>(batch, w);
+        const int64_t m = m0 + lane;
+        // refill the set that the previous round used, NSETS - 1 rounds ahead
+        const int64_t wn = w + (int64_t)(NSETS - 1) * gridDim.x;
+        if (wn < rounds) {
+            const int bn = (int)((r + NSETS - 1) % NSETS);
+            bulk_wait_read_all();  // that set's last store has left shared memory
+            issue_round_load<N>(A, wn * M, round_count<M>(batch, wn), slot_of(bn), bar + bn, lane);
+            inflight |= 1u << bn;
+        }
+        const uint32_t par = (phase_bits >> b) & 1u;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar + b, par, kMbarPolls))) {
             // The copies did not complete: mark this round's matrices and stop
-            // (after one more bounded wait for the copies in flight).
+            // (after one more bounded wait for every set's copies in flight).
             if (lane < nvalid) status[m] = -1;
-            mbar_wait(bar + b, phase[b], kMbarPolls);
-            mbar_wait(bar + (b ^ 1), phase[b ^ 1], kMbarPolls);
+#pragma unroll
+            for (int s = 0; s < NSETS; ++s)
+                if ((inflight >> s) & 1u) mbar_wait(bar + s, (phase_bits >> s) & 1u, kMbarPolls);
             break;
         }
-        phase[b] ^= 1u;
-        float* slot = slot_of[b];
+        phase_bits ^= 1u << b;
+        inflight &= ~(1u << b);
+        float* slot = slot_of(b);
 
         float a[N][N];
         if (lane < nvalid) {
@@ -182,11 +203,17 @@ int tpm_grid(K kern, size_t smem, int64_t rounds, int* per_sm_cache) {
         1, std::min<int64_t>((int64_t)std::max(sms, 1) * *per_sm_cache, rounds));
 }
 
-template <int N>
+// Matrices per round and slot sets of the n = 16 kernel: 27 lanes with two
+// sets fit four one-warp blocks per SM (one per scheduler) in 228 KB of
+// shared memory, where 32 lanes fit three.
+constexpr int kM16 = 27;
+constexpr int kSets16 = 2;
+
+template <int N, int M, int NSETS>
 cudaError_t tpm_fwd_n(const float* A, float* L, int32_t* status, int64_t batch,
                       cudaStream_t stream) {
-    const size_t smem = kBarBytes + 2 * Tpm<N>::kSlotsBytes;
-    auto kern = tpm_potrf_kernel<N>;
+    const size_t smem = Tpm<N, M, NSETS>::kSmem;
+    auto kern = tpm_potrf_kernel<N, M, NSETS>;
     static int smem_set = 0, per_sm = 0;
     if (!smem_set) {
         cudaError_t e =
@@ -194,7 +221,7 @@ cudaError_t tpm_fwd_n(const float* A, float* L, int32_t* status, int64_t batch,
         if (e != cudaSuccess) return e;
         smem_set = 1;
     }
-    const int grid = tpm_grid(kern, smem, (batch + 31) / 32, &per_sm);
+    const int grid = tpm_grid(kern, smem, (batch + M - 1) / M, &per_sm);
     kern<<<grid, 32, smem, stream>>>(A, L, status, batch);
     return cudaGetLastError();
 }
@@ -205,8 +232,8 @@ bool tpm_supported(int n) { return n == 8 || n == 16; }
 
 cudaError_t tpm_fwd(const float* A, float* L, int32_t* status, int64_t batch, int n,
                     cudaStream_t stream) {
-    if (n == 16) return tpm_fwd_n<16>(A, L, status, batch, stream);
-    if (n == 8) return tpm_fwd_n<8>(A, L, status, batch, stream);
+    if (n == 16) return tpm_fwd_n<16, kM16, kSets16>(A, L, status, batch, stream);
+    if (n == 8) return tpm_fwd_n<8, 32, 2>(A, L, status, batch, stream);
     return cudaErrorInvalidValue;
 }
 
