@@ -146,6 +146,20 @@ __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// 16-byte global -> shared copy that bypasses L1; the first `src_bytes`
+// (0..16) come from `gmem`, the rest of the 16 are zero-filled.  Both
+// addresses 16-byte aligned.  Completion: cp_async_wait_all.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem)),
+                 "l"(gmem), "r"(src_bytes)
+                 : "memory");
+}
+
+// The calling thread's cp.async copies have landed in shared memory.
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // Bring `bytes` of global memory into L2 without waiting for them (a hint:
 // nothing is written and no completion is tracked).  Address 16-byte aligned,
 // bytes a multiple of 16.

@@ -312,6 +312,21 @@ __device__ __forceinline__ void pad_row(int row, T pad_diag, T (&r)[NT]) {
     for (int k = 0; k < NT; ++k) r[k] = (k == row) ? pad_diag : T(0);
 }
 
+// Whole matrices of the padded order (n == NT) move between HBM and the group
+// as contiguous 16-byte chunks: lane t of a group takes chunks t, t + LPG,
+// t + 2 LPG, ... of each matrix, so one warp-wide access covers whole 128-byte
+// lines (a row-wise access spreads over a line per row).  Chunk c holds
+// elements u W .. u W + W - 1 of row r, with u = c % (NT / W) fixed per lane
+// when LPG is a multiple of NT / W.
+template <typename T, int NT, int LPG>
+struct Chunks {
+    static constexpr int W = 16 / (int)sizeof(T);
+    static constexpr int PER_ROW = NT / W;
+    static constexpr int PER_LANE = NT * PER_ROW / LPG;
+    static constexpr int ROW_STEP = LPG / PER_ROW;  // rows between a lane's chunks
+    static constexpr bool OK = LPG % PER_ROW == 0 && (NT * PER_ROW) % LPG == 0 && PER_LANE <= 8;
+};
+
 // adj_A is read only at the adjoint's end: one lane per matrix starts bringing
 // it into L2 at the start, so that read finds it there (orders up to 32; at 64
 // the extra L2 traffic cost more than it saved).
@@ -322,7 +337,7 @@ __device__ __forceinline__ void prefetch_abar(const T* Abar, int64_t b, int n, b
     }
 }
 
-template <typename T, int NT, int CPL, bool VEC>
+template <typename T, int NT, int CPL, bool VEC, bool FULL>
 __global__ void __launch_bounds__(AdjCfg<T, NT, CPL>::BLOCK)
 small_potrf_adj_kernel(const T* __restrict__ Lg, const T* __restrict__ Lbar,
                        T* __restrict__ Abar, const int32_t* __restrict__ status,
@@ -352,7 +367,7 @@ small_potrf_adj_kernel(const T* __restrict__ Lg, const T* __restrict__ Lbar,
 
     // When they are short, the lane's rows of adj_A are read now, so their
     // latency overlaps the solves; otherwise just before they are updated.
-    constexpr bool kEarly = NT * CPL * sizeof(T) <= 64;
+    constexpr bool kEarly = !FULL && NT * CPL * sizeof(T) <= 64;
     T old[CPL][NT];
 #pragma unroll
     for (int q = 0; q < CPL; ++q) {
@@ -368,7 +383,40 @@ small_potrf_adj_kernel(const T* __restrict__ Lg, const T* __restrict__ Lbar,
 
     // Rows col[q] of L into shared memory (identity rows for padding or
     // skipped matrices) and rows col[q] of tril(adj_L) into the transpose buffer.
-    if constexpr (NT * CPL * sizeof(T) <= 128) {
+    using CK = Chunks<T, NT, LPG>;
+    const int cu = t % CK::PER_ROW;  // the lane's chunk column (FULL)
+    const int cr = t / CK::PER_ROW;  // row of the lane's first chunk (FULL)
+    if constexpr (FULL) {
+        // whole chunks copied straight into their places (L packed, adj_L
+        // into R), no registers in between; a chunk of adj_L that reaches
+        // above the diagonal copies only its lower part and is zero-filled
+        static_assert(CK::OK, "chunk layout");
+        const V* Lm = reinterpret_cast<const V*>(in_batch ? Lg + (size_t)b * NT * NT : Lg) + t;
+        const V* Bm = reinterpret_cast<const V*>(in_batch ? Lbar + (size_t)b * NT * NT : Lbar) + t;
+#pragma unroll
+        for (int i = 0; i < CK::PER_LANE; ++i) {
+            const int r = cr + CK::ROW_STEP * i;
+            const int lower = r - cu * W + 1;  // elements of the chunk on or below the diagonal
+            const uint32_t nb =
+                in_batch ? (uint32_t)(lower <= 0 ? 0 : lower >= W ? 16 : lower * (int)sizeof(T)) : 0u;
+            if (lower > 0) cp_async16(Ls + lrow_off<T>(r) + cu * W, in_batch ? Lm + i * LPG : Lm, nb ? 16u : 0u);
+            cp_async16(R + r * RP + cu * W, in_batch ? Bm + i * LPG : Bm, nb);
+        }
+        prefetch_abar<T, NT, VEC>(Abar, b, n, t == 0 && in_batch);
+        cp_async_wait_all();
+        if (!in_batch || st != 0) {
+            // skipped matrix: identity rows of L, zero rows of adj_L
+#pragma unroll
+            for (int i = 0; i < CK::PER_LANE; ++i) {
+                const int r = cr + CK::ROW_STEP * i;
+                V l, z{};
+#pragma unroll
+                for (int e = 0; e < W; ++e) vset<T>(l, e, T(cu * W + e == r));
+                if (cu * W <= r) *reinterpret_cast<V*>(Ls + lrow_off<T>(r) + cu * W) = l;
+                *reinterpret_cast<V*>(R + r * RP + cu * W) = z;
+            }
+        }
+    } else if constexpr (NT * CPL * sizeof(T) <= 128) {
         // short rows: all of the lane's row loads are issued before any store
         T lr[CPL][NT], br[CPL][NT];
 #pragma unroll
@@ -527,6 +575,43 @@ small_potrf_adj_kernel(const T* __restrict__ Lg, const T* __restrict__ Lbar,
         for (int k = 0; k < NT; ++k) c[q][k] = fma(T(below(k, colf)), R[k * RP + col[q]], c[q][k]);
     }
 
+    if constexpr (FULL) {
+        // rows col[q] of the result through R once more, then out as chunks
+        // added to adj_A's; chunks wholly above the diagonal are not touched,
+        // and a chunk that straddles it is written element by element
+        lanes_sync<LPG>(g);  // every lane is done with R's columns
+#pragma unroll
+        for (int q = 0; q < CPL; ++q) store_row<T, NT>(R + col[q] * RP, c[q]);
+        lanes_sync<LPG>(g);
+        if (!active) return;
+        V* Am = reinterpret_cast<V*>(Abar + (size_t)b * NT * NT) + t;
+        // keep the adj_A loads here: hoisted into the solves they hold
+        // registers that cost occupancy
+        asm volatile("" ::: "memory");
+        V av[CK::PER_LANE];
+#pragma unroll
+        for (int i = 0; i < CK::PER_LANE; ++i)
+            av[i] = (cu * W <= cr + CK::ROW_STEP * i) ? Am[i * LPG] : V{};
+#pragma unroll
+        for (int i = 0; i < CK::PER_LANE; ++i) {
+            const int r = cr + CK::ROW_STEP * i;
+            if (cu * W > r) continue;
+            const V x = *reinterpret_cast<const V*>(R + r * RP + cu * W);
+            V v;
+#pragma unroll
+            for (int e = 0; e < W; ++e) vset<T>(v, e, vget<T>(av[i], e) + vget<T>(x, e));
+            if (cu * W + W - 1 <= r) {
+                Am[i * LPG] = v;
+            } else {
+                T* ap = reinterpret_cast<T*>(Am + i * LPG);
+#pragma unroll
+                for (int e = 0; e < W; ++e)
+                    if (cu * W + e <= r) ap[e] = vget<T>(v, e);
+            }
+        }
+        return;
+    }
+
     if (!active) return;
     static_for<0, CPL>([&](auto qc) {
         constexpr int q = decltype(qc)::value;
@@ -584,8 +669,24 @@ cudaError_t launch_adj_nt(const T* L, const T* Lbar, T* Abar, const int32_t* sta
     constexpr int CPL = per_lane<T, NT>();
     using S = AdjCfg<T, NT, CPL>;
     const int64_t blocks = (batch + S::G - 1) / S::G;
-    auto kern = small_potrf_adj_kernel<T, NT, CPL, VEC>;
-    constexpr int kThreadsPerBlock = S::BLOCK;
+    // whole-chunk accesses for matrices of exactly the padded order
+    constexpr bool kChunks = VEC && Chunks<T, NT, S::LPG>::OK;
+    if constexpr (kChunks) {
+        if (n == NT) {
+            auto kern = small_potrf_adj_kernel<T, NT, CPL, VEC, true>;
+            static int smem_set = 0;
+            if (S::bytes > 48 * 1024 && !smem_set) {
+                cudaError_t e = cudaFuncSetAttribute(
+                    kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::bytes);
+                if (e != cudaSuccess) return e;
+                smem_set = 1;
+            }
+            kern<<<(unsigned)blocks, S::BLOCK, S::bytes, stream>>>(L, Lbar, Abar, status, batch,
+                                                                   n);
+            return cudaGetLastError();
+        }
+    }
+    auto kern = small_potrf_adj_kernel<T, NT, CPL, VEC, false>;
     static int smem_set = 0;
     if (S::bytes > 48 * 1024 && !smem_set) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -593,7 +694,7 @@ cudaError_t launch_adj_nt(const T* L, const T* Lbar, T* Abar, const int32_t* sta
         if (e != cudaSuccess) return e;
         smem_set = 1;
     }
-    kern<<<(unsigned)blocks, kThreadsPerBlock, S::bytes, stream>>>(L, Lbar, Abar, status, batch, n);
+    kern<<<(unsigned)blocks, S::BLOCK, S::bytes, stream>>>(L, Lbar, Abar, status, batch, n);
     return cudaGetLastError();
 }
 
