@@ -57,6 +57,10 @@ def load_library(path: str | None = None):
         lib.chol_abi_version.restype = ctypes.c_int32
         lib.chol_adj_noalloc.argtypes = [i64, i32, i32, vp, vp, vp, vp, i32, vp]
         lib.chol_adj_noalloc.restype = ctypes.c_int
+        lib.chol_fwd_inplace.argtypes = [i64, i32, i32, vp, vp, i32, vp]
+        lib.chol_fwd_inplace.restype = ctypes.c_int
+        lib.chol_adj_inplace.argtypes = [i64, i32, i32, vp, vp, vp, i32, vp]
+        lib.chol_adj_inplace.restype = ctypes.c_int
         lib.chol_probe_fma_peak.argtypes = [i32, i64, vp, ctypes.POINTER(ctypes.c_double), vp]
         lib.chol_probe_fma_peak.restype = ctypes.c_int
         _lib = lib
@@ -151,6 +155,50 @@ def chol_adj(L: torch.Tensor, adj_L: torch.Tensor, adj_A: torch.Tensor | None = 
                          adj_A.data_ptr(), sp, int(tile), _stream_ptr(stream))
     _check(rc)
     return adj_A
+
+
+def chol_fwd_inplace(A: torch.Tensor, status: torch.Tensor | None = None, tile: int = 0,
+                     stream=None):
+    """Factor ``A`` in place: on return ``A`` holds what :func:`chol_fwd`
+    returns as ``L`` (zeros above the diagonal).  Returns ``A, status``."""
+    _require(A, "A")
+    if A.dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {A.dtype}")
+    batch, n = _shape(A)
+    if status is None:
+        status = torch.empty(A.shape[:-2], dtype=torch.int32, device=A.device)
+    _require(status, "status", torch.int32)
+    if status.numel() != batch:
+        raise ValueError("status must have one entry per matrix")
+    rc = load_library().chol_fwd_inplace(batch, n, _DTYPES[A.dtype], A.data_ptr(),
+                                         status.data_ptr(), int(tile), _stream_ptr(stream))
+    _check(rc)
+    return A, status
+
+
+def chol_adj_inplace(L: torch.Tensor, adj: torch.Tensor, status: torch.Tensor | None = None,
+                     tile: int = 0, stream=None):
+    """Replace the lower triangle of ``adj`` (holding ``adj_L``) by the
+    gradient :func:`chol_adj` would add to a zero ``adj_A``; matrices with
+    non-zero ``status`` get zeros there.  The upper triangle is not written.
+    Returns ``adj``."""
+    _require(L, "L")
+    if L.dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {L.dtype}")
+    _require(adj, "adj", L.dtype)
+    if tuple(adj.shape) != tuple(L.shape):
+        raise ValueError("adj must match L's shape")
+    batch, n = _shape(L)
+    sp = None
+    if status is not None:
+        _require(status, "status", torch.int32)
+        if status.numel() != batch:
+            raise ValueError("status must have one entry per matrix")
+        sp = status.data_ptr()
+    rc = load_library().chol_adj_inplace(batch, n, _DTYPES[L.dtype], L.data_ptr(), adj.data_ptr(),
+                                         sp, int(tile), _stream_ptr(stream))
+    _check(rc)
+    return adj
 
 
 def probe_fma_peak(dtype=torch.float64, iters: int = 1 << 16, stream=None) -> float:

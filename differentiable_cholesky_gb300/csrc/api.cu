@@ -83,13 +83,14 @@ int fwd_impl(int64_t batch, int32_t n, const void* A, void* L, int32_t* status, 
 
 template <typename T>
 int adj_impl(int64_t batch, int32_t n, const void* L, const void* Lbar, void* Abar,
-             const int32_t* status, int32_t tile, size_t bytes, cudaStream_t stream) {
+             const int32_t* status, int32_t tile, size_t bytes, bool accumulate,
+             cudaStream_t stream) {
     const T* l = static_cast<const T*>(L);
     const T* lb = static_cast<const T*>(Lbar);
     T* ab = static_cast<T*>(Abar);
     if (n <= kSmallMax) {
         const bool vec = vec_ok(n, sizeof(T), {L, Lbar, Abar});
-        return to_code(chol::small_adj<T>(l, lb, ab, status, batch, n, vec, stream));
+        return to_code(chol::small_adj<T>(l, lb, ab, status, batch, n, vec, accumulate, stream));
     }
     if (tile == 0) tile = chol::blocked_default_tile(n, batch);
     void* work = nullptr;
@@ -98,7 +99,7 @@ int adj_impl(int64_t batch, int32_t n, const void* L, const void* Lbar, void* Ab
         return CHOL_ENOMEM;
     }
     const int rc = to_code(chol::blocked_adj<T>(l, lb, ab, status, batch, n, tile,
-                                                static_cast<T*>(work), stream));
+                                                static_cast<T*>(work), accumulate, stream));
     if (cudaFreeAsync(work, stream) != cudaSuccess) return CHOL_ECUDA;
     return rc;
 }
@@ -153,13 +154,55 @@ int chol_adj_ex(int64_t batch, int32_t n, int32_t dtype, const void* L, const vo
         return CHOL_EALIAS;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return dtype == CHOL_F32
-               ? adj_impl<float>(batch, n, L, adj_L, adj_A, status, tile, bytes, s)
-               : adj_impl<double>(batch, n, L, adj_L, adj_A, status, tile, bytes, s);
+               ? adj_impl<float>(batch, n, L, adj_L, adj_A, status, tile, bytes, true, s)
+               : adj_impl<double>(batch, n, L, adj_L, adj_A, status, tile, bytes, true, s);
 }
 
 int chol_adj(int64_t batch, int32_t n, int32_t dtype, const void* L, const void* adj_L,
              void* adj_A, const int32_t* status, void* stream) {
     return chol_adj_ex(batch, n, dtype, L, adj_L, adj_A, status, 0, stream);
+}
+
+// In place: the kernels read every matrix (or, on the blocked path, a stage
+// copies it) in full before anything of it is written, so the output may be
+// the input buffer itself.
+int chol_fwd_inplace(int64_t batch, int32_t n, int32_t dtype, void* A, int32_t* status,
+                     int32_t tile, void* stream) {
+    size_t bytes = 0;
+    int rc = check_shape(batch, n, dtype, &bytes);
+    if (rc != CHOL_OK) return rc;
+    if ((rc = check_tile(tile)) != CHOL_OK) return rc;
+    if (batch == 0) return CHOL_OK;
+    if (A == nullptr || status == nullptr) return CHOL_EINVAL;
+    if (!aligned(A, (size_t)elem_size(dtype)) || !aligned(status, 4)) return CHOL_EINVAL;
+    if (!is_device_pointer(A) || !is_device_pointer(status)) return CHOL_EINVAL;
+    if (overlaps(range_of(A, bytes), range_of(status, (size_t)batch * 4))) return CHOL_EALIAS;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return dtype == CHOL_F32 ? fwd_impl<float>(batch, n, A, A, status, tile, s)
+                             : fwd_impl<double>(batch, n, A, A, status, tile, s);
+}
+
+int chol_adj_inplace(int64_t batch, int32_t n, int32_t dtype, const void* L, void* adj,
+                     const int32_t* status, int32_t tile, void* stream) {
+    size_t bytes = 0;
+    int rc = check_shape(batch, n, dtype, &bytes);
+    if (rc != CHOL_OK) return rc;
+    if ((rc = check_tile(tile)) != CHOL_OK) return rc;
+    if (batch == 0) return CHOL_OK;
+    if (L == nullptr || adj == nullptr) return CHOL_EINVAL;
+    const size_t es = (size_t)elem_size(dtype);
+    if (!aligned(L, es) || !aligned(adj, es)) return CHOL_EINVAL;
+    if (status != nullptr && !aligned(status, 4)) return CHOL_EINVAL;
+    if (!is_device_pointer(L) || !is_device_pointer(adj) ||
+        (status != nullptr && !is_device_pointer(status)))
+        return CHOL_EINVAL;
+    const Range rL = range_of(L, bytes), rX = range_of(adj, bytes);
+    if (overlaps(rX, rL)) return CHOL_EALIAS;
+    if (status != nullptr && overlaps(rX, range_of(status, (size_t)batch * 4)))
+        return CHOL_EALIAS;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return dtype == CHOL_F32 ? adj_impl<float>(batch, n, L, adj, adj, status, tile, bytes, false, s)
+                             : adj_impl<double>(batch, n, L, adj, adj, status, tile, bytes, false, s);
 }
 
 const char* chol_strerror(int code) {

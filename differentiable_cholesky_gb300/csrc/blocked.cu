@@ -529,18 +529,24 @@ lower_copy_kernel(const T* __restrict__ src, T* __restrict__ dst,
     }
 }
 
-// dst_ij += src_ij on the lower triangle (j <= i), matrices with status != 0 skipped.
+// On the lower triangle (j <= i): dst_ij += src_ij (accumulate; matrices with
+// status != 0 skipped), or dst_ij = src_ij (matrices with status != 0 get 0).
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 lower_add_kernel(const T* __restrict__ src, T* __restrict__ dst,
-                 const int32_t* __restrict__ status, int64_t batch, int n) {
+                 const int32_t* __restrict__ status, int64_t batch, int n, bool accumulate) {
     const int64_t nn = (int64_t)n * n;
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < batch * nn;
          e += (int64_t)gridDim.x * blockDim.x) {
         const int64_t b = e / nn, w = e % nn;
         const int i = (int)(w / n), j = (int)(w % n);
-        if (j > i || skip_matrix(status, b)) continue;
-        dst[e] += src[e];
+        if (j > i) continue;
+        const bool skip = skip_matrix(status, b);
+        if (accumulate) {
+            if (!skip) dst[e] += src[e];
+        } else {
+            dst[e] = skip ? T(0) : src[e];
+        }
     }
 }
 
@@ -615,7 +621,8 @@ cudaError_t blocked_fwd(const T* A, T* L, int32_t* status, int64_t batch, int n,
 // the 7 n^3 / 3 of forming P and solving twice.
 template <typename T>
 cudaError_t blocked_adj(const T* L, const T* Lbar, T* Abar, const int32_t* status,
-                        int64_t batch, int n, int tile, T* W, cudaStream_t stream) {
+                        int64_t batch, int n, int tile, T* W, bool accumulate,
+                        cudaStream_t stream) {
     const int nt = (n + tile - 1) / tile;
     const int64_t total = batch * (int64_t)n * n;
     lower_copy_kernel<T><<<elementwise_blocks(total), kThreads, 0, stream>>>(Lbar, W, status,
@@ -659,7 +666,7 @@ cudaError_t blocked_adj(const T* L, const T* Lbar, T* Abar, const int32_t* statu
         }
     }
     lower_add_kernel<T><<<elementwise_blocks(total), kThreads, 0, stream>>>(W, Abar, status,
-                                                                           batch, n);
+                                                                           batch, n, accumulate);
     return cudaGetLastError();
 }
 
@@ -668,8 +675,8 @@ template cudaError_t blocked_fwd<float>(const float*, float*, int32_t*, int64_t,
 template cudaError_t blocked_fwd<double>(const double*, double*, int32_t*, int64_t, int, int,
                                          cudaStream_t);
 template cudaError_t blocked_adj<float>(const float*, const float*, float*, const int32_t*,
-                                        int64_t, int, int, float*, cudaStream_t);
+                                        int64_t, int, int, float*, bool, cudaStream_t);
 template cudaError_t blocked_adj<double>(const double*, const double*, double*, const int32_t*,
-                                         int64_t, int, int, double*, cudaStream_t);
+                                         int64_t, int, int, double*, bool, cudaStream_t);
 
 }  // namespace chol

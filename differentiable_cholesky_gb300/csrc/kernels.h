@@ -14,9 +14,13 @@ int small_nt(int n);
 template <typename T>
 cudaError_t small_fwd(const T* A, T* L, int32_t* status, int64_t batch, int n, bool vec,
                       cudaStream_t stream);
+// The adjoint adds its gradient into adj_A's lower triangle (accumulate) or
+// writes it there (matrices with status != 0 then get zeros); adj_A may be
+// adj_L itself when not accumulating, since every matrix is read in full
+// before its first write.
 template <typename T>
 cudaError_t small_adj(const T* L, const T* Lbar, T* Abar, const int32_t* status, int64_t batch,
-                      int n, bool vec, cudaStream_t stream);
+                      int n, bool vec, bool accumulate, cudaStream_t stream);
 
 // The same for one padded order NT (8, 16, 32 or 64, n <= NT) and access mode
 // (VEC: 16-byte vectors).
@@ -25,7 +29,7 @@ cudaError_t small_fwd_nt(const T* A, T* L, int32_t* status, int64_t batch, int n
                          cudaStream_t stream);
 template <typename T, int NT, bool VEC>
 cudaError_t small_adj_nt(const T* L, const T* Lbar, T* Abar, const int32_t* status,
-                         int64_t batch, int n, cudaStream_t stream);
+                         int64_t batch, int n, bool accumulate, cudaStream_t stream);
 
 // Thread-per-matrix float32 forward for n in {8, 16}; A and L 16-byte aligned.
 bool tpm_supported(int n);
@@ -36,10 +40,11 @@ cudaError_t tpm_fwd(const float* A, float* L, int32_t* status, int64_t batch, in
 template <typename T>
 cudaError_t blocked_fwd(const T* A, T* L, int32_t* status, int64_t batch, int n, int tile,
                         cudaStream_t stream);
-// `work` holds batch * n * n elements of scratch.
+// `work` holds batch * n * n elements of scratch.  accumulate as small_adj.
 template <typename T>
 cudaError_t blocked_adj(const T* L, const T* Lbar, T* Abar, const int32_t* status,
-                        int64_t batch, int n, int tile, T* work, cudaStream_t stream);
+                        int64_t batch, int n, int tile, T* work, bool accumulate,
+                        cudaStream_t stream);
 
 int blocked_default_tile(int n, int64_t batch);
 

@@ -88,7 +88,7 @@ int run(int64_t batch, int32_t n, const void* L, const void* Lbar, void* Abar,
     if (n <= 64) {
         const bool vec = (n * (int)sizeof(T)) % 16 == 0 && aligned16(L) && aligned16(Lbar) &&
                          aligned16(Abar);
-        e = chol::small_adj<T>(l, lb, ab, status, batch, n, vec, stream);
+        e = chol::small_adj<T>(l, lb, ab, status, batch, n, vec, true, stream);
         return e == cudaSuccess ? CHOL_OK : CHOL_ECUDA;
     }
     const unsigned __int128 need =
@@ -97,7 +97,8 @@ int run(int64_t batch, int32_t n, const void* L, const void* Lbar, void* Abar,
     void* work = scratch_on_current_device();
     if (work == nullptr) return CHOL_ECUDA;
     if (tile == 0) tile = chol::blocked_default_tile(n, batch);
-    e = chol::blocked_adj<T>(l, lb, ab, status, batch, n, tile, static_cast<T*>(work), stream);
+    e = chol::blocked_adj<T>(l, lb, ab, status, batch, n, tile, static_cast<T*>(work), true,
+                             stream);
     return e == cudaSuccess ? CHOL_OK : CHOL_ECUDA;
 }
 

@@ -29,11 +29,11 @@ cudaError_t small_fwd(const T* A, T* L, int32_t* status, int64_t batch, int n, b
 
 template <typename T>
 cudaError_t small_adj(const T* L, const T* Lbar, T* Abar, const int32_t* status, int64_t batch,
-                      int n, bool vec, cudaStream_t stream) {
+                      int n, bool vec, bool accumulate, cudaStream_t stream) {
 #define CHOL_ADJ_CASE(NT)                                                                 \
     case NT:                                                                              \
-        return vec ? small_adj_nt<T, NT, true>(L, Lbar, Abar, status, batch, n, stream)   \
-                   : small_adj_nt<T, NT, false>(L, Lbar, Abar, status, batch, n, stream);
+        return vec ? small_adj_nt<T, NT, true>(L, Lbar, Abar, status, batch, n, accumulate, stream) \
+                   : small_adj_nt<T, NT, false>(L, Lbar, Abar, status, batch, n, accumulate, stream);
     switch (small_nt(n)) {
         CHOL_ADJ_CASE(8)
         CHOL_ADJ_CASE(16)
@@ -49,8 +49,8 @@ template cudaError_t small_fwd<float>(const float*, float*, int32_t*, int64_t, i
 template cudaError_t small_fwd<double>(const double*, double*, int32_t*, int64_t, int, bool,
                                        cudaStream_t);
 template cudaError_t small_adj<float>(const float*, const float*, float*, const int32_t*,
-                                      int64_t, int, bool, cudaStream_t);
+                                      int64_t, int, bool, bool, cudaStream_t);
 template cudaError_t small_adj<double>(const double*, const double*, double*, const int32_t*,
-                                       int64_t, int, bool, cudaStream_t);
+                                       int64_t, int, bool, bool, cudaStream_t);
 
 }  // namespace chol

@@ -341,7 +341,7 @@ template <typename T, int NT, int CPL, bool VEC, bool FULL>
 __global__ void __launch_bounds__(AdjCfg<T, NT, CPL>::BLOCK)
 small_potrf_adj_kernel(const T* __restrict__ Lg, const T* __restrict__ Lbar,
                        T* __restrict__ Abar, const int32_t* __restrict__ status,
-                       int64_t batch, int n) {
+                       int64_t batch, int n, bool accumulate) {
     using S = AdjCfg<T, NT, CPL>;
     using V = typename Vec16<T>::type;
     constexpr int W = Vec16<T>::N;
@@ -372,7 +372,7 @@ small_potrf_adj_kernel(const T* __restrict__ Lg, const T* __restrict__ Lbar,
 #pragma unroll
     for (int q = 0; q < CPL; ++q) {
         if (!kEarly) break;
-        if (in_batch && col[q] < n) {
+        if (accumulate && in_batch && col[q] < n) {
             load_lower_row<T, NT, VEC>(Abar + (size_t)b * n * n + (size_t)col[q] * n, col[q], n,
                                        old[q]);
         } else {
@@ -402,7 +402,7 @@ small_potrf_adj_kernel(const T* __restrict__ Lg, const T* __restrict__ Lbar,
             if (lower > 0) cp_async16(Ls + lrow_off<T>(r) + cu * W, in_batch ? Lm + i * LPG : Lm, nb ? 16u : 0u);
             cp_async16(R + r * RP + cu * W, in_batch ? Bm + i * LPG : Bm, nb);
         }
-        prefetch_abar<T, NT, VEC>(Abar, b, n, t == 0 && in_batch);
+        prefetch_abar<T, NT, VEC>(Abar, b, n, accumulate && t == 0 && in_batch);
         cp_async_wait_all();
         if (!in_batch || st != 0) {
             // skipped matrix: identity rows of L, zero rows of adj_L
@@ -424,7 +424,7 @@ small_potrf_adj_kernel(const T* __restrict__ Lg, const T* __restrict__ Lbar,
             fetch_adj_row<T, NT, VEC>(Lg, in_batch, b, col[q], n, T(1), lr[q]);
             fetch_adj_row<T, NT, VEC>(Lbar, in_batch, b, col[q], n, T(0), br[q]);
         }
-        prefetch_abar<T, NT, VEC>(Abar, b, n, t == 0 && in_batch);
+        prefetch_abar<T, NT, VEC>(Abar, b, n, accumulate && t == 0 && in_batch);
         if (st != 0) {
 #pragma unroll
             for (int q = 0; q < CPL; ++q) {
@@ -438,7 +438,7 @@ small_potrf_adj_kernel(const T* __restrict__ Lg, const T* __restrict__ Lbar,
             store_row<T, NT>(R + col[q] * RP, br[q]);
         }
     } else {
-        prefetch_abar<T, NT, VEC>(Abar, b, n, t == 0 && in_batch);
+        prefetch_abar<T, NT, VEC>(Abar, b, n, accumulate && t == 0 && in_batch);
 #pragma unroll
         for (int q = 0; q < CPL; ++q) {
             T r[NT];
@@ -583,7 +583,7 @@ small_potrf_adj_kernel(const T* __restrict__ Lg, const T* __restrict__ Lbar,
 #pragma unroll
         for (int q = 0; q < CPL; ++q) store_row<T, NT>(R + col[q] * RP, c[q]);
         lanes_sync<LPG>(g);
-        if (!active) return;
+        if (!in_batch || (accumulate && !active)) return;
         V* Am = reinterpret_cast<V*>(Abar + (size_t)b * NT * NT) + t;
         // keep the adj_A loads here: hoisted into the solves they hold
         // registers that cost occupancy
@@ -591,7 +591,7 @@ small_potrf_adj_kernel(const T* __restrict__ Lg, const T* __restrict__ Lbar,
         V av[CK::PER_LANE];
 #pragma unroll
         for (int i = 0; i < CK::PER_LANE; ++i)
-            av[i] = (cu * W <= cr + CK::ROW_STEP * i) ? Am[i * LPG] : V{};
+            av[i] = (accumulate && cu * W <= cr + CK::ROW_STEP * i) ? Am[i * LPG] : V{};
 #pragma unroll
         for (int i = 0; i < CK::PER_LANE; ++i) {
             const int r = cr + CK::ROW_STEP * i;
@@ -612,13 +612,22 @@ small_potrf_adj_kernel(const T* __restrict__ Lg, const T* __restrict__ Lbar,
         return;
     }
 
-    if (!active) return;
+    // Accumulating, a skipped matrix keeps adj_A as it was; overwriting, it
+    // gets the zeros its padding rows produce.
+    if (!in_batch || (accumulate && !active)) return;
     static_for<0, CPL>([&](auto qc) {
         constexpr int q = decltype(qc)::value;
         const int row = col[q];
         if (row >= n) return;
         T* rowp = Abar + (size_t)b * n * n + (size_t)row * n;
-        if constexpr (!kEarly) load_lower_row<T, NT, VEC>(rowp, row, n, old[q]);
+        if constexpr (!kEarly) {
+            if (accumulate) {
+                load_lower_row<T, NT, VEC>(rowp, row, n, old[q]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < NT; ++k) old[q][k] = T(0);
+            }
+        }
         if constexpr (VEC) {
             V* vp = reinterpret_cast<V*>(rowp);
             static_for<0, NT / W>([&](auto uc) {
@@ -665,7 +674,7 @@ cudaError_t launch_fwd_nt(const T* A, T* L, int32_t* status, int64_t batch, int 
 
 template <typename T, int NT, bool VEC>
 cudaError_t launch_adj_nt(const T* L, const T* Lbar, T* Abar, const int32_t* status,
-                          int64_t batch, int n, cudaStream_t stream) {
+                          int64_t batch, int n, bool accumulate, cudaStream_t stream) {
     constexpr int CPL = per_lane<T, NT>();
     using S = AdjCfg<T, NT, CPL>;
     const int64_t blocks = (batch + S::G - 1) / S::G;
@@ -682,7 +691,7 @@ cudaError_t launch_adj_nt(const T* L, const T* Lbar, T* Abar, const int32_t* sta
                 smem_set = 1;
             }
             kern<<<(unsigned)blocks, S::BLOCK, S::bytes, stream>>>(L, Lbar, Abar, status, batch,
-                                                                   n);
+                                                                   n, accumulate);
             return cudaGetLastError();
         }
     }
@@ -694,7 +703,8 @@ cudaError_t launch_adj_nt(const T* L, const T* Lbar, T* Abar, const int32_t* sta
         if (e != cudaSuccess) return e;
         smem_set = 1;
     }
-    kern<<<(unsigned)blocks, S::BLOCK, S::bytes, stream>>>(L, Lbar, Abar, status, batch, n);
+    kern<<<(unsigned)blocks, S::BLOCK, S::bytes, stream>>>(L, Lbar, Abar, status, batch, n,
+                                                           accumulate);
     return cudaGetLastError();
 }
 
@@ -708,8 +718,8 @@ cudaError_t small_fwd_nt(const T* A, T* L, int32_t* status, int64_t batch, int n
 
 template <typename T, int NT, bool VEC>
 cudaError_t small_adj_nt(const T* L, const T* Lbar, T* Abar, const int32_t* status,
-                         int64_t batch, int n, cudaStream_t stream) {
-    return launch_adj_nt<T, NT, VEC>(L, Lbar, Abar, status, batch, n, stream);
+                         int64_t batch, int n, bool accumulate, cudaStream_t stream) {
+    return launch_adj_nt<T, NT, VEC>(L, Lbar, Abar, status, batch, n, accumulate, stream);
 }
 
 // Explicit instantiations, one macro per kernel kind.
@@ -718,6 +728,6 @@ cudaError_t small_adj_nt(const T* L, const T* Lbar, T* Abar, const int32_t* stat
                                                   cudaStream_t);
 #define CHOL_SMALL_ADJ(T, NT, VEC)                                                  \
     template cudaError_t small_adj_nt<T, NT, VEC>(const T*, const T*, T*, const int32_t*, \
-                                                  int64_t, int, cudaStream_t);
+                                                  int64_t, int, bool, cudaStream_t);
 
 }  // namespace chol

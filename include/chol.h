@@ -1,7 +1,8 @@
 /*
  * chol.h -- C ABI of the GB300 (sm_103a) differentiable Cholesky library.
  *
- * Two calls make up the path:
+ * Two calls make up the path (chol_fwd_inplace / chol_adj_inplace are their
+ * in-place forms):
  *
  *   chol_fwd  the Cholesky factorisation A = L L^T of symmetric positive-
  *             definite matrices, lower factor, out of place, with a per-matrix
@@ -136,13 +137,49 @@ CHOL_API int chol_adj_noalloc(int64_t batch, int32_t n, int32_t dtype, const voi
                               const void* adj_L, void* adj_A, const int32_t* status,
                               int32_t tile, void* stream);
 
+/*
+ * chol_fwd_inplace -- chol_fwd with the factor written over its input.  The
+ * jaxmg docs "Cholesky factorization" donate the input to the factorization
+ * (Warning box: do not use the input array after the call) and, under
+ * "Advanced: control the outer jax.jit", return a factor that aliases the
+ * input work buffer; NVIDIA/warp issue #1316's closing comment names the
+ * in-place tile form tile_cholesky_inplace.
+ *   A       in/out: dtype[batch][n][n].  On entry its lower triangle is the
+ *                matrix (upper triangle ignored); on return the buffer holds
+ *                exactly what chol_fwd writes into L: the factor, exact zeros
+ *                above the diagonal.
+ *   status  out: as chol_fwd.  Must not overlap A (CHOL_EALIAS).
+ *   tile    as chol_fwd_ex.
+ * Results are bit-identical to chol_fwd_ex with the same tile.
+ */
+CHOL_API int chol_fwd_inplace(int64_t batch, int32_t n, int32_t dtype, void* A, int32_t* status,
+                              int32_t tile, void* stream);
+
+/*
+ * chol_adj_inplace -- the adjoint written over its seed: the in-place form's
+ * adjoint, which NVIDIA/warp issue #1316's closing comment notes
+ * tile_cholesky_inplace lacks.
+ *   L       in : as chol_adj.  Must not overlap adj (CHOL_EALIAS).
+ *   adj     in/out: dtype[batch][n][n].  On entry its lower triangle is
+ *                adj_L (the upper is taken as 0); on return the lower
+ *                triangle holds the gradient chol_adj would ADD to a zero
+ *                adj_A (M_ij + M_ji below the diagonal, M_ii on it), and a
+ *                matrix with non-zero status gets zeros there.  The upper
+ *                triangle is never written.
+ *   status  in : as chol_adj (or NULL).  Must not overlap adj.
+ *   tile    as chol_adj_ex; n > 64 takes the same workspace as chol_adj.
+ * Results are bit-identical to chol_adj_ex into a zeroed adj_A.
+ */
+CHOL_API int chol_adj_inplace(int64_t batch, int32_t n, int32_t dtype, const void* L, void* adj,
+                              const int32_t* status, int32_t tile, void* stream);
+
 /* Static text for a return code (never NULL). */
 CHOL_API const char* chol_strerror(int code);
 
 /* ABI version of this header: (major << 16) | minor. */
 CHOL_API int32_t chol_abi_version(void);
 
-#define CHOL_ABI_VERSION ((1 << 16) | 0)
+#define CHOL_ABI_VERSION ((1 << 16) | 1)
 
 #ifdef __cplusplus
 }

@@ -24,7 +24,7 @@ def declared_symbols():
 def test_header_declares_the_path():
     syms = declared_symbols()
     for s in ("chol_fwd", "chol_adj", "chol_fwd_ex", "chol_adj_ex", "chol_strerror",
-              "chol_abi_version", "chol_probe_fma_peak"):
+              "chol_abi_version", "chol_probe_fma_peak", "chol_fwd_inplace", "chol_adj_inplace"):
         assert s in syms
 
 
@@ -32,7 +32,7 @@ def test_library_exports_every_declared_symbol():
     lib = binding.load_library()
     for s in declared_symbols():
         assert hasattr(lib, s), f"{s} not exported"
-    assert lib.chol_abi_version() == (1 << 16) | 0
+    assert lib.chol_abi_version() == (1 << 16) | 1
 
 
 def test_strerror_covers_every_code():
@@ -67,6 +67,26 @@ def test_argument_checks_without_gpu():
     big = (ctypes.c_double * 64)()
     q = ctypes.addressof(big)
     assert lib.chol_fwd(1, 2, 1, q, q + 256, s, None) == CHOL_EINVAL
+
+
+def test_inplace_argument_checks_without_gpu():
+    lib = binding.load_library()
+    buf = (ctypes.c_double * 16)()
+    st = (ctypes.c_int32 * 4)()
+    p, s = ctypes.addressof(buf), ctypes.addressof(st)
+    assert lib.chol_fwd_inplace(1, 4, 7, p, s, 0, None) == CHOL_EDTYPE
+    assert lib.chol_fwd_inplace(1, 0, 1, p, s, 0, None) == CHOL_EINVAL
+    assert lib.chol_fwd_inplace(1, 100, 1, p, s, 48, None) == CHOL_EINVAL
+    assert lib.chol_fwd_inplace(0, 4, 1, None, None, 0, None) == CHOL_OK
+    assert lib.chol_fwd_inplace(1, 4, 1, None, s, 0, None) == CHOL_EINVAL
+    assert lib.chol_fwd_inplace(1, 2, 1, p + 4, s, 0, None) == CHOL_EINVAL
+    assert lib.chol_adj_inplace(1, 4, 9, p, p, None, 0, None) == CHOL_EDTYPE
+    assert lib.chol_adj_inplace(0, 4, 1, None, None, None, 0, None) == CHOL_OK
+    assert lib.chol_adj_inplace(1, 4, 1, p, None, None, 0, None) == CHOL_EINVAL
+    assert lib.chol_adj_inplace(1, 4, 1, None, p, None, 0, None) == CHOL_EINVAL
+    # host memory is rejected (not a device pointer)
+    assert lib.chol_fwd_inplace(1, 2, 1, p, s, 0, None) == CHOL_EINVAL
+    assert lib.chol_adj_inplace(1, 2, 1, p, p + 64, None, 0, None) == CHOL_EINVAL
 
 
 def test_size_overflow_rejected():
