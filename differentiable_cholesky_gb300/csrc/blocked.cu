@@ -28,6 +28,7 @@
 #include <cmath>
 
 #include "common.cuh"
+#include "chol_tile.cuh"
 #include "kernels.h"
 
 namespace chol {
@@ -80,32 +81,11 @@ potrf_diag_kernel(T* __restrict__ L, int32_t* __restrict__ status, int64_t batch
             S[r * P + c] = (c <= r) ? Lb[(int64_t)(k0 + r) * n + k0 + c] : T(0);
         }
         __syncthreads();
-        bool failed = false;
-        for (int j = 0; j < kb; ++j) {
-            const T d = S[j * P + j];
-            if (!(d > T(0))) {  // same value in every thread: uniform exit
-                if (threadIdx.x == 0) status[b] = k0 + j + 1;
-                failed = true;
-                break;
-            }
-            const T ljj = sqrt_t(d);
-            const T inv = rcp_t(ljj);  // one reciprocal per column, then products
-            __syncthreads();           // every thread has read the pivot
-            for (int i = j + 1 + threadIdx.x; i < kb; i += blockDim.x) S[i * P + j] *= inv;
-            if (threadIdx.x == 0) S[j * P + j] = ljj;
-            __syncthreads();
-            // trailing update of the lower part, 16 x 16 threads over (i, c)
-            {
-                const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
-                for (int i = j + 1 + ty; i < kb; i += THREADS / 16) {
-                    const T lij = S[i * P + j];
-                    for (int c = j + 1 + tx; c <= i; c += 16)
-                        S[i * P + c] = fma(-lij, S[c * P + j], S[i * P + c]);
-                }
-            }
-            __syncthreads();
+        const int st = chol_tile::potrf<THREADS>(S, kb, chol_tile::RowMajor{P});
+        if (st != 0) {
+            if (threadIdx.x == 0) status[b] = k0 + st;
+            continue;
         }
-        if (failed) continue;
         for (int e = threadIdx.x; e < kb * kb; e += blockDim.x) {
             const int r = e / kb, c = e % kb;
             if (c <= r) Lb[(int64_t)(k0 + r) * n + k0 + c] = S[r * P + c];
@@ -455,8 +435,7 @@ diag_rev_kernel(const T* __restrict__ L, T* __restrict__ W, const int32_t* __res
     extern __shared__ __align__(16) unsigned char smem_raw[];
     T* Ls = reinterpret_cast<T*>(smem_raw);
     T* Ws = Ls + (size_t)kb * (kb + 1) / 2;
-    __shared__ T red[THREADS / 32];
-    const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
+    const int tid = threadIdx.x;
     for (int64_t b = blockIdx.y; b < batch; b += gridDim.y) {
         if (skip_matrix(status, b)) continue;
         const T* Lb = L + b * (int64_t)n * n;
@@ -470,43 +449,7 @@ diag_rev_kernel(const T* __restrict__ L, T* __restrict__ W, const int32_t* __res
             Ws[tri(r, c)] = Wb[o];
         }
         __syncthreads();
-        for (int j = kb - 1; j >= 0; --j) {
-            // s = sum_{i > j} L_ij W_ij
-            T part = T(0);
-            for (int i = j + 1 + tid; i < kb; i += blockDim.x)
-                part = fma(Ls[tri(i, j)], Ws[tri(i, j)], part);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-            if (lane == 0) red[warp] = part;
-            __syncthreads();
-            T sum = T(0);
-#pragma unroll
-            for (int w = 0; w < THREADS / 32; ++w) sum += red[w];
-            const T inv = T(1) / Ls[tri(j, j)];
-            // column j: diagonal from the sum, the rest scaled
-            for (int i = j + 1 + tid; i < kb; i += blockDim.x) Ws[tri(i, j)] *= inv;
-            if (tid == 0) Ws[tri(j, j)] = (Ws[tri(j, j)] - sum * inv) * inv;
-            __syncthreads();
-            // row j left of the diagonal: W_jk -= sum_{i >= j} W_ij L_ik
-            for (int k = tid; k < j; k += blockDim.x) {
-                T acc = T(0);
-                for (int i = j; i < kb; ++i) acc = fma(Ws[tri(i, j)], Ls[tri(i, k)], acc);
-                Ws[tri(j, k)] -= acc;
-            }
-            // rows below, left of column j: W_ik -= W_ij L_jk
-            {
-                const int ty = tid / 16, tx = tid % 16;
-                for (int i = j + 1 + ty; i < kb; i += THREADS / 16) {
-                    const T wij = Ws[tri(i, j)];
-                    for (int k = tx; k < j; k += 16)
-                        Ws[tri(i, k)] = fma(-wij, Ls[tri(j, k)], Ws[tri(i, k)]);
-                }
-            }
-            __syncthreads();
-            if (tid == 0) Ws[tri(j, j)] *= T(0.5);
-            // (the next column's first barrier orders this write)
-        }
-        __syncthreads();
+        chol_tile::potrf_adj<THREADS>(Ls, Ws, kb, chol_tile::PackedLower{});
         for (int e = tid; e < kb * kb; e += blockDim.x) {
             const int r = e / kb, c = e % kb;
             if (c <= r) Wb[(int64_t)(j0 + r) * n + j0 + c] = Ws[tri(r, c)];
