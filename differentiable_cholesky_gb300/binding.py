@@ -57,6 +57,8 @@ def load_library(path: str | None = None):
         lib.chol_abi_version.restype = ctypes.c_int32
         lib.chol_adj_noalloc.argtypes = [i64, i32, i32, vp, vp, vp, vp, i32, vp]
         lib.chol_adj_noalloc.restype = ctypes.c_int
+        lib.chol_selftest_wait_timeout.argtypes = [i64, vp, vp, vp, ctypes.c_uint32, vp]
+        lib.chol_selftest_wait_timeout.restype = ctypes.c_int
         lib.chol_fwd_inplace.argtypes = [i64, i32, i32, vp, vp, i32, vp]
         lib.chol_fwd_inplace.restype = ctypes.c_int
         lib.chol_adj_inplace.argtypes = [i64, i32, i32, vp, vp, vp, i32, vp]

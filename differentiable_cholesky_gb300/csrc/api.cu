@@ -7,6 +7,7 @@
 #include <initializer_list>
 
 #include "chol.h"
+#include "chol_selftest.h"
 #include "kernels.h"
 
 namespace {
@@ -203,6 +204,25 @@ int chol_adj_inplace(int64_t batch, int32_t n, int32_t dtype, const void* L, voi
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return dtype == CHOL_F32 ? adj_impl<float>(batch, n, L, adj, adj, status, tile, bytes, false, s)
                              : adj_impl<double>(batch, n, L, adj, adj, status, tile, bytes, false, s);
+}
+
+int chol_selftest_wait_timeout(int64_t batch, const void* A, void* L, int32_t* status,
+                               uint32_t max_polls, void* stream) {
+    size_t bytes = 0;
+    int rc = check_shape(batch, 16, CHOL_F32, &bytes);
+    if (rc != CHOL_OK) return rc;
+    if (batch == 0) return CHOL_OK;
+    if (max_polls < 1 || max_polls > (1u << 22)) return CHOL_EINVAL;
+    if (A == nullptr || L == nullptr || status == nullptr) return CHOL_EINVAL;
+    if (!aligned(A, 16) || !aligned(L, 16) || !aligned(status, 4)) return CHOL_EINVAL;
+    if (!is_device_pointer(A) || !is_device_pointer(L) || !is_device_pointer(status))
+        return CHOL_EINVAL;
+    const Range rA = range_of(A, bytes), rL = range_of(L, bytes),
+                rS = range_of(status, (size_t)batch * 4);
+    if (overlaps(rA, rL) || overlaps(rL, rS) || overlaps(rA, rS)) return CHOL_EALIAS;
+    return to_code(chol::tpm_fwd_wait_selftest(static_cast<const float*>(A), static_cast<float*>(L),
+                                               status, batch, max_polls,
+                                               static_cast<cudaStream_t>(stream)));
 }
 
 const char* chol_strerror(int code) {

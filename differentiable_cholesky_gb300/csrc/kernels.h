@@ -35,6 +35,10 @@ cudaError_t small_adj_nt(const T* L, const T* Lbar, T* Abar, const int32_t* stat
 bool tpm_supported(int n);
 cudaError_t tpm_fwd(const float* A, float* L, int32_t* status, int64_t batch, int n,
                     cudaStream_t stream);
+// The n = 16 kernel with lane 0's copy of every round dropped and `max_polls`
+// polls per barrier wait: every warp's first round times out (status -1).
+cudaError_t tpm_fwd_wait_selftest(const float* A, float* L, int32_t* status, int64_t batch,
+                                  uint32_t max_polls, cudaStream_t stream);
 
 // n > 64, blocked with square tiles of `tile` (32, 64 or 128).
 template <typename T>

@@ -60,12 +60,14 @@ __device__ __forceinline__ void slot_load_lower(const float* slot, float (&a)[N]
 template <int N>
 __device__ __forceinline__ void issue_round_load(const float* __restrict__ src, int64_t m0,
                                                  int nvalid, float* slot, uint64_t* bar,
-                                                 int lane) {
+                                                 int lane, int drop_lane) {
     fence_proxy_async_smem();  // earlier generic accesses to the slot come first
     __syncwarp();
     if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)nvalid * (N * N * 4));
     __syncwarp();
-    if (lane < nvalid) bulk_load(slot, src + (m0 + lane) * (N * N), N * N * 4, bar);
+    // (drop_lane >= 0 only in the self-test: that lane's copy is never
+    //  issued, so the round's barrier cannot complete)
+    if (lane < nvalid && lane != drop_lane) bulk_load(slot, src + (m0 + lane) * (N * N), N * N * 4, bar);
 }
 
 template <int M>
@@ -76,7 +78,7 @@ __device__ __forceinline__ int round_count(int64_t batch, int64_t w) {
 template <int N, int M, int NSETS>
 __global__ void __launch_bounds__(32)
 tpm_potrf_kernel(const float* __restrict__ A, float* __restrict__ L, int32_t* __restrict__ status,
-                 int64_t batch) {
+                 int64_t batch, uint32_t max_polls, int drop_lane) {
     using C = Tpm<N, M, NSETS>;
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem);  // one per slot set
@@ -101,7 +103,8 @@ tpm_potrf_kernel(const float* __restrict__ A, float* __restrict__ L, int32_t* __
     for (int s = 0; s < NSETS - 1; ++s) {
         const int64_t w = w0 + (int64_t)s * gridDim.x;
         if (w < rounds) {
-            issue_round_load<N>(A, w * M, round_count<M>(batch, w), slot_of(s), bar + s, lane);
+            issue_round_load<N>(A, w * M, round_count<M>(batch, w), slot_of(s), bar + s, lane,
+                                drop_lane);
             inflight |= 1u << s;
         }
     }
@@ -116,17 +119,18 @@ tpm_potrf_kernel(const float* __restrict__ A, float* __restrict__ L, int32_t* __
         if (wn < rounds) {
             const int bn = (int)((r + NSETS - 1) % NSETS);
             bulk_wait_read_all();  // that set's last store has left shared memory
-            issue_round_load<N>(A, wn * M, round_count<M>(batch, wn), slot_of(bn), bar + bn, lane);
+            issue_round_load<N>(A, wn * M, round_count<M>(batch, wn), slot_of(bn), bar + bn, lane,
+                                drop_lane);
             inflight |= 1u << bn;
         }
         const uint32_t par = (phase_bits >> b) & 1u;
-        if (!__all_sync(0xffffffffu, mbar_wait(bar + b, par, kMbarPolls))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar + b, par, max_polls))) {
             // The copies did not complete: mark this round's matrices and stop
             // (after one more bounded wait for every set's copies in flight).
             if (lane < nvalid) status[m] = -1;
 #pragma unroll
             for (int s = 0; s < NSETS; ++s)
-                if ((inflight >> s) & 1u) mbar_wait(bar + s, (phase_bits >> s) & 1u, kMbarPolls);
+                if ((inflight >> s) & 1u) mbar_wait(bar + s, (phase_bits >> s) & 1u, max_polls);
             break;
         }
         phase_bits ^= 1u << b;
@@ -211,7 +215,7 @@ constexpr int kSets16 = 2;
 
 template <int N, int M, int NSETS>
 cudaError_t tpm_fwd_n(const float* A, float* L, int32_t* status, int64_t batch,
-                      cudaStream_t stream) {
+                      cudaStream_t stream, uint32_t max_polls = kMbarPolls, int drop_lane = -1) {
     const size_t smem = Tpm<N, M, NSETS>::kSmem;
     auto kern = tpm_potrf_kernel<N, M, NSETS>;
     static int smem_set = 0, per_sm = 0;
@@ -222,13 +226,18 @@ cudaError_t tpm_fwd_n(const float* A, float* L, int32_t* status, int64_t batch,
         smem_set = 1;
     }
     const int grid = tpm_grid(kern, smem, (batch + M - 1) / M, &per_sm);
-    kern<<<grid, 32, smem, stream>>>(A, L, status, batch);
+    kern<<<grid, 32, smem, stream>>>(A, L, status, batch, max_polls, drop_lane);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 bool tpm_supported(int n) { return n == 8 || n == 16; }
+
+cudaError_t tpm_fwd_wait_selftest(const float* A, float* L, int32_t* status, int64_t batch,
+                                  uint32_t max_polls, cudaStream_t stream) {
+    return tpm_fwd_n<16, kM16, kSets16>(A, L, status, batch, stream, max_polls, 0);
+}
 
 cudaError_t tpm_fwd(const float* A, float* L, int32_t* status, int64_t batch, int n,
                     cudaStream_t stream) {
