@@ -119,7 +119,55 @@ __device__ __forceinline__ void lanes_sync(int group) {
     }
 }
 
-template <typename T, int NT, int RPL, bool VEC>
+// Row r[0..NT) to / from a 16-byte aligned shared-memory row, as vectors.
+template <typename T, int NT>
+__device__ __forceinline__ void store_row(T* dst, const T (&r)[NT]) {
+    using V = typename Vec16<T>::type;
+    constexpr int W = Vec16<T>::N;
+#pragma unroll
+    for (int u = 0; u < NT / W; ++u) {
+        V v;
+#pragma unroll
+        for (int e = 0; e < W; ++e) vset<T>(v, e, r[u * W + e]);
+        reinterpret_cast<V*>(dst)[u] = v;
+    }
+}
+template <typename T, int NT>
+__device__ __forceinline__ void load_row(const T* src, T (&r)[NT]) {
+    using V = typename Vec16<T>::type;
+    constexpr int W = Vec16<T>::N;
+#pragma unroll
+    for (int u = 0; u < NT / W; ++u) {
+        const V v = reinterpret_cast<const V*>(src)[u];
+#pragma unroll
+        for (int e = 0; e < W; ++e) r[u * W + e] = vget<T>(v, e);
+    }
+}
+
+// Whole matrices of the padded order (n == NT) move between HBM and the group
+// as contiguous 16-byte chunks: lane t of a group takes chunks t, t + LPG,
+// t + 2 LPG, ... of each matrix, so one warp-wide access covers whole 128-byte
+// lines (a row-wise access spreads over a line per row).  Chunk c holds
+// elements u W .. u W + W - 1 of row r, with u = c % (NT / W) fixed per lane
+// when LPG is a multiple of NT / W.
+template <typename T, int NT, int LPG>
+struct Chunks {
+    static constexpr int W = 16 / (int)sizeof(T);
+    static constexpr int PER_ROW = NT / W;
+    static constexpr int PER_LANE = NT * PER_ROW / LPG;
+    static constexpr int ROW_STEP = LPG / PER_ROW;  // rows between a lane's chunks
+    static constexpr bool OK = LPG % PER_ROW == 0 && (NT * PER_ROW) % LPG == 0 && PER_LANE <= 16;
+    static constexpr int BATCH = PER_LANE < 8 ? PER_LANE : 8;  // output chunks held at once
+};
+
+// Rows of at least 128 bytes: the forward also moves whole-order matrices
+// as chunks, staged through shared memory (row pitch NT + W elements).
+template <typename T, int NT>
+constexpr bool fwd_chunks() {
+    return NT * (int)sizeof(T) >= 128;
+}
+
+template <typename T, int NT, int RPL, bool VEC, bool FULL>
 __global__ void __launch_bounds__(kBlock)
 small_potrf_kernel(const T* __restrict__ A, T* __restrict__ L, int32_t* __restrict__ status,
                    int64_t batch, int n) {
@@ -138,8 +186,48 @@ small_potrf_kernel(const T* __restrict__ A, T* __restrict__ L, int32_t* __restri
     for (int q = 0; q < RPL; ++q) rows[q] = owned_index(t, q, LPG);
 
     T a[RPL][NT];
+    using CK = Chunks<T, NT, LPG>;
+    constexpr int SP = NT + W;  // staging row pitch (FULL)
+    T* Sg = nullptr;
+    const int cu = t % CK::PER_ROW, cr = t / CK::PER_ROW;
+    if constexpr (FULL) {
+        // A's chunks straight into the group's staging area by cp.async;
+        // what lies above the diagonal (and all of a matrix past the end of
+        // the batch) is zero-filled, then each lane reads its rows
+        static_assert(LPG % CK::PER_ROW == 0 && (NT * CK::PER_ROW) % LPG == 0, "chunk layout");
+        extern __shared__ __align__(16) unsigned char stage_raw[];
+        Sg = reinterpret_cast<T*>(stage_raw) + (size_t)g * NT * SP;
+        const bool in_batch = b < batch;
+        const V* Am = reinterpret_cast<const V*>(in_batch ? A + (size_t)b * NT * NT : A) + t;
 #pragma unroll
-    for (int q = 0; q < RPL; ++q) fetch_fwd_row<T, NT, VEC>(A, b, batch, rows[q], n, a[q]);
+        for (int i = 0; i < CK::PER_LANE; ++i) {
+            const int r = cr + CK::ROW_STEP * i;
+            const int lower = r - cu * W + 1;
+            const uint32_t nb =
+                in_batch ? (uint32_t)(lower <= 0 ? 0 : lower >= W ? 16 : lower * (int)sizeof(T)) : 0u;
+            cp_async16(Sg + r * SP + cu * W, in_batch ? Am + i * LPG : Am, nb);
+        }
+        cp_async_wait_all();
+        lanes_sync<LPG>(g);
+#pragma unroll
+        for (int q = 0; q < RPL; ++q) {
+            load_row<T, NT>(Sg + rows[q] * SP, a[q]);
+            if (!in_batch) {
+#pragma unroll
+                for (int k = 0; k < NT; ++k) a[q][k] = (k == rows[q]) ? T(1) : T(0);
+            }
+        }
+        // a lane's low row (t < LPG) holds nothing at k >= LPG: constants,
+        // not registers, through the recurrence (else they stay live to the
+        // end and cost ~80 registers at order 64)
+        if constexpr (RPL == 2) {
+#pragma unroll
+            for (int k = LPG; k < NT; ++k) a[0][k] = T(0);
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < RPL; ++q) fetch_fwd_row<T, NT, VEC>(A, b, batch, rows[q], n, a[q]);
+    }
 
     int st = 0;
     static_for<0, NT>([&](auto jc) {
@@ -181,6 +269,30 @@ small_potrf_kernel(const T* __restrict__ A, T* __restrict__ L, int32_t* __restri
         });
     });
 
+    if constexpr (FULL) {
+        // rows back into the staging area (zeros above the diagonal), then
+        // out to L as whole chunks
+#pragma unroll
+        for (int q = 0; q < RPL; ++q) {
+            const int i = rows[q];
+            V* dst = reinterpret_cast<V*>(Sg + i * SP);
+#pragma unroll
+            for (int c = 0; c < NT / W; ++c) {
+                V v;
+#pragma unroll
+                for (int e = 0; e < W; ++e) vset<T>(v, e, (c * W + e <= i) ? a[q][c * W + e] : T(0));
+                dst[c] = v;
+            }
+        }
+        lanes_sync<LPG>(g);
+        if (b >= batch) return;
+        V* Lm = reinterpret_cast<V*>(L + (size_t)b * NT * NT) + t;
+#pragma unroll
+        for (int i = 0; i < CK::PER_LANE; ++i)
+            Lm[i * LPG] = *reinterpret_cast<const V*>(Sg + (cr + CK::ROW_STEP * i) * SP + cu * W);
+        if (t == 0) status[b] = st;
+        return;
+    }
     if (b >= batch) return;
 #pragma unroll
     for (int q = 0; q < RPL; ++q) {
@@ -212,31 +324,6 @@ small_potrf_kernel(const T* __restrict__ A, T* __restrict__ L, int32_t* __restri
 // CPL columns (and, after the transpose, CPL rows): columns t and NT-1-t for
 // CPL = 2, which balances the triangular work.  Every broadcast read of a row
 // of L then feeds CPL columns.
-
-// Row r[0..NT) to / from a 16-byte aligned shared-memory row, as vectors.
-template <typename T, int NT>
-__device__ __forceinline__ void store_row(T* dst, const T (&r)[NT]) {
-    using V = typename Vec16<T>::type;
-    constexpr int W = Vec16<T>::N;
-#pragma unroll
-    for (int u = 0; u < NT / W; ++u) {
-        V v;
-#pragma unroll
-        for (int e = 0; e < W; ++e) vset<T>(v, e, r[u * W + e]);
-        reinterpret_cast<V*>(dst)[u] = v;
-    }
-}
-template <typename T, int NT>
-__device__ __forceinline__ void load_row(const T* src, T (&r)[NT]) {
-    using V = typename Vec16<T>::type;
-    constexpr int W = Vec16<T>::N;
-#pragma unroll
-    for (int u = 0; u < NT / W; ++u) {
-        const V v = reinterpret_cast<const V*>(src)[u];
-#pragma unroll
-        for (int e = 0; e < W; ++e) r[u * W + e] = vget<T>(v, e);
-    }
-}
 
 // Phi's factor for row i of column col: 1 below the diagonal, 1/2 on it,
 // 0 above; and the strict-lower indicator k < col.  float uses one saturated
@@ -311,21 +398,6 @@ __device__ __forceinline__ void pad_row(int row, T pad_diag, T (&r)[NT]) {
 #pragma unroll
     for (int k = 0; k < NT; ++k) r[k] = (k == row) ? pad_diag : T(0);
 }
-
-// Whole matrices of the padded order (n == NT) move between HBM and the group
-// as contiguous 16-byte chunks: lane t of a group takes chunks t, t + LPG,
-// t + 2 LPG, ... of each matrix, so one warp-wide access covers whole 128-byte
-// lines (a row-wise access spreads over a line per row).  Chunk c holds
-// elements u W .. u W + W - 1 of row r, with u = c % (NT / W) fixed per lane
-// when LPG is a multiple of NT / W.
-template <typename T, int NT, int LPG>
-struct Chunks {
-    static constexpr int W = 16 / (int)sizeof(T);
-    static constexpr int PER_ROW = NT / W;
-    static constexpr int PER_LANE = NT * PER_ROW / LPG;
-    static constexpr int ROW_STEP = LPG / PER_ROW;  // rows between a lane's chunks
-    static constexpr bool OK = LPG % PER_ROW == 0 && (NT * PER_ROW) % LPG == 0 && PER_LANE <= 8;
-};
 
 // adj_A is read only at the adjoint's end: one lane per matrix starts bringing
 // it into L2 at the start, so that read finds it there (orders up to 32; at 64
@@ -588,27 +660,33 @@ small_potrf_adj_kernel(const T* __restrict__ Lg, const T* __restrict__ Lbar,
         // keep the adj_A loads here: hoisted into the solves they hold
         // registers that cost occupancy
         asm volatile("" ::: "memory");
-        V av[CK::PER_LANE];
+        static_for<0, CK::PER_LANE / CK::BATCH>([&](auto hc) {
+            constexpr int i0 = decltype(hc)::value * CK::BATCH;
+            V av[CK::BATCH];
 #pragma unroll
-        for (int i = 0; i < CK::PER_LANE; ++i)
-            av[i] = (accumulate && cu * W <= cr + CK::ROW_STEP * i) ? Am[i * LPG] : V{};
-#pragma unroll
-        for (int i = 0; i < CK::PER_LANE; ++i) {
-            const int r = cr + CK::ROW_STEP * i;
-            if (cu * W > r) continue;
-            const V x = *reinterpret_cast<const V*>(R + r * RP + cu * W);
-            V v;
-#pragma unroll
-            for (int e = 0; e < W; ++e) vset<T>(v, e, vget<T>(av[i], e) + vget<T>(x, e));
-            if (cu * W + W - 1 <= r) {
-                Am[i * LPG] = v;
-            } else {
-                T* ap = reinterpret_cast<T*>(Am + i * LPG);
-#pragma unroll
-                for (int e = 0; e < W; ++e)
-                    if (cu * W + e <= r) ap[e] = vget<T>(v, e);
+            for (int ii = 0; ii < CK::BATCH; ++ii) {
+                const int i = i0 + ii;
+                av[ii] = (accumulate && cu * W <= cr + CK::ROW_STEP * i) ? Am[i * LPG] : V{};
             }
-        }
+#pragma unroll
+            for (int ii = 0; ii < CK::BATCH; ++ii) {
+                const int i = i0 + ii;
+                const int r = cr + CK::ROW_STEP * i;
+                if (cu * W > r) continue;
+                const V x = *reinterpret_cast<const V*>(R + r * RP + cu * W);
+                V v;
+#pragma unroll
+                for (int e = 0; e < W; ++e) vset<T>(v, e, vget<T>(av[ii], e) + vget<T>(x, e));
+                if (cu * W + W - 1 <= r) {
+                    Am[i * LPG] = v;
+                } else {
+                    T* ap = reinterpret_cast<T*>(Am + i * LPG);
+#pragma unroll
+                    for (int e = 0; e < W; ++e)
+                        if (cu * W + e <= r) ap[e] = vget<T>(v, e);
+                }
+            }
+        });
         return;
     }
 
@@ -667,8 +745,23 @@ cudaError_t launch_fwd_nt(const T* A, T* L, int32_t* status, int64_t batch, int 
     constexpr int RPL = (NT * (int)sizeof(T) <= 256) ? 2 : 1;
     constexpr int G = kBlock / (NT / RPL);
     const int64_t blocks = (batch + G - 1) / G;
-    small_potrf_kernel<T, NT, RPL, VEC><<<(unsigned)blocks, kBlock, 0, stream>>>(A, L, status,
-                                                                                 batch, n);
+    if constexpr (VEC && fwd_chunks<T, NT>()) {
+        if (n == NT) {
+            constexpr size_t smem = (size_t)G * NT * (NT + 16 / sizeof(T)) * sizeof(T);
+            auto kern = small_potrf_kernel<T, NT, RPL, VEC, true>;
+            static int smem_set = 0;
+            if (smem > 48 * 1024 && !smem_set) {
+                cudaError_t e =
+                    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                if (e != cudaSuccess) return e;
+                smem_set = 1;
+            }
+            kern<<<(unsigned)blocks, kBlock, smem, stream>>>(A, L, status, batch, n);
+            return cudaGetLastError();
+        }
+    }
+    small_potrf_kernel<T, NT, RPL, VEC, false><<<(unsigned)blocks, kBlock, 0, stream>>>(
+        A, L, status, batch, n);
     return cudaGetLastError();
 }
 
