@@ -106,9 +106,9 @@ def launches_per_step(n: int, tile: int) -> int:
 # capture summarised in profiles/batched_16_kernels.md.  Reported only while
 # the kernel source still hashes to what was captured; otherwise null.
 MEASURED_TRAFFIC = {
-    "batched_16": {"kernel": "adj", "bytes": (201.641472 + 23.832832) * 1e6,
+    "batched_16": {"kernel": "adj", "bytes": (201.631744 + 23.393024) * 1e6,
                    "source": "differentiable_cholesky_gb300/csrc/small_kernels.cuh",
-                   "sha256": "1aff82685d317c5d5cf19a771af73298eb92a575a61412e4bcd5b2a92721c514"},
+                   "sha256": "7f46ea03a4e5efe403a315c1cf3d51f89a04f44f4a2be40d259653c9f316e5fd"},
 }
 
 
@@ -311,6 +311,10 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="batched_16")
     ap.add_argument("--e2e-steps", type=int, default=None,
                     help="end-to-end steps (default: 20 for n <= 64, else 1)")
+    ap.add_argument("--e2e-chunks", type=int, default=4,
+                    help="chunks of the batch in the end-to-end step (n <= 64)")
+    ap.add_argument("--e2e-streams", type=int, default=2,
+                    help="streams the end-to-end chunks rotate over")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     batch, n, np_dtype, desc, tile = WORKLOADS[args.workload]
@@ -439,8 +443,8 @@ def main():
     # copies overlap (the copy engines of the two directions and the SMs work
     # at once).  Every input is still copied in and every result read back
     # inside the step.
-    n_streams = 3
-    chunks = max(1, min(8, batch // 4096)) if n <= 64 else 1
+    n_streams = max(1, args.e2e_streams)
+    chunks = max(1, min(args.e2e_chunks, batch // 1024)) if n <= 64 else 1
     bounds = [batch * c // chunks for c in range(chunks + 1)]
     streams = [torch.cuda.Stream() for _ in range(n_streams)]
 
