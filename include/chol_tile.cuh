@@ -20,8 +20,11 @@
  *     storage: RowMajor{ld} (row-major, leading dimension ld) or PackedLower
  *     (the lower triangle packed by rows, n (n + 1) / 2 elements).  Only
  *     elements on and below the diagonal are read or written.
- *   - Arithmetic is in T (float or double), with the correctly rounded square
- *     root and reciprocal; no wait is unbounded and nothing traps.
+ *   - Arithmetic is in T (float or double).  For a pivot d the factor takes
+ *     1 / l_jj = rsqrt(d) from CUDA's reciprocal square root and
+ *     l_jj = d * rsqrt(d): one transcendental per column on the serial chain,
+ *     within a few ulp of the correctly rounded values.  The adjoint divides
+ *     by l_jj.  No wait is unbounded and nothing traps.
  */
 #ifndef CHOL_TILE_CUH
 #define CHOL_TILE_CUH
@@ -40,10 +43,8 @@ struct PackedLower {
 };
 
 namespace detail {
-__device__ __forceinline__ float sqrt_rn(float x) { return __fsqrt_rn(x); }
-__device__ __forceinline__ double sqrt_rn(double x) { return __dsqrt_rn(x); }
-__device__ __forceinline__ float rcp_rn(float x) { return __frcp_rn(x); }
-__device__ __forceinline__ double rcp_rn(double x) { return __drcp_rn(x); }
+__device__ __forceinline__ float rsqrt_t(float x) { return rsqrtf(x); }
+__device__ __forceinline__ double rsqrt_t(double x) { return rsqrt(x); }
 }  // namespace detail
 
 /*
@@ -63,8 +64,8 @@ __device__ int potrf(T* a, int n, Idx at) {
             __syncthreads();
             return j + 1;
         }
-        const T ljj = detail::sqrt_rn(d);
-        const T inv = detail::rcp_rn(ljj);  // one reciprocal per column, then products
+        const T inv = detail::rsqrt_t(d);  // 1 / l_jj, then products
+        const T ljj = d * inv;
         __syncthreads();                     // every thread has read the pivot
         for (int i = j + 1 + tid; i < n; i += THREADS) a[at(i, j)] *= inv;
         if (tid == 0) a[at(j, j)] = ljj;
@@ -111,10 +112,16 @@ __device__ void potrf_adj(const T* l, T* w, int n, Idx at) {
         if (tid == 0) w[at(j, j)] = (w[at(j, j)] - sum * inv) * inv;
         __syncthreads();
         // row j left of the diagonal: w_jk -= sum_{i >= j} w_ij l_ik
+        // (two partial sums halve the dependent chain)
         for (int k = tid; k < j; k += THREADS) {
-            T acc = T(0);
-            for (int i = j; i < n; ++i) acc = fma(w[at(i, j)], l[at(i, k)], acc);
-            w[at(j, k)] -= acc;
+            T acc0 = T(0), acc1 = T(0);
+            int i = j;
+            for (; i + 1 < n; i += 2) {
+                acc0 = fma(w[at(i, j)], l[at(i, k)], acc0);
+                acc1 = fma(w[at(i + 1, j)], l[at(i + 1, k)], acc1);
+            }
+            if (i < n) acc0 = fma(w[at(i, j)], l[at(i, k)], acc0);
+            w[at(j, k)] -= acc0 + acc1;
         }
         // rows below, left of column j: w_ik -= w_ij l_jk
         const int ty = tid / 16, tx = tid % 16;
