@@ -282,7 +282,9 @@ def run_reference(args, w, desc):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32" if w.dtype == np.float32 else "f64", "data": "synthetic",
-        "config": {"workload": desc, "batch": w.batch, "n": w.n,
+        "config": {"workload": f"{args.workload}: {desc}", "batch_per_gpu": w.batch, "n": w.n,
+                   "tile": (WORKLOADS[args.workload][4] or "default") if w.n > 64 else None,
+                   "parallelism": "host, one thread",
                    "step": f"oracle fwd + adjoint over {count} matrices of the batch"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"{count} of {w.batch} matrices per step, one thread"},
