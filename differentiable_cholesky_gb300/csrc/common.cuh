@@ -61,8 +61,6 @@ __device__ __forceinline__ float rsqrt_t(float x) { return rsqrtf(x); }
 __device__ __forceinline__ double rsqrt_t(double x) { return rsqrt(x); }
 __device__ __forceinline__ float rcp_t(float x) { return __frcp_rn(x); }
 __device__ __forceinline__ double rcp_t(double x) { return __drcp_rn(x); }
-__device__ __forceinline__ float sqrt_t(float x) { return __fsqrt_rn(x); }
-__device__ __forceinline__ double sqrt_t(double x) { return __dsqrt_rn(x); }
 
 }  // namespace chol
 
