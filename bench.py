@@ -313,10 +313,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="batched_16")
     ap.add_argument("--e2e-steps", type=int, default=None,
                     help="end-to-end steps (default: 20 for n <= 64, else 1)")
-    ap.add_argument("--e2e-chunks", type=int, default=4,
+    ap.add_argument("--e2e-chunks", type=int, default=2,
                     help="chunks of the batch in the end-to-end step (n <= 64)")
-    ap.add_argument("--e2e-streams", type=int, default=2,
-                    help="streams the end-to-end chunks rotate over")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     batch, n, np_dtype, desc, tile = WORKLOADS[args.workload]
@@ -438,51 +436,56 @@ def main():
     hL = torch.empty_like(hA).pin_memory()
     hG = torch.empty_like(hA).pin_memory()
     hst = torch.empty(batch, dtype=torch.int32).pin_memory()
-    dA, dLb, dL, dG, dst = sets[0]
 
-    # The batch goes through in chunks on a few streams, so that one chunk's
-    # host-to-device copies, another's kernels and a third's device-to-host
-    # copies overlap (the copy engines of the two directions and the SMs work
-    # at once).  Every input is still copied in and every result read back
-    # inside the step.
-    n_streams = max(1, args.e2e_streams)
+    # The batch goes through in chunks, and consecutive steps use the two
+    # device buffer sets in turn: chunk c of a step on set k % 2 runs on its
+    # own stream, so one chunk's host-to-device copies, another's kernels and
+    # a third's (or the previous step's) device-to-host copies overlap, while
+    # each (set, chunk) pair stays ordered on its stream.  Every input is
+    # still copied in and every result read back once per step.
     chunks = max(1, min(args.e2e_chunks, batch // 1024)) if n <= 64 else 1
     bounds = [batch * c // chunks for c in range(chunks + 1)]
-    streams = [torch.cuda.Stream() for _ in range(n_streams)]
+    streams = [torch.cuda.Stream() for _ in range(2 * chunks)]
+    host_out = [(hL, hG, hst), (torch.empty_like(hL).pin_memory(), torch.empty_like(hG).pin_memory(),
+                                torch.empty_like(hst).pin_memory())]
+    n_streams = len(streams)
 
-    def e2e_step():
-        go = torch.cuda.Event()
-        go.record(stream)
-        done = []
+    def e2e_step(k):
+        dA_, dLb_, dL_, dG_, dst_ = sets[k & 1]
+        hL_, hG_, hst_ = host_out[k & 1]
         for c in range(chunks):
             b0, b1 = bounds[c], bounds[c + 1]
-            s = streams[c % n_streams]
-            s.wait_event(go)
+            s = streams[(k & 1) * chunks + c]
             with torch.cuda.stream(s):
-                dA[b0:b1].copy_(hA[b0:b1], non_blocking=True)
-                dLb[b0:b1].copy_(hLb[b0:b1], non_blocking=True)
-                dG[b0:b1].zero_()
-                binding.chol_fwd(dA[b0:b1], L=dL[b0:b1], status=dst[b0:b1], tile=tile, stream=s)
-                binding.chol_adj(dL[b0:b1], dLb[b0:b1], adj_A=dG[b0:b1], status=dst[b0:b1],
+                dA_[b0:b1].copy_(hA[b0:b1], non_blocking=True)
+                dLb_[b0:b1].copy_(hLb[b0:b1], non_blocking=True)
+                dG_[b0:b1].zero_()
+                binding.chol_fwd(dA_[b0:b1], L=dL_[b0:b1], status=dst_[b0:b1], tile=tile, stream=s)
+                binding.chol_adj(dL_[b0:b1], dLb_[b0:b1], adj_A=dG_[b0:b1], status=dst_[b0:b1],
                                  tile=tile, stream=s)
-                hL[b0:b1].copy_(dL[b0:b1], non_blocking=True)
-                hst[b0:b1].copy_(dst[b0:b1], non_blocking=True)
-                hG[b0:b1].copy_(dG[b0:b1], non_blocking=True)
+                hL_[b0:b1].copy_(dL_[b0:b1], non_blocking=True)
+                hst_[b0:b1].copy_(dst_[b0:b1], non_blocking=True)
+                hG_[b0:b1].copy_(dG_[b0:b1], non_blocking=True)
+
+    def e2e_run(count):
+        go = torch.cuda.Event()
+        go.record(stream)
+        for s in streams:
+            s.wait_event(go)
+        for k in range(count):
+            e2e_step(k)
+        for s in streams:
             ev = torch.cuda.Event()
             ev.record(s)
-            done.append(ev)
-        for ev in done:
             stream.wait_event(ev)
 
-    for _ in range(3 if n <= 64 else 1):
-        e2e_step()
+    e2e_run(3 if n <= 64 else 1)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist is not None:
         dist.barrier()
     e0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
+    e2e_run(args.e2e_steps)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
@@ -546,7 +549,8 @@ def main():
         "e2e": {"value": e2e_value, "unit": UNIT,
                 "h2d_bytes_per_step": int(hA.numel() * esize + hLb.numel() * esize),
                 "d2h_bytes_per_step": int(hL.numel() * esize + hG.numel() * esize + hst.numel() * 4),
-                "steps": args.e2e_steps, "chunks": chunks, "streams": n_streams},
+                "steps": args.e2e_steps, "chunks": chunks, "streams": n_streams,
+                "overlap": "chunks on their own streams; consecutive steps on alternate buffer sets"},
         "clocks": clocks,
         "inplace": {"value": batch * world / ((ip_fwd_ms + ip_adj_ms) / 1e3), "unit": UNIT,
                     "fwd_ms": ip_fwd_ms, "adj_ms": ip_adj_ms, "steps": ip_steps,
