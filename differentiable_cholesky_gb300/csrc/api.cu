@@ -94,6 +94,9 @@ int adj_impl(int64_t batch, int32_t n, const void* L, const void* Lbar, void* Ab
         return to_code(chol::small_adj<T>(l, lb, ab, status, batch, n, vec, accumulate, stream));
     }
     if (tile == 0) tile = chol::blocked_default_tile(n, batch);
+    if (!accumulate && Lbar == Abar)  // in place: the sweep needs no workspace
+        return to_code(chol::blocked_adj<T>(l, lb, ab, status, batch, n, tile, nullptr, false,
+                                            stream));
     void* work = nullptr;
     if (cudaMallocAsync(&work, bytes, stream) != cudaSuccess) {
         cudaGetLastError();

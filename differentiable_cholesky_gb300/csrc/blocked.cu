@@ -353,7 +353,11 @@ gemm_kernel(GemmArgs<T> g) {
             for (int j = 0; j < MT; ++j) {
                 const int c = ccol0 + tx * MT + j;
                 if (c >= g.n) continue;
-                if (MODE == GEMM_FWD_TRAIL && c > r) continue;  // L stays zero above the diagonal
+                // nothing above the diagonal is written: L stays zero there, and the
+                // reverse sweep (which may run on the caller's own buffer) never
+                // touches W's upper triangle
+                if ((MODE == GEMM_FWD_TRAIL || (MODE == GEMM_REV_ROW && job.ci == job.cj)) && c > r)
+                    continue;
                 T* cp = Cb + (int64_t)r * g.n + c;
                 T v = T(job.alpha) * acc[i][j];
                 if (g.atomic) {
@@ -493,6 +497,21 @@ lower_add_kernel(const T* __restrict__ src, T* __restrict__ dst,
     }
 }
 
+// Lower triangle of every matrix with status != 0 set to zero (the in-place
+// adjoint's rule for skipped matrices); nothing else is touched.
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+zero_lower_skipped_kernel(T* __restrict__ dst, const int32_t* __restrict__ status, int64_t batch,
+                          int n) {
+    const int64_t nn = (int64_t)n * n;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < batch * nn;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t b = e / nn, w = e % nn;
+        const int i = (int)(w / n), j = (int)(w % n);
+        if (j <= i && skip_matrix(status, b)) dst[e] = T(0);
+    }
+}
+
 inline unsigned elementwise_blocks(int64_t total) {
     return (unsigned)std::max<int64_t>(1, std::min<int64_t>((total + kThreads - 1) / kThreads,
                                                             152 * 16));
@@ -568,9 +587,17 @@ cudaError_t blocked_adj(const T* L, const T* Lbar, T* Abar, const int32_t* statu
                         cudaStream_t stream) {
     const int nt = (n + tile - 1) / tile;
     const int64_t total = batch * (int64_t)n * n;
-    lower_copy_kernel<T><<<elementwise_blocks(total), kThreads, 0, stream>>>(Lbar, W, status,
-                                                                            batch, n);
-    CHOL_TRY(cudaGetLastError());
+    // In place (the gradient written over its seed): the sweep runs on the
+    // caller's buffer itself, whose lower triangle already holds adj_L; no
+    // stage reads or writes its upper triangle, so no workspace is needed.
+    const bool in_place = !accumulate && Lbar == Abar;
+    if (in_place) {
+        W = Abar;
+    } else {
+        lower_copy_kernel<T><<<elementwise_blocks(total), kThreads, 0, stream>>>(Lbar, W, status,
+                                                                                batch, n);
+        CHOL_TRY(cudaGetLastError());
+    }
     static int diag_smem_set = 0;
     CHOL_TRY(allow_smem(diag_rev_kernel<T, kThreads>, (size_t)128 * 129 * sizeof(T),
                         &diag_smem_set));
@@ -608,8 +635,14 @@ cudaError_t blocked_adj(const T* L, const T* Lbar, T* Abar, const int32_t* statu
             CHOL_TRY((launch_gemm<T, GEMM_REV_SYM>(g, J, stream)));
         }
     }
-    lower_add_kernel<T><<<elementwise_blocks(total), kThreads, 0, stream>>>(W, Abar, status,
-                                                                           batch, n, accumulate);
+    if (in_place) {
+        if (status != nullptr)
+            zero_lower_skipped_kernel<T><<<elementwise_blocks(total), kThreads, 0, stream>>>(
+                Abar, status, batch, n);
+    } else {
+        lower_add_kernel<T><<<elementwise_blocks(total), kThreads, 0, stream>>>(W, Abar, status,
+                                                                               batch, n, accumulate);
+    }
     return cudaGetLastError();
 }
 

@@ -45,6 +45,8 @@ template <typename T>
 cudaError_t blocked_fwd(const T* A, T* L, int32_t* status, int64_t batch, int n, int tile,
                         cudaStream_t stream);
 // `work` holds batch * n * n elements of scratch.  accumulate as small_adj.
+// Not accumulating with adj_A == adj_L (in place), the sweep runs on adj_A
+// itself and `work` is not used (may be null).
 template <typename T>
 cudaError_t blocked_adj(const T* L, const T* Lbar, T* Abar, const int32_t* status,
                         int64_t batch, int n, int tile, T* work, bool accumulate,

@@ -167,7 +167,9 @@ CHOL_API int chol_fwd_inplace(int64_t batch, int32_t n, int32_t dtype, void* A, 
  *                matrix with non-zero status gets zeros there.  The upper
  *                triangle is never written.
  *   status  in : as chol_adj (or NULL).  Must not overlap adj.
- *   tile    as chol_adj_ex; n > 64 takes the same workspace as chol_adj.
+ *   tile    as chol_adj_ex.  No workspace is taken for any n: the blocked
+ *           reverse sweep runs on `adj` itself (it never touches the upper
+ *           triangle), so the call allocates nothing.
  * Results are bit-identical to chol_adj_ex into a zeroed adj_A.
  */
 CHOL_API int chol_adj_inplace(int64_t batch, int32_t n, int32_t dtype, const void* L, void* adj,
