@@ -89,6 +89,38 @@ def test_inplace_argument_checks_without_gpu():
     assert lib.chol_adj_inplace(1, 2, 1, p, p + 64, None, 0, None) == CHOL_EINVAL
 
 
+def test_selftest_argument_checks_without_gpu():
+    lib = binding.load_library()
+    lib.chol_selftest_wait_timeout.argtypes = [ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                                               ctypes.c_void_p, ctypes.c_uint32, ctypes.c_void_p]
+    buf = (ctypes.c_float * 512)()
+    st = (ctypes.c_int32 * 2)()
+    p, s = ctypes.addressof(buf), ctypes.addressof(st)
+    assert lib.chol_selftest_wait_timeout(0, None, None, None, 10, None) == CHOL_OK
+    assert lib.chol_selftest_wait_timeout(-1, p, p, s, 10, None) == CHOL_EINVAL
+    assert lib.chol_selftest_wait_timeout(1, p, p + 1024, s, 0, None) == CHOL_EINVAL
+    assert lib.chol_selftest_wait_timeout(1, None, p, s, 10, None) == CHOL_EINVAL
+    # host memory is rejected (not a device pointer)
+    assert lib.chol_selftest_wait_timeout(1, p, p + 1024, s, 10, None) == CHOL_EINVAL
+
+
+def test_tile_header_compiles_in_a_user_kernel():
+    """include/chol_tile.cuh is header-only device code: the test kernels that
+    use it as a caller would must compile for sm_103a with only include/ on the
+    path (the GPU test runs them)."""
+    import shutil
+    import subprocess
+    import tempfile
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(nvcc):
+        pytest.skip("nvcc not available")
+    src = os.path.join(ROOT, "tests", "tile_api", "tile_api_kernels.cu")
+    with tempfile.TemporaryDirectory() as d:
+        subprocess.run([nvcc, "-std=c++17", "-O1", "-I", os.path.join(ROOT, "include"),
+                        "-gencode", "arch=compute_103a,code=sm_103a", "-c", src,
+                        "-o", os.path.join(d, "t.o")], check=True)
+
+
 def test_size_overflow_rejected():
     lib = binding.load_library()
     buf = (ctypes.c_double * 4)()
