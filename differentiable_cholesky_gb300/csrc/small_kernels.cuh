@@ -6,8 +6,9 @@
 //
 // A group of LPG lanes owns one matrix of padded order NT = 8, 16, 32 or 64
 // (the next size >= n); each lane owns two rows (or columns) of it, t and
-// NT-1-t, where registers allow (LPG = NT / 2), else one.  A 128-thread block
-// holds 128 / LPG groups.  A matrix of order n < NT is padded to
+// NT-1-t, where registers allow (LPG = NT / 2), else one.  A block holds
+// several groups: 128 threads, or one warp for the adjoint at NT <= 16.  A
+// matrix of order n < NT is padded to
 // blockdiag(A, I), whose factor is blockdiag(L, I) and whose adjoint (with a
 // zero-padded adj_L) is blockdiag(adj_A, 0): the padding changes no result.
 // Every loop over matrix indices is fully unrolled, so each lane keeps its
@@ -21,11 +22,17 @@
 //   broadcast), sets l_ij = a_ij * r and updates its trailing entries
 //   a_ik -= (l_ij r) a_kj.  A pivot that is not > 0 records status j + 1
 //   (first failure only) and is replaced by 1 so the rest of the (unspecified)
-//   factor stays finite and the group stays convergent.
+//   factor stays finite and the group stays convergent.  A lane's low row
+//   (t < LPG) skips the columns k >= LPG, which lie above its diagonal.
+//   Full-order matrices with rows of 128 bytes or more move as contiguous
+//   16-byte chunks through a shared staging area (cp.async in, chunk stores
+//   out) instead of row by row.
 //
 // Adjoint (Murray 2016 as NVIDIA/warp issue #1316's closing comment states it:
 // S = Phi(L^T adj_L), then solves against L^T and L, accumulated into the lower
-// triangle of adj_A).  L is staged in shared memory and read by broadcast.
+// triangle of adj_A).  L is staged in shared memory with packed rows and read
+// by broadcast; the reciprocals of its diagonal sit in the transpose buffer's
+// padding.
 //   1. each lane takes its columns of tril(adj_L) and forms the same columns
 //      of P = L^T tril(adj_L) in place (outer-product order over rows of L);
 //   2. S = Phi(P) on those columns;
@@ -33,8 +40,11 @@
 //   4. transpose through shared memory: the lane takes the same rows of X;
 //   5. M = X L^-1: back substitution on the rows (rows of L broadcast);
 //   6. transpose once more and add M_tk + M_kt (k < t) and M_tt into the
-//      lane's rows of adj_A's lower triangle.  Matrices with status != 0 are
-//      skipped.
+//      lane's rows of adj_A's lower triangle (or write them there, for the
+//      in-place form).  Matrices with status != 0 are skipped (or zeroed).
+// Full-order matrices move as contiguous chunks (cp.async into their shared
+// places, chunk stores out); blocks take the batch from its end, so right
+// after the forward the factors still in L2 are read first.
 
 #pragma once
 

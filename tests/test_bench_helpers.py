@@ -51,3 +51,18 @@ def test_reference_arm_prints_one_json_line():
     assert d["impl"] == "reference" and d["unit"] == "matrices/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle"
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_code_hash_ignores_comments_but_not_code():
+    import bench
+    src = "int f(int x) {  // doubles x\n    /* block\n comment */ return 2 * x;\n}\n"
+    same = "// a new header line\nint f(int x) {\n\n    return 2 * x;   // still doubles\n}\n"
+    other = "int f(int x) {\n    return 3 * x;\n}\n"
+    assert bench.code_sha256(src) == bench.code_sha256(same)
+    assert bench.code_sha256(src) != bench.code_sha256(other)
+
+
+def test_traffic_record_matches_the_current_kernel_source():
+    import bench
+    assert bench.measured_traffic("batched_16", "adj") is not None
+    assert bench.measured_traffic("batched_16", "fwd") is None
