@@ -108,17 +108,18 @@ def launches_per_step(n: int, tile: int) -> int:
 MEASURED_TRAFFIC = {
     "batched_16": {"kernel": "adj", "bytes": (201.627904 + 23.920896) * 1e6,
                    "source": "differentiable_cholesky_gb300/csrc/small_kernels.cuh",
-                   "code_sha256": "a015646f85f03f474c06e11ce363e5798e4d810e9e36a84a044b9fb4ebd2bb63"},
+                   "code_sha256": "65783f7da4b7300d2208efe580890165b364e544a7082868691a0351e74e3502"},
 }
 
 
 def code_sha256(text: str) -> str:
-    """sha256 of a C/CUDA source with its comments and blank lines removed, so
-    that a comment edit does not retire a measurement but a code edit does."""
+    """sha256 of a C/CUDA source with its comments, indentation and blank lines
+    removed, so that a comment edit does not retire a measurement but a code
+    edit does."""
     import hashlib
     import re
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    lines = [re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines()]
+    lines = [re.sub(r"//.*$", "", ln).strip() for ln in text.splitlines()]
     return hashlib.sha256("\n".join(ln for ln in lines if ln).encode()).hexdigest()
 
 
