@@ -1,17 +1,20 @@
 #!/usr/bin/env python3
 """Throughput benchmark of the Cholesky forward + adjoint hot path on GB300.
 
-One step = ``chol_fwd`` then ``chol_adj`` over one batch of synthetic input
-(default workload: 65536 independent 16x16 float32 SPD matrices,
-``A = G G^T / 16 + I``, ``adj_L = tril(N(0, 1))``).  Inputs are resident in HBM
-when the timed region starts; each step reads 256 MiB of distinct buffers, more
-than the 129 MB L2, and steps alternate between two buffer sets.
+One step = ``chol_fwd`` then ``chol_adj`` over one batch of synthetic input,
+inputs resident in HBM when the timed region starts.  The default workload is
+the largest single-GPU configuration: one 8192x8192 float64 ``A = E E^T``
+(``E`` lower banded, bandwidth 32), tile 128, ``adj_L = tril(N(0, 1))``.  In
+the same process the four other workloads (batched 65536 x 16x16 and
+8192 x 64x64 float32, one 512x512 bidiagonal and 256 x 512x512 float64) are
+timed kernel by kernel and reported under ``workloads``.
 
 Prints ONE JSON line (rank 0).  ``value`` = matrices/s over all ranks,
 ``e2e`` = the same metric through the public API with pinned host buffers and
-the host<->device copies inside the timed region, ``roofline`` = the dominant
-kernel's algorithmic bandwidth against the measured HBM copy peak,
-``cpu_baseline`` = the CPU oracle on the same workload.
+the host<->device copies inside the timed region, ``roofline`` = the
+dominant call against its measured roof (HBM copy bandwidth for the batched
+small matrices, the measured FP64 rate for the blocked path),
+``cpu_baseline`` = the CPU oracle on a bounded sample of the same workload.
 
 ``--impl reference`` times the CPU oracle itself as the reference arm.
 Multi-GPU (torchrun): every rank factors its own batch (weak scaling, no
@@ -39,6 +42,7 @@ METRIC = "Cholesky fwd+adjoint matrices/s and GFLOP/s (1 GB300), % of HBM/FP64 r
 UNIT = "matrices/s"
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1024 * 1024
+DEFAULT_WORKLOAD = "banded_8192"
 
 
 # ----------------------------------------------------------------------------
@@ -58,6 +62,12 @@ WORKLOADS = {
     "banded_8192": (1, 8192, np.float64,
                     "1 x 8192x8192 fp64, A = E E^T with E lower banded (bandwidth 32), tile 128", 128),
 }
+
+# Timed steps of the workloads reported beside the main line (each timed
+# region spans well over 100 ms, so the clock sampler sees it).
+EXTRA_STEPS = {"batched_16": 3000, "batched_64": 1000, "bidiagonal_512": 100,
+               "batched_512": 10, "banded_8192": 3}
+
 
 def lower_sector_bytes(n: int, esize: int) -> int:
     """Bytes of the 32-byte DRAM sectors that hold the lower triangle of one
@@ -82,12 +92,13 @@ def executed_flops(n: int):
     return n ** 3 / 3.0, 2.0 * n ** 3 / 3.0
 
 
-def default_tile(n: int, batch: int) -> int:
-    """The library's default blocked tile (mirrors blocked_default_tile)."""
+def default_tile(n: int, batch: int, sms: int = 152) -> int:
+    """The library's default blocked tile (mirrors blocked_default_tile) for
+    a device with `sms` multiprocessors."""
     if n >= 2048:
         return 128
     per_side = (n + 63) // 64
-    return 64 if batch * per_side * per_side >= 4 * 152 else 32
+    return 64 if batch * per_side * per_side >= 4 * sms else 32
 
 
 def launches_per_step(n: int, tile: int) -> int:
@@ -102,8 +113,8 @@ def launches_per_step(n: int, tile: int) -> int:
     return fwd + adj
 
 
-# DRAM bytes (read + write) per launch of the dominant kernel, from the ncu
-# capture summarised in profiles/batched_16_kernels.md.  Reported only while
+# DRAM bytes (read + write) per launch of a dominant kernel, from an ncu
+# capture of that kernel (the summaries under profiles/).  Reported only while
 # the kernel source still hashes to what was captured; otherwise null.
 MEASURED_TRAFFIC = {
     "batched_16": {"kernel": "adj", "bytes": (201.627904 + 23.920896) * 1e6,
@@ -153,7 +164,7 @@ def read_peaks():
 
 
 # ----------------------------------------------------------------------------
-# Clock sampling during the timed region
+# Clock sampling during the timed regions
 # ----------------------------------------------------------------------------
 
 class ClockSampler:
@@ -247,57 +258,98 @@ def gpu_identifier(torch):
 # CPU oracle timing (cpu_baseline leg and the reference arm)
 # ----------------------------------------------------------------------------
 
-def time_oracle(w, count: int, threads: int = 1):
-    """Oracle fwd + adjoint over the first `count` matrices; returns seconds."""
+def host_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def time_oracle(A, Lbar, threads: int):
+    """Oracle fwd + adjoint over the matrices of A; returns seconds."""
     import oracle
-    A = w.A[:count]
-    Lbar = w.adj_L[:count]
     t0 = time.perf_counter()
     L, st = oracle.potrf(A, threads=threads)
     oracle.potrf_adj(L, Lbar, status=st, threads=threads)
     return time.perf_counter() - t0
 
 
-def oracle_sample_size(w, budget_s: float = 2.0, cap: int | None = None):
-    """Matrices the oracle handles in about `budget_s` seconds (one thread)."""
-    probe = min(w.batch, 256)
-    t = max(time_oracle(w, probe), 1e-6)
-    count = int(min(w.batch, max(probe, probe * budget_s / t)))
-    if cap is not None:
-        count = min(count, cap)
-    return count
+class OracleSample:
+    """A bounded sample of a workload for the CPU oracle, and how one timed
+    sample scales to matrices/s of the full workload.
+
+    Batched workloads take their first `count` matrices (the unit is the
+    matrix, so the scale is 1).  A single matrix of order n takes its leading
+    m x m principal block (itself SPD, from the same construction) and counts
+    as (m/n)^3 of a matrix, the share of the n^3 flops it does; the oracle's
+    column-strided solves only get slower per flop as m grows, so this
+    extrapolation flatters the oracle."""
+
+    def __init__(self, w, budget_s: float, threads: int):
+        self.w, self.threads = w, threads
+        if w.batch > 1:
+            probe = min(w.batch, 64)
+            t = max(time_oracle(w.A[:probe], w.adj_L[:probe], threads), 1e-6)
+            self.count = int(min(w.batch, max(probe, probe * budget_s / t)))
+            self.m = w.n
+            self.A, self.Lbar = w.A[:self.count], w.adj_L[:self.count]
+            self.units = float(self.count)
+            self.desc = f"first {self.count} of {w.batch} matrices"
+        else:
+            m = min(w.n, 256)
+            t = max(time_oracle(*self._block(m), threads), 1e-6)
+            # the literal adjoint grows faster than m^3 (its column accesses
+            # leave the caches): grow m by halving steps of the cube root
+            while m < w.n:
+                m2 = min(w.n, int(m * 1.26) // 64 * 64 or m + 64)
+                if t * (m2 / m) ** 4 > budget_s:
+                    break
+                m = m2
+                t = max(time_oracle(*self._block(m), threads), 1e-6)
+            self.count = 1
+            self.m = m
+            self.A, self.Lbar = self._block(m)
+            self.units = (m / w.n) ** 3
+            self.desc = (f"leading {m}x{m} principal block of the {w.n}x{w.n} matrix, "
+                         f"counted as (m/n)^3 = {self.units:.3g} of a matrix")
+
+    def _block(self, m):
+        # a single (2-D) matrix: the oracle's threaded single-matrix routines
+        A = np.ascontiguousarray(self.w.A[0, :m, :m])
+        Lb = np.ascontiguousarray(self.w.adj_L[0, :m, :m])
+        return A, Lb
+
+    def run(self) -> float:
+        return time_oracle(self.A, self.Lbar, self.threads)
 
 
 def cpu_baseline(w):
-    count = oracle_sample_size(w, budget_s=3.0)
-    t = time_oracle(w, count)
-    return {"value": count / t, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"first {count} of {w.batch} matrices of the same workload, fwd + adjoint, "
-                      f"one thread, {t:.2f} s"}
+    threads = host_threads()
+    s = OracleSample(w, budget_s=10.0, threads=threads)
+    t = s.run()
+    return {"value": s.units / t, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{s.desc}; oracle fwd + literal adjoint, OpenMP on {threads} host "
+                      f"threads, {t:.2f} s"}
 
 
-def run_reference(args, w, desc):
+def run_reference(args, w, desc, tile):
     import oracle
     oracle.build()
+    threads = host_threads()
     # a bounded sample per step, sized so the whole run stays within ~2 minutes
-    per_step = max(0.02, min(0.5, 120.0 / max(1, args.steps + args.warmup)))
-    count = oracle_sample_size(w, budget_s=per_step)
+    per_step = max(0.05, min(5.0, 120.0 / max(1, args.steps + args.warmup)))
+    s = OracleSample(w, budget_s=per_step, threads=threads)
     for _ in range(args.warmup):
-        time_oracle(w, count)
-    times = [time_oracle(w, count) for _ in range(args.steps)]
+        s.run()
+    times = [s.run() for _ in range(args.steps)]
     total = sum(times)
-    value = args.steps * count / total
+    value = args.steps * s.units / total
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32" if w.dtype == np.float32 else "f64", "data": "synthetic",
-        "config": {"workload": f"{args.workload}: {desc}", "batch_per_gpu": w.batch, "n": w.n,
-                   "tile": (WORKLOADS[args.workload][4] or "default") if w.n > 64 else None,
-                   "parallelism": "host, one thread",
-                   "step": f"oracle fwd + adjoint over {count} matrices of the batch"},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"{count} of {w.batch} matrices per step, one thread"},
+        "config": workload_config(args.workload, desc, w, tile, 1),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{s.desc} per step; oracle fwd + literal adjoint, OpenMP on "
+                                   f"{threads} host threads"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -312,28 +364,131 @@ def make_workload(name):
     return W.WORKLOADS[name]()
 
 
+def workload_config(name, desc, w, tile, world):
+    esize = np.dtype(w.dtype).itemsize
+    return {"workload": f"{name}: {desc}", "batch_per_gpu": w.batch, "n": w.n,
+            "tile": (tile or "default") if w.n > 64 else None,
+            "parallelism": f"independent batches per GPU x{world}" if world > 1 else "1 GPU",
+            "l2": "inputs larger than L2 (two buffer sets alternated)"
+            if w.batch * w.n * w.n * esize * 2 > L2_BYTES else
+            "working set below L2 size: steps run back to back on two buffer sets"}
+
+
+class GpuWorkload:
+    """Device buffers of one workload (two sets, alternated between steps) and
+    its timed step."""
+
+    def __init__(self, name, torch, binding, dev, stream, sets=2):
+        self.name = name
+        self.batch, self.n, self.np_dtype, self.desc, self.tile = WORKLOADS[name]
+        self.torch, self.binding, self.dev, self.stream = torch, binding, dev, stream
+        self.w = make_workload(name)
+        self.esize = np.dtype(self.np_dtype).itemsize
+        self.sets = []
+        for _ in range(sets):
+            A = torch.from_numpy(self.w.A).to(dev)
+            Lb = torch.from_numpy(self.w.adj_L).to(dev)
+            self.sets.append((A, Lb, torch.empty_like(A), torch.zeros_like(A),
+                              torch.empty(self.batch, dtype=torch.int32, device=dev)))
+
+    def step(self, k, ev=None):
+        A, Lb, L, G, st = self.sets[k % len(self.sets)]
+        if ev is not None:
+            ev[0].record(self.stream)
+        self.binding.chol_fwd(A, L=L, status=st, tile=self.tile)
+        if ev is not None:
+            ev[1].record(self.stream)
+        self.binding.chol_adj(L, Lb, adj_A=G, status=st, tile=self.tile)
+        if ev is not None:
+            ev[2].record(self.stream)
+
+    def timed(self, steps, warmup, dist=None, sampler=None):
+        """Times `steps` steps after `warmup`: (total ms, mean fwd ms, mean adj
+        ms, clocks during the timed region)."""
+        torch = self.torch
+        for k in range(warmup):
+            self.step(k)
+        torch.cuda.synchronize()
+        events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.monotonic()
+        start.record(self.stream)
+        for k in range(steps):
+            self.step(k, events[k])
+        stop.record(self.stream)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t1 = time.monotonic()
+        total = start.elapsed_time(stop)
+        fwd = statistics.mean(e[0].elapsed_time(e[1]) for e in events)
+        adj = statistics.mean(e[1].elapsed_time(e[2]) for e in events)
+        clocks = sampler.summary(t0, t1) if sampler is not None else None
+        return total, fwd, adj, clocks
+
+    def kernel_report(self, fwd_ms, adj_ms, hbm_peak, fp64_peak, fp32_peak):
+        """Per-call ms, algorithmic GB/s (small path) or executed TFLOP/s
+        (blocked path), and the fraction of the relevant measured roof."""
+        n, batch = self.n, self.batch
+        fwd_b, adj_b = algorithmic_bytes(n, self.esize)
+        rep = {"fwd": {"ms": fwd_ms}, "adj": {"ms": adj_ms}}
+        if n <= 64:
+            for k, ms, b in (("fwd", fwd_ms, fwd_b), ("adj", adj_ms, adj_b)):
+                gbs = b * batch / (ms / 1e3) / 1e9
+                rep[k].update({"algorithmic_GBps": gbs, "bytes_per_matrix": b,
+                               "bound": "hbm", "frac": gbs / hbm_peak})
+        else:
+            peak = fp64_peak if self.esize == 8 else fp32_peak
+            for k, ms, f in zip(("fwd", "adj"), (fwd_ms, adj_ms), executed_flops(n)):
+                tf = f * batch / (ms / 1e3) / 1e12
+                rep[k].update({"executed_TFLOPs": tf, "flops_per_matrix": f,
+                               "bound": "fp64" if self.esize == 8 else "fp32",
+                               "frac": tf / peak})
+        rep["matrices_per_s"] = batch / ((fwd_ms + adj_ms) / 1e3)
+        return rep
+
+    def free(self):
+        self.sets = []
+        self.w = None
+
+
+def measure_fp_peaks(binding, torch):
+    """Measured FP64 rates of both pipes (FMA chains and f64 mma.sync) and the
+    FP32 FMA rate, TFLOP/s.  The FP64 roof is the faster pipe."""
+    p = {"dfma": binding.probe_fma_peak(torch.float64, iters=1 << 15) / 1e12,
+         "ffma": binding.probe_fma_peak(torch.float32, iters=1 << 15) / 1e12}
+    for s in binding.DMMA_SHAPES:
+        p[f"dmma_{s}"] = binding.probe_dmma_peak(s, iters=1 << 14) / 1e12
+    fp64 = max(v for k, v in p.items() if k == "dfma" or k.startswith("dmma"))
+    return p, fp64, p["ffma"]
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None,
-                    help="timed steps (default: 2000 for n <= 64, else 3)")
-    ap.add_argument("--warmup", type=int, default=None,
-                    help="warm-up steps (default: 20 for n <= 64, else 3)")
+                    help="timed steps (default: 2000 for n <= 64, 10 for n = 512, else 5)")
+    ap.add_argument("--warmup", type=int, default=None, help="warm-up steps (default 3)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="batched_16")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--e2e-steps", type=int, default=None,
-                    help="end-to-end steps (default: 20 for n <= 64, else 1)")
+                    help="end-to-end steps (default: 20 for n <= 64, else 2)")
     ap.add_argument("--e2e-chunks", type=int, default=2,
                     help="chunks of the batch in the end-to-end step (n <= 64)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip timing the other workloads in the same run")
     args = ap.parse_args()
     batch, n, np_dtype, desc, tile = WORKLOADS[args.workload]
     if args.steps is None:
-        args.steps = 2000 if n <= 64 else 3
+        args.steps = 2000 if n <= 64 else (10 if n <= 512 else 5)
     if args.warmup is None:
         args.warmup = 20 if n <= 64 else 3
     if args.e2e_steps is None:
-        args.e2e_steps = 20 if n <= 64 else 1
+        args.e2e_steps = 20 if n <= 64 else 2
     args.warmup = max(args.warmup, 3)
 
     rank = int(os.environ.get("RANK", "0"))
@@ -343,7 +498,7 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        run_reference(args, make_workload(args.workload), desc)
+        run_reference(args, make_workload(args.workload), desc, tile)
         return
 
     import torch
@@ -356,66 +511,26 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     binding.load_library()
     dev = torch.device("cuda", local_rank)
-
-    w = make_workload(args.workload)
-    esize = np.dtype(np_dtype).itemsize
-    tdtype = torch.float32 if np_dtype == np.float32 else torch.float64
-
-    # two buffer sets, alternated between steps
-    sets = []
-    for _ in range(2):
-        A = torch.from_numpy(w.A).to(dev)
-        Lb = torch.from_numpy(w.adj_L).to(dev)
-        L = torch.empty_like(A)
-        G = torch.zeros_like(A)
-        st = torch.empty(batch, dtype=torch.int32, device=dev)
-        sets.append((A, Lb, L, G, st))
     stream = torch.cuda.current_stream()
-
-    def step(k, ev=None):
-        A, Lb, L, G, st = sets[k & 1]
-        if ev is not None:
-            ev[0].record(stream)
-        binding.chol_fwd(A, L=L, status=st, tile=tile)
-        if ev is not None:
-            ev[1].record(stream)
-        binding.chol_adj(L, Lb, adj_A=G, status=st, tile=tile)
-        if ev is not None:
-            ev[2].record(stream)
-
-    for k in range(args.warmup):
-        step(k)
-    torch.cuda.synchronize()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
 
     sampler = ClockSampler(gpu_identifier(torch)) if rank == 0 else None
     if sampler is not None:
         time.sleep(0.3)
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t_wall0 = time.monotonic()
-    start.record(stream)
-    for k in range(args.steps):
-        step(k, events[k])
-    stop.record(stream)
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t_wall1 = time.monotonic()
-    elapsed_ms = start.elapsed_time(stop)
-    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in events)
-    adj_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in events)
+
+    # ---------------- main workload: the bench line -------------------------
+    g = GpuWorkload(args.workload, torch, binding, dev, stream)
+    w = g.w
+    esize = g.esize
+    elapsed_ms, fwd_ms, adj_ms, clocks = g.timed(args.steps, args.warmup, dist, sampler)
     elapsed_ms = max_over_ranks(elapsed_ms, dist, dev)
-    clocks = sampler.summary(t_wall0, t_wall1) if sampler is not None else None
 
     # The in-place forms on the same workload: two work sets, each restored
-    # from the pristine inputs right after its step, so that the other set's
-    # step runs in between and a step's inputs have left L2.  Events bracket
-    # the two in-place calls only.
-    ip_steps = min(args.steps, 500)
-    work = [(sets[i][0].clone(), sets[i][1].clone(), torch.empty_like(sets[i][4])) for i in range(2)]
+    # from the pristine inputs right after its step.  Events bracket the two
+    # in-place calls only.
+    ip_steps = min(args.steps, 500 if n <= 64 else 3)
+    work = [(g.sets[i][0].clone(), g.sets[i][1].clone(), torch.empty_like(g.sets[i][4]))
+            for i in range(2)]
 
     def ip_step(k, ev=None):
         X, Y, ip_st = work[k & 1]
@@ -427,10 +542,10 @@ def main():
         binding.chol_adj_inplace(X, Y, status=ip_st, tile=tile)
         if ev is not None:
             ev[2].record(stream)
-        X.copy_(sets[k & 1][0])
-        Y.copy_(sets[k & 1][1])
+        X.copy_(g.sets[k & 1][0])
+        Y.copy_(g.sets[k & 1][1])
 
-    for k in range(args.warmup):
+    for k in range(2 if n > 64 else args.warmup):
         ip_step(k)
     ip_events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(ip_steps)]
     for k in range(ip_steps):
@@ -458,10 +573,9 @@ def main():
     streams = [torch.cuda.Stream() for _ in range(2 * chunks)]
     host_out = [(hL, hG, hst), (torch.empty_like(hL).pin_memory(), torch.empty_like(hG).pin_memory(),
                                 torch.empty_like(hst).pin_memory())]
-    n_streams = len(streams)
 
     def e2e_step(k):
-        dA_, dLb_, dL_, dG_, dst_ = sets[k & 1]
+        dA_, dLb_, dL_, dG_, dst_ = g.sets[k & 1]
         hL_, hG_, hst_ = host_out[k & 1]
         for c in range(chunks):
             b0, b1 = bounds[c], bounds[c + 1]
@@ -500,6 +614,34 @@ def main():
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
     e2e_ms = max_over_ranks(e2e_ms, dist, dev)
+    h2d = int(hA.numel() * esize + hLb.numel() * esize)
+    d2h = int(hL.numel() * esize + hG.numel() * esize + hst.numel() * 4)
+    del hA, hLb, hL, hG, hst, host_out, streams
+
+    peaks, fp64_peak, fp32_peak = measure_fp_peaks(binding, torch)
+    hbm_peak, peak_src = read_peaks()
+    main_report = g.kernel_report(fwd_ms, adj_ms, hbm_peak, fp64_peak, fp32_peak)
+    g.free()
+    del g
+    torch.cuda.empty_cache()
+
+    # ---------------- the other workloads, same process ---------------------
+    others = {}
+    if not args.no_workloads:
+        for name in WORKLOADS:
+            if name == args.workload:
+                continue
+            o = GpuWorkload(name, torch, binding, dev, stream)
+            steps = EXTRA_STEPS[name]
+            tot, f_ms, a_ms, ck = o.timed(steps, 5 if o.n <= 64 else 2, None, sampler)
+            rep = o.kernel_report(f_ms, a_ms, hbm_peak, fp64_peak, fp32_peak)
+            rep.update({"steps": steps, "step_ms": tot / steps, "clocks": ck,
+                        "tile": (o.tile or default_tile(o.n, o.batch, sms)) if o.n > 64 else None,
+                        "config": f"{name}: {o.desc}"})
+            others[name] = rep
+            o.free()
+            del o
+            torch.cuda.empty_cache()
     if sampler is not None:
         sampler.stop()
 
@@ -510,62 +652,43 @@ def main():
 
     value = job_throughput(args.steps * batch, world, elapsed_ms)
     e2e_value = job_throughput(args.e2e_steps * batch, world, e2e_ms)
-    fwd_b, adj_b = algorithmic_bytes(n, esize)
     fwd_f, adj_f = nominal_flops(n)
-    hbm_peak, peak_src = read_peaks()
-    fwd_gbs = fwd_b * batch / (fwd_ms / 1e3) / 1e9
-    adj_gbs = adj_b * batch / (adj_ms / 1e3) / 1e9
     dominant = "adj" if adj_ms >= fwd_ms else "fwd"
-    kernels = {
-        "fwd": {"ms": fwd_ms, "algorithmic_GBps": fwd_gbs, "bytes_per_matrix": fwd_b},
-        "adj": {"ms": adj_ms, "algorithmic_GBps": adj_gbs, "bytes_per_matrix": adj_b},
-    }
+    dk = main_report[dominant]
     if n <= 64:
-        achieved = adj_gbs if dominant == "adj" else fwd_gbs
-        roofline = {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": hbm_peak,
-                    "unit": "GB/s", "frac": achieved / hbm_peak,
-                    "peak_source": f"{peak_src} HBM copy bandwidth",
+        roofline = {"bound": "hbm", "kernel": f"{dominant} call", "achieved": dk["algorithmic_GBps"],
+                    "peak": hbm_peak, "unit": "GB/s", "frac": dk["frac"],
+                    "peak_source": f"{peak_src} HBM copy bandwidth (MEASURED_PEAKS.json)",
                     "traffic": measured_traffic(args.workload, dominant)}
     else:
-        # FP64 FMA-pipe bound: executed flops per call against the FMA peak
-        # measured by the library's probe on this GPU.
-        ex_f, ex_a = executed_flops(n)
-        fp64_peak = binding.probe_fma_peak(tdtype, iters=1 << 15) / 1e12
-        tf_f = ex_f * batch / (fwd_ms / 1e3) / 1e12
-        tf_a = ex_a * batch / (adj_ms / 1e3) / 1e12
-        kernels["fwd"]["executed_TFLOPs"] = tf_f
-        kernels["adj"]["executed_TFLOPs"] = tf_a
-        achieved = tf_a if dominant == "adj" else tf_f
-        roofline = {"bound": "fp64" if np_dtype == np.float64 else "fp32", "kernel": dominant,
-                    "achieved": achieved, "peak": fp64_peak, "unit": "TFLOP/s",
-                    "frac": achieved / fp64_peak,
-                    "peak_source": "measured by chol_probe_fma_peak (independent FMA chains on every SM)",
-                    "traffic": None}
+        roofline = {"bound": "alu", "pipe": "fp64" if esize == 8 else "fp32",
+                    "kernel": f"{dominant} call (all its launches)",
+                    "achieved": dk["executed_TFLOPs"],
+                    "peak": fp64_peak if esize == 8 else fp32_peak, "unit": "TFLOP/s",
+                    "frac": dk["frac"],
+                    "peak_source": "measured in this run: the faster of the FP64 FMA-chain probe and "
+                                   "the f64 mma.sync (DMMA) probes, all shapes (peaks_TFLOPs)",
+                    "peaks_TFLOPs": peaks, "traffic": None}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32" if np_dtype == np.float32 else "f64", "data": "synthetic",
-        "config": {"workload": f"{args.workload}: {desc}", "batch_per_gpu": batch, "n": n,
-                   "tile": (tile or "default") if n > 64 else None,
-                   "parallelism": f"independent batches per GPU x{world}" if world > 1 else "1 GPU",
-                   "l2": "inputs larger than L2 (256 MiB of distinct buffers per step, two sets alternated)"
-                   if batch * n * n * esize * 4 > L2_BYTES else
-                   "working set below L2 size: steps run back to back on two buffer sets"},
+        "config": workload_config(args.workload, desc, w, tile, world),
         "gflops": value * (fwd_f + adj_f) / 1e9,
-        "kernels": kernels,
+        "kernels": main_report,
         "roofline": roofline,
-        "gpu_launches": launches_per_step(n, (tile or default_tile(n, batch)) if n > 64 else 0) * args.steps,
-        "e2e": {"value": e2e_value, "unit": UNIT,
-                "h2d_bytes_per_step": int(hA.numel() * esize + hLb.numel() * esize),
-                "d2h_bytes_per_step": int(hL.numel() * esize + hG.numel() * esize + hst.numel() * 4),
-                "steps": args.e2e_steps, "chunks": chunks, "streams": n_streams,
+        "gpu_launches": launches_per_step(n, (tile or default_tile(n, batch, sms)) if n > 64 else 0)
+        * args.steps,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": args.e2e_steps, "chunks": chunks,
                 "overlap": "chunks on their own streams; consecutive steps on alternate buffer sets"},
         "clocks": clocks,
         "inplace": {"value": batch * world / ((ip_fwd_ms + ip_adj_ms) / 1e3), "unit": UNIT,
                     "fwd_ms": ip_fwd_ms, "adj_ms": ip_adj_ms, "steps": ip_steps,
                     "timed": "chol_fwd_inplace + chol_adj_inplace (CUDA events around the "
                              "two calls; inputs restored outside them), rank 0"},
+        "workloads": others,
     }
     if not args.no_cpu_baseline:
         import oracle

@@ -65,6 +65,8 @@ def load_library(path: str | None = None):
         lib.chol_adj_inplace.restype = ctypes.c_int
         lib.chol_probe_fma_peak.argtypes = [i32, i64, vp, ctypes.POINTER(ctypes.c_double), vp]
         lib.chol_probe_fma_peak.restype = ctypes.c_int
+        lib.chol_probe_dmma_peak.argtypes = [i32, i64, vp, ctypes.POINTER(ctypes.c_double), vp]
+        lib.chol_probe_dmma_peak.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -211,6 +213,22 @@ def probe_fma_peak(dtype=torch.float64, iters: int = 1 << 16, stream=None) -> fl
     out = ctypes.c_double(0.0)
     rc = load_library().chol_probe_fma_peak(_DTYPES[dtype], int(iters), sink.data_ptr(),
                                             ctypes.byref(out), _stream_ptr(stream))
+    _check(rc)
+    return out.value
+
+
+DMMA_SHAPES = {"m8n8k4": 0, "m16n8k4": 1, "m16n8k8": 2, "m16n8k16": 3}
+
+
+def probe_dmma_peak(shape: str = "m8n8k4", iters: int = 1 << 14, stream=None) -> float:
+    """Measured f64 ``mma.sync`` (DMMA) throughput of the current device in
+    FLOP/s for one instruction shape (a key of ``DMMA_SHAPES``)."""
+    if shape not in DMMA_SHAPES:
+        raise ValueError(f"unknown shape {shape}; expected one of {sorted(DMMA_SHAPES)}")
+    sink = torch.zeros(1, dtype=torch.float64, device="cuda")
+    out = ctypes.c_double(0.0)
+    rc = load_library().chol_probe_dmma_peak(DMMA_SHAPES[shape], int(iters), sink.data_ptr(),
+                                             ctypes.byref(out), _stream_ptr(stream))
     _check(rc)
     return out.value
 

@@ -137,10 +137,13 @@ int chol_fwd(int64_t batch, int32_t n, int32_t dtype, const void* A, void* L, in
     return chol_fwd_ex(batch, n, dtype, A, L, status, 0, stream);
 }
 
-int chol_adj_ex(int64_t batch, int32_t n, int32_t dtype, const void* L, const void* adj_L,
-                void* adj_A, const int32_t* status, int32_t tile, void* stream) {
-    size_t bytes = 0;
-    int rc = check_shape(batch, n, dtype, &bytes);
+}  // extern "C"
+
+namespace chol {
+
+int check_adj_args(int64_t batch, int32_t n, int32_t dtype, const void* L, const void* adj_L,
+                   const void* adj_A, const int32_t* status, int32_t tile, size_t* bytes) {
+    int rc = check_shape(batch, n, dtype, bytes);
     if (rc != CHOL_OK) return rc;
     if ((rc = check_tile(tile)) != CHOL_OK) return rc;
     if (batch == 0) return CHOL_OK;
@@ -151,11 +154,23 @@ int chol_adj_ex(int64_t batch, int32_t n, int32_t dtype, const void* L, const vo
     if (!is_device_pointer(L) || !is_device_pointer(adj_L) || !is_device_pointer(adj_A) ||
         (status != nullptr && !is_device_pointer(status)))
         return CHOL_EINVAL;
-    const Range rL = range_of(L, bytes), rLb = range_of(adj_L, bytes),
-                rAb = range_of(adj_A, bytes);
+    const Range rL = range_of(L, *bytes), rLb = range_of(adj_L, *bytes),
+                rAb = range_of(adj_A, *bytes);
     if (overlaps(rAb, rL) || overlaps(rAb, rLb)) return CHOL_EALIAS;
     if (status != nullptr && overlaps(rAb, range_of(status, (size_t)batch * 4)))
         return CHOL_EALIAS;
+    return CHOL_OK;
+}
+
+}  // namespace chol
+
+extern "C" {
+
+int chol_adj_ex(int64_t batch, int32_t n, int32_t dtype, const void* L, const void* adj_L,
+                void* adj_A, const int32_t* status, int32_t tile, void* stream) {
+    size_t bytes = 0;
+    const int rc = chol::check_adj_args(batch, n, dtype, L, adj_L, adj_A, status, tile, &bytes);
+    if (rc != CHOL_OK || batch == 0) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return dtype == CHOL_F32
                ? adj_impl<float>(batch, n, L, adj_L, adj_A, status, tile, bytes, true, s)

@@ -45,10 +45,11 @@ __device__ __forceinline__ bool skip_matrix(const int32_t* status, int64_t b) {
 // ---------------------------------------------------------------------------
 // L = tril(A), status = 0
 // ---------------------------------------------------------------------------
+// A and L may be the same buffer (the in-place forward): each element is
+// read and then written by the same thread.
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
-tril_copy_kernel(const T* __restrict__ A, T* __restrict__ L, int32_t* __restrict__ status,
-                 int64_t batch, int n) {
+tril_copy_kernel(const T* A, T* L, int32_t* __restrict__ status, int64_t batch, int n) {
     const int64_t nn = (int64_t)n * n;
     const int64_t total = batch * nn;
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
@@ -375,24 +376,15 @@ size_t trsm_smem(int kb, int esize) {
     return ((size_t)(kb + kVecPerBlock) * (kb + 1) + kb) * esize;
 }
 
-// Raise a kernel's dynamic shared-memory limit once, to the largest size any
-// tile needs (attribute calls are host-synchronous, so not one per launch).
-template <typename K>
-cudaError_t allow_smem(K kern, size_t bytes, int* done) {
-    if (*done) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-    if (e == cudaSuccess) *done = 1;
-    return e;
-}
-
 template <typename T, int MODE>
 cudaError_t launch_trsm(const T* L, T* W, const int32_t* status, int64_t batch, int n, int t0,
                         int kb, int v_begin, int v_count, cudaStream_t stream) {
     if (v_count <= 0) return cudaSuccess;
     const size_t smem = trsm_smem(kb, sizeof(T));
     auto kern = trsm_kernel<T, MODE>;
-    static int smem_set = 0;
-    cudaError_t e = allow_smem(kern, trsm_smem(128, sizeof(T)), &smem_set);
+    // raised once per device to the largest size any tile needs
+    static std::atomic<uint64_t> smem_set{0};
+    cudaError_t e = allow_smem_once(kern, trsm_smem(128, sizeof(T)), smem_set);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((v_count + kVecPerBlock - 1) / kVecPerBlock), grid_y(batch));
     kern<<<grid, kThreads, smem, stream>>>(L, W, status, batch, n, t0, kb, v_begin, v_count);
@@ -513,8 +505,8 @@ zero_lower_skipped_kernel(T* __restrict__ dst, const int32_t* __restrict__ statu
 }
 
 inline unsigned elementwise_blocks(int64_t total) {
-    return (unsigned)std::max<int64_t>(1, std::min<int64_t>((total + kThreads - 1) / kThreads,
-                                                            152 * 16));
+    return (unsigned)std::max<int64_t>(
+        1, std::min<int64_t>((total + kThreads - 1) / kThreads, (int64_t)device_sm_count() * 16));
 }
 
 }  // namespace
@@ -525,7 +517,7 @@ inline unsigned elementwise_blocks(int64_t total) {
 int blocked_default_tile(int n, int64_t batch) {
     if (n >= 2048) return 128;
     const int64_t per_side = (n + 63) / 64;
-    return batch * per_side * per_side >= 4 * 152 ? 64 : 32;
+    return batch * per_side * per_side >= 4 * (int64_t)device_sm_count() ? 64 : 32;
 }
 
 #define CHOL_TRY(x)                              \
@@ -540,14 +532,15 @@ cudaError_t blocked_fwd(const T* A, T* L, int32_t* status, int64_t batch, int n,
     const int nt = (n + tile - 1) / tile;
     {
         const int64_t total = batch * (int64_t)n * n;
-        const int64_t blocks = std::min<int64_t>((total + kThreads - 1) / kThreads, 152 * 32);
+        const int64_t blocks =
+            std::min<int64_t>((total + kThreads - 1) / kThreads, (int64_t)device_sm_count() * 32);
         tril_copy_kernel<T><<<(unsigned)std::max<int64_t>(blocks, 1), kThreads, 0, stream>>>(
             A, L, status, batch, n);
         CHOL_TRY(cudaGetLastError());
     }
-    static int diag_smem_set = 0;
-    CHOL_TRY(allow_smem(potrf_diag_kernel<T, kThreads>, (size_t)128 * 129 * sizeof(T),
-                        &diag_smem_set));
+    static std::atomic<uint64_t> diag_smem_set{0};
+    CHOL_TRY(allow_smem_once(potrf_diag_kernel<T, kThreads>, (size_t)128 * 129 * sizeof(T),
+                             diag_smem_set));
     for (int k = 0; k < nt; ++k) {
         const int k0 = k * tile;
         const int kb = std::min(tile, n - k0);
@@ -598,15 +591,10 @@ cudaError_t blocked_adj(const T* L, const T* Lbar, T* Abar, const int32_t* statu
                                                                                 batch, n);
         CHOL_TRY(cudaGetLastError());
     }
-    static int diag_smem_set = 0;
-    CHOL_TRY(allow_smem(diag_rev_kernel<T, kThreads>, (size_t)128 * 129 * sizeof(T),
-                        &diag_smem_set));
-    int sms = 152;
-    {
-        int dev = 0;
-        if (cudaGetDevice(&dev) == cudaSuccess)
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    }
+    static std::atomic<uint64_t> diag_smem_set{0};
+    CHOL_TRY(allow_smem_once(diag_rev_kernel<T, kThreads>, (size_t)128 * 129 * sizeof(T),
+                             diag_smem_set));
+    const int sms = device_sm_count();
     const int bm = tile >= 64 ? 64 : 32;
     const int subs = (tile / bm) * (tile / bm);
     const int64_t bmat = std::min<int64_t>(batch, 65535);

@@ -4,11 +4,92 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
 #include <type_traits>
 
 #include "chol.h"
 
 namespace chol {
+
+// ---------------------------------------------------------------------------
+// Per-device host-side caches.  Kernel attributes (the raised dynamic
+// shared-memory limit) and occupancy figures belong to one device; a process
+// that drives several GPUs, from one thread or many, must set and look them
+// up per device.  Device ordinals >= kMaxDevices are served uncached.
+// ---------------------------------------------------------------------------
+constexpr int kMaxDevices = 64;
+
+inline std::mutex& device_cache_mutex() {
+    static std::mutex m;
+    return m;
+}
+
+// Runs `f` (returning cudaError_t) once per device for the current device;
+// success is remembered in bit `dev` of `done`, a failure is returned and
+// retried on the next call.
+template <typename F>
+cudaError_t once_per_device(std::atomic<uint64_t>& done, F&& f) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return f();
+    const uint64_t bit = 1ull << dev;
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    std::lock_guard<std::mutex> lock(device_cache_mutex());
+    if (done.load(std::memory_order_relaxed) & bit) return cudaSuccess;
+    e = f();
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
+
+// An int computed once per device by `f` (returning a value > 0, or <= 0 on
+// failure, which is not cached).
+struct PerDeviceInt {
+    std::atomic<int> v[kMaxDevices];
+    PerDeviceInt() {
+        for (auto& x : v) x.store(0, std::memory_order_relaxed);
+    }
+    template <typename F>
+    int get(F&& f) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) {
+            cudaGetLastError();
+            return f();
+        }
+        if (dev < 0 || dev >= kMaxDevices) return f();
+        int x = v[dev].load(std::memory_order_acquire);
+        if (x > 0) return x;
+        x = f();
+        if (x > 0) v[dev].store(x, std::memory_order_release);
+        return x;
+    }
+};
+
+// Streaming multiprocessors of the current device (152 on a GB300; queried,
+// never assumed).
+inline int device_sm_count() {
+    static PerDeviceInt cache;
+    const int n = cache.get([] {
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        return sms;
+    });
+    return n > 0 ? n : 1;
+}
+
+// Raise a kernel's dynamic shared-memory limit to `bytes`, once per device
+// (the attribute call is host-synchronous, so not once per launch).
+template <typename K>
+cudaError_t allow_smem_once(K kern, size_t bytes, std::atomic<uint64_t>& done) {
+    return once_per_device(done, [&] {
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    });
+}
 
 // Compile-time loop: f(std::integral_constant<int, I>) for I in [B, E).  Used
 // where every index must be a constant so that arrays stay in registers,

@@ -54,4 +54,11 @@ cudaError_t blocked_adj(const T* L, const T* Lbar, T* Abar, const int32_t* statu
 
 int blocked_default_tile(int n, int64_t batch);
 
+// Argument checks of chol_adj_ex (shape, dtype, tile, null, alignment,
+// device residency, aliasing), shared by every adjoint entry point that
+// promises the same error codes.  On CHOL_OK, *bytes is the size of one
+// [batch][n][n] array; batch == 0 passes (the caller returns at once).
+int check_adj_args(int64_t batch, int32_t n, int32_t dtype, const void* L, const void* adj_L,
+                   const void* adj_A, const int32_t* status, int32_t tile, size_t* bytes);
+
 }  // namespace chol

@@ -16,14 +16,17 @@
 //     (n <= 64 needs no scratch at all); larger problems get CHOL_ENOMEM and
 //     nothing is enqueued -- use chol_adj for them.
 //   - The first call on each device looks up the device address of the scratch
-//     array (cudaGetSymbolAddress, with that device current).  Make that first
-//     call before any stream capture begins.
+//     array (cudaGetSymbolAddress, with that device current) and remembers it
+//     with the context it belongs to; a call in another context of that
+//     device (after cudaDeviceReset, say) looks it up again.  Make the first
+//     call in a context before any stream capture begins.
 //   - Every call on a device shares the one scratch array and leaves its last
 //     contents there.  The kernels write every scratch element they read, so
 //     nothing needs clearing between calls, but calls that overlap on the GPU
 //     (on different streams, or from several host threads without ordering
 //     between their streams) race on the scratch and corrupt each other.
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -39,41 +42,70 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_adj_scratch[kScratchBytes];
 
+// The scratch address belongs to the CUDA context it was looked up in: after
+// cudaDeviceReset, or with another context made current on the same device,
+// the array lives somewhere else.  The cache therefore remembers the context
+// beside the address and looks the address up again when the context changes.
+struct ScratchEntry {
+    CUcontext ctx;
+    void* ptr;
+};
 std::mutex g_scratch_mutex;
-void* g_scratch_ptr[kMaxDevices] = {};
+ScratchEntry g_scratch[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device (set-up on first
-// use per device).  Returns nullptr if the lookup fails.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+// cuCtxGetCurrent through the runtime's driver entry-point lookup, so the
+// library needs no link-time dependency on the driver library.
+CtxGetCurrentFn ctx_get_current() {
+    static CtxGetCurrentFn fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return (CtxGetCurrentFn) nullptr;
+        }
+        return reinterpret_cast<CtxGetCurrentFn>(p);
+    }();
+    return fn;
+}
+
+// Device address of the scratch array in the current device's current
+// context (looked up on the first call there).  Returns nullptr if the lookup
+// fails.
 void* scratch_on_current_device() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
         cudaGetLastError();
         return nullptr;
     }
+    CtxGetCurrentFn get = ctx_get_current();
+    CUcontext ctx = nullptr;
+    if (get == nullptr || get(&ctx) != CUDA_SUCCESS) return nullptr;
+    if (ctx == nullptr) {
+        // the runtime makes its context current lazily; the symbol lookup
+        // (no allocation) does that
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_adj_scratch) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        if (get(&ctx) != CUDA_SUCCESS || ctx == nullptr) return nullptr;
+    }
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (g_scratch_ptr[dev] == nullptr) {
+    ScratchEntry& e = g_scratch[dev];
+    if (e.ptr == nullptr || e.ctx != ctx) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_adj_scratch) != cudaSuccess || p == nullptr) {
             cudaGetLastError();
             return nullptr;
         }
-        g_scratch_ptr[dev] = p;
+        e.ctx = ctx;
+        e.ptr = p;
     }
-    return g_scratch_ptr[dev];
-}
-
-bool on_device(const void* p) {
-    cudaPointerAttributes attr;
-    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
-        cudaGetLastError();
-        return false;
-    }
-    return attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged;
-}
-
-bool disjoint(const void* a, size_t na, const void* b, size_t nb) {
-    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
-    return x + na <= y || y + nb <= x;
+    return e.ptr;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -107,27 +139,10 @@ int run(int64_t batch, int32_t n, const void* L, const void* Lbar, void* Abar,
 extern "C" CHOL_API int chol_adj_noalloc(int64_t batch, int32_t n, int32_t dtype, const void* L,
                                          const void* adj_L, void* adj_A, const int32_t* status,
                                          int32_t tile, void* stream) {
-    const size_t es = dtype == CHOL_F32 ? 4 : dtype == CHOL_F64 ? 8 : 0;
-    if (es == 0) return CHOL_EDTYPE;
-    if (batch < 0 || n <= 0) return CHOL_EINVAL;
-    if (!(tile == 0 || tile == 32 || tile == 64 || tile == 128)) return CHOL_EINVAL;
-    const unsigned __int128 total =
-        (unsigned __int128)batch * (unsigned __int128)n * (unsigned __int128)n * es;
-    if (total > ((unsigned __int128)1 << 62)) return CHOL_EINVAL;
-    if (batch == 0) return CHOL_OK;
-    if (L == nullptr || adj_L == nullptr || adj_A == nullptr) return CHOL_EINVAL;
-    const uintptr_t mask = es - 1;
-    if ((reinterpret_cast<uintptr_t>(L) & mask) || (reinterpret_cast<uintptr_t>(adj_L) & mask) ||
-        (reinterpret_cast<uintptr_t>(adj_A) & mask) ||
-        (status != nullptr && (reinterpret_cast<uintptr_t>(status) & 3u)))
-        return CHOL_EINVAL;
-    if (!on_device(L) || !on_device(adj_L) || !on_device(adj_A) ||
-        (status != nullptr && !on_device(status)))
-        return CHOL_EINVAL;
-    const size_t bytes = (size_t)total;
-    if (!disjoint(adj_A, bytes, L, bytes) || !disjoint(adj_A, bytes, adj_L, bytes) ||
-        (status != nullptr && !disjoint(adj_A, bytes, status, (size_t)batch * 4)))
-        return CHOL_EALIAS;
+    // the same checks, in the same order, as chol_adj_ex
+    size_t bytes = 0;
+    const int rc = chol::check_adj_args(batch, n, dtype, L, adj_L, adj_A, status, tile, &bytes);
+    if (rc != CHOL_OK || batch == 0) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return dtype == CHOL_F32 ? run<float>(batch, n, L, adj_L, adj_A, status, tile, s)
                              : run<double>(batch, n, L, adj_L, adj_A, status, tile, s);

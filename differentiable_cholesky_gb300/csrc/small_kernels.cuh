@@ -62,9 +62,10 @@ constexpr int kBlock = 128;
 
 // Load the lower part of row `row` (row < n) into r[0..NT): zeros above the
 // diagonal.  Only the 16-byte chunks that hold lower-triangle elements are read.
+// Plain (coherent) loads: the in-place forms read rows of the very buffer the
+// kernel later writes.
 template <typename T, int NT, bool VEC>
-__device__ __forceinline__ void load_lower_row(const T* __restrict__ rowp, int row, int n,
-                                               T (&r)[NT]) {
+__device__ __forceinline__ void load_lower_row(const T* rowp, int row, int n, T (&r)[NT]) {
     if constexpr (VEC) {
         using V = typename Vec16<T>::type;
         constexpr int W = Vec16<T>::N;
@@ -73,7 +74,7 @@ __device__ __forceinline__ void load_lower_row(const T* __restrict__ rowp, int r
         for (int c = 0; c < NT / W; ++c) {
             V v;
             if (c * W <= row) {
-                v = __ldg(vp + c);
+                v = vp[c];
             } else {
                 v = V{};
             }
@@ -82,7 +83,7 @@ __device__ __forceinline__ void load_lower_row(const T* __restrict__ rowp, int r
         }
     } else {
 #pragma unroll
-        for (int k = 0; k < NT; ++k) r[k] = (k <= row && k < n) ? __ldg(rowp + k) : T(0);
+        for (int k = 0; k < NT; ++k) r[k] = (k <= row && k < n) ? rowp[k] : T(0);
     }
 }
 
@@ -101,7 +102,7 @@ __host__ __device__ constexpr int group_stride(int base_elems) {
 // Row `row` of matrix b for the forward: lower part of A, or an identity row
 // for padding rows and for slots past the end of the batch.
 template <typename T, int NT, bool VEC>
-__device__ __forceinline__ void fetch_fwd_row(const T* __restrict__ A, int64_t b, int64_t batch,
+__device__ __forceinline__ void fetch_fwd_row(const T* A, int64_t b, int64_t batch,
                                               int row, int n, T (&r)[NT]) {
     if (b < batch && row < n) {
         load_lower_row<T, NT, VEC>(A + (size_t)b * n * n + (size_t)row * n, row, n, r);
@@ -177,10 +178,11 @@ constexpr bool fwd_chunks() {
     return NT * (int)sizeof(T) >= 128;
 }
 
+// A and L may be the same buffer (the in-place forward): a group reads its
+// matrix in full before it writes any of it, and no other group touches it.
 template <typename T, int NT, int RPL, bool VEC, bool FULL>
 __global__ void __launch_bounds__(kBlock)
-small_potrf_kernel(const T* __restrict__ A, T* __restrict__ L, int32_t* __restrict__ status,
-                   int64_t batch, int n) {
+small_potrf_kernel(const T* A, T* L, int32_t* __restrict__ status, int64_t batch, int n) {
     constexpr int LPG = NT / RPL;
     constexpr int G = kBlock / LPG;
     constexpr int CS = group_stride<T, LPG>(2 * NT);
@@ -393,7 +395,7 @@ struct AdjCfg {
 // Row `row` of one of the adjoint's inputs, or its padding: identity rows of
 // L, zero rows of adj_L.
 template <typename T, int NT, bool VEC>
-__device__ __forceinline__ void fetch_adj_row(const T* __restrict__ src, bool active, int64_t b,
+__device__ __forceinline__ void fetch_adj_row(const T* src, bool active, int64_t b,
                                               int row, int n, T pad_diag, T (&r)[NT]) {
     if (active && row < n) {
         load_lower_row<T, NT, VEC>(src + (size_t)b * n * n + (size_t)row * n, row, n, r);
@@ -421,11 +423,12 @@ __device__ __forceinline__ void prefetch_abar(const T* Abar, int64_t b, int n, b
     }
 }
 
+// Lbar and Abar may be the same buffer (the in-place adjoint, not
+// accumulating): a group reads its matrix in full before it writes any of it.
 template <typename T, int NT, int CPL, bool VEC, bool FULL>
 __global__ void __launch_bounds__(AdjCfg<T, NT, CPL>::BLOCK)
-small_potrf_adj_kernel(const T* __restrict__ Lg, const T* __restrict__ Lbar,
-                       T* __restrict__ Abar, const int32_t* __restrict__ status,
-                       int64_t batch, int n, bool accumulate) {
+small_potrf_adj_kernel(const T* __restrict__ Lg, const T* Lbar, T* Abar,
+                       const int32_t* __restrict__ status, int64_t batch, int n, bool accumulate) {
     using S = AdjCfg<T, NT, CPL>;
     using V = typename Vec16<T>::type;
     constexpr int W = Vec16<T>::N;
@@ -764,12 +767,10 @@ cudaError_t launch_fwd_nt(const T* A, T* L, int32_t* status, int64_t batch, int 
         if (n == NT) {
             constexpr size_t smem = (size_t)G * NT * (NT + 16 / sizeof(T)) * sizeof(T);
             auto kern = small_potrf_kernel<T, NT, RPL, VEC, true>;
-            static int smem_set = 0;
-            if (smem > 48 * 1024 && !smem_set) {
-                cudaError_t e =
-                    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            static std::atomic<uint64_t> smem_set{0};
+            if (smem > 48 * 1024) {
+                cudaError_t e = allow_smem_once(kern, smem, smem_set);
                 if (e != cudaSuccess) return e;
-                smem_set = 1;
             }
             kern<<<(unsigned)blocks, kBlock, smem, stream>>>(A, L, status, batch, n);
             return cudaGetLastError();
@@ -791,12 +792,10 @@ cudaError_t launch_adj_nt(const T* L, const T* Lbar, T* Abar, const int32_t* sta
     if constexpr (kChunks) {
         if (n == NT) {
             auto kern = small_potrf_adj_kernel<T, NT, CPL, VEC, true>;
-            static int smem_set = 0;
-            if (S::bytes > 48 * 1024 && !smem_set) {
-                cudaError_t e = cudaFuncSetAttribute(
-                    kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::bytes);
+            static std::atomic<uint64_t> smem_set{0};
+            if (S::bytes > 48 * 1024) {
+                cudaError_t e = allow_smem_once(kern, S::bytes, smem_set);
                 if (e != cudaSuccess) return e;
-                smem_set = 1;
             }
             kern<<<(unsigned)blocks, S::BLOCK, S::bytes, stream>>>(L, Lbar, Abar, status, batch,
                                                                    n, accumulate);
@@ -804,12 +803,10 @@ cudaError_t launch_adj_nt(const T* L, const T* Lbar, T* Abar, const int32_t* sta
         }
     }
     auto kern = small_potrf_adj_kernel<T, NT, CPL, VEC, false>;
-    static int smem_set = 0;
-    if (S::bytes > 48 * 1024 && !smem_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)S::bytes);
+    static std::atomic<uint64_t> smem_set{0};
+    if (S::bytes > 48 * 1024) {
+        cudaError_t e = allow_smem_once(kern, S::bytes, smem_set);
         if (e != cudaSuccess) return e;
-        smem_set = 1;
     }
     kern<<<(unsigned)blocks, S::BLOCK, S::bytes, stream>>>(L, Lbar, Abar, status, batch, n,
                                                            accumulate);

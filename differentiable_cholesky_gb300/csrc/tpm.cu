@@ -58,15 +58,15 @@ __device__ __forceinline__ void slot_load_lower(const float* slot, float (&a)[N]
 // Issue the bulk loads of matrices [m0, m0 + nvalid) into the lanes' slots,
 // completion on `bar`.  Every lane of the warp calls this.
 template <int N>
-__device__ __forceinline__ void issue_round_load(const float* __restrict__ src, int64_t m0,
+__device__ __forceinline__ void issue_round_load(const float* src, int64_t m0,
                                                  int nvalid, float* slot, uint64_t* bar,
                                                  int lane, int drop_lane) {
     fence_proxy_async_smem();  // earlier generic accesses to the slot come first
     __syncwarp();
     if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)nvalid * (N * N * 4));
     __syncwarp();
-    // (drop_lane >= 0 only in the self-test: that lane's copy is never
-    //  issued, so the round's barrier cannot complete)
+    // (drop_lane >= 0 only in the self-test: that lane's copy is held back,
+    //  so the round's barrier cannot complete until the lane issues it late)
     if (lane < nvalid && lane != drop_lane) bulk_load(slot, src + (m0 + lane) * (N * N), N * N * 4, bar);
 }
 
@@ -77,8 +77,8 @@ __device__ __forceinline__ int round_count(int64_t batch, int64_t w) {
 
 template <int N, int M, int NSETS>
 __global__ void __launch_bounds__(32)
-tpm_potrf_kernel(const float* __restrict__ A, float* __restrict__ L, int32_t* __restrict__ status,
-                 int64_t batch, uint32_t max_polls, int drop_lane) {
+tpm_potrf_kernel(const float* A, float* L, int32_t* __restrict__ status, int64_t batch,
+                 uint32_t max_polls, int drop_lane) {
     using C = Tpm<N, M, NSETS>;
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem);  // one per slot set
@@ -98,13 +98,14 @@ tpm_potrf_kernel(const float* __restrict__ A, float* __restrict__ L, int32_t* __
     if (w0 >= rounds) return;
     uint32_t phase_bits = 0u;  // bit s: parity of set s's next completion
     uint32_t inflight = 0u;    // bit s: set s has a load in flight
-    // the first NSETS - 1 rounds of this warp go out at once
+    // the first NSETS - 1 rounds of this warp go out at once (in the
+    // self-test, the first of them without the dropped lane's copy)
 #pragma unroll
     for (int s = 0; s < NSETS - 1; ++s) {
         const int64_t w = w0 + (int64_t)s * gridDim.x;
         if (w < rounds) {
             issue_round_load<N>(A, w * M, round_count<M>(batch, w), slot_of(s), bar + s, lane,
-                                drop_lane);
+                                s == 0 ? drop_lane : -1);
             inflight |= 1u << s;
         }
     }
@@ -120,14 +121,19 @@ tpm_potrf_kernel(const float* __restrict__ A, float* __restrict__ L, int32_t* __
             const int bn = (int)((r + NSETS - 1) % NSETS);
             bulk_wait_read_all();  // that set's last store has left shared memory
             issue_round_load<N>(A, wn * M, round_count<M>(batch, wn), slot_of(bn), bar + bn, lane,
-                                drop_lane);
+                                -1);
             inflight |= 1u << bn;
         }
         const uint32_t par = (phase_bits >> b) & 1u;
         if (!__all_sync(0xffffffffu, mbar_wait(bar + b, par, max_polls))) {
-            // The copies did not complete: mark this round's matrices and stop
-            // (after one more bounded wait for every set's copies in flight).
+            // The copies did not complete: mark this round's matrices and stop,
+            // after one more bounded wait for every set's copies in flight so
+            // that none lands in shared memory after the block has retired.
+            // In the self-test the held-back copy (only ever in a warp's first
+            // round) is issued now, so that wait can complete.
             if (lane < nvalid) status[m] = -1;
+            if (r == 0 && lane == drop_lane && lane < nvalid)
+                bulk_load(slot_of(b), A + m * (N * N), N * N * 4, bar + b);
 #pragma unroll
             for (int s = 0; s < NSETS; ++s)
                 if ((inflight >> s) & 1u) mbar_wait(bar + s, (phase_bits >> s) & 1u, max_polls);
@@ -187,24 +193,21 @@ tpm_potrf_kernel(const float* __restrict__ A, float* __restrict__ L, int32_t* __
     bulk_wait_all();
 }
 
-// Persistent grid: resident blocks per SM (queried once per kernel) times the
-// SM count of the current device, capped by the number of rounds.
+// Persistent grid: resident blocks per SM (queried once per kernel and
+// device) times the SM count of the current device, capped by the number of
+// rounds.
 template <typename K>
-int tpm_grid(K kern, size_t smem, int64_t rounds, int* per_sm_cache) {
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (*per_sm_cache <= 0) {
-        int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32, smem) !=
-                cudaSuccess || per_sm < 1) {
+int tpm_grid(K kern, size_t smem, int64_t rounds, PerDeviceInt& per_sm_cache) {
+    const int per_sm = per_sm_cache.get([&] {
+        int x = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&x, kern, 32, smem) != cudaSuccess) {
             cudaGetLastError();
-            per_sm = 1;
+            return 0;
         }
-        *per_sm_cache = per_sm;
-    }
+        return x;
+    });
     return (int)std::max<int64_t>(
-        1, std::min<int64_t>((int64_t)std::max(sms, 1) * *per_sm_cache, rounds));
+        1, std::min<int64_t>((int64_t)device_sm_count() * std::max(per_sm, 1), rounds));
 }
 
 // Matrices per round and slot sets of the n = 16 kernel: 27 lanes with two
@@ -218,14 +221,11 @@ cudaError_t tpm_fwd_n(const float* A, float* L, int32_t* status, int64_t batch,
                       cudaStream_t stream, uint32_t max_polls = kMbarPolls, int drop_lane = -1) {
     const size_t smem = Tpm<N, M, NSETS>::kSmem;
     auto kern = tpm_potrf_kernel<N, M, NSETS>;
-    static int smem_set = 0, per_sm = 0;
-    if (!smem_set) {
-        cudaError_t e =
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        smem_set = 1;
-    }
-    const int grid = tpm_grid(kern, smem, (batch + M - 1) / M, &per_sm);
+    static std::atomic<uint64_t> smem_set{0};
+    static PerDeviceInt per_sm;
+    cudaError_t e = allow_smem_once(kern, smem, smem_set);
+    if (e != cudaSuccess) return e;
+    const int grid = tpm_grid(kern, smem, (batch + M - 1) / M, per_sm);
     kern<<<grid, 32, smem, stream>>>(A, L, status, batch, max_polls, drop_lane);
     return cudaGetLastError();
 }

@@ -1,9 +1,10 @@
 /*
  * chol_probe.h -- measurement utility shipped with the GB300 Cholesky library.
  *
- * Not part of the factorisation path: it measures the denominator that the
+ * Not part of the factorisation path: it measures the denominators that the
  * FP64 (and FP32) rooflines of the blocked path are reported against, since
- * the chip's FMA peaks are not published figures one can rely on.
+ * the chip's FP64 rates are not published figures one can rely on.  Both
+ * FP64 pipes are measured: the FMA pipe and the f64 mma.sync tensor path.
  */
 #ifndef CHOL_PROBE_H
 #define CHOL_PROBE_H
@@ -26,6 +27,25 @@ extern "C" {
  */
 CHOL_API int chol_probe_fma_peak(int32_t dtype, int64_t iters, void* sink, double* flops,
                                  void* stream);
+
+/* Shapes of the f64 mma.sync instruction (the FP64 tensor path, DMMA). */
+enum {
+    CHOL_DMMA_M8N8K4 = 0,
+    CHOL_DMMA_M16N8K4 = 1,
+    CHOL_DMMA_M16N8K8 = 2,
+    CHOL_DMMA_M16N8K16 = 3
+};
+
+/*
+ * chol_probe_dmma_peak -- the same measurement for the double-precision
+ * tensor path: every thread of a full-occupancy grid issues `iters` rounds of
+ * 4 independent warp-wide `mma.sync ... .f64` operations of the given shape
+ * (CHOL_DMMA_*).  *flops receives the rate in FLOP/s (2 M N K per warp-wide
+ * operation).  `sink` is a device buffer of at least one double.  Returns
+ * CHOL_OK, CHOL_EINVAL (bad shape, iters <= 0, null pointer) or CHOL_ECUDA.
+ */
+CHOL_API int chol_probe_dmma_peak(int32_t shape, int64_t iters, void* sink, double* flops,
+                                  void* stream);
 
 #ifdef __cplusplus
 }

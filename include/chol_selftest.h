@@ -18,12 +18,13 @@ extern "C" {
 /*
  * chol_selftest_wait_timeout -- runs the batched float32 n = 16 forward kernel
  * (the one chol_fwd uses for 16-byte-aligned float32 16x16 matrices) with one
- * matrix copy of every round deliberately never issued, a lost message, so
- * no round's arrival barrier can complete, and with `max_polls` polls per
- * barrier wait.  Every warp gives up on its first round, writes status -1 for
- * that round's matrices, waits (again at most max_polls polls per barrier)
- * for its copies still in flight and returns.  No other status entry and no
- * part of L is written.
+ * matrix copy of every warp's first round held back, a lost message, so that
+ * round's arrival barrier cannot complete, and with `max_polls` polls per
+ * barrier wait.  Every warp gives up on its first round and writes status -1
+ * for that round's matrices; the held-back copy is then issued late and the
+ * warp waits (again at most max_polls polls per barrier) until every copy it
+ * issued has landed, so no block retires with a copy in flight, and returns.
+ * No other status entry and no part of L is written.
  *   A       in : float[batch][16][16], device, 16-byte aligned.
  *   L       out: float[batch][16][16], device, 16-byte aligned, not
  *                overlapping A or status.

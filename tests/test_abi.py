@@ -135,3 +135,30 @@ def test_binding_rejects_cpu_tensors():
         binding.chol_fwd(A)
     with pytest.raises(ValueError):
         binding.chol_adj(A, A)
+
+
+def test_noalloc_adjoint_returns_the_same_codes_as_chol_adj_ex():
+    """chol_adj_noalloc promises chol_adj_ex's argument checks: both entry
+    points must answer every bad argument with the same code."""
+    lib = binding.load_library()
+    buf = (ctypes.c_double * 64)()
+    st = (ctypes.c_int32 * 4)()
+    p, s = ctypes.addressof(buf), ctypes.addressof(st)
+    cases = [
+        (1, 4, 7, p, p, p, None, 0),          # dtype
+        (1, 0, 1, p, p, p, None, 0),          # n
+        (-2, 4, 1, p, p, p, None, 0),         # batch
+        (1, 100, 1, p, p, p, None, 48),       # tile
+        (1, 4, 1, None, p, p, None, 0),       # null L
+        (1, 4, 1, p, None, p, None, 0),       # null adj_L
+        (1, 4, 1, p, p, None, None, 0),       # null adj_A
+        (1, 4, 1, p + 4, p, p, None, 0),      # misaligned L
+        (1, 4, 1, p, p, p, s + 2, 0),         # misaligned status
+        (1, 4, 1, p, p, p, None, 0),          # host pointers
+        (0, 4, 1, None, None, None, None, 0), # empty batch: no-op
+        (1 << 40, 1 << 20, 1, p, p, p, None, 0),  # size overflow
+    ]
+    for args in cases:
+        a = lib.chol_adj_ex(*args, None)
+        b = lib.chol_adj_noalloc(*args, None)
+        assert a == b, (args, a, b)

@@ -62,7 +62,10 @@ def test_code_hash_ignores_comments_but_not_code():
     assert bench.code_sha256(src) != bench.code_sha256(other)
 
 
-def test_traffic_record_matches_the_current_kernel_source():
+def test_traffic_record_follows_the_kernel_source_hash():
     import bench
-    assert bench.measured_traffic("batched_16", "adj") is not None
-    assert bench.measured_traffic("batched_16", "fwd") is None
+    for wl, rec in bench.MEASURED_TRAFFIC.items():
+        with open(os.path.join(ROOT, rec["source"])) as f:
+            live = bench.code_sha256(f.read()) == rec["code_sha256"]
+        got = bench.measured_traffic(wl, rec["kernel"])
+        assert (got == rec["bytes"]) if live else (got is None)

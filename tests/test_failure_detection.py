@@ -1,9 +1,11 @@
 """Failure detection on the GPU without a GPU fault: a bounded device wait
 that cannot complete ends in an error status the host reads, and the CUDA
-context stays usable.  The self-test entry point drops one matrix copy of
-every round of the forward kernel (a lost message), so no arrival barrier
-completes; every warp must give up after its poll limit, mark its first
-round's matrices with status -1 and return."""
+context stays usable.  The self-test entry point holds back one matrix copy
+of every warp's first round in the forward kernel (a lost message), so that
+round's arrival barrier cannot complete; every warp must give up after its
+poll limit, mark its first round's matrices with status -1, issue the
+held-back copy late, wait until every copy it issued has landed and
+return."""
 import numpy as np
 import pytest
 

@@ -175,6 +175,28 @@ def test_batched_equals_single():
     assert int(sb[4]) == 3
 
 
+@pytest.mark.parametrize("dtype", [np.float64, np.float32])
+def test_threaded_single_matrix_path_is_bit_identical(dtype):
+    """The single-matrix routines share independent rows (forward) and
+    columns/rows (adjoint solves) out over threads without changing any sum's
+    order: any thread count must give the one-thread result bit for bit."""
+    n = 97
+    A = spd(n, 21).astype(dtype)
+    Lbar = W.tril_normal(1, n, 22, dtype)[0]
+    L1, s1 = oracle.potrf(A, threads=1)
+    G1 = oracle.potrf_adj(L1, Lbar, threads=1)
+    for t in (2, 3, 8):
+        Lt, st = oracle.potrf(A, threads=t)
+        assert int(st) == int(s1) == 0
+        assert np.array_equal(Lt, L1)
+        Gt = oracle.potrf_adj(L1, Lbar, threads=t)
+        assert np.array_equal(Gt, G1)
+    # a failing pivot stops at the same column whatever the threads
+    B = A.copy()
+    B[40, 40] = -1
+    assert int(oracle.potrf(B, threads=4)[1]) == int(oracle.potrf(B, threads=1)[1]) == 41
+
+
 def test_workload_status_construction():
     w = W.batched_64(batch=500)
     _, st = oracle.potrf(w.A)
