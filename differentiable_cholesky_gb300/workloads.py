@@ -62,6 +62,28 @@ def gram_spd(batch: int, n: int, seed: int, shift: float, dtype,
     return A.astype(dtype)
 
 
+def tril_normal_complex(batch: int, n: int, seed: int, dtype) -> np.ndarray:
+    """``tril(N(0, 1) + i N(0, 1))`` in ``[batch, n, n]`` (real and imaginary
+    parts drawn in that order as one ``[2, batch, n, n]`` array), then cast."""
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((2, batch, n, n))
+    return np.tril(x[0] + 1j * x[1]).astype(dtype)
+
+
+def hermitian_spd(batch: int, n: int, seed: int, shift: float, dtype,
+                  scale: float | None = None) -> np.ndarray:
+    """``A_b = G_b G_b^H / scale + shift * I`` with complex Gaussian ``G``
+    (real and imaginary parts N(0, 1)); scale defaults to n."""
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((2, batch, n, n))
+    G = x[0] + 1j * x[1]
+    s = float(n if scale is None else scale)
+    A = np.matmul(G, np.conj(np.swapaxes(G, -1, -2))) / s
+    idx = np.arange(n)
+    A[:, idx, idx] = A[:, idx, idx].real + shift
+    return A.astype(dtype)
+
+
 def bidiagonal_E(n: int) -> np.ndarray:
     """Lower bidiagonal E: diagonal linspace(1, 2, n), sub-diagonal 0.5."""
     E = np.diag(np.linspace(1.0, 2.0, n))

@@ -15,6 +15,10 @@ ctypes.  Each function states the passage it restates:
   closing comment of NVIDIA/warp issue #1316 states it: ``S = Phi(L^T tril(Lbar))``,
   solve ``L^T X = S``, solve ``M L = X``, accumulate ``M + M^T`` into the lower
   triangle of ``Abar`` (``M_ii`` on the diagonal).
+* :func:`hpotrf` / :func:`hpotrf_adj` -- the same for complex Hermitian matrices
+  (``A = L L^H``, jaxmg docs intro: "symmetric or Hermitian"), with conjugate
+  transposes: ``P = L^H tril(Lbar)``, solves against ``L^H`` and ``L``,
+  ``Abar_ij += M_ij + conj(M_ji)`` below the diagonal and ``Re(M_ii)`` on it.
 
 Parity pins for every function are in ``tests/test_oracle_pins.py``.
 """
@@ -74,6 +78,15 @@ def _load():
             f.restype = ctypes.c_int32
             f = getattr(lib, f"orc_potrf_adj_batch_{sfx}")
             f.argtypes = [ctypes.c_int64, ctypes.c_int32, fp, fp, fp, _I32P, ctypes.c_int32]
+            f.restype = ctypes.c_int32
+        for sfx in ("z", "c"):
+            f = getattr(lib, f"orc_hpotrf_batch_{sfx}")
+            f.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                          _I32P, ctypes.c_int32]
+            f.restype = None
+            f = getattr(lib, f"orc_hpotrf_adj_batch_{sfx}")
+            f.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                          ctypes.c_void_p, _I32P, ctypes.c_int32]
             f.restype = ctypes.c_int32
         lib.orc_max_threads.argtypes = []
         lib.orc_max_threads.restype = ctypes.c_int32
@@ -161,6 +174,65 @@ def potrf_adj(L, Lbar, Abar=None, status=None, dtype=None, threads: int = 1):
         rc = getattr(lib, f"orc_potrf_adj_batch_{sfx}")(
             nb, n, L.ctypes.data_as(fp), Lbar.ctypes.data_as(fp), out.ctypes.data_as(fp),
             st.ctypes.data_as(_I32P) if st is not None else None, int(threads))
+    if rc != 0:
+        raise MemoryError("oracle adjoint could not allocate its scratch")
+    return out
+
+
+def _csfx(dtype):
+    dtype = np.dtype(dtype)
+    if dtype == np.complex128:
+        return "z"
+    if dtype == np.complex64:
+        return "c"
+    raise TypeError(f"complex oracle supports complex64/complex128, not {dtype}")
+
+
+def hpotrf(A, dtype=None, threads: int = 1):
+    """Lower Cholesky factor ``A = L L^H`` of a complex Hermitian matrix or a
+    batch ``[..., n, n]`` (complex64/complex128).  Only the lower triangle is
+    read, and only the real part of the diagonal.  Returns ``(L, status)`` as
+    :func:`potrf` does; ``L`` has a real positive diagonal."""
+    A = np.asarray(A)
+    dtype = np.dtype(dtype or A.dtype)
+    sfx = _csfx(dtype)
+    A = np.ascontiguousarray(A, dtype=dtype)
+    n = A.shape[-1]
+    if A.ndim < 2 or A.shape[-2] != n:
+        raise ValueError("A must be [..., n, n]")
+    batch_shape = A.shape[:-2]
+    nb = int(np.prod(batch_shape)) if batch_shape else 1
+    L = np.zeros_like(A)
+    status = np.zeros(nb, dtype=np.int32)
+    if nb > 0:
+        getattr(_load(), f"orc_hpotrf_batch_{sfx}")(
+            nb, n, A.ctypes.data, L.ctypes.data, status.ctypes.data_as(_I32P), int(threads))
+    return L, status.reshape(batch_shape)
+
+
+def hpotrf_adj(L, Lbar, Abar=None, status=None, dtype=None, threads: int = 1):
+    """Literal Hermitian adjoint; returns a copy of ``Abar`` (default zeros)
+    with ``M_ij + conj(M_ji)`` added below the diagonal and ``Re(M_ii)`` on
+    it, ``M = L^-H Phi(L^H tril(Lbar)) L^-1``.  ``Lbar`` is the gradient of a
+    real loss with respect to ``L`` as ``dLoss/dRe + i dLoss/dIm``.  Matrices
+    with non-zero ``status`` are skipped."""
+    L = np.asarray(L)
+    dtype = np.dtype(dtype or L.dtype)
+    sfx = _csfx(dtype)
+    L = np.ascontiguousarray(L, dtype=dtype)
+    Lbar = np.ascontiguousarray(Lbar, dtype=dtype)
+    if Lbar.shape != L.shape:
+        raise ValueError("L and Lbar must have the same shape")
+    out = np.zeros_like(L) if Abar is None else np.array(Abar, dtype=dtype, copy=True, order="C")
+    n = L.shape[-1]
+    batch_shape = L.shape[:-2]
+    nb = int(np.prod(batch_shape)) if batch_shape else 1
+    st = None
+    if status is not None:
+        st = np.ascontiguousarray(np.asarray(status, dtype=np.int32).reshape(-1))
+    rc = getattr(_load(), f"orc_hpotrf_adj_batch_{sfx}")(
+        nb, n, L.ctypes.data, Lbar.ctypes.data, out.ctypes.data,
+        st.ctypes.data_as(_I32P) if st is not None else None, int(threads))
     if rc != 0:
         raise MemoryError("oracle adjoint could not allocate its scratch")
     return out

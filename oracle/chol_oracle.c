@@ -35,12 +35,31 @@
  *             entries that the forward reads.  Upper triangles of Lbar and L
  *             are treated as zero, the upper triangle of Abar is untouched.
  *
+ * zpotrf / zpotrf_adj -- the same two operations for complex Hermitian
+ *             positive-definite matrices, A = L L^H ("a symmetric or Hermitian
+ *             positive-definite matrix", jaxmg docs "Cholesky factorization",
+ *             intro), written with conjugate transposes where the real
+ *             formulas have transposes:
+ *                 d_j  = Re(a_jj) - sum_{k<j} |l_jk|^2      (real pivot)
+ *                 l_jj = sqrt(d_j)                           (real)
+ *                 l_ij = (a_ij - sum_{k<j} l_ik conj(l_jk)) / l_jj
+ *             and, for a real loss whose gradient with respect to L is
+ *             Lbar = dLoss/dRe(L) + i dLoss/dIm(L),
+ *                 P = L^H tril(Lbar),  S = Phi(P),
+ *                 X : solve L^H X = S,  M : solve M L = X,
+ *                 Abar_ij += M_ij + conj(M_ji)  (i > j),  Abar_ii += Re(M_ii),
+ *             the derivative with respect to the lower entries the forward
+ *             reads (real and imaginary parts below the diagonal, the real
+ *             part on it: the forward ignores Im(a_jj)).  The pages state the
+ *             adjoint for the real case only; this is its Hermitian form.
+ *
  * Row-major storage, matrix b of a batch at offset b*n*n.  No blocking,
  * fusion or reordering beyond the formulas above.  The batched wrappers run
  * independent matrices on OpenMP threads (each matrix's arithmetic is the
  * same as the single-matrix routine); the single-matrix routines may split
  * independent rows/columns across threads without changing any sum's order.
  */
+#include <complex.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -186,3 +205,125 @@ int32_t orc_max_threads(void) {
     return 1;
 #endif
 }
+
+/* ---------------------------------------------------------------------- */
+/* Complex Hermitian instantiation: double complex (z) and float complex  */
+/* (c).  Same structure as above with conjugates where the real formulas  */
+/* transpose.                                                              */
+/* ---------------------------------------------------------------------- */
+#define DEFINE_ORACLE_HERMITIAN(T, R, SFX, SQRT, CONJ, CREAL)                    \
+                                                                                 \
+static int32_t hpotrf_one_##SFX(int32_t n, const T* A, T* L, int threads) {     \
+    for (size_t e = 0; e < (size_t)n * (size_t)n; ++e) L[e] = (T)0;              \
+    for (int32_t j = 0; j < n; ++j) {                                            \
+        R d = CREAL(A[IDX(j, j, n)]);                                            \
+        for (int32_t k = 0; k < j; ++k) {                                        \
+            const T l = L[IDX(j, k, n)];                                         \
+            d -= CREAL(l * CONJ(l));                                             \
+        }                                                                        \
+        if (!(d > (R)0)) return j + 1;                                           \
+        const R ljj = SQRT(d);                                                   \
+        L[IDX(j, j, n)] = (T)ljj;                                                \
+        _Pragma("omp parallel for if(threads > 1) num_threads(threads) schedule(static)") \
+        for (int32_t i = j + 1; i < n; ++i) {                                    \
+            T s = A[IDX(i, j, n)];                                               \
+            for (int32_t k = 0; k < j; ++k) s -= L[IDX(i, k, n)] * CONJ(L[IDX(j, k, n)]); \
+            L[IDX(i, j, n)] = s / ljj;                                           \
+        }                                                                        \
+    }                                                                            \
+    return 0;                                                                    \
+}                                                                                \
+                                                                                 \
+static void hpotrf_adj_one_##SFX(int32_t n, const T* L, const T* Lbar, T* Abar,  \
+                                 T* W, int threads) {                            \
+    T* P = W;                 /* P = L^H tril(Lbar), then X                 */   \
+    T* R_ = W + (size_t)n * n; /* S, then M                                  */  \
+    _Pragma("omp parallel for if(threads > 1) num_threads(threads) schedule(static)") \
+    for (int32_t i = 0; i < n; ++i) {                                            \
+        for (int32_t j = 0; j < n; ++j) P[IDX(i, j, n)] = (T)0;                  \
+        for (int32_t k = i; k < n; ++k) {                                        \
+            const T lki = CONJ(L[IDX(k, i, n)]);                                 \
+            for (int32_t j = 0; j <= k; ++j)                                     \
+                P[IDX(i, j, n)] += lki * Lbar[IDX(k, j, n)];                     \
+        }                                                                        \
+    }                                                                            \
+    /* S = Phi(P): keep the lower triangle, halve the diagonal. */               \
+    for (int32_t i = 0; i < n; ++i)                                              \
+        for (int32_t j = 0; j < n; ++j) {                                        \
+            T v = P[IDX(i, j, n)];                                               \
+            R_[IDX(i, j, n)] = (j < i) ? v : ((j == i) ? v / (R)2 : (T)0);       \
+        }                                                                        \
+    /* X: solve L^H X = S, X_ij = (S_ij - sum_{k>i} conj(L_ki) X_kj) / L_ii  */  \
+    _Pragma("omp parallel for if(threads > 1) num_threads(threads) schedule(static)") \
+    for (int32_t j = 0; j < n; ++j) {                                            \
+        for (int32_t i = n - 1; i >= 0; --i) {                                   \
+            T s = R_[IDX(i, j, n)];                                              \
+            for (int32_t k = i + 1; k < n; ++k)                                  \
+                s -= CONJ(L[IDX(k, i, n)]) * P[IDX(k, j, n)];                    \
+            P[IDX(i, j, n)] = s / CREAL(L[IDX(i, i, n)]);                        \
+        }                                                                        \
+    }                                                                            \
+    /* M: solve M L = X, M_ij = (X_ij - sum_{k>j} M_ik L_kj) / L_jj          */  \
+    _Pragma("omp parallel for if(threads > 1) num_threads(threads) schedule(static)") \
+    for (int32_t i = 0; i < n; ++i) {                                            \
+        for (int32_t j = n - 1; j >= 0; --j) {                                   \
+            T s = P[IDX(i, j, n)];                                               \
+            for (int32_t k = j + 1; k < n; ++k) s -= R_[IDX(i, k, n)] * L[IDX(k, j, n)]; \
+            R_[IDX(i, j, n)] = s / CREAL(L[IDX(j, j, n)]);                       \
+        }                                                                        \
+    }                                                                            \
+    /* Accumulate: M_ij + conj(M_ji) below the diagonal, Re(M_ii) on it.     */  \
+    for (int32_t i = 0; i < n; ++i) {                                            \
+        for (int32_t j = 0; j < i; ++j)                                          \
+            Abar[IDX(i, j, n)] += R_[IDX(i, j, n)] + CONJ(R_[IDX(j, i, n)]);     \
+        Abar[IDX(i, i, n)] += CREAL(R_[IDX(i, i, n)]);                           \
+    }                                                                            \
+}                                                                                \
+                                                                                 \
+void orc_hpotrf_batch_##SFX(int64_t batch, int32_t n, const T* A, T* L,          \
+                            int32_t* status, int32_t threads) {                  \
+    const size_t nn = (size_t)n * (size_t)n;                                     \
+    if (batch == 1) {                                                            \
+        status[0] = n > 0 ? hpotrf_one_##SFX(n, A, L, threads) : 0;              \
+        return;                                                                  \
+    }                                                                            \
+    _Pragma("omp parallel for if(threads > 1) num_threads(threads) schedule(dynamic, 16)") \
+    for (int64_t b = 0; b < batch; ++b)                                          \
+        status[b] = hpotrf_one_##SFX(n, A + b * nn, L + b * nn, 1);              \
+}                                                                                \
+                                                                                 \
+int32_t orc_hpotrf_adj_batch_##SFX(int64_t batch, int32_t n, const T* L,         \
+                                   const T* Lbar, T* Abar, const int32_t* status, \
+                                   int32_t threads) {                            \
+    const size_t nn = (size_t)n * (size_t)n;                                     \
+    if (n <= 0) return 0;                                                        \
+    if (batch == 1) {                                                            \
+        if (status && status[0] != 0) return 0;                                  \
+        T* W = (T*)malloc(2 * nn * sizeof(T));                                   \
+        if (!W) return -1;                                                       \
+        hpotrf_adj_one_##SFX(n, L, Lbar, Abar, W, threads);                      \
+        free(W);                                                                 \
+        return 0;                                                                \
+    }                                                                            \
+    int32_t rc = 0;                                                              \
+    _Pragma("omp parallel if(threads > 1) num_threads(threads)")                 \
+    {                                                                            \
+        T* W = (T*)malloc(2 * nn * sizeof(T));                                   \
+        if (!W) {                                                                \
+            _Pragma("omp atomic write")                                          \
+            rc = -1;                                                             \
+        } else {                                                                 \
+            _Pragma("omp for schedule(dynamic, 16)")                             \
+            for (int64_t b = 0; b < batch; ++b) {                                \
+                if (status && status[b] != 0) continue; /* failed factor */     \
+                hpotrf_adj_one_##SFX(n, L + b * nn, Lbar + b * nn, Abar + b * nn, \
+                                     W, 1);                                      \
+            }                                                                    \
+            free(W);                                                             \
+        }                                                                        \
+    }                                                                            \
+    return rc;                                                                   \
+}
+
+DEFINE_ORACLE_HERMITIAN(double complex, double, z, sqrt, conj, creal)
+DEFINE_ORACLE_HERMITIAN(float complex, float, c, sqrtf, conjf, crealf)
