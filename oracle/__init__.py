@@ -15,6 +15,10 @@ ctypes.  Each function states the passage it restates:
   closing comment of NVIDIA/warp issue #1316 states it: ``S = Phi(L^T tril(Lbar))``,
   solve ``L^T X = S``, solve ``M L = X``, accumulate ``M + M^T`` into the lower
   triangle of ``Abar`` (``M_ii`` on the diagonal).
+* :func:`potrs` / :func:`potrs_adj` -- the solve with the factor, ``X = A^-1 B``
+  by ``L Y = B`` then ``L^H X = Y`` (the step jaxmg's potrf leaves out, "without
+  performing a solve"), and its reverse mode: ``Bbar += A^-1 Xbar`` and
+  ``Lbar += tril((G + G^H) L)`` with ``G = -(A^-1 Xbar) X^H``.
 * :func:`hpotrf` / :func:`hpotrf_adj` -- the same for complex Hermitian matrices
   (``A = L L^H``, jaxmg docs intro: "symmetric or Hermitian"), with conjugate
   transposes: ``P = L^H tril(Lbar)``, solves against ``L^H`` and ``L``,
@@ -87,6 +91,16 @@ def _load():
             f = getattr(lib, f"orc_hpotrf_adj_batch_{sfx}")
             f.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
                           ctypes.c_void_p, _I32P, ctypes.c_int32]
+            f.restype = ctypes.c_int32
+        for sfx in ("d", "s", "z", "c"):
+            f = getattr(lib, f"orc_potrs_{sfx}")
+            f.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                          ctypes.c_void_p, ctypes.c_void_p, _I32P, ctypes.c_int32]
+            f.restype = ctypes.c_int32
+            f = getattr(lib, f"orc_potrs_adj_{sfx}")
+            f.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                          _I32P, ctypes.c_int32]
             f.restype = ctypes.c_int32
         lib.orc_max_threads.argtypes = []
         lib.orc_max_threads.restype = ctypes.c_int32
@@ -236,3 +250,62 @@ def hpotrf_adj(L, Lbar, Abar=None, status=None, dtype=None, threads: int = 1):
     if rc != 0:
         raise MemoryError("oracle adjoint could not allocate its scratch")
     return out
+
+
+_ANY_SFX = {np.dtype(np.float64): "d", np.dtype(np.float32): "s",
+            np.dtype(np.complex128): "z", np.dtype(np.complex64): "c"}
+
+
+def _status_arg(status):
+    if status is None:
+        return None, None
+    st = np.ascontiguousarray(np.asarray(status, dtype=np.int32).reshape(-1))
+    return st, st.ctypes.data_as(_I32P)
+
+
+def potrs(L, B, status=None, dtype=None, threads: int = 1):
+    """``X = A^-1 B`` with ``A = L L^H`` (``L^T`` for real types): ``L`` is
+    ``[..., n, n]`` (lower triangle read), ``B`` is ``[..., n, nrhs]``.
+    Matrices with non-zero ``status`` get ``X`` = zeros."""
+    L = np.asarray(L)
+    dtype = np.dtype(dtype or L.dtype)
+    sfx = _ANY_SFX[dtype]
+    L = np.ascontiguousarray(L, dtype=dtype)
+    B = np.ascontiguousarray(B, dtype=dtype)
+    n = L.shape[-1]
+    if B.shape[:-1] != L.shape[:-1]:
+        raise ValueError("B must be [..., n, nrhs] with L's batch shape and n")
+    nrhs = B.shape[-1]
+    nb = int(np.prod(L.shape[:-2])) if L.shape[:-2] else 1
+    X = np.zeros_like(B)
+    st, stp = _status_arg(status)
+    if nb > 0 and n > 0 and nrhs > 0:
+        rc = getattr(_load(), f"orc_potrs_{sfx}")(nb, n, nrhs, L.ctypes.data, B.ctypes.data,
+                                                  X.ctypes.data, stp, int(threads))
+        if rc != 0:
+            raise MemoryError("oracle solve could not allocate its scratch")
+    return X
+
+
+def potrs_adj(L, X, Xbar, Bbar=None, Lbar=None, status=None, dtype=None, threads: int = 1):
+    """Reverse mode of :func:`potrs`.  Returns ``(Bbar + A^-1 Xbar,
+    Lbar + tril((G + G^H) L))`` with ``G = -(A^-1 Xbar) X^H`` (copies; the
+    defaults are zeros).  Matrices with non-zero ``status`` are skipped."""
+    L = np.asarray(L)
+    dtype = np.dtype(dtype or L.dtype)
+    sfx = _ANY_SFX[dtype]
+    L = np.ascontiguousarray(L, dtype=dtype)
+    X = np.ascontiguousarray(X, dtype=dtype)
+    Xbar = np.ascontiguousarray(Xbar, dtype=dtype)
+    n, nrhs = L.shape[-1], X.shape[-1]
+    nb = int(np.prod(L.shape[:-2])) if L.shape[:-2] else 1
+    Bo = np.zeros_like(X) if Bbar is None else np.array(Bbar, dtype=dtype, copy=True, order="C")
+    Lo = np.zeros_like(L) if Lbar is None else np.array(Lbar, dtype=dtype, copy=True, order="C")
+    st, stp = _status_arg(status)
+    if nb > 0 and n > 0 and nrhs > 0:
+        rc = getattr(_load(), f"orc_potrs_adj_{sfx}")(
+            nb, n, nrhs, L.ctypes.data, X.ctypes.data, Xbar.ctypes.data, Bo.ctypes.data,
+            Lo.ctypes.data, stp, int(threads))
+        if rc != 0:
+            raise MemoryError("oracle solve adjoint could not allocate its scratch")
+    return Bo, Lo

@@ -53,6 +53,17 @@
  *             part on it: the forward ignores Im(a_jj)).  The pages state the
  *             adjoint for the real case only; this is its Hermitian form.
  *
+ * potrs / potrs_adj -- the solve with the factor that potrf leaves for later
+ *             (jaxmg docs "Cholesky factorization", intro: potrf returns the
+ *             factor "without performing a solve"): X = A^-1 B = L^-H L^-1 B
+ *             for B with nrhs columns, by forward substitution L Y = B then
+ *             back substitution L^H X = Y, and its reverse mode for a loss
+ *             gradient Xbar: Bbar += A^-1 Xbar (the same two solves) and
+ *             Lbar += tril(G + G^H) L restricted to the lower triangle, with
+ *             G = -Bbar X^H the gradient with respect to A (from
+ *             dX = -A^-1 dA X and dA = dL L^H + L dL^H).  Real types read ^H
+ *             as ^T.
+ *
  * Row-major storage, matrix b of a batch at offset b*n*n.  No blocking,
  * fusion or reordering beyond the formulas above.  The batched wrappers run
  * independent matrices on OpenMP threads (each matrix's arithmetic is the
@@ -327,3 +338,107 @@ int32_t orc_hpotrf_adj_batch_##SFX(int64_t batch, int32_t n, const T* L,        
 
 DEFINE_ORACLE_HERMITIAN(double complex, double, z, sqrt, conj, creal)
 DEFINE_ORACLE_HERMITIAN(float complex, float, c, sqrtf, conjf, crealf)
+
+/* ---------------------------------------------------------------------- */
+/* Solve with the factor and its adjoint, for all four element types.     */
+/* B, X, Xbar, Bbar: [n][nrhs] row-major per matrix; L, Lbar: [n][n].    */
+/* ---------------------------------------------------------------------- */
+#define RID(x) (x)
+#define DEFINE_POTRS(T, R, SFX, CONJ, CREAL)                                     \
+                                                                                 \
+/* X = L^-H (L^-1 B), column by column; X may be B itself. */                    \
+static void potrs_one_##SFX(int32_t n, int32_t nrhs, const T* L, const T* B,     \
+                            T* X, T* Y) {                                        \
+    for (int32_t r = 0; r < nrhs; ++r) {                                         \
+        /* forward: y_i = (b_i - sum_{k<i} L_ik y_k) / L_ii */                   \
+        for (int32_t i = 0; i < n; ++i) {                                        \
+            T s = B[IDX(i, r, nrhs)];                                            \
+            for (int32_t k = 0; k < i; ++k) s -= L[IDX(i, k, n)] * Y[k];         \
+            Y[i] = s / CREAL(L[IDX(i, i, n)]);                                   \
+        }                                                                        \
+        /* back: x_i = (y_i - sum_{k>i} conj(L_ki) x_k) / L_ii */                \
+        for (int32_t i = n - 1; i >= 0; --i) {                                   \
+            T s = Y[i];                                                          \
+            for (int32_t k = i + 1; k < n; ++k) s -= CONJ(L[IDX(k, i, n)]) * Y[n + k]; \
+            Y[n + i] = s / CREAL(L[IDX(i, i, n)]);                               \
+        }                                                                        \
+        for (int32_t i = 0; i < n; ++i) X[IDX(i, r, nrhs)] = Y[n + i];           \
+    }                                                                            \
+}                                                                                \
+                                                                                 \
+int32_t orc_potrs_##SFX(int64_t batch, int32_t n, int32_t nrhs, const T* L,      \
+                        const T* B, T* X, const int32_t* status, int32_t threads) { \
+    const size_t nn = (size_t)n * n, nb = (size_t)n * nrhs;                      \
+    int32_t rc = 0;                                                              \
+    _Pragma("omp parallel if(threads > 1) num_threads(threads)")                 \
+    {                                                                            \
+        T* Y = (T*)malloc(2 * (size_t)n * sizeof(T) + 1);                        \
+        if (!Y) {                                                                \
+            _Pragma("omp atomic write")                                          \
+            rc = -1;                                                             \
+        } else {                                                                 \
+            _Pragma("omp for schedule(dynamic, 4)")                              \
+            for (int64_t b = 0; b < batch; ++b) {                                \
+                if (status && status[b] != 0) continue;                          \
+                potrs_one_##SFX(n, nrhs, L + b * nn, B + b * nb, X + b * nb, Y); \
+            }                                                                    \
+            free(Y);                                                             \
+        }                                                                        \
+    }                                                                            \
+    return rc;                                                                   \
+}                                                                                \
+                                                                                 \
+/* Bbar += A^-1 Xbar (if Bbar); Lbar += tril((G + G^H) L), G = -Bbar_new X^H */  \
+/* with Bbar_new = A^-1 Xbar (if Lbar).                                      */  \
+int32_t orc_potrs_adj_##SFX(int64_t batch, int32_t n, int32_t nrhs, const T* L,  \
+                            const T* X, const T* Xbar, T* Bbar, T* Lbar,         \
+                            const int32_t* status, int32_t threads) {            \
+    const size_t nn = (size_t)n * n, nb = (size_t)n * nrhs;                      \
+    int32_t rc = 0;                                                              \
+    _Pragma("omp parallel if(threads > 1) num_threads(threads)")                 \
+    {                                                                            \
+        T* Y = (T*)malloc((2 * (size_t)n + nb + 2 * nn) * sizeof(T));            \
+        if (!Y) {                                                                \
+            _Pragma("omp atomic write")                                          \
+            rc = -1;                                                             \
+        } else {                                                                 \
+            T* Bb = Y + 2 * (size_t)n; /* A^-1 Xbar      */                      \
+            T* G = Bb + nb;            /* -Bb X^H        */                      \
+            T* H = G + nn;             /* (G + G^H) L    */                      \
+            _Pragma("omp for schedule(dynamic, 1)")                              \
+            for (int64_t b = 0; b < batch; ++b) {                                \
+                if (status && status[b] != 0) continue;                          \
+                const T* Lb = L + b * nn;                                        \
+                const T* Xb = X + b * nb;                                        \
+                potrs_one_##SFX(n, nrhs, Lb, Xbar + b * nb, Bb, Y);              \
+                if (Bbar)                                                        \
+                    for (size_t e = 0; e < nb; ++e) Bbar[b * nb + e] += Bb[e];   \
+                if (!Lbar) continue;                                             \
+                for (int32_t i = 0; i < n; ++i)                                  \
+                    for (int32_t j = 0; j < n; ++j) {                            \
+                        T s = (T)0;                                              \
+                        for (int32_t r = 0; r < nrhs; ++r)                       \
+                            s += Bb[IDX(i, r, nrhs)] * CONJ(Xb[IDX(j, r, nrhs)]); \
+                        G[IDX(i, j, n)] = -s;                                    \
+                    }                                                            \
+                for (int32_t i = 0; i < n; ++i)                                  \
+                    for (int32_t j = 0; j < n; ++j) {                            \
+                        T s = (T)0;                                              \
+                        for (int32_t k = 0; k < n; ++k)                          \
+                            s += (G[IDX(i, k, n)] + CONJ(G[IDX(k, i, n)])) * Lb[IDX(k, j, n)]; \
+                        H[IDX(i, j, n)] = s;                                     \
+                    }                                                            \
+                for (int32_t i = 0; i < n; ++i)                                  \
+                    for (int32_t j = 0; j <= i; ++j)                             \
+                        Lbar[b * nn + IDX(i, j, n)] += H[IDX(i, j, n)];          \
+            }                                                                    \
+            free(Y);                                                             \
+        }                                                                        \
+    }                                                                            \
+    return rc;                                                                   \
+}
+
+DEFINE_POTRS(double, double, d, RID, RID)
+DEFINE_POTRS(float, float, s, RID, RID)
+DEFINE_POTRS(double complex, double, z, conj, creal)
+DEFINE_POTRS(float complex, float, c, conjf, crealf)
