@@ -17,7 +17,10 @@ from . import build as _build
 
 CHOL_F32 = 0
 CHOL_F64 = 1
-_DTYPES = {torch.float32: CHOL_F32, torch.float64: CHOL_F64}
+CHOL_C64 = 2
+CHOL_C128 = 3
+_DTYPES = {torch.float32: CHOL_F32, torch.float64: CHOL_F64,
+           torch.complex64: CHOL_C64, torch.complex128: CHOL_C128}
 
 _lock = threading.Lock()
 _lib = None
@@ -63,6 +66,10 @@ def load_library(path: str | None = None):
         lib.chol_fwd_inplace.restype = ctypes.c_int
         lib.chol_adj_inplace.argtypes = [i64, i32, i32, vp, vp, vp, i32, vp]
         lib.chol_adj_inplace.restype = ctypes.c_int
+        lib.chol_solve.argtypes = [i64, i32, i32, i32, vp, vp, vp, vp, vp]
+        lib.chol_solve.restype = ctypes.c_int
+        lib.chol_solve_adj.argtypes = [i64, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]
+        lib.chol_solve_adj.restype = ctypes.c_int
         lib.chol_probe_fma_peak.argtypes = [i32, i64, vp, ctypes.POINTER(ctypes.c_double), vp]
         lib.chol_probe_fma_peak.restype = ctypes.c_int
         lib.chol_probe_dmma_peak.argtypes = [i32, i64, vp, ctypes.POINTER(ctypes.c_double), vp]
@@ -103,9 +110,10 @@ def _stream_ptr(stream) -> int | None:
 
 def chol_fwd(A: torch.Tensor, L: torch.Tensor | None = None, status: torch.Tensor | None = None,
              tile: int = 0, stream=None):
-    """``L, status = chol_fwd(A)`` for ``A`` of shape ``[..., n, n]`` (fp32/fp64).
+    """``L, status = chol_fwd(A)`` for ``A`` of shape ``[..., n, n]`` (float32,
+    float64, or complex64/complex128 Hermitian: ``A = L L^H``).
 
-    Only ``tril(A)`` is read.  ``status`` is int32 with the batch shape: 0, or
+    Only ``tril(A)`` is read (and only the real part of a complex diagonal).  ``status`` is int32 with the batch shape: 0, or
     the 1-based first failing pivot column.  Pre-allocated ``L``/``status`` may
     be passed to avoid allocation (they are fully overwritten).
     """
@@ -203,6 +211,78 @@ def chol_adj_inplace(L: torch.Tensor, adj: torch.Tensor, status: torch.Tensor | 
                                          sp, int(tile), _stream_ptr(stream))
     _check(rc)
     return adj
+
+
+def _rhs_shape(L: torch.Tensor, B: torch.Tensor):
+    batch, n = _shape(L)
+    if B.dim() != L.dim() or tuple(B.shape[:-1]) != tuple(L.shape[:-1]):
+        raise ValueError(f"expected right-hand sides [..., {n}, nrhs] matching L {tuple(L.shape)}, "
+                         f"got {tuple(B.shape)}")
+    return batch, n, int(B.shape[-1])
+
+
+def chol_solve(L: torch.Tensor, B: torch.Tensor, X: torch.Tensor | None = None,
+               status: torch.Tensor | None = None, stream=None):
+    """``X = A^-1 B`` with ``A = L L^H`` (``L L^T`` for real dtypes): ``L`` is
+    ``[..., n, n]`` from :func:`chol_fwd`, ``B`` is ``[..., n, nrhs]``.  ``X``
+    may be ``B`` itself (in place).  Matrices with non-zero ``status`` get
+    ``X = 0``.  Returns ``X``."""
+    _require(L, "L")
+    if L.dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {L.dtype}")
+    _require(B, "B", L.dtype)
+    batch, n, nrhs = _rhs_shape(L, B)
+    if X is None:
+        X = torch.empty_like(B)
+    _require(X, "X", L.dtype)
+    if tuple(X.shape) != tuple(B.shape):
+        raise ValueError("X must match B's shape")
+    sp = None
+    if status is not None:
+        _require(status, "status", torch.int32)
+        if status.numel() != batch:
+            raise ValueError("status must have one entry per matrix")
+        sp = status.data_ptr()
+    rc = load_library().chol_solve(batch, n, nrhs, _DTYPES[L.dtype], L.data_ptr(), B.data_ptr(),
+                                   X.data_ptr(), sp, _stream_ptr(stream))
+    _check(rc)
+    return X
+
+
+def chol_solve_adj(L: torch.Tensor, X: torch.Tensor, adj_X: torch.Tensor,
+                   adj_B: torch.Tensor | None = None, adj_L: torch.Tensor | None = None,
+                   status: torch.Tensor | None = None, want_B: bool = True, want_L: bool = True,
+                   stream=None):
+    """Reverse mode of :func:`chol_solve`: accumulates ``A^-1 adj_X`` into
+    ``adj_B`` and ``tril(-(Bb X^H + X Bb^H) L)`` into ``adj_L`` (zeros when
+    not given; skipped when ``want_B`` / ``want_L`` is false).  Returns
+    ``(adj_B, adj_L)``."""
+    _require(L, "L")
+    if L.dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {L.dtype}")
+    _require(X, "X", L.dtype)
+    _require(adj_X, "adj_X", L.dtype)
+    batch, n, nrhs = _rhs_shape(L, X)
+    if tuple(adj_X.shape) != tuple(X.shape):
+        raise ValueError("adj_X must match X's shape")
+    if want_B and adj_B is None:
+        adj_B = torch.zeros_like(X)
+    if want_L and adj_L is None:
+        adj_L = torch.zeros_like(L)
+    if adj_B is not None:
+        _require(adj_B, "adj_B", L.dtype)
+    if adj_L is not None:
+        _require(adj_L, "adj_L", L.dtype)
+    sp = None
+    if status is not None:
+        _require(status, "status", torch.int32)
+        sp = status.data_ptr()
+    rc = load_library().chol_solve_adj(
+        batch, n, nrhs, _DTYPES[L.dtype], L.data_ptr(), X.data_ptr(), adj_X.data_ptr(),
+        adj_B.data_ptr() if adj_B is not None else None,
+        adj_L.data_ptr() if adj_L is not None else None, sp, _stream_ptr(stream))
+    _check(rc)
+    return adj_B, adj_L
 
 
 def probe_fma_peak(dtype=torch.float64, iters: int = 1 << 16, stream=None) -> float:

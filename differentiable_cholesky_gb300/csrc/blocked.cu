@@ -26,6 +26,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <type_traits>
 
 #include "common.cuh"
 #include "chol_tile.cuh"
@@ -34,7 +35,26 @@
 namespace chol {
 namespace {
 
+using chol_tile::cplx;
+using chol_tile::detail::add;
+using chol_tile::detail::conj;
+using chol_tile::detail::madd;
+using chol_tile::detail::re;
+using chol_tile::detail::scale;
+using chol_tile::detail::shfl_xor;
+using chol_tile::detail::sub;
+
 constexpr int kThreads = 256;
+
+template <typename T> using real_t = typename chol_tile::detail::real_of<T>::type;
+
+// Element-wise atomic add (a complex value adds its two parts separately).
+__device__ __forceinline__ void atomic_add(float* p, float v) { atomicAdd(p, v); }
+__device__ __forceinline__ void atomic_add(double* p, double v) { atomicAdd(p, v); }
+template <typename R> __device__ __forceinline__ void atomic_add(cplx<R>* p, cplx<R> v) {
+    atomicAdd(&p->re, v.re);
+    atomicAdd(&p->im, v.im);
+}
 
 inline unsigned grid_y(int64_t batch) { return (unsigned)std::min<int64_t>(batch, 65535); }
 
@@ -56,7 +76,7 @@ tril_copy_kernel(const T* A, T* L, int32_t* __restrict__ status, int64_t batch, 
          e += (int64_t)gridDim.x * blockDim.x) {
         const int64_t w = e % nn;
         const int i = (int)(w / n), j = (int)(w % n);
-        L[e] = (j <= i) ? A[e] : T(0);
+        L[e] = (j <= i) ? A[e] : T{};
     }
     for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < batch;
          b += (int64_t)gridDim.x * blockDim.x)
@@ -79,7 +99,7 @@ potrf_diag_kernel(T* __restrict__ L, int32_t* __restrict__ status, int64_t batch
         __syncthreads();
         for (int e = threadIdx.x; e < kb * kb; e += blockDim.x) {
             const int r = e / kb, c = e % kb;
-            S[r * P + c] = (c <= r) ? Lb[(int64_t)(k0 + r) * n + k0 + c] : T(0);
+            S[r * P + c] = (c <= r) ? Lb[(int64_t)(k0 + r) * n + k0 + c] : T{};
         }
         __syncthreads();
         const int st = chol_tile::potrf<THREADS>(S, kb, chol_tile::RowMajor{P});
@@ -110,11 +130,13 @@ template <typename T, int MODE>
 __global__ void __launch_bounds__(kThreads)
 trsm_kernel(const T* L, T* W, const int32_t* __restrict__ status,
             int64_t batch, int n, int t0, int kb, int v_begin, int v_count) {
+    using R = real_t<T>;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int P = kb + 1;
     T* G = reinterpret_cast<T*>(smem_raw);          // kb x P
     T* V = G + (size_t)kb * P;                      // kVecPerBlock x P
-    T* ginv = V + (size_t)kVecPerBlock * P;         // kb reciprocals of G's diagonal
+    // kb reciprocals of G's (real) diagonal
+    R* ginv = reinterpret_cast<R*>(V + (size_t)kVecPerBlock * P);
     const int vloc = threadIdx.x >> 2;
     const int q = threadIdx.x & 3;
     const int v0 = v_begin + blockIdx.x * kVecPerBlock;
@@ -127,7 +149,7 @@ trsm_kernel(const T* L, T* W, const int32_t* __restrict__ status,
         // G: lower tile (forward) or the transposed tile (backward)
         for (int e = threadIdx.x; e < kb * kb; e += blockDim.x) {
             const int r = e / kb, c = e % kb;  // coalesced over c in global memory
-            const T x = (c <= r) ? Lb[(int64_t)(t0 + r) * n + t0 + c] : T(0);
+            const T x = (c <= r) ? Lb[(int64_t)(t0 + r) * n + t0 + c] : T{};
             if (MODE == TRSM_FWD_PANEL) G[r * P + c] = x;
             else G[c * P + r] = x;
         }
@@ -136,10 +158,10 @@ trsm_kernel(const T* L, T* W, const int32_t* __restrict__ status,
         // forward panel, where W == L)
         for (int e = threadIdx.x; e < kb * kVecPerBlock; e += blockDim.x) {
             const int v = e / kb, m = e % kb;
-            V[v * P + m] = (v < nv) ? Wb[(int64_t)(v0 + v) * n + t0 + m] : T(0);
+            V[v * P + m] = (v < nv) ? Wb[(int64_t)(v0 + v) * n + t0 + m] : T{};
         }
         __syncthreads();
-        for (int c = threadIdx.x; c < kb; c += blockDim.x) ginv[c] = rcp_t(G[c * P + c]);
+        for (int c = threadIdx.x; c < kb; c += blockDim.x) ginv[c] = rcp_t(re(G[c * P + c]));
         __syncthreads();
         {
             // every group runs the same sweep (idle groups on zero vectors
@@ -148,21 +170,22 @@ trsm_kernel(const T* L, T* W, const int32_t* __restrict__ status,
             if (MODE == TRSM_FWD_PANEL) {
                 for (int c = 0; c < kb; ++c) {
                     const T* g = G + c * P;
-                    T s = T(0);
-                    for (int m = q; m < c; m += 4) s = fma(g[m], x[m], s);
-                    s += __shfl_xor_sync(0xffffffffu, s, 1);
-                    s += __shfl_xor_sync(0xffffffffu, s, 2);
-                    if (q == 0) x[c] = (x[c] - s) * ginv[c];
+                    // x_c = (b_c - sum_{m<c} x_m conj(g_cm)) / g_cc
+                    T s = T{};
+                    for (int m = q; m < c; m += 4) s = madd(conj(g[m]), x[m], s);
+                    s = add(s, shfl_xor(s, 1));
+                    s = add(s, shfl_xor(s, 2));
+                    if (q == 0) x[c] = scale(sub(x[c], s), ginv[c]);
                     __syncwarp();
                 }
             } else {
                 for (int c = kb - 1; c >= 0; --c) {
                     const T* g = G + c * P;
-                    T s = T(0);
-                    for (int m = c + 1 + q; m < kb; m += 4) s = fma(g[m], x[m], s);
-                    s += __shfl_xor_sync(0xffffffffu, s, 1);
-                    s += __shfl_xor_sync(0xffffffffu, s, 2);
-                    if (q == 0) x[c] = (x[c] - s) * ginv[c];
+                    T s = T{};
+                    for (int m = c + 1 + q; m < kb; m += 4) s = madd(g[m], x[m], s);
+                    s = add(s, shfl_xor(s, 1));
+                    s = add(s, shfl_xor(s, 2));
+                    if (q == 0) x[c] = scale(sub(x[c], s), ginv[c]);
                     __syncwarp();
                 }
             }
@@ -265,9 +288,10 @@ __device__ __forceinline__ TileJob make_job(const GemmArgs<T>& g, int tile_id) {
 template <typename T, int BM, int MODE>
 __global__ void __launch_bounds__(kThreads)
 gemm_kernel(GemmArgs<T> g) {
+    using R = real_t<T>;
     constexpr int BK = 16;
     constexpr int MT = BM / 16;  // micro-tile per thread (MT x MT)
-    constexpr int PAD = 16 / sizeof(T);
+    constexpr int PAD = sizeof(T) >= 16 ? 1 : 16 / sizeof(T);
     __shared__ __align__(16) T As[BK][BM + PAD];
     __shared__ __align__(16) T Bs[BK][BM + PAD];
     const int subs_per_side = g.tile / BM;
@@ -291,7 +315,7 @@ gemm_kernel(GemmArgs<T> g) {
 #pragma unroll
         for (int i = 0; i < MT; ++i)
 #pragma unroll
-            for (int j = 0; j < MT; ++j) acc[i][j] = T(0);
+            for (int j = 0; j < MT; ++j) acc[i][j] = T{};
 
         const int kbeg = blockIdx.z * g.kchunk;
         const int kend = min(job.klen, kbeg + g.kchunk);
@@ -304,17 +328,19 @@ gemm_kernel(GemmArgs<T> g) {
                 else             { r = e / BK;  kk = e % BK; }  // contiguous over kk
                 int gr = job.a_trans ? job.a_row0 + k0 + kk : job.a_row0 + r_off + r;
                 int gc = job.a_trans ? job.a_col0 + r_off + r : job.a_col0 + k0 + kk;
-                T x = T(0);
+                T x = T{};
                 if (k0 + kk < kend && gr < g.n && gc < g.n) {
                     if (job.a_sym) {
-                        // (A + A^T) of a lower tile: the upper half mirrors the lower
-                        // one and the diagonal is doubled
-                        const bool diag = gc == gr;
-                        if (gc > gr) { const int t = gr; gr = gc; gc = t; }
+                        // (A + A^H) of a lower tile: the upper half mirrors the lower
+                        // one (conjugated) and the diagonal is doubled
+                        const bool diag = gc == gr, upper = gc > gr;
+                        if (upper) { const int t = gr; gr = gc; gc = t; }
                         x = Ab[(int64_t)gr * g.n + gc];
-                        if (diag) x += x;
+                        if (upper) x = conj(x);
+                        if (diag) x = add(x, x);
                     } else if (!job.a_lower || gc <= gr) {
                         x = Ab[(int64_t)gr * g.n + gc];
+                        if (job.a_trans) x = conj(x);  // a transpose is a conjugate transpose
                     }
                 }
                 As[kk][r] = x;
@@ -326,9 +352,11 @@ gemm_kernel(GemmArgs<T> g) {
                 else             { kk = e / BM; c = e % BM; }   // contiguous over c
                 const int gr = job.b_trans ? job.b_row0 + c_off + c : job.b_row0 + k0 + kk;
                 const int gc = job.b_trans ? job.b_col0 + k0 + kk : job.b_col0 + c_off + c;
-                T x = T(0);
-                if (k0 + kk < kend && gr < g.n && gc < g.n && (!job.b_lower || gc <= gr))
+                T x = T{};
+                if (k0 + kk < kend && gr < g.n && gc < g.n && (!job.b_lower || gc <= gr)) {
                     x = Bb[(int64_t)gr * g.n + gc];
+                    if (job.b_trans) x = conj(x);
+                }
                 Bs[kk][c] = x;
             }
             __syncthreads();
@@ -342,7 +370,7 @@ gemm_kernel(GemmArgs<T> g) {
 #pragma unroll
                 for (int i = 0; i < MT; ++i)
 #pragma unroll
-                    for (int j = 0; j < MT; ++j) acc[i][j] = fma(a[i], bv[j], acc[i][j]);
+                    for (int j = 0; j < MT; ++j) acc[i][j] = madd(a[i], bv[j], acc[i][j]);
             }
         }
         // epilogue
@@ -360,17 +388,21 @@ gemm_kernel(GemmArgs<T> g) {
                 if ((MODE == GEMM_FWD_TRAIL || (MODE == GEMM_REV_ROW && job.ci == job.cj)) && c > r)
                     continue;
                 T* cp = Cb + (int64_t)r * g.n + c;
-                T v = T(job.alpha) * acc[i][j];
+                T v = scale(acc[i][j], R(job.alpha));
                 if (g.atomic) {
-                    atomicAdd(cp, v);
+                    atomic_add(cp, v);
                     continue;
                 }
-                if (job.beta != 0.f) v += *cp;
+                if (job.beta != 0.f) v = add(v, *cp);
                 *cp = v;
             }
         }
     }
 }
+
+// Largest tile whose diagonal-tile kernels fit in shared memory: 128 for
+// elements of up to 8 bytes, 64 for complex double.
+template <typename T> constexpr int max_tile() { return sizeof(T) > 8 ? 64 : 128; }
 
 size_t trsm_smem(int kb, int esize) {
     return ((size_t)(kb + kVecPerBlock) * (kb + 1) + kb) * esize;
@@ -384,7 +416,7 @@ cudaError_t launch_trsm(const T* L, T* W, const int32_t* status, int64_t batch, 
     auto kern = trsm_kernel<T, MODE>;
     // raised once per device to the largest size any tile needs
     static std::atomic<uint64_t> smem_set{0};
-    cudaError_t e = allow_smem_once(kern, trsm_smem(128, sizeof(T)), smem_set);
+    cudaError_t e = allow_smem_once(kern, trsm_smem(max_tile<T>(), sizeof(T)), smem_set);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((v_count + kVecPerBlock - 1) / kVecPerBlock), grid_y(batch));
     kern<<<grid, kThreads, smem, stream>>>(L, W, status, batch, n, t0, kb, v_begin, v_count);
@@ -464,7 +496,7 @@ lower_copy_kernel(const T* __restrict__ src, T* __restrict__ dst,
         const int64_t b = e / nn, w = e % nn;
         if (skip_matrix(status, b)) continue;
         const int i = (int)(w / n), j = (int)(w % n);
-        dst[e] = (j <= i) ? src[e] : T(0);
+        dst[e] = (j <= i) ? src[e] : T{};
     }
 }
 
@@ -482,9 +514,9 @@ lower_add_kernel(const T* __restrict__ src, T* __restrict__ dst,
         if (j > i) continue;
         const bool skip = skip_matrix(status, b);
         if (accumulate) {
-            if (!skip) dst[e] += src[e];
+            if (!skip) dst[e] = add(dst[e], src[e]);
         } else {
-            dst[e] = skip ? T(0) : src[e];
+            dst[e] = skip ? T{} : src[e];
         }
     }
 }
@@ -500,7 +532,7 @@ zero_lower_skipped_kernel(T* __restrict__ dst, const int32_t* __restrict__ statu
          e += (int64_t)gridDim.x * blockDim.x) {
         const int64_t b = e / nn, w = e % nn;
         const int i = (int)(w / n), j = (int)(w % n);
-        if (j <= i && skip_matrix(status, b)) dst[e] = T(0);
+        if (j <= i && skip_matrix(status, b)) dst[e] = T{};
     }
 }
 
@@ -526,9 +558,14 @@ int blocked_default_tile(int n, int64_t batch) {
         if (e_ != cudaSuccess) return e_;        \
     } while (0)
 
+size_t blocked_fwd_workspace_bytes(bool real_double, int64_t batch, int n, int tile) {
+    if (!real_double || tile != 128 || n <= 128) return 0;
+    return ozaki_workspace_bytes(batch, n);
+}
+
 template <typename T>
 cudaError_t blocked_fwd(const T* A, T* L, int32_t* status, int64_t batch, int n, int tile,
-                        cudaStream_t stream) {
+                        void* work, cudaStream_t stream) {
     const int nt = (n + tile - 1) / tile;
     {
         const int64_t total = batch * (int64_t)n * n;
@@ -539,7 +576,8 @@ cudaError_t blocked_fwd(const T* A, T* L, int32_t* status, int64_t batch, int n,
         CHOL_TRY(cudaGetLastError());
     }
     static std::atomic<uint64_t> diag_smem_set{0};
-    CHOL_TRY(allow_smem_once(potrf_diag_kernel<T, kThreads>, (size_t)128 * 129 * sizeof(T),
+    CHOL_TRY(allow_smem_once(potrf_diag_kernel<T, kThreads>,
+                             (size_t)max_tile<T>() * (max_tile<T>() + 1) * sizeof(T),
                              diag_smem_set));
     for (int k = 0; k < nt; ++k) {
         const int k0 = k * tile;
@@ -556,6 +594,13 @@ cudaError_t blocked_fwd(const T* A, T* L, int32_t* status, int64_t batch, int n,
         if (k == nt - 1) break;
         CHOL_TRY((launch_trsm<T, TRSM_FWD_PANEL>(L, L, status, batch, n, k0, kb, k0 + kb,
                                                  n - k0 - kb, stream)));
+        if constexpr (std::is_same<T, double>::value) {
+            if (work != nullptr && tile == 128) {
+                CHOL_TRY(ozaki_trailing_update(reinterpret_cast<double*>(L), work, status, batch,
+                                               n, k, stream));
+                continue;
+            }
+        }
         const int m = nt - k - 1;
         GemmArgs<T> g{L, L, L, status, batch, n, tile, nt, k, 0, 0};
         CHOL_TRY((launch_gemm<T, GEMM_FWD_TRAIL>(g, m * (m + 1) / 2, stream)));
@@ -592,7 +637,8 @@ cudaError_t blocked_adj(const T* L, const T* Lbar, T* Abar, const int32_t* statu
         CHOL_TRY(cudaGetLastError());
     }
     static std::atomic<uint64_t> diag_smem_set{0};
-    CHOL_TRY(allow_smem_once(diag_rev_kernel<T, kThreads>, (size_t)128 * 129 * sizeof(T),
+    CHOL_TRY(allow_smem_once(diag_rev_kernel<T, kThreads>,
+                             (size_t)max_tile<T>() * (max_tile<T>() + 1) * sizeof(T),
                              diag_smem_set));
     const int sms = device_sm_count();
     const int bm = tile >= 64 ? 64 : 32;
@@ -634,13 +680,23 @@ cudaError_t blocked_adj(const T* L, const T* Lbar, T* Abar, const int32_t* statu
     return cudaGetLastError();
 }
 
-template cudaError_t blocked_fwd<float>(const float*, float*, int32_t*, int64_t, int, int,
+template cudaError_t blocked_fwd<float>(const float*, float*, int32_t*, int64_t, int, int, void*,
                                         cudaStream_t);
 template cudaError_t blocked_fwd<double>(const double*, double*, int32_t*, int64_t, int, int,
-                                         cudaStream_t);
+                                         void*, cudaStream_t);
 template cudaError_t blocked_adj<float>(const float*, const float*, float*, const int32_t*,
                                         int64_t, int, int, float*, bool, cudaStream_t);
 template cudaError_t blocked_adj<double>(const double*, const double*, double*, const int32_t*,
                                          int64_t, int, int, double*, bool, cudaStream_t);
+template cudaError_t blocked_fwd<cplx<float>>(const cplx<float>*, cplx<float>*, int32_t*, int64_t,
+                                              int, int, void*, cudaStream_t);
+template cudaError_t blocked_fwd<cplx<double>>(const cplx<double>*, cplx<double>*, int32_t*,
+                                               int64_t, int, int, void*, cudaStream_t);
+template cudaError_t blocked_adj<cplx<float>>(const cplx<float>*, const cplx<float>*, cplx<float>*,
+                                              const int32_t*, int64_t, int, int, cplx<float>*, bool,
+                                              cudaStream_t);
+template cudaError_t blocked_adj<cplx<double>>(const cplx<double>*, const cplx<double>*,
+                                               cplx<double>*, const int32_t*, int64_t, int, int,
+                                               cplx<double>*, bool, cudaStream_t);
 
 }  // namespace chol

@@ -31,6 +31,33 @@ template <typename T, int NT, bool VEC>
 cudaError_t small_adj_nt(const T* L, const T* Lbar, T* Abar, const int32_t* status,
                          int64_t batch, int n, bool accumulate, cudaStream_t stream);
 
+// Complex Hermitian elements (chol_tile::cplx<float> / cplx<double>), n <= 64:
+// one block per matrix.  adj as small_adj.
+template <typename T>
+cudaError_t hsmall_fwd(const T* A, T* L, int32_t* status, int64_t batch, int n,
+                       cudaStream_t stream);
+template <typename T>
+cudaError_t hsmall_adj(const T* L, const T* Lbar, T* Abar, const int32_t* status, int64_t batch,
+                       int n, bool accumulate, cudaStream_t stream);
+
+// Solve with the factor, X = A^-1 B (B, X: [batch][n][nrhs]; X may be B),
+// any element type; matrices with status != 0 get X = 0.
+template <typename T>
+cudaError_t potrs_solve(const T* L, const T* B, T* X, const int32_t* status, int64_t batch,
+                        int n, int nrhs, cudaStream_t stream);
+// Its reverse mode: Bbar += A^-1 Xbar (Bbar may be null); Lbar (may be null)
+// += tril(-(Bb X^H + X Bb^H) L), Bb = A^-1 Xbar.  `work` holds
+// potrs_adj_workspace_elems() elements.
+size_t potrs_adj_workspace_elems(int64_t batch, int n, int nrhs, bool want_L);
+template <typename T>
+cudaError_t potrs_adj(const T* L, const T* X, const T* Xbar, T* Bbar, T* Lbar,
+                      const int32_t* status, int64_t batch, int n, int nrhs, T* work,
+                      cudaStream_t stream);
+
+// Largest blocked tile for an element size: 64 for complex double (its
+// diagonal-tile kernels would not fit in shared memory at 128), else 128.
+inline int blocked_max_tile(int esize) { return esize > 8 ? 64 : 128; }
+
 // Thread-per-matrix float32 forward for n in {8, 16}; A and L 16-byte aligned.
 bool tpm_supported(int n);
 cudaError_t tpm_fwd(const float* A, float* L, int32_t* status, int64_t batch, int n,
@@ -40,10 +67,23 @@ cudaError_t tpm_fwd(const float* A, float* L, int32_t* status, int64_t batch, in
 cudaError_t tpm_fwd_wait_selftest(const float* A, float* L, int32_t* status, int64_t batch,
                                   uint32_t max_polls, cudaStream_t stream);
 
-// n > 64, blocked with square tiles of `tile` (32, 64 or 128).
+// n > 64, blocked with square tiles of `tile` (32, 64 or 128).  `work`
+// (may be null) holds blocked_fwd_workspace_bytes() bytes; with it, float64
+// tiles of 128 take the trailing update on the tensor cores.
 template <typename T>
 cudaError_t blocked_fwd(const T* A, T* L, int32_t* status, int64_t batch, int n, int tile,
-                        cudaStream_t stream);
+                        void* work, cudaStream_t stream);
+// Workspace the forward uses for this shape (0: none); real_double: the
+// element type is float64.
+size_t blocked_fwd_workspace_bytes(bool real_double, int64_t batch, int n, int tile);
+
+// Trailing update of step k of the float64 blocked forward with 128-wide
+// tiles on the bf16 tensor cores (exact digit-slice products): for every
+// lower tile (I, J), I >= J > k, L_IJ -= L_Ik L_Jk^T.  `work` holds
+// ozaki_workspace_bytes(batch, n) bytes.
+size_t ozaki_workspace_bytes(int64_t batch, int n);
+cudaError_t ozaki_trailing_update(double* L, void* work, int32_t* status, int64_t batch, int n,
+                                  int k, cudaStream_t stream);
 // `work` holds batch * n * n elements of scratch.  accumulate as small_adj.
 // Not accumulating with adj_A == adj_L (in place), the sweep runs on adj_A
 // itself and `work` is not used (may be null).

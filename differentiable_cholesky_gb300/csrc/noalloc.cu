@@ -30,9 +30,12 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 #include "chol.h"
+#include "chol_tile.cuh"
 #include "kernels.h"
 
 namespace {
@@ -108,6 +111,8 @@ void* scratch_on_current_device() {
     return e.ptr;
 }
 
+using chol_tile::cplx;
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 template <typename T>
@@ -118,9 +123,13 @@ int run(int64_t batch, int32_t n, const void* L, const void* Lbar, void* Abar,
     T* ab = static_cast<T*>(Abar);
     cudaError_t e;
     if (n <= 64) {
-        const bool vec = (n * (int)sizeof(T)) % 16 == 0 && aligned16(L) && aligned16(Lbar) &&
-                         aligned16(Abar);
-        e = chol::small_adj<T>(l, lb, ab, status, batch, n, vec, true, stream);
+        if constexpr (std::is_same<T, float>::value || std::is_same<T, double>::value) {
+            const bool vec = (n * (int)sizeof(T)) % 16 == 0 && aligned16(L) && aligned16(Lbar) &&
+                             aligned16(Abar);
+            e = chol::small_adj<T>(l, lb, ab, status, batch, n, vec, true, stream);
+        } else {
+            e = chol::hsmall_adj<T>(l, lb, ab, status, batch, n, true, stream);
+        }
         return e == cudaSuccess ? CHOL_OK : CHOL_ECUDA;
     }
     const unsigned __int128 need =
@@ -128,7 +137,9 @@ int run(int64_t batch, int32_t n, const void* L, const void* Lbar, void* Abar,
     if (need > kScratchBytes) return CHOL_ENOMEM;
     void* work = scratch_on_current_device();
     if (work == nullptr) return CHOL_ECUDA;
-    if (tile == 0) tile = chol::blocked_default_tile(n, batch);
+    if (tile == 0)
+        tile = std::min(chol::blocked_default_tile(n, batch),
+                        chol::blocked_max_tile((int)sizeof(T)));
     e = chol::blocked_adj<T>(l, lb, ab, status, batch, n, tile, static_cast<T*>(work), true,
                              stream);
     return e == cudaSuccess ? CHOL_OK : CHOL_ECUDA;
@@ -144,6 +155,11 @@ extern "C" CHOL_API int chol_adj_noalloc(int64_t batch, int32_t n, int32_t dtype
     const int rc = chol::check_adj_args(batch, n, dtype, L, adj_L, adj_A, status, tile, &bytes);
     if (rc != CHOL_OK || batch == 0) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return dtype == CHOL_F32 ? run<float>(batch, n, L, adj_L, adj_A, status, tile, s)
-                             : run<double>(batch, n, L, adj_L, adj_A, status, tile, s);
+    switch (dtype) {
+        case CHOL_F32: return run<float>(batch, n, L, adj_L, adj_A, status, tile, s);
+        case CHOL_F64: return run<double>(batch, n, L, adj_L, adj_A, status, tile, s);
+        case CHOL_C64: return run<cplx<float>>(batch, n, L, adj_L, adj_A, status, tile, s);
+        case CHOL_C128: return run<cplx<double>>(batch, n, L, adj_L, adj_A, status, tile, s);
+        default: return CHOL_EDTYPE;
+    }
 }

@@ -33,6 +33,17 @@
  *     (chol_strerror gives the text) and nothing is enqueued.  A matrix that
  *     is not positive definite is data, not an error: it sets its status.
  *   - batch == 0 is a no-op that returns CHOL_OK.
+ *   - Complex Hermitian matrices (CHOL_C64, CHOL_C128; the jaxmg docs
+ *     "Cholesky factorization" intro factor "a symmetric or Hermitian
+ *     positive-definite matrix"): A = L L^H with conjugate transposes where
+ *     the real case transposes.  The forward reads the lower triangle and
+ *     only the real part of the diagonal; L's diagonal is real (imaginary
+ *     part 0).  The adjoint takes adj_L as dLoss/dRe(L) + i dLoss/dIm(L) of a
+ *     real loss and adds to adj_A the derivative with respect to the entries
+ *     the forward reads: dLoss/dRe(a_ij) + i dLoss/dIm(a_ij) below the
+ *     diagonal and dLoss/dRe(a_ii) on it, i.e. M_ij + conj(M_ji) and Re(M_ii)
+ *     with M = L^-H Phi(L^H tril(adj_L)) L^-1.  The blocked tile of CHOL_C128
+ *     is at most 64 (tile 128 returns CHOL_EINVAL; the default caps at 64).
  */
 #ifndef CHOL_GB300_H
 #define CHOL_GB300_H
@@ -49,12 +60,15 @@
 extern "C" {
 #endif
 
-typedef enum { CHOL_F32 = 0, CHOL_F64 = 1 } chol_dtype_t;
+/* Element types.  The complex types hold interleaved (real, imaginary) pairs,
+ * the layout of C99 float/double complex and torch complex64/complex128; for
+ * them every call works on Hermitian matrices, A = L L^H (see below). */
+typedef enum { CHOL_F32 = 0, CHOL_F64 = 1, CHOL_C64 = 2, CHOL_C128 = 3 } chol_dtype_t;
 
 enum {
     CHOL_OK = 0,
     CHOL_EINVAL = -1,  /* null/misaligned/host pointer, n <= 0, batch < 0, bad tile, size overflow */
-    CHOL_EDTYPE = -2,  /* dtype is neither CHOL_F32 nor CHOL_F64                                     */
+    CHOL_EDTYPE = -2,  /* dtype is not one of chol_dtype_t                                           */
     CHOL_EALIAS = -3,  /* an output overlaps an input it must not overlap                            */
     CHOL_ENOMEM = -4,  /* workspace allocation failed                                                */
     CHOL_ECUDA = -5    /* a CUDA call or kernel launch failed (see cudaGetLastError)                 */
@@ -175,13 +189,53 @@ CHOL_API int chol_fwd_inplace(int64_t batch, int32_t n, int32_t dtype, void* A, 
 CHOL_API int chol_adj_inplace(int64_t batch, int32_t n, int32_t dtype, const void* L, void* adj,
                               const int32_t* status, int32_t tile, void* stream);
 
+/*
+ * chol_solve -- X_b = A_b^-1 B_b = L_b^-H L_b^-1 B_b, the solve with the
+ * factor that the jaxmg docs "Cholesky factorization" keep out of potrf
+ * (intro: the factor is returned "without performing a solve"): forward
+ * substitution L Y = B, then back substitution L^H X = Y (L^T for real
+ * types).
+ *   L       in : dtype[batch][n][n], the factor from chol_fwd; only its lower
+ *                triangle is read (and only the real part of a complex
+ *                diagonal).
+ *   B       in : dtype[batch][n][nrhs], row-major right-hand sides.
+ *   X       out: dtype[batch][n][nrhs].  May be B itself (solved in place);
+ *                must not otherwise overlap B, and must not overlap L or
+ *                status (CHOL_EALIAS).
+ *   status  in : int32[batch] from chol_fwd, or NULL.  A matrix with a
+ *                non-zero status gets X_b = 0.
+ * nrhs >= 0 (0 is a no-op).  Allocates nothing.
+ */
+CHOL_API int chol_solve(int64_t batch, int32_t n, int32_t nrhs, int32_t dtype, const void* L,
+                        const void* B, void* X, const int32_t* status, void* stream);
+
+/*
+ * chol_solve_adj -- reverse mode of chol_solve for a real loss with gradient
+ * adj_X = dLoss/dX (dLoss/dRe + i dLoss/dIm for complex types):
+ *   adj_B += Bb,  Bb = A^-1 adj_X                       (if adj_B != NULL)
+ *   adj_L += tril(-(Bb X^H + X Bb^H) L)  on the lower triangle (if adj_L != NULL)
+ * from dX = -A^-1 dA X and dA = dL L^H + L dL^H.  adj_L's upper triangle is
+ * never written; chol_adj then carries adj_L on to adj_A.
+ *   L      in : as chol_solve.        X     in : the result of chol_solve.
+ *   adj_X  in : dtype[batch][n][nrhs].
+ *   adj_B  in/out (or NULL): dtype[batch][n][nrhs].
+ *   adj_L  in/out (or NULL): dtype[batch][n][n].
+ *   status in : as chol_solve; matrices with non-zero status are skipped.
+ * The outputs must not overlap each other or any input (CHOL_EALIAS).
+ * Workspace: batch * n * nrhs elements (three times that with adj_L), taken
+ * with cudaMallocAsync/cudaFreeAsync on `stream` (CHOL_ENOMEM on failure).
+ */
+CHOL_API int chol_solve_adj(int64_t batch, int32_t n, int32_t nrhs, int32_t dtype, const void* L,
+                            const void* X, const void* adj_X, void* adj_B, void* adj_L,
+                            const int32_t* status, void* stream);
+
 /* Static text for a return code (never NULL). */
 CHOL_API const char* chol_strerror(int code);
 
 /* ABI version of this header: (major << 16) | minor. */
 CHOL_API int32_t chol_abi_version(void);
 
-#define CHOL_ABI_VERSION ((1 << 16) | 1)
+#define CHOL_ABI_VERSION ((1 << 16) | 3)
 
 #ifdef __cplusplus
 }

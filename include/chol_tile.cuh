@@ -20,11 +20,17 @@
  *     storage: RowMajor{ld} (row-major, leading dimension ld) or PackedLower
  *     (the lower triangle packed by rows, n (n + 1) / 2 elements).  Only
  *     elements on and below the diagonal are read or written.
- *   - Arithmetic is in T (float or double).  For a pivot d the factor takes
- *     1 / l_jj = rsqrt(d) from CUDA's reciprocal square root and
- *     l_jj = d * rsqrt(d): one transcendental per column on the serial chain,
- *     within a few ulp of the correctly rounded values.  The adjoint divides
- *     by l_jj.  No wait is unbounded and nothing traps.
+ *   - Arithmetic is in T: float, double, or the complex types
+ *     chol_tile::cplx<float> / cplx<double> (interleaved real and imaginary
+ *     parts, the layout of C99 complex and torch complex64/128), for which
+ *     the factor is the Hermitian A = L L^H (jaxmg docs "Cholesky
+ *     factorization", intro: "symmetric or Hermitian positive-definite"):
+ *     conjugates appear where the real recurrence transposes, the pivot is
+ *     the real part of the diagonal and L's diagonal is real.  For a pivot d
+ *     the factor takes 1 / l_jj = rsqrt(d) from CUDA's reciprocal square root
+ *     and l_jj = d * rsqrt(d): one transcendental per column on the serial
+ *     chain, within a few ulp of the correctly rounded values.  The adjoint
+ *     divides by l_jj.  No wait is unbounded and nothing traps.
  */
 #ifndef CHOL_TILE_CUH
 #define CHOL_TILE_CUH
@@ -42,9 +48,76 @@ struct PackedLower {
     __device__ __forceinline__ int operator()(int i, int j) const { return i * (i + 1) / 2 + j; }
 };
 
+// Complex element: real part, then imaginary part.
+template <typename R>
+struct __align__(2 * sizeof(R)) cplx {
+    R re, im;
+};
+
 namespace detail {
 __device__ __forceinline__ float rsqrt_t(float x) { return rsqrtf(x); }
 __device__ __forceinline__ double rsqrt_t(double x) { return rsqrt(x); }
+
+// Scalar helpers that make one recurrence serve real and complex elements.
+template <typename T> struct real_of { using type = T; };
+template <typename R> struct real_of<cplx<R>> { using type = R; };
+
+template <typename T> __device__ __forceinline__ T zero() { return T{}; }
+__device__ __forceinline__ float re(float x) { return x; }
+__device__ __forceinline__ double re(double x) { return x; }
+template <typename R> __device__ __forceinline__ R re(cplx<R> x) { return x.re; }
+__device__ __forceinline__ float conj(float x) { return x; }
+__device__ __forceinline__ double conj(double x) { return x; }
+template <typename R> __device__ __forceinline__ cplx<R> conj(cplx<R> x) { return {x.re, -x.im}; }
+// a * r for real r
+__device__ __forceinline__ float scale(float a, float r) { return a * r; }
+__device__ __forceinline__ double scale(double a, double r) { return a * r; }
+template <typename R> __device__ __forceinline__ cplx<R> scale(cplx<R> a, R r) {
+    return {a.re * r, a.im * r};
+}
+template <typename T> __device__ __forceinline__ T from_real(typename real_of<T>::type r) {
+    T x{};
+    if constexpr (sizeof(T) == sizeof(r)) {
+        x = r;
+    } else {
+        x.re = r;
+    }
+    return x;
+}
+// c + a * b and c - a * b (complex: four fused multiply-adds)
+__device__ __forceinline__ float madd(float a, float b, float c) { return fmaf(a, b, c); }
+__device__ __forceinline__ double madd(double a, double b, double c) { return fma(a, b, c); }
+template <typename R>
+__device__ __forceinline__ cplx<R> madd(cplx<R> a, cplx<R> b, cplx<R> c) {
+    return {fma(-a.im, b.im, fma(a.re, b.re, c.re)), fma(a.im, b.re, fma(a.re, b.im, c.im))};
+}
+__device__ __forceinline__ float msub(float a, float b, float c) { return fmaf(-a, b, c); }
+__device__ __forceinline__ double msub(double a, double b, double c) { return fma(-a, b, c); }
+template <typename R>
+__device__ __forceinline__ cplx<R> msub(cplx<R> a, cplx<R> b, cplx<R> c) {
+    return {fma(a.im, b.im, fma(-a.re, b.re, c.re)), fma(-a.im, b.re, fma(-a.re, b.im, c.im))};
+}
+__device__ __forceinline__ float add(float a, float b) { return a + b; }
+__device__ __forceinline__ double add(double a, double b) { return a + b; }
+template <typename R> __device__ __forceinline__ cplx<R> add(cplx<R> a, cplx<R> b) {
+    return {a.re + b.re, a.im + b.im};
+}
+__device__ __forceinline__ float sub(float a, float b) { return a - b; }
+__device__ __forceinline__ double sub(double a, double b) { return a - b; }
+template <typename R> __device__ __forceinline__ cplx<R> sub(cplx<R> a, cplx<R> b) {
+    return {a.re - b.re, a.im - b.im};
+}
+// Re(conj(a) * b) + acc
+__device__ __forceinline__ float re_dot(float a, float b, float acc) { return fmaf(a, b, acc); }
+__device__ __forceinline__ double re_dot(double a, double b, double acc) { return fma(a, b, acc); }
+template <typename R> __device__ __forceinline__ R re_dot(cplx<R> a, cplx<R> b, R acc) {
+    return fma(a.im, b.im, fma(a.re, b.re, acc));
+}
+__device__ __forceinline__ float shfl_xor(float x, int o) { return __shfl_xor_sync(0xffffffffu, x, o); }
+__device__ __forceinline__ double shfl_xor(double x, int o) { return __shfl_xor_sync(0xffffffffu, x, o); }
+template <typename R> __device__ __forceinline__ cplx<R> shfl_xor(cplx<R> x, int o) {
+    return {__shfl_xor_sync(0xffffffffu, x.re, o), __shfl_xor_sync(0xffffffffu, x.im, o)};
+}
 }  // namespace detail
 
 /*
@@ -57,24 +130,27 @@ __device__ __forceinline__ double rsqrt_t(double x) { return rsqrt(x); }
 template <int THREADS, typename T, typename Idx>
 __device__ int potrf(T* a, int n, Idx at) {
     static_assert(THREADS % 32 == 0, "THREADS is a whole number of warps");
+    using R = typename detail::real_of<T>::type;
     const int tid = threadIdx.x;
     for (int j = 0; j < n; ++j) {
-        const T d = a[at(j, j)];
-        if (!(d > T(0))) {  // every thread read the same value: a uniform exit
+        const R d = detail::re(a[at(j, j)]);
+        if (!(d > R(0))) {  // every thread read the same value: a uniform exit
             __syncthreads();
             return j + 1;
         }
-        const T inv = detail::rsqrt_t(d);  // 1 / l_jj, then products
-        const T ljj = d * inv;
+        const R inv = detail::rsqrt_t(d);  // 1 / l_jj, then products
+        const R ljj = d * inv;
         __syncthreads();                     // every thread has read the pivot
-        for (int i = j + 1 + tid; i < n; i += THREADS) a[at(i, j)] *= inv;
-        if (tid == 0) a[at(j, j)] = ljj;
+        for (int i = j + 1 + tid; i < n; i += THREADS) a[at(i, j)] = detail::scale(a[at(i, j)], inv);
+        if (tid == 0) a[at(j, j)] = detail::from_real<T>(ljj);
         __syncthreads();
-        // trailing update of the lower part, 16 x THREADS/16 threads over (i, c)
+        // trailing update of the lower part, 16 x THREADS/16 threads over (i, c):
+        // a_ic -= l_ij conj(l_cj)
         const int ty = tid / 16, tx = tid % 16;
         for (int i = j + 1 + ty; i < n; i += THREADS / 16) {
             const T lij = a[at(i, j)];
-            for (int c = j + 1 + tx; c <= i; c += 16) a[at(i, c)] = fma(-lij, a[at(c, j)], a[at(i, c)]);
+            for (int c = j + 1 + tx; c <= i; c += 16)
+                a[at(i, c)] = detail::msub(lij, detail::conj(a[at(c, j)]), a[at(i, c)]);
         }
         __syncthreads();
     }
@@ -89,48 +165,53 @@ __device__ int potrf(T* a, int n, Idx at) {
  * Phi(M + M^T) with M = l^-T Phi(l^T w) l^-1, Phi keeping the lower triangle
  * and halving the diagonal (warp issue #1316's closing comment), reached
  * column by column from j = n - 1 down to 0 in n^3 / 3 multiply-adds.
+ * Complex elements: w holds dLoss/dRe + i dLoss/dIm of a real loss; on
+ * return the entries below the diagonal hold M_ij + conj(M_ji) and the
+ * diagonal Re(M_ii) (imaginary part 0), with M = l^-H Phi(l^H w) l^-1; the
+ * sweep reads only the real part of w's diagonal.
  */
 template <int THREADS, typename T, typename Idx>
 __device__ void potrf_adj(const T* l, T* w, int n, Idx at) {
     static_assert(THREADS % 32 == 0, "THREADS is a whole number of warps");
-    __shared__ T red[THREADS / 32];
+    using R = typename detail::real_of<T>::type;
+    __shared__ R red[THREADS / 32];
     const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
     for (int j = n - 1; j >= 0; --j) {
-        // s = sum_{i > j} l_ij w_ij
-        T part = T(0);
-        for (int i = j + 1 + tid; i < n; i += THREADS) part = fma(l[at(i, j)], w[at(i, j)], part);
+        // s = Re sum_{i > j} conj(l_ij) w_ij
+        R part = R(0);
+        for (int i = j + 1 + tid; i < n; i += THREADS) part = detail::re_dot(l[at(i, j)], w[at(i, j)], part);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
         if (lane == 0) red[warp] = part;
         __syncthreads();
-        T sum = T(0);
+        R sum = R(0);
 #pragma unroll
         for (int k = 0; k < THREADS / 32; ++k) sum += red[k];
-        const T inv = T(1) / l[at(j, j)];
-        // column j: the diagonal from the sum, the rest scaled
-        for (int i = j + 1 + tid; i < n; i += THREADS) w[at(i, j)] *= inv;
-        if (tid == 0) w[at(j, j)] = (w[at(j, j)] - sum * inv) * inv;
+        const R inv = R(1) / detail::re(l[at(j, j)]);
+        // column j: the diagonal (real) from the sum, the rest scaled
+        for (int i = j + 1 + tid; i < n; i += THREADS) w[at(i, j)] = detail::scale(w[at(i, j)], inv);
+        if (tid == 0) w[at(j, j)] = detail::from_real<T>((detail::re(w[at(j, j)]) - sum * inv) * inv);
         __syncthreads();
-        // row j left of the diagonal: w_jk -= sum_{i >= j} w_ij l_ik
+        // row j left of the diagonal: w_jk -= sum_{i >= j} conj(w_ij) l_ik
         // (two partial sums halve the dependent chain)
         for (int k = tid; k < j; k += THREADS) {
-            T acc0 = T(0), acc1 = T(0);
+            T acc0 = detail::zero<T>(), acc1 = detail::zero<T>();
             int i = j;
             for (; i + 1 < n; i += 2) {
-                acc0 = fma(w[at(i, j)], l[at(i, k)], acc0);
-                acc1 = fma(w[at(i + 1, j)], l[at(i + 1, k)], acc1);
+                acc0 = detail::madd(detail::conj(w[at(i, j)]), l[at(i, k)], acc0);
+                acc1 = detail::madd(detail::conj(w[at(i + 1, j)]), l[at(i + 1, k)], acc1);
             }
-            if (i < n) acc0 = fma(w[at(i, j)], l[at(i, k)], acc0);
-            w[at(j, k)] -= acc0 + acc1;
+            if (i < n) acc0 = detail::madd(detail::conj(w[at(i, j)]), l[at(i, k)], acc0);
+            w[at(j, k)] = detail::sub(w[at(j, k)], detail::add(acc0, acc1));
         }
         // rows below, left of column j: w_ik -= w_ij l_jk
         const int ty = tid / 16, tx = tid % 16;
         for (int i = j + 1 + ty; i < n; i += THREADS / 16) {
             const T wij = w[at(i, j)];
-            for (int k = tx; k < j; k += 16) w[at(i, k)] = fma(-wij, l[at(j, k)], w[at(i, k)]);
+            for (int k = tx; k < j; k += 16) w[at(i, k)] = detail::msub(wij, l[at(j, k)], w[at(i, k)]);
         }
         __syncthreads();
-        if (tid == 0) w[at(j, j)] *= T(0.5);
+        if (tid == 0) w[at(j, j)] = detail::scale(w[at(j, j)], R(0.5));
         // (the next column's first barrier orders this write; nothing before
         //  it reads w_jj)
     }

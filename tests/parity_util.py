@@ -9,8 +9,10 @@ TOL_ADJ = {np.dtype(np.float64): 1e-10, np.dtype(np.float32): 1e-4}
 
 def max_rel_err(x, ref, mask=None, lower=False):
     """max over b of ||x_b - ref_b||_F / ||ref_b||_F (lower triangle if asked)."""
-    x = np.asarray(x, np.float64)
-    ref = np.asarray(ref, np.float64)
+    # complex results keep their imaginary parts (compared in complex128)
+    wide = np.complex128 if (np.iscomplexobj(x) or np.iscomplexobj(ref)) else np.float64
+    x = np.asarray(x, wide)
+    ref = np.asarray(ref, wide)
     if lower:
         tri = np.tril(np.ones(x.shape[-2:], bool))
         x = np.where(tri, x, 0.0)

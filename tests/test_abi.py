@@ -32,7 +32,7 @@ def test_library_exports_every_declared_symbol():
     lib = binding.load_library()
     for s in declared_symbols():
         assert hasattr(lib, s), f"{s} not exported"
-    assert lib.chol_abi_version() == (1 << 16) | 1
+    assert lib.chol_abi_version() == (1 << 16) | 3
 
 
 def test_strerror_covers_every_code():
@@ -55,6 +55,9 @@ def test_argument_checks_without_gpu():
     assert lib.chol_fwd_ex(1, 100, 1, p, p, s, 48, None) == CHOL_EINVAL
     assert lib.chol_adj(1, -3, 0, p, p, p, None, None) == CHOL_EINVAL
     assert lib.chol_adj(1, 4, 5, p, p, p, None, None) == CHOL_EDTYPE
+    # complex double takes tiles up to 64
+    assert lib.chol_fwd_ex(1, 100, 3, p, p, s, 128, None) == CHOL_EINVAL
+    assert lib.chol_adj_ex(1, 100, 3, p, p, p, None, 128, None) == CHOL_EINVAL
     # batch == 0 is a no-op, even with null pointers
     assert lib.chol_fwd(0, 4, 1, None, None, None, None) == CHOL_OK
     assert lib.chol_adj(0, 4, 1, None, None, None, None, None) == CHOL_OK

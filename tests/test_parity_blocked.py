@@ -98,7 +98,7 @@ def test_banded_8192_full_size():
         assert np.linalg.norm(lhs - rhs) <= 1e-10 * np.linalg.norm(rhs)
 
 
-@pytest.mark.parametrize("tile", [32, 64])
+@pytest.mark.parametrize("tile", [32, 64, 128])
 def test_status_global_column_and_skip(tile):
     n, batch = 200, 4
     A = W.gram_spd(batch, n, 27, 1.0, np.float64)
@@ -110,6 +110,49 @@ def test_status_global_column_and_skip(tile):
     L, st, G = check(A, Lbar, np.float64, tile=tile, adj_A0=G0)
     assert list(st) == [0, 151, 1, 200]
     assert np.all(G[1:] == 2.0)
+
+
+@pytest.mark.parametrize("tile", [64, 128])
+def test_nonfinite_off_diagonal_sets_the_status_of_its_row(tile):
+    """A NaN or Inf below the diagonal reaches the pivot of its row through
+    the panel solve and the trailing updates (with 128-wide float64 tiles,
+    through the tensor-core update's non-finite rows): the status is that
+    row's column + 1, as in the oracle."""
+    n, batch = 300, 3
+    A = W.gram_spd(batch, n, 41, 1.0, np.float64)
+    A[0, 170, 20] = np.nan
+    A[1, 250, 140] = np.inf
+    Lbar = W.tril_normal(batch, n, 42, np.float64)
+    L, st, G = check(A, Lbar, np.float64, tile=tile)
+    assert list(st) == [171, 251, 0]
+
+
+@pytest.mark.parametrize("n", [129, 255, 256, 257, 383, 640])
+def test_tensor_core_trailing_update_sizes(n):
+    """float64 with 128-wide tiles: the trailing update runs on the tensor
+    cores (digit slices, exact fp32 accumulation); ragged last tiles, one and
+    several trailing tiles, odd batches."""
+    A = W.gram_spd(3, n, 43 + n, 1.0, np.float64)
+    Lbar = W.tril_normal(3, n, 44 + n, np.float64)
+    check(A, Lbar, np.float64, tile=128)
+
+
+def test_tensor_core_update_wide_dynamic_range():
+    """Rows of very different scales (a diagonal scaling D A D with D spanning
+    2^-40 .. 2^40): each row is split with its own power-of-two scale, so the
+    factor keeps full relative accuracy, D L, as the FP64 recurrence does."""
+    n = 384
+    A = W.gram_spd(1, n, 45, 1.0, np.float64)[0]
+    d = np.exp2(np.linspace(-40, 40, n))
+    As = (d[:, None] * A * d[None, :])[None]
+    Lbar = W.tril_normal(1, n, 46, np.float64)
+    L, st, _ = gpu_fwd_adj(As, Lbar, tile=128)
+    assert int(st[0]) == 0
+    L_ref, _ = oracle.potrf(As[0])
+    # compare row by row, relative to each row's own scale
+    Lr = L[0] / d[:, None]
+    Rr = L_ref / d[:, None]
+    assert np.max(np.abs(Lr - Rr)) <= 1e-12 * np.max(np.abs(Rr))
 
 
 def test_upper_triangles_ignored_and_untouched():
