@@ -151,14 +151,21 @@ int adj_impl(int64_t batch, int32_t n, const void* L, const void* Lbar, void* Ab
     tile = pick_tile(tile, n, batch, sizeof(T));
     if (!accumulate && Lbar == Abar)  // in place: the sweep needs no workspace
         return to_code(chol::blocked_adj<T>(l, lb, ab, status, batch, n, tile, nullptr, false,
-                                            stream));
+                                            nullptr, stream));
+    // float64 with 128-wide tiles also takes the tensor-core updates' operand
+    // slices, after the batch * n * n working matrices (256-byte aligned)
+    const size_t oz_bytes = (std::is_same<T, double>::value && tile == 128)
+                                ? chol::ozaki_adj_workspace_bytes(batch, n)
+                                : 0;
+    const size_t wbytes = (bytes + 255) / 256 * 256;
     void* work = nullptr;
-    if (cudaMallocAsync(&work, bytes, stream) != cudaSuccess) {
+    if (cudaMallocAsync(&work, wbytes + oz_bytes, stream) != cudaSuccess) {
         cudaGetLastError();
         return CHOL_ENOMEM;
     }
+    void* oz = oz_bytes > 0 ? static_cast<void*>(static_cast<char*>(work) + wbytes) : nullptr;
     const int rc = to_code(chol::blocked_adj<T>(l, lb, ab, status, batch, n, tile,
-                                                static_cast<T*>(work), accumulate, stream));
+                                                static_cast<T*>(work), accumulate, oz, stream));
     if (cudaFreeAsync(work, stream) != cudaSuccess) return CHOL_ECUDA;
     return rc;
 }

@@ -592,15 +592,18 @@ cudaError_t blocked_fwd(const T* A, T* L, int32_t* status, int64_t batch, int n,
                 L, status, batch, n, k0, kb);
         CHOL_TRY(cudaGetLastError());
         if (k == nt - 1) break;
-        CHOL_TRY((launch_trsm<T, TRSM_FWD_PANEL>(L, L, status, batch, n, k0, kb, k0 + kb,
-                                                 n - k0 - kb, stream)));
         if constexpr (std::is_same<T, double>::value) {
             if (work != nullptr && tile == 128) {
+                // panel solve and trailing update on the tensor cores
+                CHOL_TRY(ozaki_panel_solve(reinterpret_cast<double*>(L), work, status, batch, n,
+                                           k, stream));
                 CHOL_TRY(ozaki_trailing_update(reinterpret_cast<double*>(L), work, status, batch,
                                                n, k, stream));
                 continue;
             }
         }
+        CHOL_TRY((launch_trsm<T, TRSM_FWD_PANEL>(L, L, status, batch, n, k0, kb, k0 + kb,
+                                                 n - k0 - kb, stream)));
         const int m = nt - k - 1;
         GemmArgs<T> g{L, L, L, status, batch, n, tile, nt, k, 0, 0};
         CHOL_TRY((launch_gemm<T, GEMM_FWD_TRAIL>(g, m * (m + 1) / 2, stream)));
@@ -621,7 +624,7 @@ cudaError_t blocked_fwd(const T* A, T* L, int32_t* status, int64_t batch, int n,
 // the 7 n^3 / 3 of forming P and solving twice.
 template <typename T>
 cudaError_t blocked_adj(const T* L, const T* Lbar, T* Abar, const int32_t* status,
-                        int64_t batch, int n, int tile, T* W, bool accumulate,
+                        int64_t batch, int n, int tile, T* W, bool accumulate, void* oz_work,
                         cudaStream_t stream) {
     const int nt = (n + tile - 1) / tile;
     const int64_t total = batch * (int64_t)n * n;
@@ -644,8 +647,29 @@ cudaError_t blocked_adj(const T* L, const T* Lbar, T* Abar, const int32_t* statu
     const int bm = tile >= 64 ? 64 : 32;
     const int subs = (tile / bm) * (tile / bm);
     const int64_t bmat = std::min<int64_t>(batch, 65535);
+    // float64 with 128-wide tiles: the two large updates on the tensor cores
+    bool oz = false;
+    if constexpr (std::is_same<T, double>::value) {
+        oz = oz_work != nullptr && tile == 128;
+        if (oz) CHOL_TRY(ozaki_adj_prepare(L, oz_work, status, batch, n, stream));
+    }
     for (int J = nt - 1; J >= 0; --J) {
         const int j0 = J * tile, kb = std::min(tile, n - j0), r0 = j0 + kb, nb = n - r0;
+        if constexpr (std::is_same<T, double>::value) {
+            if (oz) {
+                if (nb > 0) {
+                    CHOL_TRY(ozaki_adj_solve(L, W, oz_work, status, batch, n, J, stream));
+                    CHOL_TRY(ozaki_adj_row(L, W, oz_work, status, batch, n, J, stream));
+                }
+                const size_t dsm = (size_t)kb * (kb + 1) * sizeof(T);
+                diag_rev_kernel<T, kThreads><<<dim3(1, grid_y(batch)), kThreads, dsm, stream>>>(
+                    L, W, status, batch, n, j0, kb);
+                CHOL_TRY(cudaGetLastError());
+                // W_IK -= C_I L_JK (I > J) and W_JK -= (W_JJ + W_JJ^T) L_JK, K < J
+                CHOL_TRY(ozaki_adj_upd(L, W, oz_work, status, batch, n, J, stream));
+                continue;
+            }
+        }
         if (nb > 0) {
             CHOL_TRY((launch_trsm<T, TRSM_ADJ_M>(L, W, status, batch, n, j0, kb, r0, nb, stream)));
             GemmArgs<T> g{W, L, W, status, batch, n, tile, nt, J, 0, 0};
@@ -685,18 +709,18 @@ template cudaError_t blocked_fwd<float>(const float*, float*, int32_t*, int64_t,
 template cudaError_t blocked_fwd<double>(const double*, double*, int32_t*, int64_t, int, int,
                                          void*, cudaStream_t);
 template cudaError_t blocked_adj<float>(const float*, const float*, float*, const int32_t*,
-                                        int64_t, int, int, float*, bool, cudaStream_t);
+                                        int64_t, int, int, float*, bool, void*, cudaStream_t);
 template cudaError_t blocked_adj<double>(const double*, const double*, double*, const int32_t*,
-                                         int64_t, int, int, double*, bool, cudaStream_t);
+                                         int64_t, int, int, double*, bool, void*, cudaStream_t);
 template cudaError_t blocked_fwd<cplx<float>>(const cplx<float>*, cplx<float>*, int32_t*, int64_t,
                                               int, int, void*, cudaStream_t);
 template cudaError_t blocked_fwd<cplx<double>>(const cplx<double>*, cplx<double>*, int32_t*,
                                                int64_t, int, int, void*, cudaStream_t);
 template cudaError_t blocked_adj<cplx<float>>(const cplx<float>*, const cplx<float>*, cplx<float>*,
                                               const int32_t*, int64_t, int, int, cplx<float>*, bool,
-                                              cudaStream_t);
+                                              void*, cudaStream_t);
 template cudaError_t blocked_adj<cplx<double>>(const cplx<double>*, const cplx<double>*,
                                                cplx<double>*, const int32_t*, int64_t, int, int,
-                                               cplx<double>*, bool, cudaStream_t);
+                                               cplx<double>*, bool, void*, cudaStream_t);
 
 }  // namespace chol

@@ -84,12 +84,33 @@ size_t blocked_fwd_workspace_bytes(bool real_double, int64_t batch, int n, int t
 size_t ozaki_workspace_bytes(int64_t batch, int n);
 cudaError_t ozaki_trailing_update(double* L, void* work, int32_t* status, int64_t batch, int n,
                                   int k, cudaStream_t stream);
+// The panel solve of step k on the tensor cores: L_Ik <- L_Ik G^-T, I > k,
+// with G^-1 the inverse of the (factored) diagonal tile.
+cudaError_t ozaki_panel_solve(double* L, void* work, int32_t* status, int64_t batch, int n,
+                              int k, cudaStream_t stream);
+// The same for the float64 blocked adjoint with 128-wide tiles: `work` holds
+// ozaki_adj_workspace_bytes(batch, n) bytes; prepare slices L once, then per
+// tile column J: row (W_JK -= C^T L_{below J, K}, K <= J) before the
+// diagonal sweep, upd (W_IK -= Chat_I L_JK, I >= J > K, Chat = [W_JJ + W_JJ^T;
+// C]) after it.
+size_t ozaki_adj_workspace_bytes(int64_t batch, int n);
+cudaError_t ozaki_adj_prepare(const double* L, void* work, const int32_t* status, int64_t batch,
+                              int n, cudaStream_t stream);
+// The adjoint's panel solve C <- C L_JJ^-1 (rows below tile J).
+cudaError_t ozaki_adj_solve(const double* L, double* W, void* work, const int32_t* status,
+                            int64_t batch, int n, int J, cudaStream_t stream);
+cudaError_t ozaki_adj_row(const double* L, double* W, void* work, const int32_t* status,
+                          int64_t batch, int n, int J, cudaStream_t stream);
+cudaError_t ozaki_adj_upd(const double* L, double* W, void* work, const int32_t* status,
+                          int64_t batch, int n, int J, cudaStream_t stream);
 // `work` holds batch * n * n elements of scratch.  accumulate as small_adj.
 // Not accumulating with adj_A == adj_L (in place), the sweep runs on adj_A
-// itself and `work` is not used (may be null).
+// itself and `work` is not used (may be null).  `oz_work` (may be null) holds
+// ozaki_adj_workspace_bytes(batch, n) bytes; with it, float64 tiles of 128
+// take the two large updates on the tensor cores.
 template <typename T>
 cudaError_t blocked_adj(const T* L, const T* Lbar, T* Abar, const int32_t* status,
-                        int64_t batch, int n, int tile, T* work, bool accumulate,
+                        int64_t batch, int n, int tile, T* work, bool accumulate, void* oz_work,
                         cudaStream_t stream);
 
 int blocked_default_tile(int n, int64_t batch);

@@ -141,7 +141,7 @@ int run(int64_t batch, int32_t n, const void* L, const void* Lbar, void* Abar,
         tile = std::min(chol::blocked_default_tile(n, batch),
                         chol::blocked_max_tile((int)sizeof(T)));
     e = chol::blocked_adj<T>(l, lb, ab, status, batch, n, tile, static_cast<T*>(work), true,
-                             stream);
+                             nullptr, stream);
     return e == cudaSuccess ? CHOL_OK : CHOL_ECUDA;
 }
 

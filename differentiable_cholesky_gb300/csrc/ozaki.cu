@@ -1,34 +1,40 @@
-// FP64 trailing update of the blocked Cholesky forward on the bf16 tensor
-// cores (tcgen05), for 128-wide tiles.
+// FP64 GEMM-shaped steps of the blocked Cholesky (128-wide tiles) on the bf16
+// tensor cores (tcgen05): the forward's trailing update and the adjoint's
+// two large updates.
 //
 // The trailing update L_IJ -= L_Ik L_Jk^T (jaxmg docs "Cholesky
 // factorization": the tiled factorisation with tile size T_A = 128) is the
-// only dense contraction of the forward.  On sm_103a the FP64 pipes (FMA and
-// the f64 mma.sync path) deliver about 1.1 TFLOP/s in all, while the bf16
-// tensor cores deliver about 2 PFLOP/s.  The update is therefore computed as
-// an exact sum of bf16 products (the splitting scheme of Ozaki et al., with
-// one power-of-two scale per row):
+// only dense contraction of the forward, and Murray's blocked reverse sweep
+// (the adjoint NVIDIA/warp issue #1316's closing comment states, evaluated
+// blockwise) spends its flops in two more: W_JK -= C^T L_{below J, K} and
+// W_IK -= C_I L_JK (+ the symmetric diagonal term).  On sm_103a the FP64 pipes
+// (FMA and the f64 mma.sync path) deliver about 1.1 TFLOP/s in all, while the
+// bf16 tensor cores deliver about 2 PFLOP/s.  Each contraction is therefore
+// computed as an exact sum of bf16 products (the splitting scheme of Ozaki et
+// al., with one power-of-two scale per operand row):
 //
-//   1. slice_kernel: every row x of the panel L_{.,k} (128 values) is scaled
-//      by 2^-e, e = 1 + floor(log2 ||x||_2), so that ||x 2^-e||_2 < 1, and
-//      written as 7 signed base-256 digits, x 2^-e = sum_p d_p 2^(-7-8p) with
-//      integers |d_p| <= 128 (exact in bf16) and a remainder below 2^-56.
-//      The digits go to a workspace in the tensor cores' shared-memory tile
-//      layout, so that one bulk copy moves a whole stage.
-//   2. trail_kernel (one CTA per 128 x 64 half of an output tile): for
-//      d = 0..6 the products of digit slices p + q = d are accumulated in one
-//      fp32 TMEM accumulator, acc_d = sum_{p+q=d} D_p(I) D_q(J)^T over the
-//      128-long reduction.  Every product is an integer of at most 2^14 and
-//      an accumulator sums at most 7 * 128 of them (< 2^24), so fp32 holds it
-//      exactly.  The epilogue combines v = sum_d acc_d 256^(6-d) in int64
-//      (exact: by Cauchy-Schwarz |v| <= 2^62) and applies
-//      L_IJ -= v 2^(e_r + e_c - 62) with one FP64 fused multiply-add.
+//   1. Slicing: every 128-long operand vector x (a row of a panel, or a
+//      column of a 128-row chunk) is scaled by 2^-e, e = 1 + floor(log2
+//      ||x||_2), so that ||x 2^-e||_2 < 1, truncated to a multiple of 2^-55
+//      and written as 7 balanced base-256 digits, x 2^-e ~ sum_p d_p
+//      2^(-7-8p), integers |d_p| <= 128 (exact in bf16), by integer
+//      arithmetic on the float64 bits.  The digits go to a workspace in the
+//      tensor cores' shared-memory tile layout (8 x 8 core matrices), so that
+//      one bulk copy moves a whole pipeline stage.
+//   2. oz_gemm_kernel (one CTA per 128 x 64 half of an output tile): per
+//      128-long reduction chunk, for d = 0..6 the products of digit slices
+//      p + q = d are accumulated in one fp32 TMEM accumulator,
+//      acc_d = sum_{p+q=d} D_p(A) D_q(B)^T.  Every product is an integer of at
+//      most 2^14 and an accumulator sums at most 7 * 128 of them (< 2^24), so
+//      fp32 holds it exactly.  The epilogue combines v = sum_d acc_d
+//      256^(6-d) in int64 (exact: by Cauchy-Schwarz |v| <= 2^62) and applies
+//      out -= v 2^(e_r + e_c - 62) with one FP64 fused multiply-add per chunk.
 //
 // The result differs from an FP64 GEMM only by the dropped digit products
-// (p + q >= 7) and the digit remainders, both below 2^-53 of the row-norm
-// scale 2^(e_r + e_c); the one rounding is that of the final FMA.  A row with
-// a non-finite value keeps its NaN/Inf: its exponent is a sentinel and the
-// epilogue writes NaN into every entry that row touches.
+// (p + q >= 7) and the truncation below 2^-55, both below 2^-53 of the
+// row-norm scale 2^(e_r + e_c); the one rounding per chunk is that of the FMA.
+// An operand vector with a non-finite value keeps its NaN/Inf: its exponent
+// is a sentinel and the epilogue writes NaN into every entry it touches.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -42,20 +48,22 @@
 namespace chol {
 namespace {
 
-constexpr int kT = 128;                      // tile: rows per block, reduction length
+constexpr int kT = 128;                      // tile: rows per block, reduction chunk
 constexpr int kS = 7;                        // digit slices
 constexpr int kKC = 32;                      // reduction per pipeline stage
-constexpr int kChunks = kT / kKC;            // stages per output tile
+constexpr int kChunks = kT / kKC;            // stages per reduction chunk
 constexpr int kN = 64;                       // output columns per CTA
 constexpr int kSliceElems = kT * kKC;        // one slice of one block, one stage: 8 KB
-constexpr int kBlockElems = kChunks * kS * kSliceElems;  // one 128-row block: 224 KB
+constexpr int kBlockElems = kChunks * kS * kSliceElems;  // one 128 x 128 operand block: 224 KB
 constexpr uint32_t kStageA = kS * kSliceElems * 2;       // 56 KB
 constexpr uint32_t kStageB = kS * kN * kKC * 2;          // 28 KB
 constexpr uint32_t kStageBytes = kStageA + kStageB;
 constexpr int kStages = 2;
 constexpr int kTmemCols = 512;               // 7 accumulators x 64 columns, rounded up
-constexpr size_t kTrailSmem = 128 + (size_t)kStages * kStageBytes + 128;
-constexpr int32_t kNonFinite = INT_MIN;      // exponent sentinel of a non-finite row
+constexpr size_t kGemmSmem = 128 + (size_t)kStages * kStageBytes + 128;
+constexpr int32_t kNonFinite = INT_MIN;      // exponent sentinel of a non-finite vector
+
+using bf16 = __nv_bfloat16;
 
 // Offset (elements) of element (r, kk) of a 128 x 32 slice: 8 x 8 core
 // matrices (8 rows of 16 bytes), four along the reduction per row group.
@@ -63,53 +71,222 @@ __host__ __device__ constexpr int core_offset(int r, int kk) {
     return ((r >> 3) * (kKC / 8) + (kk >> 3)) * 64 + (r & 7) * 8 + (kk & 7);
 }
 
+// Offset of element (m, k) (operand index m, reduction index k, both < 128)
+// of digit slice p inside one operand block.
+__device__ __forceinline__ int block_offset(int m, int k, int p) {
+    return (k >> 5) * (kS * kSliceElems) + p * kSliceElems + core_offset(m, k & 31);
+}
+
+// 2^E as a double for E in the normal range, 0 below it and +Inf above.
+__device__ __forceinline__ double pow2(int E) {
+    if (E < -1022) return 0.0;
+    if (E > 1023) return __longlong_as_double(0x7ff0000000000000LL);
+    return __longlong_as_double((long long)(E + 1023) << 52);
+}
+
+// Scale exponent of the 128-long vector a warp holds four values per lane:
+// 2^e > ||x||_2, 0 for a vector below 2^-1022 (its digits are all zero) and
+// the sentinel for a non-finite one.  Integer and fp32 arithmetic only (the
+// FP64 pipe is the scarce one): the largest binary exponent by an integer
+// warp maximum, then the squares of the values relative to it in fp32, whose
+// sum is inflated by 2^-16 so that rounding cannot place 2^e at or below the
+// exact norm.  A slightly large e only costs the last fraction of a bit.
+__device__ __forceinline__ int warp_scale_exponent(const double (&v)[kChunks], bool finite_lane) {
+    if (!__all_sync(0xffffffffu, finite_lane)) return kNonFinite;
+    unsigned emax = 0;
+#pragma unroll
+    for (int j = 0; j < kChunks; ++j) {
+        const unsigned E = (unsigned)((__double_as_longlong(v[j]) >> 52) & 0x7ff);
+        emax = E > emax ? E : emax;
+    }
+    emax = __reduce_max_sync(0xffffffffu, emax);
+    if (emax == 0) return 0;  // zeros and subnormals only
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < kChunks; ++j) {
+        const long long bits = __double_as_longlong(v[j]);
+        const int E = (int)((bits >> 52) & 0x7ff);
+        const int fe = E - (int)emax + 127;  // |x| 2^-(emax-1023) as a float, in [2^-126, 2)
+        if (E == 0 || fe < 1) continue;      // below 2^-126 of the largest: negligible
+        const unsigned fbits = ((unsigned)fe << 23) | (unsigned)((bits >> 29) & 0x7fffff);
+        const float xs = __uint_as_float(fbits);
+        ss = fmaf(xs, xs, ss);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    // the truncated mantissas and the fp32 sums only lose: a margin keeps 2^e above
+    ss *= 1.0f + 0x1p-16f;
+    return (int)emax - 1023 + ilogbf(sqrtf(ss)) + 1;  // ss in [1, 512)
+}
+
+// The 7 balanced base-256 digits of v 2^(55-e) (|v| < 2^e), truncated toward
+// zero below 2^(e-55), most significant first, from the float64's bits.
+__device__ __forceinline__ void to_digits(double v, int e, int (&d)[kS]) {
+    const long long bits = __double_as_longlong(v);
+    const int E = (int)((bits >> 52) & 0x7ff);
+    long long X = 0;
+    if (E != 0 && e != kNonFinite) {  // zeros and subnormals (< 2^-1022) give 0
+        const long long M = (bits & ((1ll << 52) - 1)) | (1ll << 52);
+        const int s = E - 1075 + 55 - e;  // X = M 2^s, s <= 2 since |v| < 2^e
+        X = s >= 0 ? (M << s) : (s > -64 ? (M >> -s) : 0);
+        if (bits < 0) X = -X;
+    }
+#pragma unroll
+    for (int p = kS - 1; p >= 1; --p) {
+        const int lo = (int)(signed char)(X & 0xff);  // in [-128, 127]
+        d[p] = lo;
+        X = (X - lo) >> 8;                            // exact
+    }
+    d[0] = (int)X;  // |d_0| <= 128
+}
+
+// Balancing of the reduction index.  A product sum_r a_r b_r is unchanged
+// when a_r is multiplied and b_r divided by the same power of two 2^s_r.
+// Cholesky operands carry the factor's row scales along the reduction (rows
+// of L scale like sqrt(a_rr), the panel before its solve like a_rr, the
+// gradient like 1 / sqrt(a_rr)), so each term is balanced with
+// s_r = ilogb(L_rr) before the per-vector scaling: the digits then resolve
+// every term to the same relative precision even when the rows span many
+// binades.  sign = +1 multiplies, -1 divides, 0 leaves the operand as it is.
+struct Bal {
+    const int32_t* exp;  // s_r per reduction index (per batch entry: stride)
+    size_t stride;
+    int off;             // reduction index of the slicer's element 0
+    int sign;
+};
+
+__device__ __forceinline__ double balance(double x, const Bal& bal, int64_t b, int r) {
+    if (bal.sign == 0) return x;
+    return ldexp(x, bal.sign * bal.exp[b * bal.stride + bal.off + r]);
+}
+
 // ---------------------------------------------------------------------------
-// Digit slices of the panel: rows [r_begin, nt * 128) of column block k.
-// One warp per row; lane l holds columns l, l + 32, l + 64, l + 96, i.e.
-// reduction index l of each of the four stages.
+// Row slicing: rows [row0, row0 + nrows) of the 128 columns [col0, col0+128)
+// of src (n x n, row-major); one warp per row, lane l holding reduction
+// indices l, l + 32, l + 64, l + 96.  Row r goes to operand block r / 128 at
+// position r % 128, its exponent to ex[r].  With sym_blocks, the first 128 rows
+// (block row0 / 128, which must equal col0 / 128) are read as the Hermitian
+// matrix S + S^T of the lower triangle of that diagonal block: the upper half
+// mirrors the lower one and the diagonal is doubled.  Rows >= n are zeros.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256)
-slice_kernel(const double* __restrict__ L, __nv_bfloat16* __restrict__ ws,
-             int32_t* __restrict__ ex, const int32_t* __restrict__ status, int64_t batch, int n,
-             int nt, int k0, int r_begin) {
+slice_rows_kernel(const double* __restrict__ src, bf16* __restrict__ dst,
+                  int32_t* __restrict__ ex, const int32_t* __restrict__ status, int64_t batch,
+                  int n, int row0, int nrows, int col0, bool sym_first, size_t dst_stride,
+                  size_t ex_stride, Bal bal) {
     const int lane = threadIdx.x & 31;
-    const int row = r_begin + (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
-    if (row >= nt * kT) return;
+    const int rl = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    if (rl >= nrows) return;
+    const int row = row0 + rl;
     for (int64_t b = blockIdx.y; b < batch; b += gridDim.y) {
         if (status != nullptr && status[b] != 0) continue;
+        const double* S = src + (size_t)b * n * n;
         double v[kChunks];
-        double ss = 0.0;
         bool finite = true;
 #pragma unroll
         for (int j = 0; j < kChunks; ++j) {
-            v[j] = row < n ? L[(size_t)b * n * n + (size_t)row * n + k0 + lane + 32 * j] : 0.0;
-            finite = finite && isfinite(v[j]);
-            ss = fma(v[j], v[j], ss);
+            const int col = col0 + lane + 32 * j;
+            double x = 0.0;
+            if (row < n && col < n) {
+                if (sym_first && rl < kT) {
+                    x = col <= row ? S[(size_t)row * n + col] : S[(size_t)col * n + row];
+                    if (col == row) x += x;
+                } else {
+                    x = S[(size_t)row * n + col];
+                }
+                x = balance(x, bal, b, col);
+            }
+            v[j] = x;
+            finite = finite && isfinite(x);
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        finite = __all_sync(0xffffffffu, finite) && isfinite(ss);
-        int e = 0;
-        if (!finite) {
-            e = kNonFinite;
-        } else if (ss > 0.0) {
-            e = ilogb(sqrt(ss)) + 1;  // 2^e > ||row||_2 >= every |x|
-        }
-        const double scale = (finite && ss > 0.0) ? ldexp(128.0, -e) : 0.0;
-        const int I = row / kT, r = row % kT;
-        __nv_bfloat16* blk = ws + ((size_t)b * nt + I) * kBlockElems;
+        const int e = warp_scale_exponent(v, finite);
+        bf16* blk = dst + b * dst_stride + (size_t)(row / kT) * kBlockElems;
 #pragma unroll
         for (int j = 0; j < kChunks; ++j) {
-            double t = v[j] * scale;  // in [-128, 128]
-            __nv_bfloat16* dst = blk + (size_t)j * kS * kSliceElems + core_offset(r, lane);
+            int d[kS];
+            to_digits(v[j], e, d);
 #pragma unroll
-            for (int p = 0; p < kS; ++p) {
-                const double d = rint(t);
-                dst[p * kSliceElems] = __double2bfloat16(d);
-                t = (t - d) * 256.0;
-            }
+            for (int p = 0; p < kS; ++p)
+                blk[block_offset(row % kT, lane + 32 * j, p)] = __int2bfloat16_rn(d[p]);
         }
-        if (lane == 0) ex[(size_t)b * nt * kT + row] = e;
+        if (lane == 0) ex[b * ex_stride + row] = e;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Column slicing: for every 128-row chunk c of a list and every column block
+// K of it, the columns x = src[c*128 .. c*128+127, K*128 + m] (the reduction
+// runs down the rows) go to operand block blk(c, K) at position m.  With
+// lower_only, entries above the diagonal (row < column) read as zero (the
+// upper triangle of a factor is never read).  One block of 256 threads per
+// (chunk, column block): the 128 x 128 tile goes through shared memory, read
+// by rows (coalesced), sliced by columns.
+// Chunk list: chunks c = c_begin .. c_end - 1; column blocks K = 0 .. kmax(c)
+// where kmax(c) = (tri ? c : k_fixed), so blocks are (c, K <= c) packed
+// lower-triangle-wise (tri) or (c, k_fixed) one per chunk.
+// ---------------------------------------------------------------------------
+constexpr int kColThreads = 256;
+
+__global__ void __launch_bounds__(kColThreads)
+slice_cols_kernel(const double* __restrict__ src, bf16* __restrict__ dst,
+                  int32_t* __restrict__ ex, const int32_t* __restrict__ status, int64_t batch,
+                  int n, int c_begin, bool tri, int k_fixed, bool lower_only, size_t dst_stride,
+                  size_t ex_stride, Bal bal) {
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    double* tile = reinterpret_cast<double*>(smem_raw);  // 128 x 129
+    constexpr int P = kT + 1;
+    // which (c, K): blockIdx.x enumerates them
+    int c, K, slot;
+    if (tri) {
+        // slot t = c (c + 1) / 2 + K over c >= c_begin: t0 = c_begin (c_begin + 1) / 2
+        const int t = c_begin * (c_begin + 1) / 2 + (int)blockIdx.x;
+        int r = (int)((sqrt(8.0 * t + 1.0) - 1.0) * 0.5);
+        while ((r + 1) * (r + 2) / 2 <= t) ++r;
+        while (r * (r + 1) / 2 > t) --r;
+        c = r;
+        K = t - r * (r + 1) / 2;
+        slot = t;
+    } else {
+        c = c_begin + (int)blockIdx.x;
+        K = k_fixed;
+        slot = c;
+    }
+    const int r0 = c * kT, q0 = K * kT;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int64_t b = blockIdx.y; b < batch; b += gridDim.y) {
+        if (status != nullptr && status[b] != 0) continue;
+        const double* S = src + (size_t)b * n * n;
+        __syncthreads();
+        for (int e = threadIdx.x; e < kT * kT; e += kColThreads) {
+            const int i = e / kT, j = e % kT;
+            const int row = r0 + i, col = q0 + j;
+            double x = 0.0;
+            if (row < n && col < n && (!lower_only || col <= row))
+                x = balance(S[(size_t)row * n + col], bal, b, row);
+            tile[i * P + j] = x;
+        }
+        __syncthreads();
+        bf16* blk = dst + b * dst_stride + (size_t)slot * kBlockElems;
+        // warp w takes columns w, w + 8, ...; lane l holds rows l, l+32, l+64, l+96
+        for (int m = warp; m < kT; m += kColThreads / 32) {
+            double v[kChunks];
+            bool finite = true;
+#pragma unroll
+            for (int j = 0; j < kChunks; ++j) {
+                v[j] = tile[(lane + 32 * j) * P + m];
+                finite = finite && isfinite(v[j]);
+            }
+            const int e = warp_scale_exponent(v, finite);
+#pragma unroll
+            for (int j = 0; j < kChunks; ++j) {
+                int d[kS];
+                to_digits(v[j], e, d);
+#pragma unroll
+                for (int p = 0; p < kS; ++p)
+                    blk[block_offset(m, lane + 32 * j, p)] = __int2bfloat16_rn(d[p]);
+            }
+            if (lane == 0) ex[b * ex_stride + (size_t)slot * kT + m] = e;
+        }
     }
 }
 
@@ -177,38 +354,145 @@ __device__ __forceinline__ void tri_index(int t, int& i, int& j) {
     j = t - r * (r + 1) / 2;
 }
 
-// 2^E as a double for E in the normal range, 0 below it (such a contribution
-// is under 2^-1022 and lost in any entry it meets).
-__device__ __forceinline__ double pow2(int E) {
-    if (E < -1022) return 0.0;
-    if (E > 1023) return __longlong_as_double(0x7ff0000000000000LL);
-    return __longlong_as_double((long long)(E + 1023) << 52);
+
+// ---------------------------------------------------------------------------
+// The three contractions.  Per output half tile (128 rows x 64 columns) a CTA
+// runs one or more 128-long reduction chunks, each with its own operand
+// blocks and scales.
+// ---------------------------------------------------------------------------
+enum OzMode {
+    OZ_FWD_TRAIL = 0,  // L_IJ -= L_Ik L_Jk^T, I >= J > k           (A, B: row slices of the panel)
+    OZ_REV_ROW = 1,    // W_JK -= sum_{c > J} C_c^T L_cK, K <= J     (A: column slices of C per chunk,
+                       //                                             B: column slices of L per chunk)
+    OZ_REV_UPD = 2,    // W_IK -= Chat_I L_JK, I >= J, K < J         (A: row slices of Chat,
+                       //                                             B: column slices of L, chunk J)
+    OZ_ASSIGN = 3      // X_I = P_I G^T, I > step: a panel solve by the inverse of its diagonal
+                       // tile (A: row slices of the panel, B: slices of the inverse, written
+                       // over the panel)
+};
+
+struct OzArgs {
+    double* out;          // the matrix updated (L or W), n x n per batch entry
+    const bf16* a;        // A operand blocks
+    const int32_t* ea;    // their exponents (128 per block)
+    const bf16* b;        // B operand blocks
+    const int32_t* eb;
+    size_t a_stride, ea_stride, b_stride, eb_stride;  // per batch entry (elements)
+    const int32_t* status;  // matrices with status != 0 are skipped
+    int32_t* fail;          // where a device wait that ran out is reported (or null)
+    int64_t batch;
+    int n, nt, step;      // step: k (forward) or J (adjoint)
+    int splits;           // OZ_REV_ROW: the reduction split over this many CTAs
+    double* part;         // ... each writing its partial sum here (splits > 1)
+};
+
+struct OzJob {
+    int out_r0, out_c0;   // output half tile origin
+    bool lower;           // diagonal tile: only entries with col <= row
+    int ch_begin, ch_end; // reduction chunks of this CTA
+    int h;                // which 64-column half of the B block
+    int split;            // which part of a split reduction (OZ_REV_ROW)
+};
+
+template <int MODE>
+__device__ __forceinline__ OzJob oz_job(const OzArgs& g, int job, int& p0, int& p1) {
+    OzJob o{};
+    o.h = job & 1;
+    const int t = job >> 1;
+    if (MODE == OZ_FWD_TRAIL) {
+        int i, j;
+        tri_index(t, i, j);
+        const int I = g.step + 1 + i, J = g.step + 1 + j;
+        o.out_r0 = I * kT;
+        o.out_c0 = J * kT + o.h * kN;
+        o.lower = I == J;
+        o.ch_begin = 0;
+        o.ch_end = 1;
+        p0 = I;  // A: row-slice block I, B: row-slice block J
+        p1 = J;
+    } else if (MODE == OZ_REV_ROW) {
+        const int K = t / g.splits;  // K <= J
+        o.split = t % g.splits;
+        o.out_r0 = g.step * kT;
+        o.out_c0 = K * kT + o.h * kN;
+        o.lower = K == g.step;
+        const int chunks = g.nt - g.step - 1;
+        const int per = (chunks + g.splits - 1) / g.splits;
+        o.ch_begin = o.split * per;
+        o.ch_end = min(chunks, o.ch_begin + per);
+        p0 = K;
+        p1 = 0;
+    } else if (MODE == OZ_ASSIGN) {
+        const int I = g.step + 1 + t;
+        o.out_r0 = I * kT;
+        o.out_c0 = g.step * kT + o.h * kN;
+        o.lower = false;
+        o.ch_begin = 0;
+        o.ch_end = 1;
+        p0 = I;
+        p1 = 0;
+    } else {
+        const int J = g.step;
+        const int I = J + t / J, K = t % J;  // I >= J, K < J
+        o.out_r0 = I * kT;
+        o.out_c0 = K * kT + o.h * kN;
+        o.lower = false;
+        o.ch_begin = 0;
+        o.ch_end = 1;
+        p0 = I;
+        p1 = K;
+    }
+    return o;
 }
 
-// ---------------------------------------------------------------------------
-// One CTA: the 128 x 64 half h of lower output tile (I, J), I >= J > k.
+// Operand blocks of chunk `ch` of a job (element offsets within a batch entry).
+template <int MODE>
+__device__ __forceinline__ void oz_chunk(const OzArgs& g, int p0, int p1, int ch, size_t& ablk,
+                                         size_t& eaoff, size_t& bblk, size_t& eboff) {
+    if (MODE == OZ_FWD_TRAIL) {
+        ablk = (size_t)p0 * kBlockElems;
+        eaoff = (size_t)p0 * kT;
+        bblk = (size_t)p1 * kBlockElems;
+        eboff = (size_t)p1 * kT;
+    } else if (MODE == OZ_REV_ROW) {
+        const int c = g.step + 1 + ch;       // reduction chunk: rows c*128 ..
+        ablk = (size_t)c * kBlockElems;      // column slices of C, chunk c
+        eaoff = (size_t)c * kT;
+        const size_t slot = (size_t)c * (c + 1) / 2 + p0;  // column slices of L, (c, K)
+        bblk = slot * kBlockElems;
+        eboff = slot * kT;
+    } else if (MODE == OZ_ASSIGN) {
+        ablk = (size_t)p0 * kBlockElems;     // row slices of the panel, block I
+        eaoff = (size_t)p0 * kT;
+        bblk = 0;                            // slices of the inverse (one block)
+        eboff = 0;
+    } else {
+        ablk = (size_t)p0 * kBlockElems;     // row slices of Chat, block I
+        eaoff = (size_t)p0 * kT;
+        const size_t slot = (size_t)g.step * (g.step + 1) / 2 + p1;  // L (J, K)
+        bblk = slot * kBlockElems;
+        eboff = slot * kT;
+    }
+}
+
 // Warp 0 owns TMEM and (lane 0) issues the MMAs; warp 1 lane 0 issues the
 // bulk copies; all four warps run the epilogue (warp w reads TMEM lanes
-// 32w .. 32w + 31, i.e. rows 32w .. of the tile).
-// ---------------------------------------------------------------------------
+// 32w .. 32w + 31, i.e. output rows 32w .. of the tile).
+template <int MODE>
 __global__ void __launch_bounds__(128, 1)
-trail_kernel(double* __restrict__ L, const __nv_bfloat16* __restrict__ ws,
-             const int32_t* __restrict__ ex, int32_t* __restrict__ status, int64_t batch, int n,
-             int nt, int k, uint32_t max_polls) {
+oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    unsigned char* base = smem_raw;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(base);  // full[2], empty[2], done
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + 64);
-    unsigned char* stages = base + 128;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw);  // full[2], empty[2], done
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + 64);
+    unsigned char* stages = smem_raw + 128;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    const int job = blockIdx.x;
-    const int h = job & 1;
-    int ti, tj;
-    tri_index(job >> 1, ti, tj);
-    const int I = k + 1 + ti, J = k + 1 + tj;
-    const int col0 = J * kT + h * kN;  // first output column
-    if (col0 >= n) return;             // (uniform over the block)
+    int p0 = 0, p1 = 0;
+    const OzJob job = oz_job<MODE>(g, blockIdx.x, p0, p1);
+    if (job.out_c0 >= g.n || job.out_r0 >= g.n || job.ch_begin >= job.ch_end) return;  // uniform
+    // A split reduction writes its partial sums (positive) to its own 128 x 128
+    // tile of g.part; otherwise the product is subtracted from the output.
+    const bool partial = MODE == OZ_REV_ROW && g.splits > 1;
 
     if (tid == 0) {
         for (int i = 0; i < 5; ++i) mbar_init(bars + i, 1);
@@ -226,103 +510,126 @@ trail_kernel(double* __restrict__ L, const __nv_bfloat16* __restrict__ ws,
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    uint32_t it = 0;  // output tiles handled by this CTA (one per matrix)
+    uint32_t it = 0;   // reduction chunks handled by this CTA
     bool failed = false;
-    for (int64_t b = blockIdx.y; b < batch; b += gridDim.y, ++it) {
-        if (status != nullptr && status[b] != 0) continue;  // uniform
-        const __nv_bfloat16* blkA = ws + ((size_t)b * nt + I) * kBlockElems;
-        const __nv_bfloat16* blkB = ws + ((size_t)b * nt + J) * kBlockElems + h * (kN * kKC);
-        if (tid == 32) {
-            // producer: the four stages of this tile
-            for (int kc = 0; kc < kChunks; ++kc) {
-                const uint32_t g = it * kChunks + kc, s = g & 1, u = g >> 1;
-                if (u > 0 && !mbar_wait(bars + 2 + s, (u - 1) & 1, max_polls)) {
-                    failed = true;
-                    break;
+    for (int64_t b = blockIdx.y; b < g.batch && !failed; b += gridDim.y) {
+        if (g.status != nullptr && g.status[b] != 0) continue;  // uniform
+        double* out = g.out + (size_t)b * g.n * g.n;
+        size_t ld = (size_t)g.n;
+        int dst_r0 = 0, dst_c0 = 0;
+        if (partial) {
+            out = g.part + (((size_t)b * g.splits + job.split) * (g.step + 1) + p0) * kT * kT;
+            ld = kT;
+            dst_r0 = job.out_r0;
+            dst_c0 = p0 * kT;
+        }
+        for (int ch = job.ch_begin; ch < job.ch_end; ++ch, ++it) {
+            const bool first = ch == job.ch_begin;
+            size_t ablk, eaoff, bblk, eboff;
+            oz_chunk<MODE>(g, p0, p1, ch, ablk, eaoff, bblk, eboff);
+            const bf16* blkA = g.a + b * g.a_stride + ablk;
+            const bf16* blkB = g.b + b * g.b_stride + bblk + job.h * (kN * kKC);
+            if (tid == 32) {
+                // producer: the four stages of this chunk
+                for (int kc = 0; kc < kChunks; ++kc) {
+                    const uint32_t s_ = (it * kChunks + kc) & 1, u = (it * kChunks + kc) >> 1;
+                    if (u > 0 && !mbar_wait(bars + 2 + s_, (u - 1) & 1, max_polls)) {
+                        failed = true;
+                        break;
+                    }
+                    unsigned char* st = stages + s_ * kStageBytes;
+                    mbar_arrive_expect_tx(bars + s_, kStageBytes);
+                    bulk_load(st, blkA + (size_t)kc * kS * kSliceElems, kStageA, bars + s_);
+                    for (int q = 0; q < kS; ++q)
+                        bulk_load(st + kStageA + q * (kN * kKC * 2),
+                                  blkB + (size_t)kc * kS * kSliceElems + (size_t)q * kSliceElems,
+                                  kN * kKC * 2, bars + s_);
                 }
-                unsigned char* st = stages + s * kStageBytes;
-                mbar_arrive_expect_tx(bars + s, kStageBytes);
-                bulk_load(st, blkA + (size_t)kc * kS * kSliceElems, kStageA, bars + s);
-                for (int q = 0; q < kS; ++q)
-                    bulk_load(st + kStageA + q * (kN * kKC * 2),
-                              blkB + (size_t)kc * kS * kSliceElems + (size_t)q * kSliceElems,
-                              kN * kKC * 2, bars + s);
+            } else if (tid == 0) {
+                // MMA issuer: acc_d = sum_{p+q=d} D_p(A) D_q(B)^T over the chunk
+                for (int kc = 0; kc < kChunks && !failed; ++kc) {
+                    const uint32_t s_ = (it * kChunks + kc) & 1, u = (it * kChunks + kc) >> 1;
+                    if (!mbar_wait(bars + s_, u & 1, max_polls)) {
+                        failed = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(stages + s_ * kStageBytes);
+                    const uint32_t sb = sa + kStageA;
+#pragma unroll
+                    for (int d = 0; d < kS; ++d) {
+#pragma unroll
+                        for (int p = 0; p <= d; ++p) {
+                            const int q = d - p;
+#pragma unroll
+                            for (int ks = 0; ks < kKC / 16; ++ks) {
+                                const uint64_t da =
+                                    smem_desc(sa + p * (kSliceElems * 2) + ks * 256, 128, 512);
+                                const uint64_t db =
+                                    smem_desc(sb + q * (kN * kKC * 2) + ks * 256, 128, 512);
+                                tc_mma(tmem + d * kN, da, db, (kc | p | ks) != 0);
+                            }
+                        }
+                    }
+                    tc_commit(bars + 2 + s_);  // the stage may be refilled once these finish
+                }
+                if (!failed) tc_commit(bars + 4);
             }
-        } else if (tid == 0) {
-            // MMA issuer: acc_d += D_p(I) D_q(J)^T for p + q = d
-            for (int kc = 0; kc < kChunks && !failed; ++kc) {
-                const uint32_t g = it * kChunks + kc, s = g & 1, u = g >> 1;
-                if (!mbar_wait(bars + s, u & 1, max_polls)) {
-                    failed = true;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t sa = smem_u32(stages + s * kStageBytes);
-                const uint32_t sb = sa + kStageA;
+            // epilogue: every thread waits for the accumulators
+            const bool ok = __syncthreads_and(!failed) && mbar_wait(bars + 4, it & 1, max_polls);
+            tc_fence_after();
+            const int rl = warp * 32 + lane;
+            const int row = job.out_r0 + rl;
+            if (!__all_sync(0xffffffffu, ok)) {
+                if (tid == 0 && g.fail != nullptr) g.fail[b] = -1;  // reported, not hung
+                failed = true;
+            } else {
+                const int32_t* ea = g.ea + b * g.ea_stride + eaoff;
+                const int32_t* eb = g.eb + b * g.eb_stride + eboff + job.h * kN;
+                const int er = ea[rl];
+                double* orow = out + (size_t)(row - dst_r0) * ld - dst_c0;
+#pragma unroll 1
+                for (int cc = 0; cc < kN / 16; ++cc) {
+                    uint32_t acc[kS][16];
 #pragma unroll
-                for (int d = 0; d < kS; ++d) {
+                    for (int d = 0; d < kS; ++d)
+                        tc_ld16(tmem + ((uint32_t)(warp * 32) << 16) + d * kN + cc * 16, acc[d]);
+                    tc_wait_ld();
+                    if (row >= g.n) continue;
 #pragma unroll
-                    for (int p = 0; p <= d; ++p) {
-                        const int q = d - p;
+                    for (int j = 0; j < 16; ++j) {
+                        const int col = job.out_c0 + cc * 16 + j;
+                        if (col >= g.n || (job.lower && col > row)) continue;
+                        const int ec = eb[cc * 16 + j];
+                        // sum_d acc_d 256^(6-d), modulo 2^64 (exact: |sum| <= 2^62)
+                        unsigned long long v = 0;
 #pragma unroll
-                        for (int ks = 0; ks < kKC / 16; ++ks) {
-                            const uint64_t da =
-                                smem_desc(sa + p * (kSliceElems * 2) + ks * 256, 128, 512);
-                            const uint64_t db =
-                                smem_desc(sb + q * (kN * kKC * 2) + ks * 256, 128, 512);
-                            tc_mma(tmem + d * kN, da, db, (kc | p | ks) != 0);
+                        for (int d = 0; d < kS; ++d)
+                            v = v * 256ull + (unsigned long long)(long long)__float2int_rn(
+                                                 __uint_as_float(acc[d][j]));
+                        if (er == kNonFinite || ec == kNonFinite) {
+                            orow[col] = __longlong_as_double(0x7ff8000000000000LL);  // NaN
+                        } else if (MODE == OZ_ASSIGN) {
+                            orow[col] = v == 0 ? 0.0
+                                               : ldexp(__ll2double_rn((long long)v), er + ec - 62);
+                        } else if (partial) {
+                            const int E = er + ec - 62;
+                            const double t = v == 0 ? 0.0 : ldexp(__ll2double_rn((long long)v), E);
+                            orow[col] = first ? t : orow[col] + t;
+                        } else if (v != 0) {
+                            const int E = er + ec - 62;
+                            const double vd = __ll2double_rn((long long)v);
+                            orow[col] = (E >= -1022 && E <= 1023) ? fma(-vd, pow2(E), orow[col])
+                                                                  : orow[col] - ldexp(vd, E);
                         }
                     }
                 }
-                tc_commit(bars + 2 + s);  // the stage may be refilled once these finish
             }
-            if (!failed) tc_commit(bars + 4);
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+            if (failed) break;
         }
-        // epilogue: every thread waits for the accumulators
-        const bool ok = __syncthreads_and(!failed) && mbar_wait(bars + 4, it & 1, max_polls);
-        tc_fence_after();
-        const int rl = warp * 32 + lane;
-        const int row = I * kT + rl;
-        if (!__all_sync(0xffffffffu, ok)) {
-            if (tid == 0) status[b] = -1;  // a device wait ran out: reported, not hung
-            failed = true;
-        } else {
-            const int er = row < n ? ex[(size_t)b * nt * kT + row] : 0;
-            double* Lrow = L + (size_t)b * n * n + (size_t)row * n;
-#pragma unroll 1
-            for (int cc = 0; cc < kN / 16; ++cc) {
-                uint32_t acc[kS][16];
-#pragma unroll
-                for (int d = 0; d < kS; ++d)
-                    tc_ld16(tmem + ((uint32_t)(warp * 32) << 16) + d * kN + cc * 16, acc[d]);
-                tc_wait_ld();
-                if (row >= n) continue;
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int col = col0 + cc * 16 + j;
-                    if (col >= n || (I == J && col > row)) continue;
-                    const int ec = ex[(size_t)b * nt * kT + col];
-                    // sum_d acc_d 256^(6-d), modulo 2^64 (exact: |sum| <= 2^62)
-                    unsigned long long v = 0;
-#pragma unroll
-                    for (int d = 0; d < kS; ++d)
-                        v = v * 256ull +
-                            (unsigned long long)(long long)__float2int_rn(__uint_as_float(acc[d][j]));
-                    double c;
-                    if (er == kNonFinite || ec == kNonFinite) {
-                        c = __longlong_as_double(0x7ff8000000000000LL);  // NaN
-                        Lrow[col] = c;
-                    } else {
-                        const double scale = pow2(er + ec - 62);
-                        Lrow[col] = fma(-__ll2double_rn((long long)v), scale, Lrow[col]);
-                    }
-                }
-            }
-        }
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        if (failed) break;
     }
     if (failed && tid == 32) {
         // let copies still in flight land before the block retires
@@ -336,37 +643,399 @@ trail_kernel(double* __restrict__ L, const __nv_bfloat16* __restrict__ ws,
     }
 }
 
+inline unsigned gy(int64_t batch) { return (unsigned)std::min<int64_t>(batch, 65535); }
+
+template <int MODE>
+cudaError_t launch_oz(const OzArgs& g, unsigned jobs, cudaStream_t stream) {
+    if (jobs == 0) return cudaSuccess;
+    static std::atomic<uint64_t> smem_set{0};
+    cudaError_t e = allow_smem_once(oz_gemm_kernel<MODE>, kGemmSmem, smem_set);
+    if (e != cudaSuccess) return e;
+    oz_gemm_kernel<MODE><<<dim3(jobs, gy(g.batch)), 128, kGemmSmem, stream>>>(g, kMbarPolls);
+    return cudaGetLastError();
+}
+
+constexpr size_t kColSmem = (size_t)kT * (kT + 1) * sizeof(double);
+
+cudaError_t launch_slice_rows(const double* src, bf16* dst, int32_t* ex, const int32_t* status,
+                              int64_t batch, int n, int row0, int nrows, int col0, bool sym,
+                              size_t dst_stride, size_t ex_stride, Bal bal, cudaStream_t stream) {
+    if (nrows <= 0) return cudaSuccess;
+    const unsigned blocks = (unsigned)((nrows * 32 + 255) / 256);
+    slice_rows_kernel<<<dim3(blocks, gy(batch)), 256, 0, stream>>>(
+        src, dst, ex, status, batch, n, row0, nrows, col0, sym, dst_stride, ex_stride, bal);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_slice_cols(const double* src, bf16* dst, int32_t* ex, const int32_t* status,
+                              int64_t batch, int n, int c_begin, unsigned count, bool tri,
+                              int k_fixed, bool lower_only, size_t dst_stride, size_t ex_stride,
+                              Bal bal, cudaStream_t stream) {
+    if (count == 0) return cudaSuccess;
+    static std::atomic<uint64_t> smem_set{0};
+    cudaError_t e = allow_smem_once(slice_cols_kernel, kColSmem, smem_set);
+    if (e != cudaSuccess) return e;
+    slice_cols_kernel<<<dim3(count, gy(batch)), kColThreads, kColSmem, stream>>>(
+        src, dst, ex, status, batch, n, c_begin, tri, k_fixed, lower_only, dst_stride, ex_stride,
+        bal);
+    return cudaGetLastError();
+}
+
+inline int tiles_of(int n) { return (n + kT - 1) / kT; }
+
+// W_JK -= sum_s part[s][K] for K <= J (lower part of the diagonal tile),
+// the partial sums added in split order, so the result does not depend on
+// which CTA finished first.
+__global__ void __launch_bounds__(256)
+split_reduce_kernel(double* __restrict__ W, const double* __restrict__ part,
+                    const int32_t* __restrict__ status, int64_t batch, int n, int J, int splits) {
+    const int64_t per = (int64_t)(J + 1) * kT * kT;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < batch * per;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t b = e / per;
+        if (status != nullptr && status[b] != 0) continue;
+        const int64_t w = e % per;
+        const int K = (int)(w / (kT * kT)), m = (int)((w / kT) % kT), c = (int)(w % kT);
+        const int row = J * kT + m, col = K * kT + c;
+        if (row >= n || col >= n || (K == J && c > m)) continue;
+        double s = 0.0;
+        for (int sp = 0; sp < splits; ++sp) s += part[((b * splits + sp) * (J + 1)) * kT * kT + w];
+        W[(size_t)b * n * n + (size_t)row * n + col] -= s;
+    }
+}
+
+// Split of OZ_REV_ROW's reduction: enough CTAs for two per SM, the partial
+// tiles bounded by 2 * SMs per call.
+inline int row_splits(int64_t batch, int J, int chunks) {
+    const int64_t tiles = batch * (J + 1);
+    const int64_t want = (2 * (int64_t)device_sm_count() + 2 * tiles - 1) / (2 * tiles);
+    return (int)std::max<int64_t>(1, std::min<int64_t>(want, chunks));
+}
+
+inline size_t part_elems() { return (size_t)2 * (device_sm_count() + 1) * kT * kT; }
+
+// Adjoint workspace, per batch entry: column slices of L (all (c, K <= c)),
+// column slices of C (one block per chunk), row slices of Chat (one block per
+// row block), then the three exponent arrays.
+// Bump layout of a workspace: every region 256-byte aligned.
+struct Carve {
+    uintptr_t p;
+    template <typename X>
+    X* take(size_t count) {
+        X* r = reinterpret_cast<X*>(p);
+        p += (count * sizeof(X) + 255) / 256 * 256;
+        return r;
+    }
+};
+
+// The inverse of a diagonal tile and what slices it (per batch entry: one
+// 128 x 128 float64 matrix, one operand block and its exponents), and the
+// balancing exponents of every row (nt * 128 per batch entry).
+struct InvWs {
+    double* inv;
+    bf16* sl;
+    int32_t* ex;
+    int32_t* bal;
+};
+
+template <typename C>
+InvWs carve_inv(C& c, int64_t batch, int nt) {
+    InvWs w;
+    w.inv = c.template take<double>((size_t)batch * kT * kT);
+    w.sl = c.template take<bf16>((size_t)batch * kBlockElems);
+    w.ex = c.template take<int32_t>((size_t)batch * kT);
+    w.bal = c.template take<int32_t>((size_t)batch * nt * kT);
+    return w;
+}
+
+// Forward workspace: row slices of the panel (nt blocks per batch entry),
+// their exponents, and the inverse parts.
+struct FwdWs {
+    bf16* rs;
+    int32_t* ers;
+    InvWs iv;
+};
+
+FwdWs fwd_layout(Carve& c, int64_t batch, int n) {
+    const int nt = tiles_of(n);
+    FwdWs w;
+    w.rs = c.take<bf16>((size_t)batch * nt * kBlockElems);
+    w.ers = c.take<int32_t>((size_t)batch * nt * kT);
+    w.iv = carve_inv(c, batch, nt);
+    return w;
+}
+
+FwdWs fwd_ws(void* work, int64_t batch, int n) {
+    Carve c{reinterpret_cast<uintptr_t>(work)};
+    return fwd_layout(c, batch, n);
+}
+
+// Adjoint workspace, per batch entry: column slices of L (all (c, K <= c)),
+// column slices of C (one block per chunk), row slices of Chat (one block per
+// row block), their exponents, the inverse parts, and the partial sums of the
+// split reduction.
+struct AdjWs {
+    bf16 *lc, *cc, *ch;
+    int32_t *elc, *ecc, *ech;
+    InvWs iv;
+    double* part;  // partial sums of split reductions (part_elems())
+    size_t lc_stride, cc_stride, ch_stride, elc_stride, ecc_stride, ech_stride;
+};
+
+AdjWs adj_layout(uintptr_t base, int64_t batch, int n) {
+    const size_t nt = tiles_of(n), ntri = nt * (nt + 1) / 2;
+    AdjWs w{};
+    w.lc_stride = ntri * kBlockElems;
+    w.cc_stride = nt * kBlockElems;
+    w.ch_stride = nt * kBlockElems;
+    w.elc_stride = ntri * kT;
+    w.ecc_stride = nt * kT;
+    w.ech_stride = nt * kT;
+    Carve c{base};
+    w.lc = c.take<bf16>(batch * w.lc_stride);
+    w.cc = c.take<bf16>(batch * w.cc_stride);
+    w.ch = c.take<bf16>(batch * w.ch_stride);
+    w.elc = c.take<int32_t>(batch * w.elc_stride);
+    w.ecc = c.take<int32_t>(batch * w.ecc_stride);
+    w.ech = c.take<int32_t>(batch * w.ech_stride);
+    w.iv = carve_inv(c, batch, (int)nt);
+    w.part = c.take<double>(part_elems());
+    return w;
+}
+
+AdjWs adj_ws(void* work, int64_t batch, int n) {
+    return adj_layout(reinterpret_cast<uintptr_t>(work), batch, n);
+}
+
+// ---------------------------------------------------------------------------
+// Inverse of the diagonal tile G = L[k0 .. k0+kb, k0 .. k0+kb] (lower,
+// kb <= 128): X = G^-1, column by column, X_cc = 1 / g_cc and
+// X_ic = -(sum_{c <= m < i} g_im X_mc) / g_ii for i > c, one warp per column
+// (the lanes split each sum).  X is written as a 128 x 128 matrix (zeros
+// above the diagonal and beyond kb).  Block 0 also writes the balancing
+// exponents ilogb(g_ii) of the tile's rows to bal[k0 + i].
+// ---------------------------------------------------------------------------
+constexpr int kInvCols = 1;  // columns (warps) per block: one, so the FP64 work spreads over SMs
+constexpr size_t kInvSmem = ((size_t)kT * (kT + 1) + kT + (size_t)kInvCols * kT) * sizeof(double);
+
+__global__ void __launch_bounds__(kInvCols * 32)
+tri_inverse_kernel(const double* __restrict__ L, double* __restrict__ Inv,
+                   int32_t* __restrict__ bal, const int32_t* __restrict__ status, int64_t batch,
+                   int n, int nt, int k0, int kb) {
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    constexpr int P = kT + 1;
+    double* G = reinterpret_cast<double*>(smem_raw);  // kb x kb, pitch P
+    double* rinv = G + (size_t)kT * P;                // 1 / g_ii
+    double* X = rinv + kT;                            // kInvCols columns of 128
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = blockIdx.x * kInvCols + warp;
+    for (int64_t b = blockIdx.y; b < batch; b += gridDim.y) {
+        if (status != nullptr && status[b] != 0) continue;
+        const double* Lb = L + (size_t)b * n * n;
+        __syncthreads();
+        for (int e = threadIdx.x; e < kb * kb; e += blockDim.x) {
+            const int i = e / kb, j = e % kb;
+            G[i * P + j] = j <= i ? Lb[(size_t)(k0 + i) * n + k0 + j] : 0.0;
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < kb; i += blockDim.x) {
+            const double d = G[i * P + i];
+            rinv[i] = 1.0 / d;
+            if (blockIdx.x == 0)
+                bal[b * (size_t)nt * kT + k0 + i] = (d > 0.0 && isfinite(d)) ? ilogb(d) : 0;
+        }
+        __syncthreads();
+        double* x = X + warp * kT;
+        if (c < kb) {
+            if (lane == 0) x[c] = rinv[c];
+            __syncwarp();
+            for (int i = c + 1; i < kb; ++i) {
+                double part = 0.0;
+                for (int m = c + lane; m < i; m += 32) part = fma(G[i * P + m], x[m], part);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+                if (lane == 0) x[i] = -part * rinv[i];
+                __syncwarp();
+            }
+        }
+        __syncwarp();
+        if (c < kT) {
+            double* Ib = Inv + (size_t)b * kT * kT;
+            for (int i = lane; i < kT; i += 32)
+                Ib[(size_t)i * kT + c] = (c < kb && i >= c && i < kb) ? x[i] : 0.0;
+        }
+    }
+}
+
+cudaError_t launch_tri_inverse(const double* L, double* Inv, int32_t* bal, const int32_t* status,
+                               int64_t batch, int n, int k0, int kb, cudaStream_t stream) {
+    static std::atomic<uint64_t> smem_set{0};
+    cudaError_t e = allow_smem_once(tri_inverse_kernel, kInvSmem, smem_set);
+    if (e != cudaSuccess) return e;
+    tri_inverse_kernel<<<dim3(kT / kInvCols, gy(batch)), kInvCols * 32, kInvSmem, stream>>>(
+        L, Inv, bal, status, batch, n, tiles_of(n), k0, kb);
+    return cudaGetLastError();
+}
+
+// bal[b][r] = ilogb(L_rr) (0 where L_rr is not a positive number, and for
+// r >= n), r < nt * 128.
+__global__ void __launch_bounds__(256)
+diag_exp_kernel(const double* __restrict__ L, int32_t* __restrict__ bal,
+                const int32_t* __restrict__ status, int64_t batch, int n, int nt) {
+    const int64_t per = (int64_t)nt * kT;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < batch * per;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t b = e / per;
+        const int r = (int)(e % per);
+        int s = 0;
+        if (r < n && !(status != nullptr && status[b] != 0)) {
+            const double d = L[(size_t)b * n * n + (size_t)r * n + r];
+            if (d > 0.0 && isfinite(d)) s = ilogb(d);
+        }
+        bal[e] = s;
+    }
+}
+
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// Forward, step k: the panel solve and the trailing update.  Workspace: row
+// slices of the panel, their exponents, the inverse of the diagonal tile and
+// its slices, the balancing exponents.
+// ---------------------------------------------------------------------------
 size_t ozaki_workspace_bytes(int64_t batch, int n) {
-    const int64_t nt = (n + kT - 1) / kT;
-    return (size_t)batch * nt * kBlockElems * sizeof(__nv_bfloat16) +
-           (size_t)batch * nt * kT * sizeof(int32_t);
+    Carve c{0};
+    fwd_layout(c, batch, n);
+    return (size_t)c.p;
+}
+
+cudaError_t ozaki_panel_solve(double* L, void* work, int32_t* status, int64_t batch, int n,
+                              int k, cudaStream_t stream) {
+    const int nt = tiles_of(n);
+    const int m = nt - k - 1;
+    if (m <= 0) return cudaSuccess;
+    const FwdWs w = fwd_ws(work, batch, n);
+    const size_t stride = (size_t)nt * kBlockElems, estride = (size_t)nt * kT;
+    const size_t bstride = (size_t)nt * kT;
+    // G^-1 of the (full) diagonal tile, and the balancing exponents of its rows
+    cudaError_t e = launch_tri_inverse(L, w.iv.inv, w.iv.bal, status, batch, n, k * kT, kT, stream);
+    if (e != cudaSuccess) return e;
+    // L_Ik <- L_Ik G^-T: A = the panel's rows (reduction over the tile's
+    // columns, divided by the balancing factors), B = rows of G^-1 (multiplied)
+    e = launch_slice_rows(L, w.rs, w.ers, status, batch, n, (k + 1) * kT, m * kT, k * kT, false,
+                          stride, estride, Bal{w.iv.bal, bstride, 0, -1}, stream);
+    if (e != cudaSuccess) return e;
+    e = launch_slice_rows(w.iv.inv, w.iv.sl, w.iv.ex, status, batch, kT, 0, kT, 0, false,
+                          kBlockElems, kT, Bal{w.iv.bal, bstride, k * kT, 1}, stream);
+    if (e != cudaSuccess) return e;
+    OzArgs g{L, w.rs, w.ers, w.iv.sl, w.iv.ex, stride, estride, kBlockElems, kT, status, status,
+             batch, n, nt, k, 1, nullptr};
+    return launch_oz<OZ_ASSIGN>(g, (unsigned)(2 * m), stream);
 }
 
 cudaError_t ozaki_trailing_update(double* L, void* work, int32_t* status, int64_t batch, int n,
                                   int k, cudaStream_t stream) {
-    const int nt = (n + kT - 1) / kT;
+    const int nt = tiles_of(n);
     const int m = nt - k - 1;
     if (m <= 0) return cudaSuccess;
-    __nv_bfloat16* ws = static_cast<__nv_bfloat16*>(work);
-    int32_t* ex = reinterpret_cast<int32_t*>(ws + (size_t)batch * nt * kBlockElems);
-    const unsigned gy = (unsigned)std::min<int64_t>(batch, 65535);
-    {
-        const int rows = m * kT;  // rows (k + 1) * 128 .. nt * 128
-        const unsigned blocks = (unsigned)((rows * 32 + 255) / 256);
-        slice_kernel<<<dim3(blocks, gy), 256, 0, stream>>>(L, ws, ex, status, batch, n, nt,
-                                                           k * kT, (k + 1) * kT);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
-    static std::atomic<uint64_t> smem_set{0};
-    cudaError_t e = allow_smem_once(trail_kernel, kTrailSmem, smem_set);
+    const FwdWs w = fwd_ws(work, batch, n);
+    const size_t stride = (size_t)nt * kBlockElems, estride = (size_t)nt * kT;
+    cudaError_t e = launch_slice_rows(L, w.rs, w.ers, status, batch, n, (k + 1) * kT, m * kT,
+                                      k * kT, false, stride, estride, Bal{nullptr, 0, 0, 0},
+                                      stream);
     if (e != cudaSuccess) return e;
-    const unsigned jobs = (unsigned)(m * (m + 1) / 2 * 2);
-    trail_kernel<<<dim3(jobs, gy), 128, kTrailSmem, stream>>>(L, ws, ex, status, batch, n, nt, k,
-                                                              kMbarPolls);
+    OzArgs g{L, w.rs, w.ers, w.rs, w.ers, stride, estride, stride, estride, status, status,
+             batch, n, nt, k, 1, nullptr};
+    return launch_oz<OZ_FWD_TRAIL>(g, (unsigned)(m * (m + 1)), stream);
+}
+
+// ---------------------------------------------------------------------------
+// Adjoint (Murray's blocked reverse sweep, see blocked_adj): the column
+// slices of L and the balancing exponents once, then per tile column J the
+// panel solve and the two contractions.
+// ---------------------------------------------------------------------------
+size_t ozaki_adj_workspace_bytes(int64_t batch, int n) {
+    const AdjWs w = adj_layout(0, batch, n);
+    return reinterpret_cast<uintptr_t>(w.part + part_elems()) + 256;
+}
+
+cudaError_t ozaki_adj_prepare(const double* L, void* work, const int32_t* status, int64_t batch,
+                              int n, cudaStream_t stream) {
+    const int nt = tiles_of(n);
+    const AdjWs w = adj_ws(work, batch, n);
+    const size_t bstride = (size_t)nt * kT;
+    const int64_t total = batch * (int64_t)bstride;
+    diag_exp_kernel<<<(unsigned)std::min<int64_t>((total + 255) / 256,
+                                                  (int64_t)device_sm_count() * 16),
+                      256, 0, stream>>>(L, w.iv.bal, status, batch, n, nt);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // L's rows divided by their balancing factors (the gradient operands are
+    // multiplied by the same ones)
+    return launch_slice_cols(L, w.lc, w.elc, status, batch, n, 0,
+                             (unsigned)(nt * (nt + 1) / 2), true, 0, true, w.lc_stride,
+                             w.elc_stride, Bal{w.iv.bal, bstride, 0, -1}, stream);
+}
+
+cudaError_t ozaki_adj_solve(const double* L, double* W, void* work, const int32_t* status,
+                            int64_t batch, int n, int J, cudaStream_t stream) {
+    const int nt = tiles_of(n);
+    const int m = nt - J - 1;
+    if (m <= 0) return cudaSuccess;
+    const AdjWs w = adj_ws(work, batch, n);
+    // C <- C L_JJ^-1: A = C's rows (reduction over the tile's columns), B =
+    // columns of L_JJ^-1; the inverse scales like C along the reduction, so no
+    // balancing is needed here
+    cudaError_t e = launch_tri_inverse(L, w.iv.inv, w.iv.bal, status, batch, n, J * kT, kT, stream);
+    if (e != cudaSuccess) return e;
+    e = launch_slice_rows(W, w.ch, w.ech, status, batch, n, (J + 1) * kT, m * kT, J * kT, false,
+                          w.ch_stride, w.ech_stride, Bal{nullptr, 0, 0, 0}, stream);
+    if (e != cudaSuccess) return e;
+    e = launch_slice_cols(w.iv.inv, w.iv.sl, w.iv.ex, status, batch, kT, 0, 1, false, 0, false,
+                          kBlockElems, kT, Bal{nullptr, 0, 0, 0}, stream);
+    if (e != cudaSuccess) return e;
+    OzArgs g{W, w.ch, w.ech, w.iv.sl, w.iv.ex, w.ch_stride, w.ech_stride, kBlockElems, kT, status,
+             nullptr, batch, n, nt, J, 1, nullptr};
+    return launch_oz<OZ_ASSIGN>(g, (unsigned)(2 * m), stream);
+}
+
+cudaError_t ozaki_adj_row(const double* L, double* W, void* work, const int32_t* status,
+                          int64_t batch, int n, int J, cudaStream_t stream) {
+    const int nt = tiles_of(n);
+    if (J >= nt - 1) return cudaSuccess;
+    const AdjWs w = adj_ws(work, batch, n);
+    const size_t bstride = (size_t)nt * kT;
+    // C (W's rows below tile J, block column J), sliced by columns per chunk
+    cudaError_t e = launch_slice_cols(W, w.cc, w.ecc, status, batch, n, J + 1,
+                                      (unsigned)(nt - J - 1), false, J, false, w.cc_stride,
+                                      w.ecc_stride, Bal{w.iv.bal, bstride, 0, 1}, stream);
+    if (e != cudaSuccess) return e;
+    const int splits = row_splits(batch, J, nt - J - 1);
+    OzArgs g{W, w.cc, w.ecc, w.lc, w.elc, w.cc_stride, w.ecc_stride, w.lc_stride, w.elc_stride,
+             status, nullptr, batch, n, nt, J, splits, w.part};
+    e = launch_oz<OZ_REV_ROW>(g, (unsigned)(2 * (J + 1) * splits), stream);
+    if (e != cudaSuccess || splits == 1) return e;
+    const int64_t total = batch * (int64_t)(J + 1) * kT * kT;
+    const unsigned blocks = (unsigned)std::min<int64_t>((total + 255) / 256,
+                                                        (int64_t)device_sm_count() * 16);
+    split_reduce_kernel<<<blocks, 256, 0, stream>>>(W, w.part, status, batch, n, J, splits);
     return cudaGetLastError();
+}
+
+cudaError_t ozaki_adj_upd(const double* L, double* W, void* work, const int32_t* status,
+                          int64_t batch, int n, int J, cudaStream_t stream) {
+    const int nt = tiles_of(n);
+    if (J <= 0) return cudaSuccess;
+    const AdjWs w = adj_ws(work, batch, n);
+    const size_t bstride = (size_t)nt * kT;
+    // Chat = [W_JJ + W_JJ^T; C], rows J*128 .., block column J, sliced by rows
+    cudaError_t e = launch_slice_rows(W, w.ch, w.ech, status, batch, n, J * kT, (nt - J) * kT,
+                                      J * kT, true, w.ch_stride, w.ech_stride,
+                                      Bal{w.iv.bal, bstride, 0, 1}, stream);
+    if (e != cudaSuccess) return e;
+    OzArgs g{W, w.ch, w.ech, w.lc, w.elc, w.ch_stride, w.ech_stride, w.lc_stride, w.elc_stride,
+             status, nullptr, batch, n, nt, J, 1, nullptr};
+    return launch_oz<OZ_REV_UPD>(g, (unsigned)(2 * (nt - J) * J), stream);
 }
 
 }  // namespace chol

@@ -131,6 +131,7 @@ template <int THREADS, typename T, typename Idx>
 __device__ int potrf(T* a, int n, Idx at) {
     static_assert(THREADS % 32 == 0, "THREADS is a whole number of warps");
     using R = typename detail::real_of<T>::type;
+    __shared__ R s_inv;
     const int tid = threadIdx.x;
     for (int j = 0; j < n; ++j) {
         const R d = detail::re(a[at(j, j)]);
@@ -138,11 +139,14 @@ __device__ int potrf(T* a, int n, Idx at) {
             __syncthreads();
             return j + 1;
         }
-        const R inv = detail::rsqrt_t(d);  // 1 / l_jj, then products
-        const R ljj = d * inv;
+        // one thread takes 1 / l_jj (the transcendental is the slowest step
+        // of the column's chain and the same for every thread), the others
+        // read it after the barrier
+        if (tid == 0) s_inv = detail::rsqrt_t(d);
         __syncthreads();                     // every thread has read the pivot
+        const R inv = s_inv;
         for (int i = j + 1 + tid; i < n; i += THREADS) a[at(i, j)] = detail::scale(a[at(i, j)], inv);
-        if (tid == 0) a[at(j, j)] = detail::from_real<T>(ljj);
+        if (tid == 0) a[at(j, j)] = detail::from_real<T>(d * inv);
         __syncthreads();
         // trailing update of the lower part, 16 x THREADS/16 threads over (i, c):
         // a_ic -= l_ij conj(l_cj)
@@ -174,8 +178,17 @@ template <int THREADS, typename T, typename Idx>
 __device__ void potrf_adj(const T* l, T* w, int n, Idx at) {
     static_assert(THREADS % 32 == 0, "THREADS is a whole number of warps");
     using R = typename detail::real_of<T>::type;
+    constexpr int kRinv = 128;  // reciprocals of the diagonal kept for tiles up to this order
     __shared__ R red[THREADS / 32];
+    __shared__ R rinv[kRinv];
     const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
+    // 1 / l_jj for every column up front, one division per thread, so no
+    // column's chain waits for one
+    const bool pre = n <= kRinv;
+    if (pre) {
+        for (int j = tid; j < n; j += THREADS) rinv[j] = R(1) / detail::re(l[at(j, j)]);
+        __syncthreads();
+    }
     for (int j = n - 1; j >= 0; --j) {
         // s = Re sum_{i > j} conj(l_ij) w_ij
         R part = R(0);
@@ -184,13 +197,16 @@ __device__ void potrf_adj(const T* l, T* w, int n, Idx at) {
         for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
         if (lane == 0) red[warp] = part;
         __syncthreads();
-        R sum = R(0);
-#pragma unroll
-        for (int k = 0; k < THREADS / 32; ++k) sum += red[k];
-        const R inv = R(1) / detail::re(l[at(j, j)]);
-        // column j: the diagonal (real) from the sum, the rest scaled
+        const R inv = pre ? rinv[j] : R(1) / detail::re(l[at(j, j)]);
+        // column j: the diagonal (real) from the sum (one thread forms it),
+        // the rest scaled
         for (int i = j + 1 + tid; i < n; i += THREADS) w[at(i, j)] = detail::scale(w[at(i, j)], inv);
-        if (tid == 0) w[at(j, j)] = detail::from_real<T>((detail::re(w[at(j, j)]) - sum * inv) * inv);
+        if (tid == 0) {
+            R sum = R(0);
+#pragma unroll
+            for (int k = 0; k < THREADS / 32; ++k) sum += red[k];
+            w[at(j, j)] = detail::from_real<T>((detail::re(w[at(j, j)]) - sum * inv) * inv);
+        }
         __syncthreads();
         // row j left of the diagonal: w_jk -= sum_{i >= j} conj(w_ij) l_ik
         // (two partial sums halve the dependent chain)

@@ -146,13 +146,42 @@ def test_tensor_core_update_wide_dynamic_range():
     d = np.exp2(np.linspace(-40, 40, n))
     As = (d[:, None] * A * d[None, :])[None]
     Lbar = W.tril_normal(1, n, 46, np.float64)
-    L, st, _ = gpu_fwd_adj(As, Lbar, tile=128)
+    L, st, G = gpu_fwd_adj(As, Lbar, tile=128)
     assert int(st[0]) == 0
     L_ref, _ = oracle.potrf(As[0])
     # compare row by row, relative to each row's own scale
     Lr = L[0] / d[:, None]
     Rr = L_ref / d[:, None]
     assert np.max(np.abs(Lr - Rr)) <= 1e-12 * np.max(np.abs(Rr))
+    # the adjoint scales as D^-1 G D^-1 (G of the unscaled problem with
+    # adj_L scaled by D^-1 ... compared entrywise after undoing the scaling)
+    G_ref = oracle.potrf_adj(L_ref, Lbar[0])
+    Gr = np.tril(G[0]) * d[:, None] * d[None, :]
+    Rg = np.tril(G_ref) * d[:, None] * d[None, :]
+    assert np.max(np.abs(Gr - Rg)) <= 1e-10 * np.max(np.abs(Rg))
+
+
+@pytest.mark.parametrize("n", [200, 384])
+def test_tensor_core_adjoint_agrees_with_the_fp64_sweep(n):
+    """float64 with 128-wide tiles: chol_adj takes the adjoint's two large
+    updates on the tensor cores (digit slices), while chol_adj_inplace runs
+    the same reverse sweep on the FP64 pipe; both match the oracle and each
+    other."""
+    import torch
+    from differentiable_cholesky_gb300 import binding
+    A = W.gram_spd(3, n, 47 + n, 1.0, np.float64)
+    Lbar = W.tril_normal(3, n, 48 + n, np.float64)
+    dev = torch.device("cuda:0")
+    Lt, st = binding.chol_fwd(torch.from_numpy(A).to(dev), tile=128)
+    G_tc = binding.chol_adj(Lt, torch.from_numpy(Lbar).to(dev), status=st, tile=128)
+    G_ip = binding.chol_adj_inplace(Lt, torch.from_numpy(Lbar).to(dev), status=st, tile=128)
+    torch.cuda.synchronize()
+    L_ref, _ = oracle.potrf(A)
+    G_ref = oracle.potrf_adj(L_ref, Lbar)
+    g1, g2 = G_tc.cpu().numpy(), G_ip.cpu().numpy()
+    assert max_rel_err(g1, G_ref, lower=True) <= 1e-10
+    assert max_rel_err(g2, G_ref, lower=True) <= 1e-10
+    assert max_rel_err(g1, g2, lower=True) <= 1e-12
 
 
 def test_upper_triangles_ignored_and_untouched():
