@@ -584,7 +584,16 @@ cudaError_t blocked_fwd(const T* A, T* L, int32_t* status, int64_t batch, int n,
         const int kb = std::min(tile, n - k0);
         // small tiles: two warps, so the per-column barriers stay cheap
         const size_t dsm = (size_t)kb * (kb + 1) * sizeof(T);
-        if (kb <= 32)
+        bool on_cluster = false;
+        if constexpr (std::is_same<T, double>::value || std::is_same<T, float>::value) {
+            if (cluster_diag_pays(batch, kb)) {
+                // few matrices: the tile on a cluster of SMs
+                CHOL_TRY(cluster_potrf_diag(L, status, batch, n, k0, kb, stream));
+                on_cluster = true;
+            }
+        }
+        if (on_cluster) {
+        } else if (kb <= 32)
             potrf_diag_kernel<T, 64><<<dim3(1, grid_y(batch)), 64, dsm, stream>>>(L, status, batch,
                                                                                  n, k0, kb);
         else

@@ -1,0 +1,272 @@
+// Diagonal-tile factor of the blocked path on a thread-block cluster, for
+// few matrices (sm_103a).
+//
+// One matrix's diagonal tile (order kb <= 128) is factored by a cluster of
+// C blocks on C SMs instead of one block on one SM.  On GB300 a warp issues
+// at most one FP64 instruction every 64 cycles whatever its active lanes, so
+// a 128-wide tile on one SM is bound by that SM's FP64 rate (about 1.7
+// multiply-adds per cycle) and by the column chain; C SMs share the first.
+//
+// The tile's rows are dealt round-robin: block r of the cluster holds rows
+// i = r, r + C, ... in shared memory.  The factor runs right-looking over
+// 16-column panels (jaxmg docs "Cholesky factorization": the tiled potrf's
+// diagonal factor, panel solve and trailing update, here within one tile),
+// each panel in three steps separated by cluster barriers:
+//   A. every block writes its rows' panel columns into every block's panel
+//      buffer (distributed shared memory);
+//   B. every block factors the panel's 16 x 16 diagonal block from its own
+//      copy (the same arithmetic in every block, so the same result), four
+//      warps sharing the column updates so the chain of reciprocal square
+//      roots is not held up by them;
+//   C. every block solves its own rows of the panel against that block and
+//      hands the results to every block's panel buffer;
+//   D. every block applies the panel to the trailing columns of its rows.
+// Panel buffers alternate between panels, so step A of one panel never
+// overwrites what another block may still read in step D of the previous.
+//
+// The arithmetic is that of the single-block tile factor: pivot d, 1 / l_jj =
+// rsqrt(d), l_jj = d * rsqrt(d), the first pivot that is not > 0 (zero,
+// negative, NaN) is the status; the order of the sums differs, so results
+// agree with the other paths to rounding.  Every barrier is a hardware
+// cluster barrier: no block spins on a flag.
+#include <cooperative_groups.h>
+
+#include <algorithm>
+#include <climits>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace chol {
+
+namespace cg = cooperative_groups;
+
+namespace {
+
+constexpr int kClThreads = 256;
+constexpr int kPW = 16;        // panel width
+constexpr int kPP = kPW + 1;   // pitch of a panel-buffer row
+constexpr int kTileMax = 128;  // largest tile order
+
+template <int C>
+struct ClLayout {
+    static constexpr int R = kTileMax / C;  // rows per block
+    static constexpr int AP = kTileMax;     // pitch of a held row
+    // element offsets (in T) of the shared-memory regions
+    static constexpr int a_off = 0;                          // R x AP held rows
+    static constexpr int pb_off = a_off + R * AP;            // 2 x 128 x kPP panel buffers
+    static constexpr int h_off = pb_off + 2 * kTileMax * kPP;  // kPW x kPP scaled diagonal block
+    static constexpr int col_off = h_off + kPW * kPP;        // 2 x kPW column hand-off
+    static constexpr int rinv_off = col_off + 2 * kPW;       // kPW reciprocals
+    static constexpr int elems = rinv_off + kPW;
+};
+
+template <typename T, int C>
+size_t cl_smem_bytes() {
+    return (size_t)ClLayout<C>::elems * sizeof(T) + 16;
+}
+
+__device__ __forceinline__ float rsqrt_t(float x) { return rsqrtf(x); }
+__device__ __forceinline__ double rsqrt_t(double x) { return rsqrt(x); }
+
+// Rows of the held set at or below row `lo`: t = first .. cnt - 1.
+template <int C>
+__device__ __forceinline__ int first_at_or_below(int rank, int lo) {
+    return lo <= rank ? 0 : (lo - rank + C - 1) / C;
+}
+
+template <typename T, int C>
+__global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kClThreads)
+cl_potrf_kernel(T* __restrict__ L, int32_t* __restrict__ status, int64_t batch, int n, int k0,
+                int kb) {
+    using Lay = ClLayout<C>;
+    constexpr int AP = Lay::AP;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    T* sm = reinterpret_cast<T*>(smem_raw);
+    T* A = sm + Lay::a_off;
+    T* PB = sm + Lay::pb_off;
+    T* H = sm + Lay::h_off;
+    T* colbuf = sm + Lay::col_off;
+    T* rinv = sm + Lay::rinv_off;
+    __shared__ int s_fail;
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = (int)cluster.block_rank();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // rows held by this block: i = rank + C t, t < nrows
+    const int nrows = kb > rank ? (kb - rank + C - 1) / C : 0;
+
+    for (int64_t b = blockIdx.y; b < batch; b += gridDim.y) {
+        // nobody still reads a panel buffer of the previous matrix
+        cluster.sync();
+        if (status != nullptr && status[b] != 0) continue;
+        T* Lb = L + b * (int64_t)n * n;
+        for (int e = tid; e < nrows * AP; e += kClThreads) {
+            const int t = e / AP, j = e % AP, i = rank + C * t;
+            A[t * AP + j] = (j <= i && j < kb) ? Lb[(int64_t)(k0 + i) * n + k0 + j] : T(0);
+        }
+        if (tid == 0) s_fail = INT_MAX;
+        __syncthreads();
+        bool failed = false;
+        const int npanels = (kb + kPW - 1) / kPW;
+        for (int q = 0; q < npanels; ++q) {
+            const int c0 = q * kPW, w = min(kPW, kb - c0);
+            T* pb = PB + (q & 1) * kTileMax * kPP;
+            // A. this block's rows i >= c0, panel columns (zeros past w), to every block
+            {
+                const int t0 = first_at_or_below<C>(rank, c0);
+                const int cnt = (nrows - t0) * kPW;
+                for (int e = tid; e < cnt * C; e += kClThreads) {
+                    const int d = e / cnt, f = e % cnt;
+                    const int t = t0 + f / kPW, k = f % kPW, i = rank + C * t;
+                    const T v = k < w ? A[t * AP + c0 + k] : T(0);
+                    cluster.map_shared_rank(pb, d)[i * kPP + k] = v;
+                }
+            }
+            cluster.sync();
+            // B. the diagonal block (rows c0 .. c0 + 15 of pb), four warps: warp
+            // u holds columns u, u + 4, u + 8, u + 12 of row lane % 16
+            if (warp < 4) {
+                const int r = lane & 15;
+                T a[4];
+#pragma unroll
+                for (int s = 0; s < 4; ++s) a[s] = pb[(c0 + r) * kPP + warp + 4 * s];
+#pragma unroll
+                for (int j = 0; j < kPW; ++j) {
+                    T* cb = colbuf + (j & 1) * kPW;
+                    if (warp == (j & 3)) {
+                        const T d = __shfl_sync(0xffffffffu, a[j >> 2], j);
+                        if (!(d > T(0)) && j < w && lane == 0) atomicMin(&s_fail, j);
+                        const T ri = rsqrt_t(d);
+                        T l = a[j >> 2] * ri;
+                        if (r == j) l = d * ri;
+                        a[j >> 2] = l;
+                        if (lane < 16) cb[r] = l;
+                        if (lane == 0) rinv[j] = j < w ? ri : T(0);
+                    }
+                    asm volatile("bar.sync 1, 128;" ::: "memory");
+                    const T lij = cb[r];
+                    // columns k > j of this warp, the nearest first (it is the
+                    // next pivot's column for one of the warps)
+#pragma unroll
+                    for (int s = 0; s < 4; ++s) {
+                        const int k = warp + 4 * s;
+                        if (k > j) a[s] = fma(-lij, cb[k], a[s]);
+                    }
+                }
+                if (lane < 16) {
+#pragma unroll
+                    for (int s = 0; s < 4; ++s) pb[(c0 + r) * kPP + warp + 4 * s] = a[s];
+                }
+            }
+            __syncthreads();
+            if (s_fail < w) {
+                // the same pivot failed in every block of the cluster
+                if (rank == 0 && tid == 0) status[b] = k0 + c0 + s_fail + 1;
+                failed = true;
+                break;
+            }
+            // the diagonal block's rows scaled by 1 / l_kk (strictly lower part)
+            for (int e = tid; e < kPW * kPW; e += kClThreads) {
+                const int k = e / kPW, m = e % kPW;
+                H[k * kPP + m] = (m < k && k < w) ? pb[(c0 + k) * kPP + m] * rinv[k] : T(0);
+            }
+            // rows of this block inside the diagonal block: their factor rows
+            {
+                const int t0 = first_at_or_below<C>(rank, c0);
+                for (int e = tid; e < (nrows - t0) * kPW; e += kClThreads) {
+                    const int t = t0 + e / kPW, k = e % kPW, i = rank + C * t;
+                    if (i < c0 + w && k <= i - c0) A[t * AP + c0 + k] = pb[i * kPP + k];
+                }
+            }
+            __syncthreads();
+            // C. this block's rows below the diagonal block: x = a L_D^-T, one
+            // half-warp per row, lane k holding x_k
+            {
+                const int t0 = first_at_or_below<C>(rank, c0 + w);
+                const int k = lane & 15;
+                for (int t = t0 + 2 * warp + (lane >> 4); t - (lane >> 4) < nrows;
+                     t += 2 * (kClThreads / 32)) {
+                    const bool live = t < nrows;
+                    const int i = rank + C * t;
+                    T acc = live ? pb[i * kPP + k] * rinv[k] : T(0);
+#pragma unroll
+                    for (int m = 0; m < kPW - 1; ++m) {
+                        const T xm = __shfl_sync(0xffffffffu, acc, m, 16);
+                        if (k > m) acc = fma(-xm, H[k * kPP + m], acc);
+                    }
+                    if (live && k < w) {
+                        A[t * AP + c0 + k] = acc;
+#pragma unroll
+                        for (int d = 0; d < C; ++d) cluster.map_shared_rank(pb, d)[i * kPP + k] = acc;
+                    }
+                }
+            }
+            cluster.sync();
+            // D. trailing update of this block's rows: a_ij -= x_i . x_j for
+            // c0 + w <= j <= i
+            {
+                const int lo = c0 + w;
+                const int t0 = first_at_or_below<C>(rank, lo);
+                // flattened (t, j) pairs; row t has i - lo + 1 of them
+                int total = 0;
+                for (int t = t0; t < nrows; ++t) total += rank + C * t - lo + 1;
+                for (int e = tid; e < total; e += kClThreads) {
+                    int t = t0, rem = e;
+                    while (rem > rank + C * t - lo) {
+                        rem -= rank + C * t - lo + 1;
+                        ++t;
+                    }
+                    const int i = rank + C * t, j = lo + rem;
+                    const T* xi = pb + i * kPP;
+                    const T* xj = pb + j * kPP;
+                    T acc = A[t * AP + j];
+#pragma unroll
+                    for (int k = 0; k < kPW; ++k) acc = fma(-xi[k], xj[k], acc);
+                    A[t * AP + j] = acc;
+                }
+            }
+            __syncthreads();
+        }
+        if (failed) continue;
+        for (int e = tid; e < nrows * AP; e += kClThreads) {
+            const int t = e / AP, j = e % AP, i = rank + C * t;
+            if (j <= i) Lb[(int64_t)(k0 + i) * n + k0 + j] = A[t * AP + j];
+        }
+    }
+    // no block leaves while another may still write into its panel buffers
+    cluster.sync();
+}
+
+template <typename T, int C>
+cudaError_t launch_cl_potrf(T* L, int32_t* status, int64_t batch, int n, int k0, int kb,
+                            cudaStream_t stream) {
+    const size_t smem = cl_smem_bytes<T, C>();
+    static std::atomic<uint64_t> smem_set{0};
+    cudaError_t e = allow_smem_once(cl_potrf_kernel<T, C>, smem, smem_set);
+    if (e != cudaSuccess) return e;
+    const unsigned gy = (unsigned)std::min<int64_t>(batch, 65535);
+    cl_potrf_kernel<T, C><<<dim3(C, gy), kClThreads, smem, stream>>>(L, status, batch, n, k0, kb);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool cluster_diag_pays(int64_t batch, int kb) {
+    // one cluster of 8 SMs per matrix while the clusters leave most SMs idle
+    return kb > 32 && kb <= kTileMax && batch * 8 <= device_sm_count();
+}
+
+template <typename T>
+cudaError_t cluster_potrf_diag(T* L, int32_t* status, int64_t batch, int n, int k0, int kb,
+                               cudaStream_t stream) {
+    if (kb <= 0 || kb > kTileMax) return cudaErrorInvalidValue;
+    return launch_cl_potrf<T, 8>(L, status, batch, n, k0, kb, stream);
+}
+
+template cudaError_t cluster_potrf_diag<float>(float*, int32_t*, int64_t, int, int, int,
+                                               cudaStream_t);
+template cudaError_t cluster_potrf_diag<double>(double*, int32_t*, int64_t, int, int, int,
+                                                cudaStream_t);
+
+}  // namespace chol

@@ -77,6 +77,15 @@ cudaError_t blocked_fwd(const T* A, T* L, int32_t* status, int64_t batch, int n,
 // element type is float64.
 size_t blocked_fwd_workspace_bytes(bool real_double, int64_t batch, int n, int tile);
 
+// Diagonal-tile factor of the blocked forward on a cluster of 8 blocks
+// (8 SMs) per matrix: the tile L[k0 .. k0+kb, k0 .. k0+kb] (kb <= 128,
+// lower part) factored in place, status[b] = k0 + the failing column + 1.
+// cluster_diag_pays: few enough matrices that the clusters leave SMs idle.
+bool cluster_diag_pays(int64_t batch, int kb);
+template <typename T>
+cudaError_t cluster_potrf_diag(T* L, int32_t* status, int64_t batch, int n, int k0, int kb,
+                               cudaStream_t stream);
+
 // Trailing update of step k of the float64 blocked forward with 128-wide
 // tiles on the bf16 tensor cores (exact digit-slice products): for every
 // lower tile (I, J), I >= J > k, L_IJ -= L_Ik L_Jk^T.  `work` holds

@@ -728,8 +728,8 @@ struct Carve {
     }
 };
 
-// The inverse of a diagonal tile and what slices it (per batch entry: one
-// 128 x 128 float64 matrix, one operand block and its exponents), and the
+// Inverses of diagonal tiles and what slices them (per batch entry: `count`
+// 128 x 128 float64 matrices, operand blocks and their exponents), and the
 // balancing exponents of every row (nt * 128 per batch entry).
 struct InvWs {
     double* inv;
@@ -739,11 +739,11 @@ struct InvWs {
 };
 
 template <typename C>
-InvWs carve_inv(C& c, int64_t batch, int nt) {
+InvWs carve_inv(C& c, int64_t batch, int nt, int count) {
     InvWs w;
-    w.inv = c.template take<double>((size_t)batch * kT * kT);
-    w.sl = c.template take<bf16>((size_t)batch * kBlockElems);
-    w.ex = c.template take<int32_t>((size_t)batch * kT);
+    w.inv = c.template take<double>((size_t)batch * count * kT * kT);
+    w.sl = c.template take<bf16>((size_t)batch * count * kBlockElems);
+    w.ex = c.template take<int32_t>((size_t)batch * count * kT);
     w.bal = c.template take<int32_t>((size_t)batch * nt * kT);
     return w;
 }
@@ -761,7 +761,7 @@ FwdWs fwd_layout(Carve& c, int64_t batch, int n) {
     FwdWs w;
     w.rs = c.take<bf16>((size_t)batch * nt * kBlockElems);
     w.ers = c.take<int32_t>((size_t)batch * nt * kT);
-    w.iv = carve_inv(c, batch, nt);
+    w.iv = carve_inv(c, batch, nt, 1);
     return w;
 }
 
@@ -772,8 +772,8 @@ FwdWs fwd_ws(void* work, int64_t batch, int n) {
 
 // Adjoint workspace, per batch entry: column slices of L (all (c, K <= c)),
 // column slices of C (one block per chunk), row slices of Chat (one block per
-// row block), their exponents, the inverse parts, and the partial sums of the
-// split reduction.
+// row block), their exponents, the inverses of the diagonal tiles and their
+// slices, and the partial sums of the split reduction.
 struct AdjWs {
     bf16 *lc, *cc, *ch;
     int32_t *elc, *ecc, *ech;
@@ -781,6 +781,10 @@ struct AdjWs {
     double* part;  // partial sums of split reductions (part_elems())
     size_t lc_stride, cc_stride, ch_stride, elc_stride, ecc_stride, ech_stride;
 };
+
+// The adjoint inverts every diagonal tile with rows below it (0 .. nt - 2) up
+// front, since L is fixed: one launch instead of one per tile column.
+inline int adj_inverses(int nt) { return nt > 1 ? nt - 1 : 1; }
 
 AdjWs adj_layout(uintptr_t base, int64_t batch, int n) {
     const size_t nt = tiles_of(n), ntri = nt * (nt + 1) / 2;
@@ -798,7 +802,7 @@ AdjWs adj_layout(uintptr_t base, int64_t batch, int n) {
     w.elc = c.take<int32_t>(batch * w.elc_stride);
     w.ecc = c.take<int32_t>(batch * w.ecc_stride);
     w.ech = c.take<int32_t>(batch * w.ech_stride);
-    w.iv = carve_inv(c, batch, (int)nt);
+    w.iv = carve_inv(c, batch, (int)nt, adj_inverses((int)nt));
     w.part = c.take<double>(part_elems());
     return w;
 }
@@ -808,72 +812,110 @@ AdjWs adj_ws(void* work, int64_t batch, int n) {
 }
 
 // ---------------------------------------------------------------------------
-// Inverse of the diagonal tile G = L[k0 .. k0+kb, k0 .. k0+kb] (lower,
-// kb <= 128): X = G^-1, column by column, X_cc = 1 / g_cc and
-// X_ic = -(sum_{c <= m < i} g_im X_mc) / g_ii for i > c, one warp per column
-// (the lanes split each sum).  X is written as a 128 x 128 matrix (zeros
-// above the diagonal and beyond kb).  Block 0 also writes the balancing
+// Inverses of diagonal tiles G = L[k0 .. k0+kb, k0 .. k0+kb] (lower,
+// kb <= 128), X = G^-1, tiles k = tile0 + blockIdx.z.  Column c of X solves
+// G x = e_c by forward substitution in its right-looking (column) form on
+// the rows scaled by 1 / g_ii: with H_im = g_im / g_ii and x_c = 1 / g_cc,
+// x_m is final at step m and every row i > m takes acc_i -= H_im x_m, the lane
+// owning row m handing x_m to the others by a shuffle.  The dependent chain
+// per row is one shuffle and one fused multiply-add.  One warp per column at
+// a time: an FP64 instruction occupies an SM sub-partition's FP64 unit for
+// its whole warp, so columns spread over warps (and, for few matrices, over
+// blocks) rather than rows over more lanes.  X is written as a 128 x 128
+// matrix (zeros above the diagonal and beyond kb; all zeros for a matrix
+// whose status is set).  With bal, block x = 0 also writes the balancing
 // exponents ilogb(g_ii) of the tile's rows to bal[k0 + i].
 // ---------------------------------------------------------------------------
-constexpr int kInvCols = 1;  // columns (warps) per block: one, so the FP64 work spreads over SMs
-constexpr size_t kInvSmem = ((size_t)kT * (kT + 1) + kT + (size_t)kInvCols * kT) * sizeof(double);
+constexpr size_t kInvSmem = ((size_t)kT * (kT + 1) + kT) * sizeof(double);
 
-__global__ void __launch_bounds__(kInvCols * 32)
+template <int WARPS>
+__global__ void __launch_bounds__(WARPS * 32)
 tri_inverse_kernel(const double* __restrict__ L, double* __restrict__ Inv,
                    int32_t* __restrict__ bal, const int32_t* __restrict__ status, int64_t batch,
-                   int n, int nt, int k0, int kb) {
+                   int n, int nt, int tile0) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     constexpr int P = kT + 1;
-    double* G = reinterpret_cast<double*>(smem_raw);  // kb x kb, pitch P
-    double* rinv = G + (size_t)kT * P;                // 1 / g_ii
-    double* X = rinv + kT;                            // kInvCols columns of 128
+    constexpr int Q = kT / 32;                        // rows per lane
+    double* H = reinterpret_cast<double*>(smem_raw);  // kb x kb, pitch P
+    double* rinv = H + (size_t)kT * P;                // 1 / g_ii
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int c = blockIdx.x * kInvCols + warp;
+    const int k0 = (tile0 + (int)blockIdx.z) * kT;
+    const int kb = min(kT, n - k0);
+    // columns of this warp: blockIdx.x + gridDim.x * (warp + WARPS * t)
+    const int cstep = (int)gridDim.x * WARPS;
+    const int cfirst = (int)blockIdx.x + (int)gridDim.x * warp;
     for (int64_t b = blockIdx.y; b < batch; b += gridDim.y) {
-        if (status != nullptr && status[b] != 0) continue;
+        double* Ib = Inv + ((size_t)b * gridDim.z + blockIdx.z) * kT * kT;
+        if (status != nullptr && status[b] != 0) {
+            for (int c = cfirst; c < kT; c += cstep)
+                for (int i = lane; i < kT; i += 32) Ib[(size_t)i * kT + c] = 0.0;
+            continue;
+        }
         const double* Lb = L + (size_t)b * n * n;
         __syncthreads();
-        for (int e = threadIdx.x; e < kb * kb; e += blockDim.x) {
-            const int i = e / kb, j = e % kb;
-            G[i * P + j] = j <= i ? Lb[(size_t)(k0 + i) * n + k0 + j] : 0.0;
-        }
-        __syncthreads();
         for (int i = threadIdx.x; i < kb; i += blockDim.x) {
-            const double d = G[i * P + i];
+            const double d = Lb[(size_t)(k0 + i) * n + k0 + i];
             rinv[i] = 1.0 / d;
-            if (blockIdx.x == 0)
+            if (bal != nullptr && blockIdx.x == 0)
                 bal[b * (size_t)nt * kT + k0 + i] = (d > 0.0 && isfinite(d)) ? ilogb(d) : 0;
         }
         __syncthreads();
-        double* x = X + warp * kT;
-        if (c < kb) {
-            if (lane == 0) x[c] = rinv[c];
-            __syncwarp();
-            for (int i = c + 1; i < kb; ++i) {
-                double part = 0.0;
-                for (int m = c + lane; m < i; m += 32) part = fma(G[i * P + m], x[m], part);
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-                if (lane == 0) x[i] = -part * rinv[i];
-                __syncwarp();
-            }
+        for (int e = threadIdx.x; e < kb * kT; e += blockDim.x) {
+            const int i = e / kT, j = e % kT;
+            H[i * P + j] = j < i ? Lb[(size_t)(k0 + i) * n + k0 + j] * rinv[i] : 0.0;
         }
-        __syncwarp();
-        if (c < kT) {
-            double* Ib = Inv + (size_t)b * kT * kT;
-            for (int i = lane; i < kT; i += 32)
-                Ib[(size_t)i * kT + c] = (c < kb && i >= c && i < kb) ? x[i] : 0.0;
+        __syncthreads();
+        for (int c = cfirst; c < kT; c += cstep) {
+            // acc[q] holds row lane + 32 q: 1 / g_cc at row c, then the
+            // partial solve, then (from its own step on) the solution
+            double acc[Q];
+#pragma unroll
+            for (int q = 0; q < Q; ++q) acc[q] = (lane + 32 * q == c && c < kb) ? rinv[c] : 0.0;
+            for (int m = c; m < kb - 1; ++m) {
+                const int slot = m >> 5;
+                double v = acc[0];
+#pragma unroll
+                for (int q = 1; q < Q; ++q) v = slot == q ? acc[q] : v;
+                const double xm = __shfl_sync(0xffffffffu, v, m & 31);
+#pragma unroll
+                for (int q = 0; q < Q; ++q) {
+                    if (32 * q + 31 <= m) continue;  // (warp-uniform) no row of this slot is left
+                    const int i = lane + 32 * q;
+                    if (i > m && i < kb) acc[q] = fma(-H[i * P + m], xm, acc[q]);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < Q; ++q) {
+                const int i = lane + 32 * q;
+                Ib[(size_t)i * kT + c] = (c < kb && i >= c && i < kb) ? acc[q] : 0.0;
+            }
         }
     }
 }
 
+// Inverts tiles tile0 .. tile0 + count - 1 of every matrix into
+// Inv[b][t][128][128].  Few matrices: 4-warp blocks, the columns of a tile
+// spread over up to 32 blocks (the dependent chains run side by side on
+// different SMs); many: one 8-warp block per tile.
 cudaError_t launch_tri_inverse(const double* L, double* Inv, int32_t* bal, const int32_t* status,
-                               int64_t batch, int n, int k0, int kb, cudaStream_t stream) {
-    static std::atomic<uint64_t> smem_set{0};
-    cudaError_t e = allow_smem_once(tri_inverse_kernel, kInvSmem, smem_set);
-    if (e != cudaSuccess) return e;
-    tri_inverse_kernel<<<dim3(kT / kInvCols, gy(batch)), kInvCols * 32, kInvSmem, stream>>>(
-        L, Inv, bal, status, batch, n, tiles_of(n), k0, kb);
+                               int64_t batch, int n, int tile0, int count, cudaStream_t stream) {
+    const int64_t tiles = batch * count;
+    int gx = 1;
+    while (gx < 32 && tiles * gx * 2 <= device_sm_count()) gx *= 2;
+    const dim3 grid((unsigned)gx, gy(batch), (unsigned)count);
+    if (gx > 1) {
+        static std::atomic<uint64_t> smem_set{0};
+        cudaError_t e = allow_smem_once(tri_inverse_kernel<4>, kInvSmem, smem_set);
+        if (e != cudaSuccess) return e;
+        tri_inverse_kernel<4><<<grid, 128, kInvSmem, stream>>>(L, Inv, bal, status, batch, n,
+                                                              tiles_of(n), tile0);
+    } else {
+        static std::atomic<uint64_t> smem_set{0};
+        cudaError_t e = allow_smem_once(tri_inverse_kernel<8>, kInvSmem, smem_set);
+        if (e != cudaSuccess) return e;
+        tri_inverse_kernel<8><<<grid, 256, kInvSmem, stream>>>(L, Inv, bal, status, batch, n,
+                                                              tiles_of(n), tile0);
+    }
     return cudaGetLastError();
 }
 
@@ -918,7 +960,7 @@ cudaError_t ozaki_panel_solve(double* L, void* work, int32_t* status, int64_t ba
     const size_t stride = (size_t)nt * kBlockElems, estride = (size_t)nt * kT;
     const size_t bstride = (size_t)nt * kT;
     // G^-1 of the (full) diagonal tile, and the balancing exponents of its rows
-    cudaError_t e = launch_tri_inverse(L, w.iv.inv, w.iv.bal, status, batch, n, k * kT, kT, stream);
+    cudaError_t e = launch_tri_inverse(L, w.iv.inv, w.iv.bal, status, batch, n, k, 1, stream);
     if (e != cudaSuccess) return e;
     // L_Ik <- L_Ik G^-T: A = the panel's rows (reduction over the tile's
     // columns, divided by the balancing factors), B = rows of G^-1 (multiplied)
@@ -972,9 +1014,18 @@ cudaError_t ozaki_adj_prepare(const double* L, void* work, const int32_t* status
     if (e != cudaSuccess) return e;
     // L's rows divided by their balancing factors (the gradient operands are
     // multiplied by the same ones)
-    return launch_slice_cols(L, w.lc, w.elc, status, batch, n, 0,
-                             (unsigned)(nt * (nt + 1) / 2), true, 0, true, w.lc_stride,
-                             w.elc_stride, Bal{w.iv.bal, bstride, 0, -1}, stream);
+    e = launch_slice_cols(L, w.lc, w.elc, status, batch, n, 0, (unsigned)(nt * (nt + 1) / 2),
+                          true, 0, true, w.lc_stride, w.elc_stride,
+                          Bal{w.iv.bal, bstride, 0, -1}, stream);
+    if (e != cudaSuccess || nt < 2) return e;
+    // L_JJ^-1 for every tile column J with rows below it, and its column
+    // slices (the inverses, batch * (nt - 1) matrices of order 128, are
+    // zeros for a matrix whose status is set)
+    const int cnt = adj_inverses(nt);
+    e = launch_tri_inverse(L, w.iv.inv, nullptr, status, batch, n, 0, cnt, stream);
+    if (e != cudaSuccess) return e;
+    return launch_slice_cols(w.iv.inv, w.iv.sl, w.iv.ex, nullptr, batch * cnt, kT, 0, 1, false, 0,
+                             false, kBlockElems, kT, Bal{nullptr, 0, 0, 0}, stream);
 }
 
 cudaError_t ozaki_adj_solve(const double* L, double* W, void* work, const int32_t* status,
@@ -984,18 +1035,16 @@ cudaError_t ozaki_adj_solve(const double* L, double* W, void* work, const int32_
     if (m <= 0) return cudaSuccess;
     const AdjWs w = adj_ws(work, batch, n);
     // C <- C L_JJ^-1: A = C's rows (reduction over the tile's columns), B =
-    // columns of L_JJ^-1; the inverse scales like C along the reduction, so no
-    // balancing is needed here
-    cudaError_t e = launch_tri_inverse(L, w.iv.inv, w.iv.bal, status, batch, n, J * kT, kT, stream);
+    // columns of L_JJ^-1 (sliced up front); the inverse scales like C along
+    // the reduction, so no balancing is needed here
+    cudaError_t e = launch_slice_rows(W, w.ch, w.ech, status, batch, n, (J + 1) * kT, m * kT,
+                                      J * kT, false, w.ch_stride, w.ech_stride,
+                                      Bal{nullptr, 0, 0, 0}, stream);
     if (e != cudaSuccess) return e;
-    e = launch_slice_rows(W, w.ch, w.ech, status, batch, n, (J + 1) * kT, m * kT, J * kT, false,
-                          w.ch_stride, w.ech_stride, Bal{nullptr, 0, 0, 0}, stream);
-    if (e != cudaSuccess) return e;
-    e = launch_slice_cols(w.iv.inv, w.iv.sl, w.iv.ex, status, batch, kT, 0, 1, false, 0, false,
-                          kBlockElems, kT, Bal{nullptr, 0, 0, 0}, stream);
-    if (e != cudaSuccess) return e;
-    OzArgs g{W, w.ch, w.ech, w.iv.sl, w.iv.ex, w.ch_stride, w.ech_stride, kBlockElems, kT, status,
-             nullptr, batch, n, nt, J, 1, nullptr};
+    const size_t cnt = (size_t)adj_inverses(nt);
+    OzArgs g{W, w.ch, w.ech, w.iv.sl + (size_t)J * kBlockElems, w.iv.ex + (size_t)J * kT,
+             w.ch_stride, w.ech_stride, cnt * kBlockElems, cnt * kT, status, nullptr, batch, n,
+             nt, J, 1, nullptr};
     return launch_oz<OZ_ASSIGN>(g, (unsigned)(2 * m), stream);
 }
 

@@ -388,6 +388,18 @@ struct AdjCfg {
     // They are read into registers when they are few, else as used.
     static constexpr bool RV = NT * sizeof(T) <= 64;
     static constexpr int per_group = group_stride<T, LPG>(LSIZE + NT * RP);
+    // Murray's reverse sweep instead of the literal P / Phi / two solves:
+    // n^3 / 3 multiply-adds, the column of W being retired handed to the
+    // group by shuffles (or, when the group spans warps, shared memory) once
+    // per column instead of rows of L read by broadcast for every step; the
+    // gradient is the same up to rounding (pinned against the literal
+    // oracle).  Used where a lane owns two columns and the group fits in a
+    // warp (order <= 32 for float, <= 16 for double).  With one column per
+    // lane the owner's serial diagonal sum and scaling sit on the critical
+    // path of every column (batched 8192 x 64x64 float: 0.27 ms literal,
+    // 0.92 ms swept through shared memory), so those orders keep the literal
+    // form.
+    static constexpr bool SWEEP = CPL == 2 && LPG <= 32 && NT * CPL * 2 * sizeof(T) <= 512;
     static constexpr size_t bytes = (size_t)G * per_group * sizeof(T);
 };
 
@@ -552,6 +564,72 @@ small_potrf_adj_kernel(const T* __restrict__ Lg, const T* Lbar, T* Abar,
 #pragma unroll
         for (int k = 0; k < NT; ++k) c[q][k] = R[k * RP + col[q]];
 
+    constexpr bool kSweep = S::SWEEP;
+    if constexpr (kSweep) {
+        // Murray's unblocked reverse sweep, column-per-lane (see AdjCfg::SWEEP):
+        // c[q] holds column col[q] of W = tril(adj_L), l[q] the same column of L.
+        T l[CPL][NT];
+#pragma unroll
+        for (int q = 0; q < CPL; ++q)
+#pragma unroll
+            for (int i = 0; i < NT; ++i) l[q][i] = i >= col[q] ? Ls[lrow_off<T>(i) + col[q]] : T(0);
+        lanes_sync<LPG>(g);  // rinv visible to the group; every lane is done with R's columns
+        static_for<0, NT>([&](auto jc) {
+            constexpr int j = NT - 1 - decltype(jc)::value;
+            // the lane that owns column j, and which of its columns it is
+            constexpr int qo = (CPL == 2 && j >= LPG) ? 1 : 0;
+            constexpr int towner = (CPL == 2 && j >= LPG) ? NT - 1 - j : j;
+            const bool own = t == towner;
+            const T rj = rinv(j);
+            if (own) {
+                // the diagonal from s = sum_{i > j} l_ij w_ij, the column scaled
+                T s0 = T(0), s1 = T(0);
+                static_for<j + 1, NT>([&](auto ic) {
+                    constexpr int i = decltype(ic)::value;
+                    if constexpr ((i - j) & 1) s0 = fma(l[qo][i], c[qo][i], s0);
+                    else s1 = fma(l[qo][i], c[qo][i], s1);
+                });
+                static_for<j + 1, NT>([&](auto ic) {
+                    constexpr int i = decltype(ic)::value;
+                    c[qo][i] *= rj;
+                });
+                c[qo][j] = (c[qo][j] - (s0 + s1) * rj) * rj;
+            }
+            // column j of W (rows i >= j) to the group; lanes whose columns lie
+            // left of j take  w_jk -= sum_{i >= j} w_ij l_ik  and
+            // w_ik -= w_ij l_jk (i > j)
+            T acc[CPL];
+#pragma unroll
+            for (int q = 0; q < CPL; ++q) acc[q] = T(0);
+            static_for<j, NT>([&](auto ic) {
+                constexpr int i = decltype(ic)::value;
+                const T v = __shfl_sync(0xffffffffu, c[qo][i], towner, LPG);
+#pragma unroll
+                for (int q = 0; q < CPL; ++q) {
+                    if (col[q] < j) {
+                        acc[q] = fma(v, l[q][i], acc[q]);
+                        if constexpr (i > j) c[q][i] = fma(-v, l[q][j], c[q][i]);
+                    }
+                }
+            });
+#pragma unroll
+            for (int q = 0; q < CPL; ++q)
+                if (col[q] < j) c[q][j] -= acc[q];
+            if (own) c[qo][j] *= T(0.5);
+        });
+        // the columns of the gradient through R, so rows come back out
+        lanes_sync<LPG>(g);
+#pragma unroll
+        for (int q = 0; q < CPL; ++q)
+#pragma unroll
+            for (int i = 0; i < NT; ++i) R[i * RP + col[q]] = c[q][i];
+        lanes_sync<LPG>(g);
+        if constexpr (!FULL) {
+#pragma unroll
+            for (int q = 0; q < CPL; ++q) load_row<T, NT>(R + col[q] * RP, c[q]);
+        }
+    } else {
+
     // 1. columns of P = L^T tril(adj_L), in place: slot k is finished once
     //    row k of L has been applied, so it can take p_k's first term.
     static_for<0, NT>([&](auto kc) {
@@ -664,15 +742,19 @@ small_potrf_adj_kernel(const T* __restrict__ Lg, const T* Lbar, T* Abar,
 #pragma unroll
         for (int k = 0; k < NT; ++k) c[q][k] = fma(T(below(k, colf)), R[k * RP + col[q]], c[q][k]);
     }
-
     if constexpr (FULL) {
-        // rows col[q] of the result through R once more, then out as chunks
-        // added to adj_A's; chunks wholly above the diagonal are not touched,
-        // and a chunk that straddles it is written element by element
+        // rows col[q] of the result through R once more
         lanes_sync<LPG>(g);  // every lane is done with R's columns
 #pragma unroll
         for (int q = 0; q < CPL; ++q) store_row<T, NT>(R + col[q] * RP, c[q]);
         lanes_sync<LPG>(g);
+    }
+    }  // literal form
+
+    if constexpr (FULL) {
+        // the result's rows (in R) out as chunks added to adj_A's; chunks
+        // wholly above the diagonal are not touched, and a chunk that
+        // straddles it is written element by element
         if (!in_batch || (accumulate && !active)) return;
         V* Am = reinterpret_cast<V*>(Abar + (size_t)b * NT * NT) + t;
         // keep the adj_A loads here: hoisted into the solves they hold

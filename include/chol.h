@@ -89,7 +89,11 @@ enum {
  * n <= 64 runs one fused register/shared-memory kernel per batch; larger n
  * runs the blocked right-looking algorithm (diagonal-tile factor, panel
  * triangular solve, trailing update) with the default tile: 128 for
- * n >= 2048, else 64 when batch * ceil(n/64)^2 >= 608, else 32.
+ * n >= 2048, else 64 when batch * ceil(n/64)^2 >= 4 * (SMs of the device),
+ * else 32 (complex double: at most 64).  float64 with 128-wide tiles runs
+ * the panel solve and the trailing update on the tensor cores (exact digit
+ * products); it takes a workspace of about 224 KB per 128 rows per matrix
+ * with cudaMallocAsync/cudaFreeAsync on `stream` (CHOL_ENOMEM on failure).
  */
 CHOL_API int chol_fwd(int64_t batch, int32_t n, int32_t dtype, const void* A, void* L,
              int32_t* status, void* stream);
@@ -120,7 +124,10 @@ CHOL_API int chol_fwd_ex(int64_t batch, int32_t n, int32_t dtype, const void* A,
  * The gradient of torch.linalg.cholesky (a symmetric matrix G) relates to this
  * one by adj_A = tril(G + G^T) - diag(G).
  * n > 64 needs batch * n * n elements of device workspace, taken with
- * cudaMallocAsync/cudaFreeAsync on `stream` (CHOL_ENOMEM on failure).
+ * cudaMallocAsync/cudaFreeAsync on `stream` (CHOL_ENOMEM on failure);
+ * float64 with 128-wide tiles also takes the operand slices of its
+ * tensor-core updates (about 224 KB per 128 x 128 block of L's lower
+ * triangle, plus a few tens of MB).
  */
 CHOL_API int chol_adj(int64_t batch, int32_t n, int32_t dtype, const void* L, const void* adj_L,
              void* adj_A, const int32_t* status, void* stream);
@@ -135,8 +142,10 @@ CHOL_API int chol_adj_ex(int64_t batch, int32_t n, int32_t dtype, const void* L,
  * memory pool, hosts that forbid device allocation after start-up, plug-ins
  * whose host application owns every allocation).  It has no counterpart in the
  * pages: it exists for those callers only.
- *   Same arguments, results and error codes as chol_adj_ex, but it calls no
- *   allocator: for n > 64 the blocked path's workspace is a fixed 16 MiB
+ *   Same arguments and error codes as chol_adj_ex, and the same results
+ *   except for float64 with 128-wide tiles and n > 128, where chol_adj_ex
+ *   takes its tensor-core updates and this call keeps the FMA-pipe ones
+ *   (the two agree to about 1e-12 relative).  It calls no allocator: for n > 64 the blocked path's workspace is a fixed 16 MiB
  *   scratch array inside the library (held by every GPU that loads the library
  *   until the process exits), so batch * n * n * element size must be at most
  *   16 MiB, else CHOL_ENOMEM and nothing is enqueued.  n <= 64 needs no
@@ -184,7 +193,10 @@ CHOL_API int chol_fwd_inplace(int64_t batch, int32_t n, int32_t dtype, void* A, 
  *   tile    as chol_adj_ex.  No workspace is taken for any n: the blocked
  *           reverse sweep runs on `adj` itself (it never touches the upper
  *           triangle), so the call allocates nothing.
- * Results are bit-identical to chol_adj_ex into a zeroed adj_A.
+ * Results are bit-identical to chol_adj_ex into a zeroed adj_A, except for
+ * float64 with 128-wide tiles and n > 128, where chol_adj_ex takes its
+ * tensor-core updates and this call keeps the FMA-pipe ones (no workspace);
+ * there the two agree to about 1e-12 relative.
  */
 CHOL_API int chol_adj_inplace(int64_t batch, int32_t n, int32_t dtype, const void* L, void* adj,
                               const int32_t* status, int32_t tile, void* stream);

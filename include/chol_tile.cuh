@@ -120,15 +120,19 @@ template <typename R> __device__ __forceinline__ cplx<R> shfl_xor(cplx<R> x, int
 }
 }  // namespace detail
 
-/*
- * potrf -- in place, a = chol(a), lower: the right-looking column recurrence
- * (jaxmg docs "Cholesky factorization": the lower factor and a status).
- * Returns 0, or j + 1 for the first column j whose pivot is not > 0 (zero,
- * negative or NaN), the same value in every thread; the tile from column j on
- * is then unspecified.
- */
+namespace detail {
+
+// Element (i, j) of the diagonal sub-tile that starts at (o, o).
+template <typename Idx>
+struct Shift {
+    Idx at;
+    int o;
+    __device__ __forceinline__ int operator()(int i, int j) const { return at(o + i, o + j); }
+};
+
+// The column recurrence of potrf (below), one column per step.
 template <int THREADS, typename T, typename Idx>
-__device__ int potrf(T* a, int n, Idx at) {
+__device__ int potrf_columns(T* a, int n, Idx at) {
     static_assert(THREADS % 32 == 0, "THREADS is a whole number of warps");
     using R = typename detail::real_of<T>::type;
     __shared__ R s_inv;
@@ -161,21 +165,9 @@ __device__ int potrf(T* a, int n, Idx at) {
     return 0;
 }
 
-/*
- * potrf_adj -- Murray's (2016) unblocked reverse sweep, in place on w:
- * l is the factor from potrf (read only); on entry w holds the gradient of
- * the loss with respect to l's lower entries, on return the gradient with
- * respect to the lower entries a_ij (i >= j) that potrf read.  That is
- * Phi(M + M^T) with M = l^-T Phi(l^T w) l^-1, Phi keeping the lower triangle
- * and halving the diagonal (warp issue #1316's closing comment), reached
- * column by column from j = n - 1 down to 0 in n^3 / 3 multiply-adds.
- * Complex elements: w holds dLoss/dRe + i dLoss/dIm of a real loss; on
- * return the entries below the diagonal hold M_ij + conj(M_ji) and the
- * diagonal Re(M_ii) (imaginary part 0), with M = l^-H Phi(l^H w) l^-1; the
- * sweep reads only the real part of w's diagonal.
- */
+// The unblocked reverse sweep of potrf_adj (below), one column per step.
 template <int THREADS, typename T, typename Idx>
-__device__ void potrf_adj(const T* l, T* w, int n, Idx at) {
+__device__ void potrf_adj_columns(const T* l, T* w, int n, Idx at) {
     static_assert(THREADS % 32 == 0, "THREADS is a whole number of warps");
     using R = typename detail::real_of<T>::type;
     constexpr int kRinv = 128;  // reciprocals of the diagonal kept for tiles up to this order
@@ -232,6 +224,190 @@ __device__ void potrf_adj(const T* l, T* w, int n, Idx at) {
         //  it reads w_jj)
     }
     __syncthreads();
+}
+
+constexpr int kSub = 32;  // sub-tile of the blocked forms
+
+// Right-looking blocked factor for larger tiles: per 32-column sub-tile the
+// column recurrence on the diagonal sub-tile, a panel solve of the rows below
+// (one thread per row, the row in registers) and the trailing update of the
+// lower part; the two bulk steps keep every warp busy between barriers.
+template <int THREADS, typename T, typename Idx>
+__device__ int potrf_blocked(T* a, int n, Idx at) {
+    using R = typename real_of<T>::type;
+    __shared__ R rinv[kSub];
+    const int tid = threadIdx.x;
+    for (int q0 = 0; q0 < n; q0 += kSub) {
+        const int m = min(kSub, n - q0);
+        const int st = potrf_columns<THREADS>(a, m, Shift<Idx>{at, q0});
+        if (st != 0) return q0 + st;  // the same in every thread
+        const int r0 = q0 + m;
+        if (r0 >= n) break;
+        for (int c = tid; c < m; c += THREADS) rinv[c] = R(1) / re(a[at(q0 + c, q0 + c)]);
+        __syncthreads();
+        // rows below: x L_S^H = a_r (forward substitution), L_S the sub-tile's
+        // factor (rows below exist only under a full sub-tile: m == kSub)
+        for (int r = r0 + tid; r < n; r += THREADS) {
+            T x[kSub];
+#pragma unroll
+            for (int c = 0; c < kSub; ++c) {
+                T s = a[at(r, q0 + c)];
+#pragma unroll
+                for (int k = 0; k < c; ++k) s = msub(x[k], conj(a[at(q0 + c, q0 + k)]), s);
+                x[c] = scale(s, rinv[c]);
+            }
+#pragma unroll
+            for (int c = 0; c < kSub; ++c) a[at(r, q0 + c)] = x[c];
+        }
+        __syncthreads();
+        // trailing lower part: a_rc -= sum_k l_rk conj(l_ck), r >= c >= r0
+        const int ty = tid / 16, tx = tid % 16;
+        for (int r = r0 + ty; r < n; r += THREADS / 16) {
+            for (int c = r0 + tx; c <= r; c += 16) {
+                T s0 = zero<T>(), s1 = zero<T>();
+                int k = 0;
+                for (; k + 1 < m; k += 2) {
+                    s0 = madd(a[at(r, q0 + k)], conj(a[at(c, q0 + k)]), s0);
+                    s1 = madd(a[at(r, q0 + k + 1)], conj(a[at(c, q0 + k + 1)]), s1);
+                }
+                if (k < m) s0 = madd(a[at(r, q0 + k)], conj(a[at(c, q0 + k)]), s0);
+                a[at(r, c)] = sub(a[at(r, c)], add(s0, s1));
+            }
+        }
+        __syncthreads();
+    }
+    return 0;
+}
+
+// Murray's blocked reverse sweep over 32-column sub-tiles, the same steps as
+// the library's blocked adjoint inside one tile: for sub-tile columns J from
+// the last, with C the rows of w below the sub-tile:
+//   C <- C L_JJ^-1; w_JK -= C^H L_{below, K} (K <= J); w_IK -= C L_JK
+//   (I > J, K < J); the column sweep of w_JJ; w_JK -= (w_JJ + w_JJ^H) L_JK.
+template <int THREADS, typename T, typename Idx>
+__device__ void potrf_adj_blocked(const T* l, T* w, int n, Idx at) {
+    using R = typename real_of<T>::type;
+    __shared__ R rinv[kSub];
+    const int tid = threadIdx.x;
+    const int nb = (n + kSub - 1) / kSub;
+    for (int jb = nb - 1; jb >= 0; --jb) {
+        const int j0 = jb * kSub, m = min(kSub, n - j0), r0 = j0 + m;
+        for (int c = tid; c < m; c += THREADS) rinv[c] = R(1) / re(l[at(j0 + c, j0 + c)]);
+        __syncthreads();
+        // C <- C L_JJ^-1, one row per thread: m_c = (c_c - sum_{k>c} m_k l_kc) / l_cc
+        // (rows below exist only under a full sub-tile: m == kSub)
+        for (int r = r0 + tid; r < n; r += THREADS) {
+            T x[kSub];
+#pragma unroll
+            for (int c = 0; c < kSub; ++c) x[c] = w[at(r, j0 + c)];
+#pragma unroll
+            for (int cc = 0; cc < kSub; ++cc) {
+                const int c = kSub - 1 - cc;
+                T s = x[c];
+#pragma unroll
+                for (int k = c + 1; k < kSub; ++k) s = msub(x[k], l[at(j0 + k, j0 + c)], s);
+                x[c] = scale(s, rinv[c]);
+            }
+#pragma unroll
+            for (int c = 0; c < kSub; ++c) w[at(r, j0 + c)] = x[c];
+        }
+        __syncthreads();
+        // w_JK -= C^H L_{below, K} for columns b < j0 + m (lower part inside
+        // the sub-tile), and w_IK -= C L_JK for rows r >= r0, columns b < j0:
+        // the two touch different entries and only read C, so they share a phase
+        const int wb = j0 + m;
+        const int n_row = m * wb;
+        const int n_upd = (n - r0) * j0;
+        for (int t = tid; t < n_row + n_upd; t += THREADS) {
+            if (t < n_row) {
+                const int a = t / wb, b = t % wb;
+                if (b > j0 + a) continue;
+                T s0 = zero<T>(), s1 = zero<T>();
+                int r = r0;
+                for (; r + 1 < n; r += 2) {
+                    s0 = madd(conj(w[at(r, j0 + a)]), l[at(r, b)], s0);
+                    s1 = madd(conj(w[at(r + 1, j0 + a)]), l[at(r + 1, b)], s1);
+                }
+                if (r < n) s0 = madd(conj(w[at(r, j0 + a)]), l[at(r, b)], s0);
+                w[at(j0 + a, b)] = sub(w[at(j0 + a, b)], add(s0, s1));
+            } else {
+                const int u = t - n_row;
+                const int r = r0 + u / j0, b = u % j0;
+                T s0 = zero<T>(), s1 = zero<T>();
+                int c = 0;
+                for (; c + 1 < m; c += 2) {
+                    s0 = madd(w[at(r, j0 + c)], l[at(j0 + c, b)], s0);
+                    s1 = madd(w[at(r, j0 + c + 1)], l[at(j0 + c + 1, b)], s1);
+                }
+                if (c < m) s0 = madd(w[at(r, j0 + c)], l[at(j0 + c, b)], s0);
+                w[at(r, b)] = sub(w[at(r, b)], add(s0, s1));
+            }
+        }
+        __syncthreads();
+        // the diagonal sub-tile's own sweep
+        potrf_adj_columns<THREADS>(l, w, m, Shift<Idx>{at, j0});
+        // w_JK -= (w_JJ + w_JJ^H) L_JK, K < J: the lower part of w_JJ, mirrored
+        // (conjugated) above the diagonal, doubled on it
+        for (int t = tid; t < m * j0; t += THREADS) {
+            const int a = t / j0, b = t % j0;
+            T s = zero<T>();
+            for (int c = 0; c < m; ++c) {
+                T x;
+                if (c < a) {
+                    x = w[at(j0 + a, j0 + c)];
+                } else if (c > a) {
+                    x = conj(w[at(j0 + c, j0 + a)]);
+                } else {
+                    x = w[at(j0 + a, j0 + a)];
+                    x = add(x, x);
+                }
+                s = madd(x, l[at(j0 + c, b)], s);
+            }
+            w[at(j0 + a, b)] = sub(w[at(j0 + a, b)], s);
+        }
+        __syncthreads();
+    }
+}
+
+}  // namespace detail
+
+/*
+ * potrf -- in place, a = chol(a), lower: the right-looking column recurrence
+ * (jaxmg docs "Cholesky factorization": the lower factor and a status), in
+ * 32-column blocks for n > 64.  Returns 0, or j + 1 for the first column j
+ * whose pivot is not > 0 (zero, negative or NaN), the same value in every
+ * thread; the tile from column j on is then unspecified.
+ */
+template <int THREADS, typename T, typename Idx>
+__device__ int potrf(T* a, int n, Idx at) {
+    static_assert(THREADS % 32 == 0, "THREADS is a whole number of warps");
+    if (n > 64) return detail::potrf_blocked<THREADS>(a, n, at);
+    return detail::potrf_columns<THREADS>(a, n, at);
+}
+
+/*
+ * potrf_adj -- Murray's (2016) unblocked reverse sweep, in place on w:
+ * l is the factor from potrf (read only); on entry w holds the gradient of
+ * the loss with respect to l's lower entries, on return the gradient with
+ * respect to the lower entries a_ij (i >= j) that potrf read.  That is
+ * Phi(M + M^T) with M = l^-T Phi(l^T w) l^-1, Phi keeping the lower triangle
+ * and halving the diagonal (warp issue #1316's closing comment), reached
+ * column by column from j = n - 1 down to 0 in n^3 / 3 multiply-adds (for
+ * n > 64 in 32-column blocks, the same steps as the library's blocked
+ * adjoint, so that the bulk of the work runs between few barriers).
+ * Complex elements: w holds dLoss/dRe + i dLoss/dIm of a real loss; on
+ * return the entries below the diagonal hold M_ij + conj(M_ji) and the
+ * diagonal Re(M_ii) (imaginary part 0), with M = l^-H Phi(l^H w) l^-1; the
+ * sweep reads only the real part of w's diagonal.
+ */
+template <int THREADS, typename T, typename Idx>
+__device__ void potrf_adj(const T* l, T* w, int n, Idx at) {
+    static_assert(THREADS % 32 == 0, "THREADS is a whole number of warps");
+    if (n > 64) {
+        detail::potrf_adj_blocked<THREADS>(l, w, n, at);
+        return;
+    }
+    detail::potrf_adj_columns<THREADS>(l, w, n, at);
 }
 
 }  // namespace chol_tile
