@@ -670,10 +670,15 @@ cudaError_t blocked_adj(const T* L, const T* Lbar, T* Abar, const int32_t* statu
                     CHOL_TRY(ozaki_adj_solve(L, W, oz_work, status, batch, n, J, stream));
                     CHOL_TRY(ozaki_adj_row(L, W, oz_work, status, batch, n, J, stream));
                 }
-                const size_t dsm = (size_t)kb * (kb + 1) * sizeof(T);
-                diag_rev_kernel<T, kThreads><<<dim3(1, grid_y(batch)), kThreads, dsm, stream>>>(
-                    L, W, status, batch, n, j0, kb);
-                CHOL_TRY(cudaGetLastError());
+                if (ozaki_adj_lit_pays(batch)) {
+                    // few matrices: the tile's adjoint as three parallel products
+                    CHOL_TRY(ozaki_adj_diag(L, W, oz_work, status, batch, n, J, stream));
+                } else {
+                    const size_t dsm = (size_t)kb * (kb + 1) * sizeof(T);
+                    diag_rev_kernel<T, kThreads><<<dim3(1, grid_y(batch)), kThreads, dsm,
+                                                   stream>>>(L, W, status, batch, n, j0, kb);
+                    CHOL_TRY(cudaGetLastError());
+                }
                 // W_IK -= C_I L_JK (I > J) and W_JK -= (W_JJ + W_JJ^T) L_JK, K < J
                 CHOL_TRY(ozaki_adj_upd(L, W, oz_work, status, batch, n, J, stream));
                 continue;

@@ -110,6 +110,13 @@ cudaError_t ozaki_adj_solve(const double* L, double* W, void* work, const int32_
                             int64_t batch, int n, int J, cudaStream_t stream);
 cudaError_t ozaki_adj_row(const double* L, double* W, void* work, const int32_t* status,
                           int64_t batch, int n, int J, cudaStream_t stream);
+// Adjoint of diagonal tile J by the literal formula Phi(M + M^T),
+// M = X^T Phi(L_JJ^T W_JJ) X with X = L_JJ^-1 from ozaki_adj_prepare, in
+// place on W_JJ (three products, no column chain).  ozaki_adj_lit_pays: few
+// enough matrices that this beats the one-block reverse sweep.
+bool ozaki_adj_lit_pays(int64_t batch);
+cudaError_t ozaki_adj_diag(const double* L, double* W, void* work, const int32_t* status,
+                           int64_t batch, int n, int J, cudaStream_t stream);
 cudaError_t ozaki_adj_upd(const double* L, double* W, void* work, const int32_t* status,
                           int64_t batch, int n, int J, cudaStream_t stream);
 // `work` holds batch * n * n elements of scratch.  accumulate as small_adj.

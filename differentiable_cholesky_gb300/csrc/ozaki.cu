@@ -782,9 +782,10 @@ struct AdjWs {
     size_t lc_stride, cc_stride, ch_stride, elc_stride, ecc_stride, ech_stride;
 };
 
-// The adjoint inverts every diagonal tile with rows below it (0 .. nt - 2) up
-// front, since L is fixed: one launch instead of one per tile column.
-inline int adj_inverses(int nt) { return nt > 1 ? nt - 1 : 1; }
+// The adjoint inverts every diagonal tile up front, since L is fixed: one
+// launch instead of one per tile column.  The inverses serve the panel solves
+// (tiles 0 .. nt - 2) and the literal diagonal-tile adjoint (every tile).
+inline int adj_inverses(int nt) { return nt; }
 
 AdjWs adj_layout(uintptr_t base, int64_t batch, int n) {
     const size_t nt = tiles_of(n), ntri = nt * (nt + 1) / 2;
@@ -938,6 +939,99 @@ diag_exp_kernel(const double* __restrict__ L, int32_t* __restrict__ bal,
     }
 }
 
+// ---------------------------------------------------------------------------
+// Adjoint of one diagonal tile by its literal formula (warp issue #1316,
+// closing comment): with G = L_JJ, X = G^-1 (inverted up front) and W_JJ the
+// gradient with respect to G's lower entries,
+//   S = Phi(G^T W_JJ),  T = S X,  M = X^T T,  W_JJ <- Phi(M + M^T),
+// Phi keeping the lower triangle and halving the diagonal.  This is the
+// gradient the reverse sweep reaches column by column, but as three products
+// with no dependent chain: for few matrices the sweep's 128-step chain on one
+// SM costs far more than the formula's 2.5x larger FP64 work spread over
+// 136 blocks.  S, T and every operand are lower triangular, so each sum runs
+// only where both factors can be non-zero.
+//
+// One block per 8 x 8 output block (ba, bb), ba >= bb, of the tile's lower
+// part; 256 threads = 64 outputs x 4 groups that split the reduction index
+// (interleaved) and add their partial sums in a fixed order.  The operand
+// strips the block needs (at most 128 x 8 per operand) are staged in shared
+// memory first.  S and T live in a scratch area of 128 x 128 per matrix.
+// ---------------------------------------------------------------------------
+constexpr int kLB = 8;
+constexpr int kLitThreads = 256;
+enum LitStep { LIT_S = 0, LIT_T = 1, LIT_A = 2 };
+
+template <int STEP>
+__global__ void __launch_bounds__(kLitThreads)
+lit_diag_kernel(const double* __restrict__ L, double* __restrict__ W,
+                const double* __restrict__ X, size_t x_stride, double* __restrict__ S,
+                double* __restrict__ Tm, const int32_t* __restrict__ status, int64_t batch, int n,
+                int j0, int kb) {
+    __shared__ double sA[kT * kLB], sB[kT * kLB], sC[kT * kLB], sD[kT * kLB];
+    __shared__ double red[4][kLB * kLB];
+    int ba, bb;
+    tri_index((int)blockIdx.x, ba, bb);
+    const int tid = threadIdx.x, g = tid >> 6, o = tid & 63, ty = o >> 3, tx = o & 7;
+    const int a = kLB * ba + ty, bcol = kLB * bb + tx;
+    const int a0 = kLB * ba, b0 = kLB * bb;
+    // reduction range [c_lo, c_hi)
+    const int c_lo = STEP == LIT_T ? b0 : a0;
+    const int c_hi = STEP == LIT_T ? min(a0 + kLB, kb) : kb;
+    const int len = c_hi - c_lo;
+    for (int64_t b = blockIdx.y; b < batch; b += gridDim.y) {
+        if (status != nullptr && status[b] != 0) continue;
+        const double* Lb = L + b * (size_t)n * n;
+        double* Wb = W + b * (size_t)n * n;
+        const double* Xb = X + b * x_stride;
+        double* Sb = S + b * (size_t)kT * kT;
+        double* Tb = Tm + b * (size_t)kT * kT;
+        __syncthreads();
+        // strips: element [c'][i] for c = c_lo + c', i < 8
+        for (int e = tid; e < len * kLB; e += kLitThreads) {
+            const int cc = e / kLB, i = e % kLB, c = c_lo + cc;
+            const int ra = a0 + i, rb = b0 + i;
+            if (STEP == LIT_S) {
+                // G_c,a (c >= a) and W_c,b (c >= b), inside the tile
+                sA[e] = (ra < kb && c >= ra) ? Lb[(size_t)(j0 + c) * n + j0 + ra] : 0.0;
+                sB[e] = (rb < kb && c >= rb) ? Wb[(size_t)(j0 + c) * n + j0 + rb] : 0.0;
+            } else if (STEP == LIT_T) {
+                // S_a,c (c <= a) and X_c,b (c >= b)
+                sA[e] = (ra < kb && c <= ra) ? Sb[(size_t)ra * kT + c] : 0.0;
+                sB[e] = (rb < kb && c >= rb) ? Xb[(size_t)c * kT + rb] : 0.0;
+            } else {
+                // X_c,a, T_c,b, X_c,b, T_c,a (all lower: zero for c above)
+                sA[e] = (ra < kb && c >= ra) ? Xb[(size_t)c * kT + ra] : 0.0;
+                sB[e] = (rb < kb && c >= rb) ? Tb[(size_t)c * kT + rb] : 0.0;
+                sC[e] = (rb < kb && c >= rb) ? Xb[(size_t)c * kT + rb] : 0.0;
+                sD[e] = (ra < kb && c >= ra) ? Tb[(size_t)c * kT + ra] : 0.0;
+            }
+        }
+        __syncthreads();
+        double acc = 0.0;
+        if (STEP == LIT_A) {
+            const bool diag = a == bcol;
+            for (int cc = g; cc < len; cc += 4) {
+                acc = fma(sA[cc * kLB + ty], sB[cc * kLB + tx], acc);
+                if (!diag) acc = fma(sC[cc * kLB + tx], sD[cc * kLB + ty], acc);
+            }
+        } else {
+            for (int cc = g; cc < len; cc += 4) acc = fma(sA[cc * kLB + ty], sB[cc * kLB + tx], acc);
+        }
+        red[g][o] = acc;
+        __syncthreads();
+        if (g == 0 && a < kb && bcol < kb) {
+            const double v = (red[0][o] + red[1][o]) + (red[2][o] + red[3][o]);
+            if (STEP == LIT_S) {
+                Sb[(size_t)a * kT + bcol] = a > bcol ? v : (a == bcol ? 0.5 * v : 0.0);
+            } else if (STEP == LIT_T) {
+                Tb[(size_t)a * kT + bcol] = a >= bcol ? v : 0.0;
+            } else if (a >= bcol) {
+                Wb[(size_t)(j0 + a) * n + j0 + bcol] = v;
+            }
+        }
+    }
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -1017,10 +1111,10 @@ cudaError_t ozaki_adj_prepare(const double* L, void* work, const int32_t* status
     e = launch_slice_cols(L, w.lc, w.elc, status, batch, n, 0, (unsigned)(nt * (nt + 1) / 2),
                           true, 0, true, w.lc_stride, w.elc_stride,
                           Bal{w.iv.bal, bstride, 0, -1}, stream);
-    if (e != cudaSuccess || nt < 2) return e;
-    // L_JJ^-1 for every tile column J with rows below it, and its column
-    // slices (the inverses, batch * (nt - 1) matrices of order 128, are
-    // zeros for a matrix whose status is set)
+    if (e != cudaSuccess) return e;
+    // L_JJ^-1 for every tile column J and its column slices (the inverses,
+    // batch * nt matrices of order 128, are zeros for a matrix whose status
+    // is set)
     const int cnt = adj_inverses(nt);
     e = launch_tri_inverse(L, w.iv.inv, nullptr, status, batch, n, 0, cnt, stream);
     if (e != cudaSuccess) return e;
@@ -1085,6 +1179,35 @@ cudaError_t ozaki_adj_upd(const double* L, double* W, void* work, const int32_t*
     OzArgs g{W, w.ch, w.ech, w.lc, w.elc, w.ch_stride, w.ech_stride, w.lc_stride, w.elc_stride,
              status, nullptr, batch, n, nt, J, 1, nullptr};
     return launch_oz<OZ_REV_UPD>(g, (unsigned)(2 * (nt - J) * J), stream);
+}
+
+
+bool ozaki_adj_lit_pays(int64_t batch) {
+    // the literal form's products fill the GPU from one matrix on; its FP64
+    // work is 2.5x the sweep's, which wins once the sweeps alone fill it
+    return batch * 4 <= device_sm_count();
+}
+
+cudaError_t ozaki_adj_diag(const double* L, double* W, void* work, const int32_t* status,
+                           int64_t batch, int n, int J, cudaStream_t stream) {
+    const int nt = tiles_of(n);
+    const AdjWs w = adj_ws(work, batch, n);
+    if ((size_t)2 * batch * kT * kT > part_elems()) return cudaErrorInvalidValue;
+    const int j0 = J * kT, kb = std::min(kT, n - j0);
+    const int nb = (kb + kLB - 1) / kLB;
+    const dim3 grid((unsigned)(nb * (nb + 1) / 2), gy(batch));
+    const size_t cnt = (size_t)adj_inverses(nt);
+    const double* X = w.iv.inv + (size_t)J * kT * kT;
+    const size_t xs = cnt * kT * kT;
+    double* S = w.part;
+    double* T = w.part + (size_t)batch * kT * kT;
+    lit_diag_kernel<LIT_S><<<grid, kLitThreads, 0, stream>>>(L, W, X, xs, S, T, status, batch, n,
+                                                            j0, kb);
+    lit_diag_kernel<LIT_T><<<grid, kLitThreads, 0, stream>>>(L, W, X, xs, S, T, status, batch, n,
+                                                            j0, kb);
+    lit_diag_kernel<LIT_A><<<grid, kLitThreads, 0, stream>>>(L, W, X, xs, S, T, status, batch, n,
+                                                            j0, kb);
+    return cudaGetLastError();
 }
 
 }  // namespace chol

@@ -229,10 +229,11 @@ def test_autograd_wrapper_matches_the_adjoint():
 @pytest.mark.parametrize("dtype", [np.float64, np.float32])
 @pytest.mark.parametrize("n,tile", [(128, 128), (200, 128), (300, 64), (383, 128), (97, 64)])
 def test_cluster_diagonal_factor_matches_the_single_block_factor(n, tile, dtype):
-    """Few matrices factor their diagonal tiles on a cluster of SMs; many
-    matrices on one block each.  The same matrix in a batch of 1 (cluster)
-    and inside a batch of 40 (one block per tile) agrees to rounding, and both
-    match the oracle, ragged last tiles included."""
+    """Few matrices factor their diagonal tiles on a cluster of SMs and (float64,
+    128-wide tiles) take each diagonal tile's adjoint by its literal formula;
+    many matrices use one block per tile and the reverse sweep.  The same
+    matrix in a batch of 1 and inside a batch of 40 agrees to rounding, and
+    both match the oracle, ragged last tiles included."""
     dtype = np.dtype(dtype)
     A1 = W.gram_spd(1, n, 61 + n, 1.0, dtype)
     Lbar1 = W.tril_normal(1, n, 62 + n, dtype)
@@ -242,6 +243,7 @@ def test_cluster_diagonal_factor_matches_the_single_block_factor(n, tile, dtype)
     L40, s40, G40 = check(A40, Lbar40, dtype, tile=tile)
     tol = 1e-13 if dtype == np.float64 else 2e-6
     assert max_rel_err(L1, L40[-1:]) <= tol
+    assert max_rel_err(G1, G40[-1:], lower=True) <= (1e-11 if dtype == np.float64 else 2e-5)
 
 
 @pytest.mark.parametrize("tile", [64, 128])
