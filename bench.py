@@ -92,24 +92,52 @@ def executed_flops(n: int):
     return n ** 3 / 3.0, 2.0 * n ** 3 / 3.0
 
 
-def default_tile(n: int, batch: int, sms: int = 152) -> int:
-    """The library's default blocked tile (mirrors blocked_default_tile) for
-    a device with `sms` multiprocessors."""
+def default_tile(n: int, batch: int, sms: int = 152, float64: bool = False) -> int:
+    """The library's default blocked tile (mirrors pick_tile and
+    blocked_default_tile) for a device with `sms` multiprocessors."""
+    if float64 and n > 128 and batch * 8 <= sms:
+        return 128
     if n >= 2048:
         return 128
     per_side = (n + 63) // 64
     return 64 if batch * per_side * per_side >= 4 * sms else 32
 
 
-def launches_per_step(n: int, tile: int) -> int:
-    """Kernels the library launches for one chol_fwd + chol_adj."""
+def launches_per_step(n: int, tile: int, batch: int = 1, float64: bool = False,
+                      sms: int = 152) -> int:
+    """Kernels the library launches for one chol_fwd + chol_adj (mirrors the
+    dispatch of blocked.cu and ozaki.cu; float64 with 128-wide tiles takes
+    the tensor-core path, with lookahead once there are three tile columns)."""
     if n <= 64:
         return 2
     nt = (n + tile - 1) // tile
-    fwd = 1 + nt + 2 * (nt - 1)              # copy, diagonal factors, panel solves + updates
-    # copy, per tile column: solve, row update, panel update, diagonal sweep,
-    # symmetric update (the first and last columns skip some), accumulate
-    adj = 3 if nt == 1 else 5 * nt - 3
+    tc = float64 and tile == 128
+    tc_fwd = tc and n > 128
+    look = tc_fwd and nt >= 3
+    fwd = 1 + nt                              # copy, diagonal factors
+    for k in range(nt - 1):
+        if tc_fwd:
+            # inverse, 2 slicings, assign; slicing, update (lookahead: column
+            # k + 1, then the rest while there is one)
+            fwd += 4 + 1 + ((1 + (1 if nt - k - 1 >= 2 else 0)) if look else 1)
+        else:
+            fwd += 2                          # panel solve, trailing update
+    if not tc:
+        # copy, per tile column: solve, row update, panel update, diagonal
+        # sweep, symmetric update (the first and last columns skip some), add
+        adj = 3 if nt == 1 else 5 * nt - 3
+        return fwd + adj
+    adj = 1 + 4 + 1                           # copy, prepare (4), add
+    lit = batch * 4 <= sms
+    for J in range(nt):
+        if J < nt - 1:
+            chunks = nt - J - 1
+            tiles = batch * (J + 1)
+            splits = max(1, min((2 * sms + 2 * tiles - 1) // (2 * tiles), chunks))
+            adj += 2 + 2 + (1 if splits > 1 else 0)   # solve; row (+ ordered reduce)
+        adj += 3 if lit else 1                # diagonal tile: literal form or sweep
+        if J > 0:
+            adj += 2                          # update
     return fwd + adj
 
 
@@ -650,7 +678,8 @@ def main():
             tot, f_ms, a_ms, ck = o.timed(steps, 5 if o.n <= 64 else 2, None, sampler)
             rep = o.kernel_report(f_ms, a_ms, hbm_peak, fp64_peak, fp32_peak)
             rep.update({"steps": steps, "step_ms": tot / steps, "clocks": ck,
-                        "tile": (o.tile or default_tile(o.n, o.batch, sms)) if o.n > 64 else None,
+                        "tile": (o.tile or default_tile(o.n, o.batch, sms, o.np_dtype == np.float64))
+                        if o.n > 64 else None,
                         "config": f"{name}: {o.desc}"})
             others[name] = rep
             o.free()
@@ -692,8 +721,9 @@ def main():
         "gflops": value * (fwd_f + adj_f) / 1e9,
         "kernels": main_report,
         "roofline": roofline,
-        "gpu_launches": launches_per_step(n, (tile or default_tile(n, batch, sms)) if n > 64 else 0)
-        * args.steps,
+        "gpu_launches": launches_per_step(
+            n, (tile or default_tile(n, batch, sms, np_dtype == np.float64)) if n > 64 else 0,
+            batch, np_dtype == np.float64, sms) * args.steps,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": args.e2e_steps, "chunks": chunks,
                 "overlap": "chunks on their own streams, consecutive steps on alternate buffer sets: "

@@ -26,6 +26,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <mutex>
 #include <type_traits>
 
 #include "common.cuh"
@@ -45,6 +46,57 @@ using chol_tile::detail::shfl_xor;
 using chol_tile::detail::sub;
 
 constexpr int kThreads = 256;
+
+// ---------------------------------------------------------------------------
+// Lookahead of the float64 tensor-core forward: a second stream per device
+// (and two events) on which the trailing update of step k, minus block column
+// k + 1, runs beside step k + 1's diagonal factor and panel solve.  The
+// caller's stream waits for it before it touches those columns again and
+// before the forward returns, so the caller sees one stream's ordering.  The
+// enqueue sequence of one forward holds the device's lock, so concurrent
+// callers cannot interleave their event records.
+// ---------------------------------------------------------------------------
+struct SideStream {
+    cudaStream_t s = nullptr;
+    cudaEvent_t look = nullptr;  // the caller's stream reached step k's lookahead column
+    cudaEvent_t rest = nullptr;  // the side stream finished step k's remaining columns
+};
+
+SideStream g_side[kMaxDevices];
+std::mutex g_side_lock[kMaxDevices];
+std::atomic<uint64_t> g_side_made{0};
+
+// The device's side stream (created on first use); false if there is none.
+bool side_stream(int& dev, SideStream& out) {
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return false;
+    }
+    const cudaError_t e = once_per_device(g_side_made, [&]() -> cudaError_t {
+        SideStream sd;
+        cudaError_t r = cudaStreamCreateWithFlags(&sd.s, cudaStreamNonBlocking);
+        if (r == cudaSuccess) r = cudaEventCreateWithFlags(&sd.look, cudaEventDisableTiming);
+        if (r == cudaSuccess) r = cudaEventCreateWithFlags(&sd.rest, cudaEventDisableTiming);
+        if (r == cudaSuccess) g_side[dev] = sd;
+        return r;
+    });
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    out = g_side[dev];
+    return true;
+}
+
+// On scope exit: the caller's stream waits for the side stream's last work.
+struct JoinSide {
+    cudaStream_t main;
+    const SideStream* sd;
+    bool pending = false;
+    ~JoinSide() {
+        if (pending) cudaStreamWaitEvent(main, sd->rest, 0);
+    }
+};
 
 template <typename T> using real_t = typename chol_tile::detail::real_of<T>::type;
 
@@ -579,6 +631,23 @@ cudaError_t blocked_fwd(const T* A, T* L, int32_t* status, int64_t batch, int n,
     CHOL_TRY(allow_smem_once(potrf_diag_kernel<T, kThreads>,
                              (size_t)max_tile<T>() * (max_tile<T>() + 1) * sizeof(T),
                              diag_smem_set));
+    // float64, 128-wide tiles, workspace: the tensor-core path, with lookahead
+    // on a side stream when there are at least three tile columns and the
+    // caller's stream is not being captured into a graph
+    const bool oz = std::is_same<T, double>::value && work != nullptr && tile == 128;
+    SideStream sd;
+    int dev = 0;
+    bool look = false;
+    if (oz && nt >= 3) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        const bool idle = cudaStreamIsCapturing(stream, &cs) == cudaSuccess &&
+                          cs == cudaStreamCaptureStatusNone;
+        cudaGetLastError();
+        look = idle && side_stream(dev, sd);
+    }
+    std::unique_lock<std::mutex> side_lock;
+    if (look) side_lock = std::unique_lock<std::mutex>(g_side_lock[dev]);
+    JoinSide join{stream, &sd};
     for (int k = 0; k < nt; ++k) {
         const int k0 = k * tile;
         const int kb = std::min(tile, n - k0);
@@ -602,12 +671,30 @@ cudaError_t blocked_fwd(const T* A, T* L, int32_t* status, int64_t batch, int n,
         CHOL_TRY(cudaGetLastError());
         if (k == nt - 1) break;
         if constexpr (std::is_same<T, double>::value) {
-            if (work != nullptr && tile == 128) {
+            if (oz) {
                 // panel solve and trailing update on the tensor cores
-                CHOL_TRY(ozaki_panel_solve(reinterpret_cast<double*>(L), work, status, batch, n,
-                                           k, stream));
-                CHOL_TRY(ozaki_trailing_update(reinterpret_cast<double*>(L), work, status, batch,
-                                               n, k, stream));
+                double* Ld = reinterpret_cast<double*>(L);
+                CHOL_TRY(ozaki_panel_solve(Ld, work, status, batch, n, k, stream));
+                CHOL_TRY(ozaki_trailing_slice(Ld, work, status, batch, n, k, stream));
+                if (!look) {
+                    CHOL_TRY(ozaki_trailing_gemm(Ld, work, status, batch, n, k, 0, stream));
+                    continue;
+                }
+                // block column k + 1 here (the last step's remaining columns,
+                // which include it, first); the columns right of it on the
+                // side stream, beside the next step's factor and panel solve
+                if (join.pending) {
+                    CHOL_TRY(cudaStreamWaitEvent(stream, sd.rest, 0));
+                    join.pending = false;
+                }
+                CHOL_TRY(ozaki_trailing_gemm(Ld, work, status, batch, n, k, 1, stream));
+                if (nt - k - 1 >= 2) {
+                    CHOL_TRY(cudaEventRecord(sd.look, stream));
+                    CHOL_TRY(cudaStreamWaitEvent(sd.s, sd.look, 0));
+                    CHOL_TRY(ozaki_trailing_gemm(Ld, work, status, batch, n, k, 2, sd.s));
+                    CHOL_TRY(cudaEventRecord(sd.rest, sd.s));
+                    join.pending = true;
+                }
                 continue;
             }
         }

@@ -93,6 +93,14 @@ cudaError_t cluster_potrf_diag(T* L, int32_t* status, int64_t batch, int n, int 
 size_t ozaki_workspace_bytes(int64_t batch, int n);
 cudaError_t ozaki_trailing_update(double* L, void* work, int32_t* status, int64_t batch, int n,
                                   int k, cudaStream_t stream);
+// The same in two parts: slicing the panel's rows, then the products for all
+// trailing tiles (part 0), only block column k + 1 (part 1) or the block
+// columns right of it (part 2).  Step k's slices stay valid until step k + 2
+// slices its panel, so part 2 of step k may run beside step k + 1.
+cudaError_t ozaki_trailing_slice(double* L, void* work, int32_t* status, int64_t batch, int n,
+                                 int k, cudaStream_t stream);
+cudaError_t ozaki_trailing_gemm(double* L, void* work, int32_t* status, int64_t batch, int n,
+                                int k, int part, cudaStream_t stream);
 // The panel solve of step k on the tensor cores: L_Ik <- L_Ik G^-T, I > k,
 // with G^-1 the inverse of the (factored) diagonal tile.
 cudaError_t ozaki_panel_solve(double* L, void* work, int32_t* status, int64_t batch, int n,

@@ -384,6 +384,8 @@ struct OzArgs {
     int n, nt, step;      // step: k (forward) or J (adjoint)
     int splits;           // OZ_REV_ROW: the reduction split over this many CTAs
     double* part;         // ... each writing its partial sum here (splits > 1)
+    int sub;              // OZ_FWD_TRAIL: 0 every trailing tile, 1 only block column
+                          // step + 1, 2 only block columns >= step + 2
 };
 
 struct OzJob {
@@ -401,8 +403,14 @@ __device__ __forceinline__ OzJob oz_job(const OzArgs& g, int job, int& p0, int& 
     const int t = job >> 1;
     if (MODE == OZ_FWD_TRAIL) {
         int i, j;
-        tri_index(t, i, j);
-        const int I = g.step + 1 + i, J = g.step + 1 + j;
+        if (g.sub == 1) {
+            i = t;
+            j = 0;
+        } else {
+            tri_index(t, i, j);
+        }
+        const int off = g.sub == 2 ? 1 : 0;
+        const int I = g.step + 1 + off + i, J = g.step + 1 + off + j;
         o.out_r0 = I * kT;
         o.out_c0 = J * kT + o.h * kN;
         o.lower = I == J;
@@ -748,19 +756,23 @@ InvWs carve_inv(C& c, int64_t batch, int nt, int count) {
     return w;
 }
 
-// Forward workspace: row slices of the panel (nt blocks per batch entry),
-// their exponents, and the inverse parts.
+// Forward workspace: row slices of the panel (nt blocks per batch entry) and
+// their exponents, twice (step k uses set k % 2, so the trailing update of
+// one step may still read its slices while the next step slices its panel),
+// and the inverse parts.
 struct FwdWs {
-    bf16* rs;
-    int32_t* ers;
+    bf16* rs[2];
+    int32_t* ers[2];
     InvWs iv;
 };
 
 FwdWs fwd_layout(Carve& c, int64_t batch, int n) {
     const int nt = tiles_of(n);
     FwdWs w;
-    w.rs = c.take<bf16>((size_t)batch * nt * kBlockElems);
-    w.ers = c.take<int32_t>((size_t)batch * nt * kT);
+    for (int s = 0; s < 2; ++s) {
+        w.rs[s] = c.take<bf16>((size_t)batch * nt * kBlockElems);
+        w.ers[s] = c.take<int32_t>((size_t)batch * nt * kT);
+    }
     w.iv = carve_inv(c, batch, nt, 1);
     return w;
 }
@@ -1058,31 +1070,50 @@ cudaError_t ozaki_panel_solve(double* L, void* work, int32_t* status, int64_t ba
     if (e != cudaSuccess) return e;
     // L_Ik <- L_Ik G^-T: A = the panel's rows (reduction over the tile's
     // columns, divided by the balancing factors), B = rows of G^-1 (multiplied)
-    e = launch_slice_rows(L, w.rs, w.ers, status, batch, n, (k + 1) * kT, m * kT, k * kT, false,
+    bf16* rs = w.rs[k & 1];
+    int32_t* ers = w.ers[k & 1];
+    e = launch_slice_rows(L, rs, ers, status, batch, n, (k + 1) * kT, m * kT, k * kT, false,
                           stride, estride, Bal{w.iv.bal, bstride, 0, -1}, stream);
     if (e != cudaSuccess) return e;
     e = launch_slice_rows(w.iv.inv, w.iv.sl, w.iv.ex, status, batch, kT, 0, kT, 0, false,
                           kBlockElems, kT, Bal{w.iv.bal, bstride, k * kT, 1}, stream);
     if (e != cudaSuccess) return e;
-    OzArgs g{L, w.rs, w.ers, w.iv.sl, w.iv.ex, stride, estride, kBlockElems, kT, status, status,
+    OzArgs g{L, rs, ers, w.iv.sl, w.iv.ex, stride, estride, kBlockElems, kT, status, status,
              batch, n, nt, k, 1, nullptr};
     return launch_oz<OZ_ASSIGN>(g, (unsigned)(2 * m), stream);
 }
 
-cudaError_t ozaki_trailing_update(double* L, void* work, int32_t* status, int64_t batch, int n,
-                                  int k, cudaStream_t stream) {
+cudaError_t ozaki_trailing_slice(double* L, void* work, int32_t* status, int64_t batch, int n,
+                                 int k, cudaStream_t stream) {
     const int nt = tiles_of(n);
     const int m = nt - k - 1;
     if (m <= 0) return cudaSuccess;
     const FwdWs w = fwd_ws(work, batch, n);
     const size_t stride = (size_t)nt * kBlockElems, estride = (size_t)nt * kT;
-    cudaError_t e = launch_slice_rows(L, w.rs, w.ers, status, batch, n, (k + 1) * kT, m * kT,
-                                      k * kT, false, stride, estride, Bal{nullptr, 0, 0, 0},
-                                      stream);
+    return launch_slice_rows(L, w.rs[k & 1], w.ers[k & 1], status, batch, n, (k + 1) * kT,
+                             m * kT, k * kT, false, stride, estride, Bal{nullptr, 0, 0, 0},
+                             stream);
+}
+
+cudaError_t ozaki_trailing_gemm(double* L, void* work, int32_t* status, int64_t batch, int n,
+                                int k, int part, cudaStream_t stream) {
+    const int nt = tiles_of(n);
+    const int m = nt - k - 1;
+    // tiles: all m (m + 1) / 2, the m of block column k + 1, or the rest
+    const int tiles = part == 0 ? m * (m + 1) / 2 : (part == 1 ? m : (m - 1) * m / 2);
+    if (m <= 0 || tiles <= 0) return cudaSuccess;
+    const FwdWs w = fwd_ws(work, batch, n);
+    const size_t stride = (size_t)nt * kBlockElems, estride = (size_t)nt * kT;
+    OzArgs g{L, w.rs[k & 1], w.ers[k & 1], w.rs[k & 1], w.ers[k & 1], stride, estride, stride,
+             estride, status, status, batch, n, nt, k, 1, nullptr, part};
+    return launch_oz<OZ_FWD_TRAIL>(g, (unsigned)(2 * tiles), stream);
+}
+
+cudaError_t ozaki_trailing_update(double* L, void* work, int32_t* status, int64_t batch, int n,
+                                  int k, cudaStream_t stream) {
+    cudaError_t e = ozaki_trailing_slice(L, work, status, batch, n, k, stream);
     if (e != cudaSuccess) return e;
-    OzArgs g{L, w.rs, w.ers, w.rs, w.ers, stride, estride, stride, estride, status, status,
-             batch, n, nt, k, 1, nullptr};
-    return launch_oz<OZ_FWD_TRAIL>(g, (unsigned)(m * (m + 1)), stream);
+    return ozaki_trailing_gemm(L, work, status, batch, n, k, 0, stream);
 }
 
 // ---------------------------------------------------------------------------

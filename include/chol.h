@@ -89,11 +89,18 @@ enum {
  * n <= 64 runs one fused register/shared-memory kernel per batch; larger n
  * runs the blocked right-looking algorithm (diagonal-tile factor, panel
  * triangular solve, trailing update) with the default tile: 128 for
- * n >= 2048, else 64 when batch * ceil(n/64)^2 >= 4 * (SMs of the device),
- * else 32 (complex double: at most 64).  float64 with 128-wide tiles runs
- * the panel solve and the trailing update on the tensor cores (exact digit
- * products); it takes a workspace of about 224 KB per 128 rows per matrix
- * with cudaMallocAsync/cudaFreeAsync on `stream` (CHOL_ENOMEM on failure).
+ * float64 with n > 128 and batch * 8 <= SMs of the device, and for
+ * n >= 2048; else 64 when batch * ceil(n/64)^2 >= 4 * SMs; else 32
+ * (complex double: at most 64).  float64 with 128-wide tiles runs the panel
+ * solve and the trailing update on the tensor cores (exact digit products);
+ * it takes a workspace of about 450 KB per 128 rows per matrix with
+ * cudaMallocAsync/cudaFreeAsync on `stream` (CHOL_ENOMEM on failure).  With
+ * at least three tile columns and `stream` not being captured, part of each
+ * trailing update runs on a second stream of the library's, beside the next
+ * diagonal factor; `stream` waits for it before the call's work ends, so the
+ * call is ordered on `stream` like any other.  For batch * 8 <= SMs the
+ * diagonal tiles (orders 33 .. 128, float and double) are factored by a
+ * thread-block cluster of 8 SMs per matrix.
  */
 CHOL_API int chol_fwd(int64_t batch, int32_t n, int32_t dtype, const void* A, void* L,
              int32_t* status, void* stream);
@@ -127,7 +134,11 @@ CHOL_API int chol_fwd_ex(int64_t batch, int32_t n, int32_t dtype, const void* A,
  * cudaMallocAsync/cudaFreeAsync on `stream` (CHOL_ENOMEM on failure);
  * float64 with 128-wide tiles also takes the operand slices of its
  * tensor-core updates (about 224 KB per 128 x 128 block of L's lower
- * triangle, plus a few tens of MB).
+ * triangle), the inverses of the diagonal tiles and their slices (about
+ * 350 KB per tile), plus a few tens of MB.  For batch * 4 <= SMs each
+ * diagonal tile's own adjoint is then taken by its literal formula above
+ * (three parallel products with the tile's inverse) instead of the serial
+ * reverse sweep; the two agree to rounding.  The default tile is chol_fwd's.
  */
 CHOL_API int chol_adj(int64_t batch, int32_t n, int32_t dtype, const void* L, const void* adj_L,
              void* adj_A, const int32_t* status, void* stream);

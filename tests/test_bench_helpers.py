@@ -21,14 +21,27 @@ def test_lower_sector_bytes_and_algorithmic_bytes():
 
 def test_launch_counts():
     assert bench.launches_per_step(16, 0) == 2
-    # nt = 4: forward 1 + 4 + 6, adjoint 5 * 4 - 3
-    assert bench.launches_per_step(512, 128) == 11 + 17
+    # FMA-pipe tiles, nt = 4: forward 1 + 4 + 6, adjoint 5 * 4 - 3
+    assert bench.launches_per_step(512, 128, 1, False) == 11 + 17
     assert bench.launches_per_step(100, 128) == 1 + 1 + 0 + 3
+    # float64, 128-wide tiles, one 8192 x 8192 matrix: 1081 kernels per step
+    # without the lookahead's 62 extra launches (an ncu launch list of one
+    # step counted 1081 before the lookahead was added)
+    assert bench.launches_per_step(8192, 128, 1, True) == 1081 + 62
+    # many matrices: no literal diagonal adjoint, no split reduction
+    nt = 4
+    fwd = 1 + nt + 3 * 6 + 2 * 1          # lookahead: 2 extra launches (k = 0, 1)
+    adj = 6 + 3 * 4 + nt * 1 + 3 * 2
+    assert bench.launches_per_step(512, 128, 256, True) == fwd + adj
 
 
 def test_default_tile_mirrors_the_library_rule():
     assert bench.default_tile(8192, 1) == 128
     assert bench.default_tile(512, 1) == 32
+    assert bench.default_tile(512, 1, 152, True) == 128
+    assert bench.default_tile(128, 1, 152, True) == 32
+    assert bench.default_tile(512, 19, 152, True) == 128
+    assert bench.default_tile(512, 20, 152, True) == 64
     assert bench.default_tile(512, 256) == 64
 
 
