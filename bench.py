@@ -137,7 +137,9 @@ def launches_per_step(n: int, tile: int, batch: int = 1, float64: bool = False,
             adj += 2 + 2 + (1 if splits > 1 else 0)   # solve; row (+ ordered reduce)
         adj += 3 if lit else 1                # diagonal tile: literal form or sweep
         if J > 0:
-            adj += 2                          # update
+            # update: slicing, products (lookahead: block column J - 1, then
+            # the rest while there is one)
+            adj += 2 + (1 if look and J >= 2 else 0)
     return fwd + adj
 
 

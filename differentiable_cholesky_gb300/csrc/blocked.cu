@@ -749,6 +749,22 @@ cudaError_t blocked_adj(const T* L, const T* Lbar, T* Abar, const int32_t* statu
         oz = oz_work != nullptr && tile == 128;
         if (oz) CHOL_TRY(ozaki_adj_prepare(L, oz_work, status, batch, n, stream));
     }
+    // lookahead (as in the forward): tile column J's update of block column
+    // J - 1 here, its update of the columns left of that on the side stream,
+    // beside tile column J - 1's solve, row update and diagonal tile
+    SideStream sd;
+    int dev = 0;
+    bool look = false;
+    if (oz && nt >= 3) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        const bool idle = cudaStreamIsCapturing(stream, &cs) == cudaSuccess &&
+                          cs == cudaStreamCaptureStatusNone;
+        cudaGetLastError();
+        look = idle && side_stream(dev, sd);
+    }
+    std::unique_lock<std::mutex> side_lock;
+    if (look) side_lock = std::unique_lock<std::mutex>(g_side_lock[dev]);
+    JoinSide join{stream, &sd};
     for (int J = nt - 1; J >= 0; --J) {
         const int j0 = J * tile, kb = std::min(tile, n - j0), r0 = j0 + kb, nb = n - r0;
         if constexpr (std::is_same<T, double>::value) {
@@ -767,7 +783,25 @@ cudaError_t blocked_adj(const T* L, const T* Lbar, T* Abar, const int32_t* statu
                     CHOL_TRY(cudaGetLastError());
                 }
                 // W_IK -= C_I L_JK (I > J) and W_JK -= (W_JJ + W_JJ^T) L_JK, K < J
-                CHOL_TRY(ozaki_adj_upd(L, W, oz_work, status, batch, n, J, stream));
+                if (J == 0) continue;
+                double* Wd = reinterpret_cast<double*>(W);
+                CHOL_TRY(ozaki_adj_upd_slice(Wd, oz_work, status, batch, n, J, stream));
+                if (!look) {
+                    CHOL_TRY(ozaki_adj_upd_gemm(Wd, oz_work, status, batch, n, J, 0, stream));
+                    continue;
+                }
+                if (join.pending) {
+                    CHOL_TRY(cudaStreamWaitEvent(stream, sd.rest, 0));
+                    join.pending = false;
+                }
+                CHOL_TRY(ozaki_adj_upd_gemm(Wd, oz_work, status, batch, n, J, 1, stream));
+                if (J >= 2) {
+                    CHOL_TRY(cudaEventRecord(sd.look, stream));
+                    CHOL_TRY(cudaStreamWaitEvent(sd.s, sd.look, 0));
+                    CHOL_TRY(ozaki_adj_upd_gemm(Wd, oz_work, status, batch, n, J, 2, sd.s));
+                    CHOL_TRY(cudaEventRecord(sd.rest, sd.s));
+                    join.pending = true;
+                }
                 continue;
             }
         }
@@ -793,6 +827,11 @@ cudaError_t blocked_adj(const T* L, const T* Lbar, T* Abar, const int32_t* statu
             GemmArgs<T> g{W, L, W, status, batch, n, tile, nt, J, 0, 0};
             CHOL_TRY((launch_gemm<T, GEMM_REV_SYM>(g, J, stream)));
         }
+    }
+    // the side stream's last update lands before W is read below
+    if (join.pending) {
+        CHOL_TRY(cudaStreamWaitEvent(stream, sd.rest, 0));
+        join.pending = false;
     }
     if (in_place) {
         if (status != nullptr)

@@ -127,6 +127,14 @@ cudaError_t ozaki_adj_diag(const double* L, double* W, void* work, const int32_t
                            int64_t batch, int n, int J, cudaStream_t stream);
 cudaError_t ozaki_adj_upd(const double* L, double* W, void* work, const int32_t* status,
                           int64_t batch, int n, int J, cudaStream_t stream);
+// The same in two parts: slicing Chat, then the products for every K < J
+// (part 0), only K = J - 1 (part 1) or only K < J - 1 (part 2).  Tile column
+// J's slices stay valid until tile column J - 2 slices its own, so part 2 of
+// J may run beside the solve, row update and diagonal tile of J - 1.
+cudaError_t ozaki_adj_upd_slice(double* W, void* work, const int32_t* status, int64_t batch,
+                                int n, int J, cudaStream_t stream);
+cudaError_t ozaki_adj_upd_gemm(double* W, void* work, const int32_t* status, int64_t batch,
+                               int n, int J, int part, cudaStream_t stream);
 // `work` holds batch * n * n elements of scratch.  accumulate as small_adj.
 // Not accumulating with adj_A == adj_L (in place), the sweep runs on adj_A
 // itself and `work` is not used (may be null).  `oz_work` (may be null) holds

@@ -62,6 +62,9 @@ constexpr int kStages = 2;
 constexpr int kTmemCols = 512;               // 7 accumulators x 64 columns, rounded up
 constexpr size_t kGemmSmem = 128 + (size_t)kStages * kStageBytes + 128;
 constexpr int32_t kNonFinite = INT_MIN;      // exponent sentinel of a non-finite vector
+constexpr int kEC = 8;                       // output columns per epilogue pass
+constexpr int kEpP = kEC + 1;                // pitch (doubles) of the epilogue's staged rows
+constexpr int kEpR = 32 / kEC;               // rows per warp-wide access of a pass
 
 using bf16 = __nv_bfloat16;
 
@@ -78,10 +81,15 @@ __device__ __forceinline__ int block_offset(int m, int k, int p) {
 }
 
 // 2^E as a double for E in the normal range, 0 below it and +Inf above.
-__device__ __forceinline__ double pow2(int E) {
-    if (E < -1022) return 0.0;
-    if (E > 1023) return __longlong_as_double(0x7ff0000000000000LL);
-    return __longlong_as_double((long long)(E + 1023) << 52);
+// v * 2^E for an integer |v| <= 2^62: one int64 -> float64 conversion, then
+// the exponent moved by an integer add where the result stays normal (|v| in
+// [1, 2^62], so the new exponent lies in [E, E + 62]); ldexp otherwise.
+__device__ __forceinline__ double scale_int(long long v, int E) {
+    if (v == 0) return 0.0;
+    const double vd = __ll2double_rn(v);
+    if (E >= -1022 && E <= 1023 - 62)
+        return __longlong_as_double(__double_as_longlong(vd) + ((long long)E << 52));
+    return ldexp(vd, E);
 }
 
 // Scale exponent of the 128-long vector a warp holds four values per lane:
@@ -331,15 +339,12 @@ __device__ __forceinline__ void tc_fence_after() {
 }
 
 // 16 consecutive fp32 columns of this warp's 32 TMEM lanes.
-__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&v)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-        "%14,%15}, [%16];"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
-          "=r"(v[14]), "=r"(v[15])
-        : "r"(taddr)
-        : "memory");
+__device__ __forceinline__ void tc_ld8(uint32_t taddr, uint32_t (&v)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
+                   "=r"(v[6]), "=r"(v[7])
+                 : "r"(taddr)
+                 : "memory");
 }
 __device__ __forceinline__ void tc_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
@@ -385,7 +390,8 @@ struct OzArgs {
     int splits;           // OZ_REV_ROW: the reduction split over this many CTAs
     double* part;         // ... each writing its partial sum here (splits > 1)
     int sub;              // OZ_FWD_TRAIL: 0 every trailing tile, 1 only block column
-                          // step + 1, 2 only block columns >= step + 2
+                          // step + 1, 2 only block columns >= step + 2; OZ_REV_UPD:
+                          // 0 every K < J, 1 only K = J - 1, 2 only K < J - 1
 };
 
 struct OzJob {
@@ -441,7 +447,9 @@ __device__ __forceinline__ OzJob oz_job(const OzArgs& g, int job, int& p0, int& 
         p1 = 0;
     } else {
         const int J = g.step;
-        const int I = J + t / J, K = t % J;  // I >= J, K < J
+        // I >= J and K < J; or only K = J - 1 (sub 1); or only K < J - 1 (sub 2)
+        const int kw = g.sub == 0 ? J : (g.sub == 1 ? 1 : J - 1);
+        const int I = J + t / kw, K = t % kw + (g.sub == 1 ? J - 1 : 0);
         o.out_r0 = I * kT;
         o.out_c0 = K * kT + o.h * kN;
         o.lower = false;
@@ -583,11 +591,34 @@ oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
                 }
                 if (!failed) tc_commit(bars + 4);
             }
-            // epilogue: every thread waits for the accumulators
+            // epilogue, in passes of kEC = 8 columns.  Each warp owns 32 rows
+            // of the output tile; the old output values it updates are read
+            // 8 at a time (lane l on column l % 8 of row l / 8 of each group
+            // of 4 rows), the first ones before the accumulators are ready,
+            // the next while the current ones are combined, so the reads
+            // overlap the MMAs and each other.  The products go through the
+            // (now idle) stage buffers from the row-per-lane layout of the
+            // accumulators to that column-per-lane layout, so the output is
+            // read and written by whole 64-byte row segments.
+            const int wrow0 = job.out_r0 + warp * 32;
+            const int ecol = lane % kEC;
+            const bool need_old = MODE != OZ_ASSIGN && !(partial && first);
+            double ov[kEC];
+            auto out_at = [&](int cc, int i, bool& ok) -> double* {
+                const int r = wrow0 + kEpR * i + lane / kEC;
+                const int col = job.out_c0 + cc * kEC + ecol;
+                ok = r < g.n && col < g.n && !(job.lower && col > r);
+                return out + (size_t)(r - dst_r0) * ld + (col - dst_c0);
+            };
+#pragma unroll
+            for (int i = 0; i < kEC; ++i) {
+                bool okf;
+                const double* o = out_at(0, i, okf);
+                ov[i] = (need_old && okf) ? *o : 0.0;
+            }
             const bool ok = __syncthreads_and(!failed) && mbar_wait(bars + 4, it & 1, max_polls);
             tc_fence_after();
             const int rl = warp * 32 + lane;
-            const int row = job.out_r0 + rl;
             if (!__all_sync(0xffffffffu, ok)) {
                 if (tid == 0 && g.fail != nullptr) g.fail[b] = -1;  // reported, not hung
                 failed = true;
@@ -595,43 +626,53 @@ oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
                 const int32_t* ea = g.ea + b * g.ea_stride + eaoff;
                 const int32_t* eb = g.eb + b * g.eb_stride + eboff + job.h * kN;
                 const int er = ea[rl];
-                double* orow = out + (size_t)(row - dst_r0) * ld - dst_c0;
+                double* stg = reinterpret_cast<double*>(stages) + warp * (32 * kEpP);
 #pragma unroll 1
-                for (int cc = 0; cc < kN / 16; ++cc) {
-                    uint32_t acc[kS][16];
+                for (int cc = 0; cc < kN / kEC; ++cc) {
+                    uint32_t acc[kS][kEC];
 #pragma unroll
                     for (int d = 0; d < kS; ++d)
-                        tc_ld16(tmem + ((uint32_t)(warp * 32) << 16) + d * kN + cc * 16, acc[d]);
+                        tc_ld8(tmem + ((uint32_t)(warp * 32) << 16) + d * kN + cc * kEC, acc[d]);
                     tc_wait_ld();
-                    if (row >= g.n) continue;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int col = job.out_c0 + cc * 16 + j;
-                        if (col >= g.n || (job.lower && col > row)) continue;
-                        const int ec = eb[cc * 16 + j];
+                    for (int j = 0; j < kEC; ++j) {
+                        const int ec = eb[cc * kEC + j];
                         // sum_d acc_d 256^(6-d), modulo 2^64 (exact: |sum| <= 2^62)
                         unsigned long long v = 0;
 #pragma unroll
                         for (int d = 0; d < kS; ++d)
                             v = v * 256ull + (unsigned long long)(long long)__float2int_rn(
                                                  __uint_as_float(acc[d][j]));
-                        if (er == kNonFinite || ec == kNonFinite) {
-                            orow[col] = __longlong_as_double(0x7ff8000000000000LL);  // NaN
-                        } else if (MODE == OZ_ASSIGN) {
-                            orow[col] = v == 0 ? 0.0
-                                               : ldexp(__ll2double_rn((long long)v), er + ec - 62);
-                        } else if (partial) {
-                            const int E = er + ec - 62;
-                            const double t = v == 0 ? 0.0 : ldexp(__ll2double_rn((long long)v), E);
-                            orow[col] = first ? t : orow[col] + t;
-                        } else if (v != 0) {
-                            const int E = er + ec - 62;
-                            const double vd = __ll2double_rn((long long)v);
-                            orow[col] = (E >= -1022 && E <= 1023) ? fma(-vd, pow2(E), orow[col])
-                                                                  : orow[col] - ldexp(vd, E);
-                        }
+                        stg[lane * kEpP + j] =
+                            (er == kNonFinite || ec == kNonFinite)
+                                ? __longlong_as_double(0x7ff8000000000000LL)  // NaN
+                                : scale_int((long long)v, er + ec - 62);
                     }
+                    __syncwarp();
+                    // the next pass's old values, in flight while these are
+                    // combined and stored
+                    double nx[kEC];
+#pragma unroll
+                    for (int i = 0; i < kEC; ++i) {
+                        bool okn = false;
+                        const double* o = out_at(cc + 1, i, okn);
+                        nx[i] = (cc + 1 < kN / kEC && need_old && okn) ? *o : 0.0;
+                    }
+#pragma unroll
+                    for (int i = 0; i < kEC; ++i) {
+                        bool oks;
+                        double* o = out_at(cc, i, oks);
+                        const double t = stg[(kEpR * i + lane / kEC) * kEpP + ecol];
+                        if (oks)
+                            *o = MODE == OZ_ASSIGN ? t
+                                                   : (partial ? (first ? t : ov[i] + t) : ov[i] - t);
+                        ov[i] = nx[i];
+                    }
+                    __syncwarp();
                 }
+                // the staging writes and reads (generic proxy) come before the
+                // next chunk's bulk copies into the same buffers (async proxy)
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             }
             tc_fence_before();
             __syncthreads();
@@ -787,8 +828,8 @@ FwdWs fwd_ws(void* work, int64_t batch, int n) {
 // row block), their exponents, the inverses of the diagonal tiles and their
 // slices, and the partial sums of the split reduction.
 struct AdjWs {
-    bf16 *lc, *cc, *ch;
-    int32_t *elc, *ecc, *ech;
+    bf16 *lc, *cc, *ch[2];   // Chat / C row slices: set J % 2 for tile column J
+    int32_t *elc, *ecc, *ech[2];
     InvWs iv;
     double* part;  // partial sums of split reductions (part_elems())
     size_t lc_stride, cc_stride, ch_stride, elc_stride, ecc_stride, ech_stride;
@@ -811,10 +852,10 @@ AdjWs adj_layout(uintptr_t base, int64_t batch, int n) {
     Carve c{base};
     w.lc = c.take<bf16>(batch * w.lc_stride);
     w.cc = c.take<bf16>(batch * w.cc_stride);
-    w.ch = c.take<bf16>(batch * w.ch_stride);
+    for (int s = 0; s < 2; ++s) w.ch[s] = c.take<bf16>(batch * w.ch_stride);
     w.elc = c.take<int32_t>(batch * w.elc_stride);
     w.ecc = c.take<int32_t>(batch * w.ecc_stride);
-    w.ech = c.take<int32_t>(batch * w.ech_stride);
+    for (int s = 0; s < 2; ++s) w.ech[s] = c.take<int32_t>(batch * w.ech_stride);
     w.iv = carve_inv(c, batch, (int)nt, adj_inverses((int)nt));
     w.part = c.take<double>(part_elems());
     return w;
@@ -1162,12 +1203,14 @@ cudaError_t ozaki_adj_solve(const double* L, double* W, void* work, const int32_
     // C <- C L_JJ^-1: A = C's rows (reduction over the tile's columns), B =
     // columns of L_JJ^-1 (sliced up front); the inverse scales like C along
     // the reduction, so no balancing is needed here
-    cudaError_t e = launch_slice_rows(W, w.ch, w.ech, status, batch, n, (J + 1) * kT, m * kT,
-                                      J * kT, false, w.ch_stride, w.ech_stride,
+    cudaError_t e = launch_slice_rows(W, w.ch[J & 1], w.ech[J & 1], status, batch, n,
+                                      (J + 1) * kT, m * kT, J * kT, false, w.ch_stride,
+                                      w.ech_stride,
                                       Bal{nullptr, 0, 0, 0}, stream);
     if (e != cudaSuccess) return e;
     const size_t cnt = (size_t)adj_inverses(nt);
-    OzArgs g{W, w.ch, w.ech, w.iv.sl + (size_t)J * kBlockElems, w.iv.ex + (size_t)J * kT,
+    OzArgs g{W, w.ch[J & 1], w.ech[J & 1], w.iv.sl + (size_t)J * kBlockElems,
+             w.iv.ex + (size_t)J * kT,
              w.ch_stride, w.ech_stride, cnt * kBlockElems, cnt * kT, status, nullptr, batch, n,
              nt, J, 1, nullptr};
     return launch_oz<OZ_ASSIGN>(g, (unsigned)(2 * m), stream);
@@ -1196,20 +1239,35 @@ cudaError_t ozaki_adj_row(const double* L, double* W, void* work, const int32_t*
     return cudaGetLastError();
 }
 
-cudaError_t ozaki_adj_upd(const double* L, double* W, void* work, const int32_t* status,
-                          int64_t batch, int n, int J, cudaStream_t stream) {
+cudaError_t ozaki_adj_upd_slice(double* W, void* work, const int32_t* status, int64_t batch,
+                                int n, int J, cudaStream_t stream) {
     const int nt = tiles_of(n);
     if (J <= 0) return cudaSuccess;
     const AdjWs w = adj_ws(work, batch, n);
     const size_t bstride = (size_t)nt * kT;
     // Chat = [W_JJ + W_JJ^T; C], rows J*128 .., block column J, sliced by rows
-    cudaError_t e = launch_slice_rows(W, w.ch, w.ech, status, batch, n, J * kT, (nt - J) * kT,
-                                      J * kT, true, w.ch_stride, w.ech_stride,
-                                      Bal{w.iv.bal, bstride, 0, 1}, stream);
+    return launch_slice_rows(W, w.ch[J & 1], w.ech[J & 1], status, batch, n, J * kT,
+                             (nt - J) * kT, J * kT, true, w.ch_stride, w.ech_stride,
+                             Bal{w.iv.bal, bstride, 0, 1}, stream);
+}
+
+cudaError_t ozaki_adj_upd_gemm(double* W, void* work, const int32_t* status, int64_t batch,
+                               int n, int J, int part, cudaStream_t stream) {
+    const int nt = tiles_of(n);
+    const int kw = part == 0 ? J : (part == 1 ? 1 : J - 1);
+    if (J <= 0 || kw <= 0) return cudaSuccess;
+    const AdjWs w = adj_ws(work, batch, n);
+    OzArgs g{W, w.ch[J & 1], w.ech[J & 1], w.lc, w.elc, w.ch_stride, w.ech_stride, w.lc_stride,
+             w.elc_stride, status, nullptr, batch, n, nt, J, 1, nullptr, part};
+    return launch_oz<OZ_REV_UPD>(g, (unsigned)(2 * (nt - J) * kw), stream);
+}
+
+cudaError_t ozaki_adj_upd(const double* L, double* W, void* work, const int32_t* status,
+                          int64_t batch, int n, int J, cudaStream_t stream) {
+    (void)L;
+    cudaError_t e = ozaki_adj_upd_slice(W, work, status, batch, n, J, stream);
     if (e != cudaSuccess) return e;
-    OzArgs g{W, w.ch, w.ech, w.lc, w.elc, w.ch_stride, w.ech_stride, w.lc_stride, w.elc_stride,
-             status, nullptr, batch, n, nt, J, 1, nullptr};
-    return launch_oz<OZ_REV_UPD>(g, (unsigned)(2 * (nt - J) * J), stream);
+    return ozaki_adj_upd_gemm(W, work, status, batch, n, J, 0, stream);
 }
 
 

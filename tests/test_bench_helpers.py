@@ -25,13 +25,13 @@ def test_launch_counts():
     assert bench.launches_per_step(512, 128, 1, False) == 11 + 17
     assert bench.launches_per_step(100, 128) == 1 + 1 + 0 + 3
     # float64, 128-wide tiles, one 8192 x 8192 matrix: 1081 kernels per step
-    # without the lookahead's 62 extra launches (an ncu launch list of one
-    # step counted 1081 before the lookahead was added)
-    assert bench.launches_per_step(8192, 128, 1, True) == 1081 + 62
+    # without the lookaheads' 62 + 62 extra launches (ncu launch lists of one
+    # step counted 1081 before the lookahead and 1143 with the forward's)
+    assert bench.launches_per_step(8192, 128, 1, True) == 1081 + 62 + 62
     # many matrices: no literal diagonal adjoint, no split reduction
     nt = 4
     fwd = 1 + nt + 3 * 6 + 2 * 1          # lookahead: 2 extra launches (k = 0, 1)
-    adj = 6 + 3 * 4 + nt * 1 + 3 * 2
+    adj = 6 + 3 * 4 + nt * 1 + 3 * 2 + 2   # lookahead: J = 3, 2
     assert bench.launches_per_step(512, 128, 256, True) == fwd + adj
 
 
