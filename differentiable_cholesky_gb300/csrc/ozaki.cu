@@ -339,6 +339,16 @@ __device__ __forceinline__ void tc_fence_after() {
 }
 
 // 16 consecutive fp32 columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+          "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr)
+        : "memory");
+}
 __device__ __forceinline__ void tc_ld8(uint32_t taddr, uint32_t (&v)[8]) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                  : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
@@ -591,15 +601,22 @@ oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
                 }
                 if (!failed) tc_commit(bars + 4);
             }
-            // epilogue, in passes of kEC = 8 columns.  Each warp owns 32 rows
-            // of the output tile; the old output values it updates are read
-            // 8 at a time (lane l on column l % 8 of row l / 8 of each group
-            // of 4 rows), the first ones before the accumulators are ready,
-            // the next while the current ones are combined, so the reads
-            // overlap the MMAs and each other.  The products go through the
-            // (now idle) stage buffers from the row-per-lane layout of the
-            // accumulators to that column-per-lane layout, so the output is
-            // read and written by whole 64-byte row segments.
+            // epilogue.  Two layouts of the output accesses, chosen per mode
+            // by measurement (8192 x 8192 float64 step, ncu launch lists):
+            // - the trailing and adjoint updates (one chunk per CTA, a
+            //   read-modify-write of rows of L or W that come cold from HBM)
+            //   keep the accumulators' row-per-lane layout: each lane walks
+            //   its own row, so after the first access of a line the next
+            //   ones hit in L1;
+            // - the split row update (partial tiles, hot in L2 or written
+            //   without a read) and the panel solves (written without a read)
+            //   go through the stage buffers in passes of kEC = 8 columns, so
+            //   the output is written by whole 64-byte row segments; the old
+            //   values are read 8 at a time (lane l on column l % 8 of row
+            //   l / 8 of each group of 4 rows), the first ones before the
+            //   accumulators are ready, the next while the current ones are
+            //   combined.
+            constexpr bool kStaged = MODE == OZ_REV_ROW || MODE == OZ_ASSIGN;
             const int wrow0 = job.out_r0 + warp * 32;
             const int ecol = lane % kEC;
             const bool need_old = MODE != OZ_ASSIGN && !(partial && first);
@@ -610,11 +627,13 @@ oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
                 ok = r < g.n && col < g.n && !(job.lower && col > r);
                 return out + (size_t)(r - dst_r0) * ld + (col - dst_c0);
             };
+            if constexpr (kStaged) {
 #pragma unroll
-            for (int i = 0; i < kEC; ++i) {
-                bool okf;
-                const double* o = out_at(0, i, okf);
-                ov[i] = (need_old && okf) ? *o : 0.0;
+                for (int i = 0; i < kEC; ++i) {
+                    bool okf;
+                    const double* o = out_at(0, i, okf);
+                    ov[i] = (need_old && okf) ? *o : 0.0;
+                }
             }
             const bool ok = __syncthreads_and(!failed) && mbar_wait(bars + 4, it & 1, max_polls);
             tc_fence_after();
@@ -622,7 +641,7 @@ oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
             if (!__all_sync(0xffffffffu, ok)) {
                 if (tid == 0 && g.fail != nullptr) g.fail[b] = -1;  // reported, not hung
                 failed = true;
-            } else {
+            } else if constexpr (kStaged) {
                 const int32_t* ea = g.ea + b * g.ea_stride + eaoff;
                 const int32_t* eb = g.eb + b * g.eb_stride + eboff + job.h * kN;
                 const int er = ea[rl];
@@ -673,6 +692,37 @@ oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
                 // the staging writes and reads (generic proxy) come before the
                 // next chunk's bulk copies into the same buffers (async proxy)
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            } else {
+                // out -= v 2^E, row per lane
+                const int32_t* ea = g.ea + b * g.ea_stride + eaoff;
+                const int32_t* eb = g.eb + b * g.eb_stride + eboff + job.h * kN;
+                const int er = ea[rl];
+                const int row = job.out_r0 + rl;
+                double* orow = out + (size_t)(row - dst_r0) * ld - dst_c0;
+#pragma unroll 1
+                for (int cc = 0; cc < kN / 16; ++cc) {
+                    uint32_t acc[kS][16];
+#pragma unroll
+                    for (int d = 0; d < kS; ++d)
+                        tc_ld16(tmem + ((uint32_t)(warp * 32) << 16) + d * kN + cc * 16, acc[d]);
+                    tc_wait_ld();
+                    if (row >= g.n) continue;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int col = job.out_c0 + cc * 16 + j;
+                        if (col >= g.n || (job.lower && col > row)) continue;
+                        const int ec = eb[cc * 16 + j];
+                        unsigned long long v = 0;
+#pragma unroll
+                        for (int d = 0; d < kS; ++d)
+                            v = v * 256ull + (unsigned long long)(long long)__float2int_rn(
+                                                 __uint_as_float(acc[d][j]));
+                        if (er == kNonFinite || ec == kNonFinite)
+                            orow[col] = __longlong_as_double(0x7ff8000000000000LL);  // NaN
+                        else if (v != 0)
+                            orow[col] -= scale_int((long long)v, er + ec - 62);
+                    }
+                }
             }
             tc_fence_before();
             __syncthreads();
