@@ -50,16 +50,22 @@ namespace {
 
 constexpr int kT = 128;                      // tile: rows per block, reduction chunk
 constexpr int kS = 7;                        // digit slices
-constexpr int kKC = 32;                      // reduction per pipeline stage
+// Two CTAs share an SM, so that one's MMAs overlap the other's epilogue: each
+// takes 128 x 32 outputs (7 accumulators x 32 TMEM columns = 224, 256
+// allocated) and three pipeline stages of 16 reduction steps (105 KB).
+constexpr int kKC = 16;                      // reduction per pipeline stage
 constexpr int kChunks = kT / kKC;            // stages per reduction chunk
-constexpr int kN = 64;                       // output columns per CTA
-constexpr int kSliceElems = kT * kKC;        // one slice of one block, one stage: 8 KB
+constexpr int kLaneElems = kT / 32;          // a 128-long vector's elements per lane (slicing)
+constexpr int kN = 32;                       // output columns per CTA
+constexpr int kParts = kT / kN;              // CTAs per 128 x 128 output tile
+constexpr int kSliceElems = kT * kKC;        // one slice of one block, one stage: 4 KB
 constexpr int kBlockElems = kChunks * kS * kSliceElems;  // one 128 x 128 operand block: 224 KB
-constexpr uint32_t kStageA = kS * kSliceElems * 2;       // 56 KB
-constexpr uint32_t kStageB = kS * kN * kKC * 2;          // 28 KB
+constexpr uint32_t kStageA = kS * kSliceElems * 2;       // 28 KB
+constexpr uint32_t kStageB = kS * kN * kKC * 2;          // 7 KB
 constexpr uint32_t kStageBytes = kStageA + kStageB;
-constexpr int kStages = 2;
-constexpr int kTmemCols = 512;               // 7 accumulators x 64 columns, rounded up
+constexpr int kStages = 3;
+constexpr int kTmemCols = 256;               // 7 accumulators x 32 columns, rounded up
+constexpr uint32_t kSbo = kKC / 8 * 128;     // bytes between 8-row core-matrix groups
 constexpr size_t kGemmSmem = 128 + (size_t)kStages * kStageBytes + 128;
 constexpr int32_t kNonFinite = INT_MIN;      // exponent sentinel of a non-finite vector
 constexpr int kEC = 8;                       // output columns per epilogue pass
@@ -68,8 +74,8 @@ constexpr int kEpR = 32 / kEC;               // rows per warp-wide access of a p
 
 using bf16 = __nv_bfloat16;
 
-// Offset (elements) of element (r, kk) of a 128 x 32 slice: 8 x 8 core
-// matrices (8 rows of 16 bytes), four along the reduction per row group.
+// Offset (elements) of element (r, kk) of a 128 x kKC slice: 8 x 8 core
+// matrices (8 rows of 16 bytes), kKC / 8 along the reduction per row group.
 __host__ __device__ constexpr int core_offset(int r, int kk) {
     return ((r >> 3) * (kKC / 8) + (kk >> 3)) * 64 + (r & 7) * 8 + (kk & 7);
 }
@@ -77,10 +83,9 @@ __host__ __device__ constexpr int core_offset(int r, int kk) {
 // Offset of element (m, k) (operand index m, reduction index k, both < 128)
 // of digit slice p inside one operand block.
 __device__ __forceinline__ int block_offset(int m, int k, int p) {
-    return (k >> 5) * (kS * kSliceElems) + p * kSliceElems + core_offset(m, k & 31);
+    return (k / kKC) * (kS * kSliceElems) + p * kSliceElems + core_offset(m, k % kKC);
 }
 
-// 2^E as a double for E in the normal range, 0 below it and +Inf above.
 // v * 2^E for an integer |v| <= 2^62: one int64 -> float64 conversion, then
 // the exponent moved by an integer add where the result stays normal (|v| in
 // [1, 2^62], so the new exponent lies in [E, E + 62]); ldexp otherwise.
@@ -99,11 +104,12 @@ __device__ __forceinline__ double scale_int(long long v, int E) {
 // warp maximum, then the squares of the values relative to it in fp32, whose
 // sum is inflated by 2^-16 so that rounding cannot place 2^e at or below the
 // exact norm.  A slightly large e only costs the last fraction of a bit.
-__device__ __forceinline__ int warp_scale_exponent(const double (&v)[kChunks], bool finite_lane) {
+__device__ __forceinline__ int warp_scale_exponent(const double (&v)[kLaneElems],
+                                                   bool finite_lane) {
     if (!__all_sync(0xffffffffu, finite_lane)) return kNonFinite;
     unsigned emax = 0;
 #pragma unroll
-    for (int j = 0; j < kChunks; ++j) {
+    for (int j = 0; j < kLaneElems; ++j) {
         const unsigned E = (unsigned)((__double_as_longlong(v[j]) >> 52) & 0x7ff);
         emax = E > emax ? E : emax;
     }
@@ -111,7 +117,7 @@ __device__ __forceinline__ int warp_scale_exponent(const double (&v)[kChunks], b
     if (emax == 0) return 0;  // zeros and subnormals only
     float ss = 0.f;
 #pragma unroll
-    for (int j = 0; j < kChunks; ++j) {
+    for (int j = 0; j < kLaneElems; ++j) {
         const long long bits = __double_as_longlong(v[j]);
         const int E = (int)((bits >> 52) & 0x7ff);
         const int fe = E - (int)emax + 127;  // |x| 2^-(emax-1023) as a float, in [2^-126, 2)
@@ -189,10 +195,10 @@ slice_rows_kernel(const double* __restrict__ src, bf16* __restrict__ dst,
     for (int64_t b = blockIdx.y; b < batch; b += gridDim.y) {
         if (status != nullptr && status[b] != 0) continue;
         const double* S = src + (size_t)b * n * n;
-        double v[kChunks];
+        double v[kLaneElems];
         bool finite = true;
 #pragma unroll
-        for (int j = 0; j < kChunks; ++j) {
+        for (int j = 0; j < kLaneElems; ++j) {
             const int col = col0 + lane + 32 * j;
             double x = 0.0;
             if (row < n && col < n) {
@@ -210,7 +216,7 @@ slice_rows_kernel(const double* __restrict__ src, bf16* __restrict__ dst,
         const int e = warp_scale_exponent(v, finite);
         bf16* blk = dst + b * dst_stride + (size_t)(row / kT) * kBlockElems;
 #pragma unroll
-        for (int j = 0; j < kChunks; ++j) {
+        for (int j = 0; j < kLaneElems; ++j) {
             int d[kS];
             to_digits(v[j], e, d);
 #pragma unroll
@@ -231,9 +237,13 @@ slice_rows_kernel(const double* __restrict__ src, bf16* __restrict__ dst,
 // by rows (coalesced), sliced by columns.
 // Chunk list: chunks c = c_begin .. c_end - 1; column blocks K = 0 .. kmax(c)
 // where kmax(c) = (tri ? c : k_fixed), so blocks are (c, K <= c) packed
-// lower-triangle-wise (tri) or (c, k_fixed) one per chunk.
+// lower-triangle-wise (tri) or (c, k_fixed) one per chunk.  Each (c, K) is
+// split over kColGroups blocks of 32 columns (more blocks than chunks: one
+// matrix's few chunks would leave most SMs idle).
 // ---------------------------------------------------------------------------
 constexpr int kColThreads = 256;
+constexpr int kColGroups = 4;
+constexpr int kColW = kT / kColGroups;  // columns per block
 
 __global__ void __launch_bounds__(kColThreads)
 slice_cols_kernel(const double* __restrict__ src, bf16* __restrict__ dst,
@@ -241,13 +251,15 @@ slice_cols_kernel(const double* __restrict__ src, bf16* __restrict__ dst,
                   int n, int c_begin, bool tri, int k_fixed, bool lower_only, size_t dst_stride,
                   size_t ex_stride, Bal bal) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    double* tile = reinterpret_cast<double*>(smem_raw);  // 128 x 129
-    constexpr int P = kT + 1;
-    // which (c, K): blockIdx.x enumerates them
+    double* tile = reinterpret_cast<double*>(smem_raw);  // 128 x (kColW + 1)
+    constexpr int P = kColW + 1;
+    // which (c, K) and which group of its columns: blockIdx.x enumerates them
+    const int grp = (int)blockIdx.x % kColGroups;
+    const int item = (int)blockIdx.x / kColGroups;
     int c, K, slot;
     if (tri) {
         // slot t = c (c + 1) / 2 + K over c >= c_begin: t0 = c_begin (c_begin + 1) / 2
-        const int t = c_begin * (c_begin + 1) / 2 + (int)blockIdx.x;
+        const int t = c_begin * (c_begin + 1) / 2 + item;
         int r = (int)((sqrt(8.0 * t + 1.0) - 1.0) * 0.5);
         while ((r + 1) * (r + 2) / 2 <= t) ++r;
         while (r * (r + 1) / 2 > t) --r;
@@ -255,18 +267,18 @@ slice_cols_kernel(const double* __restrict__ src, bf16* __restrict__ dst,
         K = t - r * (r + 1) / 2;
         slot = t;
     } else {
-        c = c_begin + (int)blockIdx.x;
+        c = c_begin + item;
         K = k_fixed;
         slot = c;
     }
-    const int r0 = c * kT, q0 = K * kT;
+    const int r0 = c * kT, q0 = K * kT + grp * kColW;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int64_t b = blockIdx.y; b < batch; b += gridDim.y) {
         if (status != nullptr && status[b] != 0) continue;
         const double* S = src + (size_t)b * n * n;
         __syncthreads();
-        for (int e = threadIdx.x; e < kT * kT; e += kColThreads) {
-            const int i = e / kT, j = e % kT;
+        for (int e = threadIdx.x; e < kT * kColW; e += kColThreads) {
+            const int i = e / kColW, j = e % kColW;
             const int row = r0 + i, col = q0 + j;
             double x = 0.0;
             if (row < n && col < n && (!lower_only || col <= row))
@@ -276,24 +288,25 @@ slice_cols_kernel(const double* __restrict__ src, bf16* __restrict__ dst,
         __syncthreads();
         bf16* blk = dst + b * dst_stride + (size_t)slot * kBlockElems;
         // warp w takes columns w, w + 8, ...; lane l holds rows l, l+32, l+64, l+96
-        for (int m = warp; m < kT; m += kColThreads / 32) {
-            double v[kChunks];
+        for (int m = warp; m < kColW; m += kColThreads / 32) {
+            const int mb = grp * kColW + m;  // position in the operand block
+            double v[kLaneElems];
             bool finite = true;
 #pragma unroll
-            for (int j = 0; j < kChunks; ++j) {
+            for (int j = 0; j < kLaneElems; ++j) {
                 v[j] = tile[(lane + 32 * j) * P + m];
                 finite = finite && isfinite(v[j]);
             }
             const int e = warp_scale_exponent(v, finite);
 #pragma unroll
-            for (int j = 0; j < kChunks; ++j) {
+            for (int j = 0; j < kLaneElems; ++j) {
                 int d[kS];
                 to_digits(v[j], e, d);
 #pragma unroll
                 for (int p = 0; p < kS; ++p)
-                    blk[block_offset(m, lane + 32 * j, p)] = __int2bfloat16_rn(d[p]);
+                    blk[block_offset(mb, lane + 32 * j, p)] = __int2bfloat16_rn(d[p]);
             }
-            if (lane == 0) ex[b * ex_stride + (size_t)slot * kT + m] = e;
+            if (lane == 0) ex[b * ex_stride + (size_t)slot * kT + mb] = e;
         }
     }
 }
@@ -415,8 +428,8 @@ struct OzJob {
 template <int MODE>
 __device__ __forceinline__ OzJob oz_job(const OzArgs& g, int job, int& p0, int& p1) {
     OzJob o{};
-    o.h = job & 1;
-    const int t = job >> 1;
+    o.h = job % kParts;
+    const int t = job / kParts;
     if (MODE == OZ_FWD_TRAIL) {
         int i, j;
         if (g.sub == 1) {
@@ -505,10 +518,14 @@ __device__ __forceinline__ void oz_chunk(const OzArgs& g, int p0, int p1, int ch
 // bulk copies; all four warps run the epilogue (warp w reads TMEM lanes
 // 32w .. 32w + 31, i.e. output rows 32w .. of the tile).
 template <int MODE>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(128, 2)
 oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw);  // full[2], empty[2], done
+    // full[kStages], empty[kStages], done
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + kStages;
+    uint64_t* done = bars + 2 * kStages;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + 64);
     unsigned char* stages = smem_raw + 128;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -521,7 +538,7 @@ oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
     const bool partial = MODE == OZ_REV_ROW && g.splits > 1;
 
     if (tid == 0) {
-        for (int i = 0; i < 5; ++i) mbar_init(bars + i, 1);
+        for (int i = 0; i < 2 * kStages + 1; ++i) mbar_init(bars + i, 1);
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -556,26 +573,28 @@ oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
             const bf16* blkA = g.a + b * g.a_stride + ablk;
             const bf16* blkB = g.b + b * g.b_stride + bblk + job.h * (kN * kKC);
             if (tid == 32) {
-                // producer: the four stages of this chunk
+                // producer: the stages of this chunk, through a ring of kStages
                 for (int kc = 0; kc < kChunks; ++kc) {
-                    const uint32_t s_ = (it * kChunks + kc) & 1, u = (it * kChunks + kc) >> 1;
-                    if (u > 0 && !mbar_wait(bars + 2 + s_, (u - 1) & 1, max_polls)) {
+                    const uint32_t i_ = it * kChunks + kc;
+                    const uint32_t s_ = i_ % kStages, u = i_ / kStages;
+                    if (u > 0 && !mbar_wait(empty + s_, (u - 1) & 1, max_polls)) {
                         failed = true;
                         break;
                     }
                     unsigned char* st = stages + s_ * kStageBytes;
-                    mbar_arrive_expect_tx(bars + s_, kStageBytes);
-                    bulk_load(st, blkA + (size_t)kc * kS * kSliceElems, kStageA, bars + s_);
+                    mbar_arrive_expect_tx(full + s_, kStageBytes);
+                    bulk_load(st, blkA + (size_t)kc * kS * kSliceElems, kStageA, full + s_);
                     for (int q = 0; q < kS; ++q)
                         bulk_load(st + kStageA + q * (kN * kKC * 2),
                                   blkB + (size_t)kc * kS * kSliceElems + (size_t)q * kSliceElems,
-                                  kN * kKC * 2, bars + s_);
+                                  kN * kKC * 2, full + s_);
                 }
             } else if (tid == 0) {
                 // MMA issuer: acc_d = sum_{p+q=d} D_p(A) D_q(B)^T over the chunk
                 for (int kc = 0; kc < kChunks && !failed; ++kc) {
-                    const uint32_t s_ = (it * kChunks + kc) & 1, u = (it * kChunks + kc) >> 1;
-                    if (!mbar_wait(bars + s_, u & 1, max_polls)) {
+                    const uint32_t i_ = it * kChunks + kc;
+                    const uint32_t s_ = i_ % kStages, u = i_ / kStages;
+                    if (!mbar_wait(full + s_, u & 1, max_polls)) {
                         failed = true;
                         break;
                     }
@@ -590,16 +609,16 @@ oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
 #pragma unroll
                             for (int ks = 0; ks < kKC / 16; ++ks) {
                                 const uint64_t da =
-                                    smem_desc(sa + p * (kSliceElems * 2) + ks * 256, 128, 512);
+                                    smem_desc(sa + p * (kSliceElems * 2) + ks * 256, 128, kSbo);
                                 const uint64_t db =
-                                    smem_desc(sb + q * (kN * kKC * 2) + ks * 256, 128, 512);
+                                    smem_desc(sb + q * (kN * kKC * 2) + ks * 256, 128, kSbo);
                                 tc_mma(tmem + d * kN, da, db, (kc | p | ks) != 0);
                             }
                         }
                     }
-                    tc_commit(bars + 2 + s_);  // the stage may be refilled once these finish
+                    tc_commit(empty + s_);  // the stage may be refilled once these finish
                 }
-                if (!failed) tc_commit(bars + 4);
+                if (!failed) tc_commit(done);
             }
             // epilogue.  Two layouts of the output accesses, chosen per mode
             // by measurement (8192 x 8192 float64 step, ncu launch lists):
@@ -635,7 +654,7 @@ oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
                     ov[i] = (need_old && okf) ? *o : 0.0;
                 }
             }
-            const bool ok = __syncthreads_and(!failed) && mbar_wait(bars + 4, it & 1, max_polls);
+            const bool ok = __syncthreads_and(!failed) && mbar_wait(done, it & 1, max_polls);
             tc_fence_after();
             const int rl = warp * 32 + lane;
             if (!__all_sync(0xffffffffu, ok)) {
@@ -732,7 +751,7 @@ oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
     }
     if (failed && tid == 32) {
         // let copies still in flight land before the block retires
-        for (int s = 0; s < 2; ++s) mbar_wait(bars + s, 0, max_polls);
+        for (int s = 0; s < kStages; ++s) mbar_wait(full + s, 0, max_polls);
     }
     __syncthreads();
     if (warp == 0) {
@@ -747,14 +766,24 @@ inline unsigned gy(int64_t batch) { return (unsigned)std::min<int64_t>(batch, 65
 template <int MODE>
 cudaError_t launch_oz(const OzArgs& g, unsigned jobs, cudaStream_t stream) {
     if (jobs == 0) return cudaSuccess;
-    static std::atomic<uint64_t> smem_set{0};
-    cudaError_t e = allow_smem_once(oz_gemm_kernel<MODE>, kGemmSmem, smem_set);
+    static std::atomic<uint64_t> attr_set{0};
+    cudaError_t e = once_per_device(attr_set, [] {
+        cudaError_t r = cudaFuncSetAttribute(oz_gemm_kernel<MODE>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kGemmSmem);
+        // the whole unified L1 / shared array as shared memory, so two CTAs fit
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(oz_gemm_kernel<MODE>,
+                                     cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     (int)cudaSharedmemCarveoutMaxShared);
+        return r;
+    });
     if (e != cudaSuccess) return e;
     oz_gemm_kernel<MODE><<<dim3(jobs, gy(g.batch)), 128, kGemmSmem, stream>>>(g, kMbarPolls);
     return cudaGetLastError();
 }
 
-constexpr size_t kColSmem = (size_t)kT * (kT + 1) * sizeof(double);
+constexpr size_t kColSmem = (size_t)kT * (kColW + 1) * sizeof(double);
 
 cudaError_t launch_slice_rows(const double* src, bf16* dst, int32_t* ex, const int32_t* status,
                               int64_t batch, int n, int row0, int nrows, int col0, bool sym,
@@ -774,7 +803,7 @@ cudaError_t launch_slice_cols(const double* src, bf16* dst, int32_t* ex, const i
     static std::atomic<uint64_t> smem_set{0};
     cudaError_t e = allow_smem_once(slice_cols_kernel, kColSmem, smem_set);
     if (e != cudaSuccess) return e;
-    slice_cols_kernel<<<dim3(count, gy(batch)), kColThreads, kColSmem, stream>>>(
+    slice_cols_kernel<<<dim3(count * kColGroups, gy(batch)), kColThreads, kColSmem, stream>>>(
         src, dst, ex, status, batch, n, c_begin, tri, k_fixed, lower_only, dst_stride, ex_stride,
         bal);
     return cudaGetLastError();
@@ -1171,7 +1200,7 @@ cudaError_t ozaki_panel_solve(double* L, void* work, int32_t* status, int64_t ba
     if (e != cudaSuccess) return e;
     OzArgs g{L, rs, ers, w.iv.sl, w.iv.ex, stride, estride, kBlockElems, kT, status, status,
              batch, n, nt, k, 1, nullptr};
-    return launch_oz<OZ_ASSIGN>(g, (unsigned)(2 * m), stream);
+    return launch_oz<OZ_ASSIGN>(g, (unsigned)(kParts * m), stream);
 }
 
 cudaError_t ozaki_trailing_slice(double* L, void* work, int32_t* status, int64_t batch, int n,
@@ -1197,7 +1226,7 @@ cudaError_t ozaki_trailing_gemm(double* L, void* work, int32_t* status, int64_t 
     const size_t stride = (size_t)nt * kBlockElems, estride = (size_t)nt * kT;
     OzArgs g{L, w.rs[k & 1], w.ers[k & 1], w.rs[k & 1], w.ers[k & 1], stride, estride, stride,
              estride, status, status, batch, n, nt, k, 1, nullptr, part};
-    return launch_oz<OZ_FWD_TRAIL>(g, (unsigned)(2 * tiles), stream);
+    return launch_oz<OZ_FWD_TRAIL>(g, (unsigned)(kParts * tiles), stream);
 }
 
 cudaError_t ozaki_trailing_update(double* L, void* work, int32_t* status, int64_t batch, int n,
@@ -1263,7 +1292,7 @@ cudaError_t ozaki_adj_solve(const double* L, double* W, void* work, const int32_
              w.iv.ex + (size_t)J * kT,
              w.ch_stride, w.ech_stride, cnt * kBlockElems, cnt * kT, status, nullptr, batch, n,
              nt, J, 1, nullptr};
-    return launch_oz<OZ_ASSIGN>(g, (unsigned)(2 * m), stream);
+    return launch_oz<OZ_ASSIGN>(g, (unsigned)(kParts * m), stream);
 }
 
 cudaError_t ozaki_adj_row(const double* L, double* W, void* work, const int32_t* status,
@@ -1280,7 +1309,7 @@ cudaError_t ozaki_adj_row(const double* L, double* W, void* work, const int32_t*
     const int splits = row_splits(batch, J, nt - J - 1);
     OzArgs g{W, w.cc, w.ecc, w.lc, w.elc, w.cc_stride, w.ecc_stride, w.lc_stride, w.elc_stride,
              status, nullptr, batch, n, nt, J, splits, w.part};
-    e = launch_oz<OZ_REV_ROW>(g, (unsigned)(2 * (J + 1) * splits), stream);
+    e = launch_oz<OZ_REV_ROW>(g, (unsigned)(kParts * (J + 1) * splits), stream);
     if (e != cudaSuccess || splits == 1) return e;
     const int64_t total = batch * (int64_t)(J + 1) * kT * kT;
     const unsigned blocks = (unsigned)std::min<int64_t>((total + 255) / 256,
@@ -1309,7 +1338,7 @@ cudaError_t ozaki_adj_upd_gemm(double* W, void* work, const int32_t* status, int
     const AdjWs w = adj_ws(work, batch, n);
     OzArgs g{W, w.ch[J & 1], w.ech[J & 1], w.lc, w.elc, w.ch_stride, w.ech_stride, w.lc_stride,
              w.elc_stride, status, nullptr, batch, n, nt, J, 1, nullptr, part};
-    return launch_oz<OZ_REV_UPD>(g, (unsigned)(2 * (nt - J) * kw), stream);
+    return launch_oz<OZ_REV_UPD>(g, (unsigned)(kParts * (nt - J) * kw), stream);
 }
 
 cudaError_t ozaki_adj_upd(const double* L, double* W, void* work, const int32_t* status,
