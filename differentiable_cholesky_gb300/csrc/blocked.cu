@@ -656,8 +656,18 @@ cudaError_t blocked_fwd(const T* A, T* L, int32_t* status, int64_t batch, int n,
         bool on_cluster = false;
         if constexpr (std::is_same<T, double>::value || std::is_same<T, float>::value) {
             if (cluster_diag_pays(batch, kb)) {
-                // few matrices: the tile on a cluster of SMs
-                CHOL_TRY(cluster_potrf_diag(L, status, batch, n, k0, kb, stream));
+                // few matrices: the tile on a cluster of SMs, which for the
+                // tensor-core panel solve also inverts it
+                T* inv = nullptr;
+                int32_t* bal = nullptr;
+                if constexpr (std::is_same<T, double>::value) {
+                    if (oz && k < nt - 1) {
+                        double* id = nullptr;
+                        ozaki_fwd_inverse(work, batch, n, &id, &bal);
+                        inv = id;
+                    }
+                }
+                CHOL_TRY(cluster_potrf_diag(L, status, batch, n, k0, kb, inv, bal, stream));
                 on_cluster = true;
             }
         }
@@ -674,7 +684,7 @@ cudaError_t blocked_fwd(const T* A, T* L, int32_t* status, int64_t batch, int n,
             if (oz) {
                 // panel solve and trailing update on the tensor cores
                 double* Ld = reinterpret_cast<double*>(L);
-                CHOL_TRY(ozaki_panel_solve(Ld, work, status, batch, n, k, stream));
+                CHOL_TRY(ozaki_panel_solve(Ld, work, status, batch, n, k, on_cluster, stream));
                 CHOL_TRY(ozaki_trailing_slice(Ld, work, status, batch, n, k, stream));
                 if (!look) {
                     CHOL_TRY(ozaki_trailing_gemm(Ld, work, status, batch, n, k, 0, stream));

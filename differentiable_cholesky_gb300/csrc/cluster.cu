@@ -21,6 +21,8 @@
 //   C. every block solves its own rows of the panel against that block and
 //      hands the results to every block's panel buffer;
 //   D. every block applies the panel to the trailing columns of its rows.
+// On request the cluster then also inverts the factored tile (for the
+// tensor-core panel solve), each block 16 of its columns.
 // Panel buffers alternate between panels, so step A of one panel never
 // overwrites what another block may still read in step D of the previous.
 //
@@ -59,12 +61,19 @@ struct ClLayout {
     static constexpr int col_off = h_off + kPW * kPP;        // 2 x kPW column hand-off
     static constexpr int rinv_off = col_off + 2 * kPW;       // kPW reciprocals
     static constexpr int elems = rinv_off + kPW;
+    // with the inverse: the whole factor's rows scaled by 1 / l_ii (packed
+    // lower, strictly below the diagonal) and the reciprocals 1 / l_ii
+    static constexpr int hs_off = elems;
+    static constexpr int rd_off = hs_off + kTileMax * (kTileMax + 1) / 2;
+    static constexpr int elems_inv = rd_off + kTileMax;
 };
 
 template <typename T, int C>
-size_t cl_smem_bytes() {
-    return (size_t)ClLayout<C>::elems * sizeof(T) + 16;
+size_t cl_smem_bytes(bool with_inverse) {
+    return (size_t)(with_inverse ? ClLayout<C>::elems_inv : ClLayout<C>::elems) * sizeof(T) + 16;
 }
+
+__device__ __forceinline__ int packed(int i, int j) { return i * (i + 1) / 2 + j; }
 
 __device__ __forceinline__ float rsqrt_t(float x) { return rsqrtf(x); }
 __device__ __forceinline__ double rsqrt_t(double x) { return rsqrt(x); }
@@ -76,9 +85,9 @@ __device__ __forceinline__ int first_at_or_below(int rank, int lo) {
 }
 
 template <typename T, int C>
-__global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kClThreads)
+__global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kClThreads, 1)
 cl_potrf_kernel(T* __restrict__ L, int32_t* __restrict__ status, int64_t batch, int n, int k0,
-                int kb) {
+                int kb, T* __restrict__ Inv, int32_t* __restrict__ bal, int nt) {
     using Lay = ClLayout<C>;
     constexpr int AP = Lay::AP;
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -233,20 +242,74 @@ cl_potrf_kernel(T* __restrict__ L, int32_t* __restrict__ status, int64_t batch, 
             const int t = e / AP, j = e % AP, i = rank + C * t;
             if (j <= i) Lb[(int64_t)(k0 + i) * n + k0 + j] = A[t * AP + j];
         }
+        if (Inv == nullptr) continue;
+        // The inverse X = G^-1 of the factored tile G, written as a 128 x 128
+        // matrix Inv[b] (zeros above the diagonal and beyond kb), for the
+        // panel solve's product.  Every block receives the whole factor, its
+        // rows scaled by 1 / g_ii (H_im = g_im / g_ii), then solves 16 of the
+        // columns: G x = e_c by forward substitution in its right-looking
+        // form, x_c = 1 / g_cc, then acc_i -= H_im x_m for the rows i > m,
+        // x_m handed from the lane that owns row m by a shuffle.  Each block also
+        // writes the balancing exponents ilogb(g_ii) of its own rows.
+        T* Hs = sm + Lay::hs_off;
+        T* rd = sm + Lay::rd_off;
+        for (int e = tid; e < nrows * AP; e += kClThreads) {
+            const int t = e / AP, j = e % AP, i = rank + C * t;
+            if (j > i) continue;
+            const T gii = A[t * AP + i];
+            if (j == i) {
+#pragma unroll 1
+                for (int d = 0; d < C; ++d) cluster.map_shared_rank(rd, d)[i] = T(1) / gii;
+                if (bal != nullptr)  // each block for its own rows
+                    bal[b * (int64_t)nt * kTileMax + k0 + i] =
+                        (gii > T(0) && isfinite(gii)) ? ilogb(gii) : 0;
+            } else {
+                const T h = A[t * AP + j] / gii;
+#pragma unroll 1
+                for (int d = 0; d < C; ++d) cluster.map_shared_rank(Hs, d)[packed(i, j)] = h;
+            }
+        }
+        cluster.sync();
+        T* Ib = Inv + b * (int64_t)kTileMax * kTileMax;
+        constexpr int Q = kTileMax / 32;  // rows per lane
+        for (int c = rank + C * warp; c < kTileMax; c += C * (kClThreads / 32)) {
+            T acc[Q];
+#pragma unroll
+            for (int q = 0; q < Q; ++q) acc[q] = (lane + 32 * q == c && c < kb) ? rd[c] : T(0);
+            for (int m = c; m < kb - 1; ++m) {
+                const int slot = m >> 5;
+                T v = acc[0];
+#pragma unroll
+                for (int q = 1; q < Q; ++q) v = slot == q ? acc[q] : v;
+                const T xm = __shfl_sync(0xffffffffu, v, m & 31);
+#pragma unroll
+                for (int q = 0; q < Q; ++q) {
+                    if (32 * q + 31 <= m) continue;  // (warp-uniform) no row of this slot is left
+                    const int i = lane + 32 * q;
+                    if (i > m && i < kb) acc[q] = fma(-Hs[packed(i, m)], xm, acc[q]);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < Q; ++q) {
+                const int i = lane + 32 * q;
+                Ib[(int64_t)i * kTileMax + c] = (c < kb && i >= c && i < kb) ? acc[q] : T(0);
+            }
+        }
     }
-    // no block leaves while another may still write into its panel buffers
+    // no block leaves while another may still write into its shared memory
     cluster.sync();
 }
 
 template <typename T, int C>
 cudaError_t launch_cl_potrf(T* L, int32_t* status, int64_t batch, int n, int k0, int kb,
-                            cudaStream_t stream) {
-    const size_t smem = cl_smem_bytes<T, C>();
+                            T* Inv, int32_t* bal, int nt, cudaStream_t stream) {
+    const size_t smem = cl_smem_bytes<T, C>(Inv != nullptr);
     static std::atomic<uint64_t> smem_set{0};
-    cudaError_t e = allow_smem_once(cl_potrf_kernel<T, C>, smem, smem_set);
+    cudaError_t e = allow_smem_once(cl_potrf_kernel<T, C>, cl_smem_bytes<T, C>(true), smem_set);
     if (e != cudaSuccess) return e;
     const unsigned gy = (unsigned)std::min<int64_t>(batch, 65535);
-    cl_potrf_kernel<T, C><<<dim3(C, gy), kClThreads, smem, stream>>>(L, status, batch, n, k0, kb);
+    cl_potrf_kernel<T, C><<<dim3(C, gy), kClThreads, smem, stream>>>(L, status, batch, n, k0, kb,
+                                                                     Inv, bal, nt);
     return cudaGetLastError();
 }
 
@@ -259,14 +322,15 @@ bool cluster_diag_pays(int64_t batch, int kb) {
 
 template <typename T>
 cudaError_t cluster_potrf_diag(T* L, int32_t* status, int64_t batch, int n, int k0, int kb,
-                               cudaStream_t stream) {
+                               T* Inv, int32_t* bal, cudaStream_t stream) {
     if (kb <= 0 || kb > kTileMax) return cudaErrorInvalidValue;
-    return launch_cl_potrf<T, 8>(L, status, batch, n, k0, kb, stream);
+    const int nt = (n + kTileMax - 1) / kTileMax;
+    return launch_cl_potrf<T, 8>(L, status, batch, n, k0, kb, Inv, bal, nt, stream);
 }
 
-template cudaError_t cluster_potrf_diag<float>(float*, int32_t*, int64_t, int, int, int,
-                                               cudaStream_t);
+template cudaError_t cluster_potrf_diag<float>(float*, int32_t*, int64_t, int, int, int, float*,
+                                               int32_t*, cudaStream_t);
 template cudaError_t cluster_potrf_diag<double>(double*, int32_t*, int64_t, int, int, int,
-                                                cudaStream_t);
+                                                double*, int32_t*, cudaStream_t);
 
 }  // namespace chol

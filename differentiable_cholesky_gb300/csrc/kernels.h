@@ -80,11 +80,14 @@ size_t blocked_fwd_workspace_bytes(bool real_double, int64_t batch, int n, int t
 // Diagonal-tile factor of the blocked forward on a cluster of 8 blocks
 // (8 SMs) per matrix: the tile L[k0 .. k0+kb, k0 .. k0+kb] (kb <= 128,
 // lower part) factored in place, status[b] = k0 + the failing column + 1.
+// With Inv (else null): also the tile's inverse into Inv[b] (128 x 128,
+// zeros above the diagonal and beyond kb) and, with bal, the balancing
+// exponents ilogb(l_ii) of its rows into bal[b * ceil(n/128) * 128 + k0 + i].
 // cluster_diag_pays: few enough matrices that the clusters leave SMs idle.
 bool cluster_diag_pays(int64_t batch, int kb);
 template <typename T>
 cudaError_t cluster_potrf_diag(T* L, int32_t* status, int64_t batch, int n, int k0, int kb,
-                               cudaStream_t stream);
+                               T* Inv, int32_t* bal, cudaStream_t stream);
 
 // Trailing update of step k of the float64 blocked forward with 128-wide
 // tiles on the bf16 tensor cores (exact digit-slice products): for every
@@ -102,9 +105,14 @@ cudaError_t ozaki_trailing_slice(double* L, void* work, int32_t* status, int64_t
 cudaError_t ozaki_trailing_gemm(double* L, void* work, int32_t* status, int64_t batch, int n,
                                 int k, int part, cudaStream_t stream);
 // The panel solve of step k on the tensor cores: L_Ik <- L_Ik G^-T, I > k,
-// with G^-1 the inverse of the (factored) diagonal tile.
+// with G^-1 the inverse of the (factored) diagonal tile, computed here unless
+// have_inverse (the diagonal factor wrote it to the workspace's inverse and
+// balancing arrays, ozaki_fwd_inverse).
 cudaError_t ozaki_panel_solve(double* L, void* work, int32_t* status, int64_t batch, int n,
-                              int k, cudaStream_t stream);
+                              int k, bool have_inverse, cudaStream_t stream);
+// Where the forward's workspace keeps the diagonal tile's inverse
+// (batch x 128 x 128) and the balancing exponents (batch x ceil(n/128) x 128).
+void ozaki_fwd_inverse(void* work, int64_t batch, int n, double** inv, int32_t** bal);
 // The same for the float64 blocked adjoint with 128-wide tiles: `work` holds
 // ozaki_adj_workspace_bytes(batch, n) bytes; prepare slices L once, then per
 // tile column J: row (W_JK -= C^T L_{below J, K}, K <= J) before the

@@ -1177,8 +1177,14 @@ size_t ozaki_workspace_bytes(int64_t batch, int n) {
     return (size_t)c.p;
 }
 
+void ozaki_fwd_inverse(void* work, int64_t batch, int n, double** inv, int32_t** bal) {
+    const FwdWs w = fwd_ws(work, batch, n);
+    *inv = w.iv.inv;
+    *bal = w.iv.bal;
+}
+
 cudaError_t ozaki_panel_solve(double* L, void* work, int32_t* status, int64_t batch, int n,
-                              int k, cudaStream_t stream) {
+                              int k, bool have_inverse, cudaStream_t stream) {
     const int nt = tiles_of(n);
     const int m = nt - k - 1;
     if (m <= 0) return cudaSuccess;
@@ -1186,7 +1192,9 @@ cudaError_t ozaki_panel_solve(double* L, void* work, int32_t* status, int64_t ba
     const size_t stride = (size_t)nt * kBlockElems, estride = (size_t)nt * kT;
     const size_t bstride = (size_t)nt * kT;
     // G^-1 of the (full) diagonal tile, and the balancing exponents of its rows
-    cudaError_t e = launch_tri_inverse(L, w.iv.inv, w.iv.bal, status, batch, n, k, 1, stream);
+    cudaError_t e = have_inverse
+                        ? cudaSuccess
+                        : launch_tri_inverse(L, w.iv.inv, w.iv.bal, status, batch, n, k, 1, stream);
     if (e != cudaSuccess) return e;
     // L_Ik <- L_Ik G^-T: A = the panel's rows (reduction over the tile's
     // columns, divided by the balancing factors), B = rows of G^-1 (multiplied)
