@@ -114,12 +114,14 @@ def launches_per_step(n: int, tile: int, batch: int = 1, float64: bool = False,
     tc = float64 and tile == 128
     tc_fwd = tc and n > 128
     look = tc_fwd and nt >= 3
+    cluster = batch * 8 <= sms and tile > 32  # the cluster factor also inverts the tile
     fwd = 1 + nt                              # copy, diagonal factors
     for k in range(nt - 1):
         if tc_fwd:
-            # inverse, 2 slicings, assign; slicing, update (lookahead: column
-            # k + 1, then the rest while there is one)
-            fwd += 4 + 1 + ((1 + (1 if nt - k - 1 >= 2 else 0)) if look else 1)
+            # inverse (unless the cluster factor made it), 2 slicings, assign;
+            # slicing, update (lookahead: column k + 1, then the rest while
+            # there is one)
+            fwd += (3 if cluster else 4) + 1 + ((1 + (1 if nt - k - 1 >= 2 else 0)) if look else 1)
         else:
             fwd += 2                          # panel solve, trailing update
     if not tc:
