@@ -131,12 +131,21 @@ def launches_per_step(n: int, tile: int, batch: int = 1, float64: bool = False,
         return fwd + adj
     adj = 1 + 4 + 1                           # copy, prepare (4), add
     lit = batch * 4 <= sms
+
+    def splits(k_n, chunks):
+        tiles = batch * k_n
+        return max(1, min((2 * sms + 2 * tiles - 1) // (2 * tiles), chunks))
+
     for J in range(nt):
         if J < nt - 1:
             chunks = nt - J - 1
-            tiles = batch * (J + 1)
-            splits = max(1, min((2 * sms + 2 * tiles - 1) // (2 * tiles), chunks))
-            adj += 2 + 2 + (1 if splits > 1 else 0)   # solve; row (+ ordered reduce)
+            adj += 2 + 2                      # solve (slicing, assign); row (slicing, products)
+            if look and J >= 2:
+                # row update of block columns J - 1 .. J, then (side stream) the rest
+                adj += 1 if splits(2, chunks) > 1 else 0
+                adj += 1 + (1 if splits(J - 1, chunks) > 1 else 0)
+            else:
+                adj += 1 if splits(J + 1, chunks) > 1 else 0   # ordered reduce
         adj += 3 if lit else 1                # diagonal tile: literal form or sweep
         if J > 0:
             # update: slicing, products (lookahead: block column J - 1, then

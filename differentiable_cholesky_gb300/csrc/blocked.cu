@@ -759,9 +759,9 @@ cudaError_t blocked_adj(const T* L, const T* Lbar, T* Abar, const int32_t* statu
         oz = oz_work != nullptr && tile == 128;
         if (oz) CHOL_TRY(ozaki_adj_prepare(L, oz_work, status, batch, n, stream));
     }
-    // lookahead (as in the forward): tile column J's update of block column
-    // J - 1 here, its update of the columns left of that on the side stream,
-    // beside tile column J - 1's solve, row update and diagonal tile
+    // lookahead (as in the forward): tile column J's row update and update of
+    // block columns J - 1 .. J here, of the columns left of those on the side
+    // stream, beside tile column J - 1's solve, row update and diagonal tile
     SideStream sd;
     int dev = 0;
     bool look = false;
@@ -779,9 +779,13 @@ cudaError_t blocked_adj(const T* L, const T* Lbar, T* Abar, const int32_t* statu
         const int j0 = J * tile, kb = std::min(tile, n - j0), r0 = j0 + kb, nb = n - r0;
         if constexpr (std::is_same<T, double>::value) {
             if (oz) {
+                // with lookahead the row update's block columns K < J - 1 go to
+                // the side stream (below), after the update of column J - 1
+                const bool split_row = look && J >= 2;
                 if (nb > 0) {
                     CHOL_TRY(ozaki_adj_solve(L, W, oz_work, status, batch, n, J, stream));
-                    CHOL_TRY(ozaki_adj_row(L, W, oz_work, status, batch, n, J, stream));
+                    CHOL_TRY(ozaki_adj_row(L, W, oz_work, status, batch, n, J, split_row ? 1 : 0,
+                                           stream));
                 }
                 if (ozaki_adj_lit_pays(batch)) {
                     // few matrices: the tile's adjoint as three parallel products
@@ -808,6 +812,8 @@ cudaError_t blocked_adj(const T* L, const T* Lbar, T* Abar, const int32_t* statu
                 if (J >= 2) {
                     CHOL_TRY(cudaEventRecord(sd.look, stream));
                     CHOL_TRY(cudaStreamWaitEvent(sd.s, sd.look, 0));
+                    if (split_row && nb > 0)
+                        CHOL_TRY(ozaki_adj_row(L, W, oz_work, status, batch, n, J, 2, sd.s));
                     CHOL_TRY(ozaki_adj_upd_gemm(Wd, oz_work, status, batch, n, J, 2, sd.s));
                     CHOL_TRY(cudaEventRecord(sd.rest, sd.s));
                     join.pending = true;

@@ -124,8 +124,13 @@ cudaError_t ozaki_adj_prepare(const double* L, void* work, const int32_t* status
 // The adjoint's panel solve C <- C L_JJ^-1 (rows below tile J).
 cudaError_t ozaki_adj_solve(const double* L, double* W, void* work, const int32_t* status,
                             int64_t batch, int n, int J, cudaStream_t stream);
+// The adjoint's row update W_JK -= C^T L_{below J, K} for the output block
+// columns K <= J (part 0), K = J - 1 .. J only (part 1, which also slices C)
+// or K < J - 1 only (part 2, which reuses part 1's slices of C and its own
+// partial-sum buffer, so it may run on the side stream beside tile column
+// J - 1's solve and row update).
 cudaError_t ozaki_adj_row(const double* L, double* W, void* work, const int32_t* status,
-                          int64_t batch, int n, int J, cudaStream_t stream);
+                          int64_t batch, int n, int J, int part, cudaStream_t stream);
 // Adjoint of diagonal tile J by the literal formula Phi(M + M^T),
 // M = X^T Phi(L_JJ^T W_JJ) X with X = L_JJ^-1 from ozaki_adj_prepare, in
 // place on W_JJ (three products, no column chain).  ozaki_adj_lit_pays: few

@@ -415,6 +415,7 @@ struct OzArgs {
     int sub;              // OZ_FWD_TRAIL: 0 every trailing tile, 1 only block column
                           // step + 1, 2 only block columns >= step + 2; OZ_REV_UPD:
                           // 0 every K < J, 1 only K = J - 1, 2 only K < J - 1
+    int k_lo, k_n;        // OZ_REV_ROW: output block columns K = k_lo .. k_lo + k_n - 1
 };
 
 struct OzJob {
@@ -448,7 +449,7 @@ __device__ __forceinline__ OzJob oz_job(const OzArgs& g, int job, int& p0, int& 
         p0 = I;  // A: row-slice block I, B: row-slice block J
         p1 = J;
     } else if (MODE == OZ_REV_ROW) {
-        const int K = t / g.splits;  // K <= J
+        const int K = g.k_lo + t / g.splits;  // K <= J
         o.split = t % g.splits;
         o.out_r0 = g.step * kT;
         o.out_c0 = K * kT + o.h * kN;
@@ -561,7 +562,8 @@ oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
         size_t ld = (size_t)g.n;
         int dst_r0 = 0, dst_c0 = 0;
         if (partial) {
-            out = g.part + (((size_t)b * g.splits + job.split) * (g.step + 1) + p0) * kT * kT;
+            out = g.part +
+                  (((size_t)b * g.splits + job.split) * g.k_n + (p0 - g.k_lo)) * kT * kT;
             ld = kT;
             dst_r0 = job.out_r0;
             dst_c0 = p0 * kT;
@@ -816,26 +818,27 @@ inline int tiles_of(int n) { return (n + kT - 1) / kT; }
 // which CTA finished first.
 __global__ void __launch_bounds__(256)
 split_reduce_kernel(double* __restrict__ W, const double* __restrict__ part,
-                    const int32_t* __restrict__ status, int64_t batch, int n, int J, int splits) {
-    const int64_t per = (int64_t)(J + 1) * kT * kT;
+                    const int32_t* __restrict__ status, int64_t batch, int n, int J, int splits,
+                    int k_lo, int k_n) {
+    const int64_t per = (int64_t)k_n * kT * kT;
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < batch * per;
          e += (int64_t)gridDim.x * blockDim.x) {
         const int64_t b = e / per;
         if (status != nullptr && status[b] != 0) continue;
         const int64_t w = e % per;
-        const int K = (int)(w / (kT * kT)), m = (int)((w / kT) % kT), c = (int)(w % kT);
+        const int K = k_lo + (int)(w / (kT * kT)), m = (int)((w / kT) % kT), c = (int)(w % kT);
         const int row = J * kT + m, col = K * kT + c;
         if (row >= n || col >= n || (K == J && c > m)) continue;
         double s = 0.0;
-        for (int sp = 0; sp < splits; ++sp) s += part[((b * splits + sp) * (J + 1)) * kT * kT + w];
+        for (int sp = 0; sp < splits; ++sp) s += part[((b * splits + sp) * k_n) * kT * kT + w];
         W[(size_t)b * n * n + (size_t)row * n + col] -= s;
     }
 }
 
 // Split of OZ_REV_ROW's reduction: enough CTAs for two per SM, the partial
 // tiles bounded by 2 * SMs per call.
-inline int row_splits(int64_t batch, int J, int chunks) {
-    const int64_t tiles = batch * (J + 1);
+inline int row_splits(int64_t batch, int k_n, int chunks) {
+    const int64_t tiles = batch * k_n;
     const int64_t want = (2 * (int64_t)device_sm_count() + 2 * tiles - 1) / (2 * tiles);
     return (int)std::max<int64_t>(1, std::min<int64_t>(want, chunks));
 }
@@ -907,10 +910,13 @@ FwdWs fwd_ws(void* work, int64_t batch, int n) {
 // row block), their exponents, the inverses of the diagonal tiles and their
 // slices, and the partial sums of the split reduction.
 struct AdjWs {
-    bf16 *lc, *cc, *ch[2];   // Chat / C row slices: set J % 2 for tile column J
-    int32_t *elc, *ecc, *ech[2];
+    // C column slices and Chat / C row slices: set J % 2 for tile column J
+    bf16 *lc, *cc[2], *ch[2];
+    int32_t *elc, *ecc[2], *ech[2];
     InvWs iv;
-    double* part;  // partial sums of split reductions (part_elems())
+    double* part;   // partial sums of split reductions (part_elems()), the caller's stream
+    double* part2;  // the same for the row update's part on the side stream
+    double* lit;    // S and T of the literal diagonal-tile adjoint (2 x 128 x 128 per matrix)
     size_t lc_stride, cc_stride, ch_stride, elc_stride, ecc_stride, ech_stride;
 };
 
@@ -930,13 +936,15 @@ AdjWs adj_layout(uintptr_t base, int64_t batch, int n) {
     w.ech_stride = nt * kT;
     Carve c{base};
     w.lc = c.take<bf16>(batch * w.lc_stride);
-    w.cc = c.take<bf16>(batch * w.cc_stride);
+    for (int s = 0; s < 2; ++s) w.cc[s] = c.take<bf16>(batch * w.cc_stride);
     for (int s = 0; s < 2; ++s) w.ch[s] = c.take<bf16>(batch * w.ch_stride);
     w.elc = c.take<int32_t>(batch * w.elc_stride);
-    w.ecc = c.take<int32_t>(batch * w.ecc_stride);
+    for (int s = 0; s < 2; ++s) w.ecc[s] = c.take<int32_t>(batch * w.ecc_stride);
     for (int s = 0; s < 2; ++s) w.ech[s] = c.take<int32_t>(batch * w.ech_stride);
     w.iv = carve_inv(c, batch, (int)nt, adj_inverses((int)nt));
     w.part = c.take<double>(part_elems());
+    w.part2 = c.take<double>(part_elems());
+    w.lit = c.take<double>((size_t)2 * batch * kT * kT);
     return w;
 }
 
@@ -1251,7 +1259,7 @@ cudaError_t ozaki_trailing_update(double* L, void* work, int32_t* status, int64_
 // ---------------------------------------------------------------------------
 size_t ozaki_adj_workspace_bytes(int64_t batch, int n) {
     const AdjWs w = adj_layout(0, batch, n);
-    return reinterpret_cast<uintptr_t>(w.part + part_elems()) + 256;
+    return reinterpret_cast<uintptr_t>(w.lit + (size_t)2 * batch * kT * kT) + 256;
 }
 
 cudaError_t ozaki_adj_prepare(const double* L, void* work, const int32_t* status, int64_t batch,
@@ -1304,25 +1312,36 @@ cudaError_t ozaki_adj_solve(const double* L, double* W, void* work, const int32_
 }
 
 cudaError_t ozaki_adj_row(const double* L, double* W, void* work, const int32_t* status,
-                          int64_t batch, int n, int J, cudaStream_t stream) {
+                          int64_t batch, int n, int J, int part, cudaStream_t stream) {
+    (void)L;
     const int nt = tiles_of(n);
     if (J >= nt - 1) return cudaSuccess;
+    // output block columns: all K <= J (part 0), K = J - 1 .. J (part 1), K < J - 1 (part 2)
+    const int k_lo = part == 1 ? std::max(0, J - 1) : 0;
+    const int k_hi = part == 2 ? J - 2 : J;
+    if (k_hi < k_lo) return cudaSuccess;
+    const int k_n = k_hi - k_lo + 1;
     const AdjWs w = adj_ws(work, batch, n);
     const size_t bstride = (size_t)nt * kT;
-    // C (W's rows below tile J, block column J), sliced by columns per chunk
-    cudaError_t e = launch_slice_cols(W, w.cc, w.ecc, status, batch, n, J + 1,
-                                      (unsigned)(nt - J - 1), false, J, false, w.cc_stride,
-                                      w.ecc_stride, Bal{w.iv.bal, bstride, 0, 1}, stream);
-    if (e != cudaSuccess) return e;
-    const int splits = row_splits(batch, J, nt - J - 1);
-    OzArgs g{W, w.cc, w.ecc, w.lc, w.elc, w.cc_stride, w.ecc_stride, w.lc_stride, w.elc_stride,
-             status, nullptr, batch, n, nt, J, splits, w.part};
-    e = launch_oz<OZ_REV_ROW>(g, (unsigned)(kParts * (J + 1) * splits), stream);
+    cudaError_t e = cudaSuccess;
+    if (part != 2) {
+        // C (W's rows below tile J, block column J), sliced by columns per chunk
+        e = launch_slice_cols(W, w.cc[J & 1], w.ecc[J & 1], status, batch, n, J + 1,
+                              (unsigned)(nt - J - 1), false, J, false, w.cc_stride, w.ecc_stride,
+                              Bal{w.iv.bal, bstride, 0, 1}, stream);
+        if (e != cudaSuccess) return e;
+    }
+    double* pbuf = part == 2 ? w.part2 : w.part;
+    const int splits = row_splits(batch, k_n, nt - J - 1);
+    OzArgs g{W, w.cc[J & 1], w.ecc[J & 1], w.lc, w.elc, w.cc_stride, w.ecc_stride, w.lc_stride,
+             w.elc_stride, status, nullptr, batch, n, nt, J, splits, pbuf, 0, k_lo, k_n};
+    e = launch_oz<OZ_REV_ROW>(g, (unsigned)(kParts * k_n * splits), stream);
     if (e != cudaSuccess || splits == 1) return e;
-    const int64_t total = batch * (int64_t)(J + 1) * kT * kT;
+    const int64_t total = batch * (int64_t)k_n * kT * kT;
     const unsigned blocks = (unsigned)std::min<int64_t>((total + 255) / 256,
                                                         (int64_t)device_sm_count() * 16);
-    split_reduce_kernel<<<blocks, 256, 0, stream>>>(W, w.part, status, batch, n, J, splits);
+    split_reduce_kernel<<<blocks, 256, 0, stream>>>(W, pbuf, status, batch, n, J, splits, k_lo,
+                                                    k_n);
     return cudaGetLastError();
 }
 
@@ -1368,15 +1387,14 @@ cudaError_t ozaki_adj_diag(const double* L, double* W, void* work, const int32_t
                            int64_t batch, int n, int J, cudaStream_t stream) {
     const int nt = tiles_of(n);
     const AdjWs w = adj_ws(work, batch, n);
-    if ((size_t)2 * batch * kT * kT > part_elems()) return cudaErrorInvalidValue;
     const int j0 = J * kT, kb = std::min(kT, n - j0);
     const int nb = (kb + kLB - 1) / kLB;
     const dim3 grid((unsigned)(nb * (nb + 1) / 2), gy(batch));
     const size_t cnt = (size_t)adj_inverses(nt);
     const double* X = w.iv.inv + (size_t)J * kT * kT;
     const size_t xs = cnt * kT * kT;
-    double* S = w.part;
-    double* T = w.part + (size_t)batch * kT * kT;
+    double* S = w.lit;
+    double* T = w.lit + (size_t)batch * kT * kT;
     lit_diag_kernel<LIT_S><<<grid, kLitThreads, 0, stream>>>(L, W, X, xs, S, T, status, batch, n,
                                                             j0, kb);
     lit_diag_kernel<LIT_T><<<grid, kLitThreads, 0, stream>>>(L, W, X, xs, S, T, status, batch, n,
