@@ -40,6 +40,7 @@ if ROOT not in sys.path:
 
 METRIC = "Cholesky fwd+adjoint matrices/s and GFLOP/s (1 GB300), % of HBM/FP64 roofline"
 UNIT = "matrices/s"
+FALLBACK_BF16_TFLOPS = 1900.0   # the profiling recipe's fallback, if no measured file
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1024 * 1024
 DEFAULT_WORKLOAD = "banded_8192"
@@ -186,6 +187,18 @@ def measured_traffic(workload: str, kernel: str):
     except OSError:
         return None
     return rec["bytes"]
+
+
+def read_bf16_peak():
+    """The measured bf16 dense matmul rate (burst), TFLOP/s, or the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        if "bf16_tflops" in d:
+            return float(d["bf16_tflops"]), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def read_peaks():
@@ -676,6 +689,18 @@ def main():
     peaks, fp64_peak, fp32_peak = measure_fp_peaks(binding, torch)
     hbm_peak, peak_src = read_peaks()
     main_report = g.kernel_report(fwd_ms, adj_ms, hbm_peak, fp64_peak, fp32_peak)
+    # the dominant kernel of the float64 tensor-core path timed alone: step 0's
+    # trailing update of one matrix, on a scratch copy of its factor
+    tc_probe = None
+    if np_dtype == np.float64:
+        t_eff = tile or default_tile(n, batch, sms, True)
+        if n > 128 and t_eff == 128:
+            scratch = g.sets[0][2][0].clone()
+            ms_l, bf_l, fp_l = binding.probe_tc_update(scratch, k=0, reps=3, stream=stream)
+            m = (n + 127) // 128 - 1
+            tc_probe = {"ms": ms_l, "bf16_TFLOPs": bf_l / 1e12, "fp64_equiv_TFLOPs": fp_l / 1e12,
+                        "tiles": m * (m + 1) // 2, "ctas": 4 * (m * (m + 1) // 2)}
+            del scratch
     g.free()
     del g
     torch.cuda.empty_cache()
@@ -716,6 +741,20 @@ def main():
                     "peak": hbm_peak, "unit": "GB/s", "frac": dk["frac"],
                     "peak_source": f"{peak_src} HBM copy bandwidth (MEASURED_PEAKS.json)",
                     "traffic": measured_traffic(args.workload, dominant)}
+    elif tc_probe is not None:
+        bf16_peak, bf16_src = read_bf16_peak()
+        roofline = {"bound": "tensor",
+                    "kernel": "oz_gemm_kernel: the forward's trailing update of step 0 on the bf16 "
+                              f"tensor cores ({tc_probe['tiles']} lower 128x128 tiles, "
+                              f"{tc_probe['ctas']} CTAs), timed alone with CUDA events "
+                              "(chol_probe_tc_update)",
+                    "achieved": tc_probe["bf16_TFLOPs"], "peak": bf16_peak, "unit": "TFLOP/s",
+                    "frac": tc_probe["bf16_TFLOPs"] / bf16_peak,
+                    "peak_source": f"{bf16_src} bf16 dense matmul, burst (MEASURED_PEAKS.json)",
+                    "launch_ms": tc_probe["ms"],
+                    "fp64_equivalent_TFLOPs": tc_probe["fp64_equiv_TFLOPs"],
+                    "fp64_roof_TFLOPs": fp64_peak, "peaks_TFLOPs": peaks,
+                    "traffic": measured_traffic(args.workload, "tc_update")}
     else:
         roofline = {"bound": "alu", "pipe": "fp64" if esize == 8 else "fp32",
                     "kernel": f"{dominant} call (all its launches)",

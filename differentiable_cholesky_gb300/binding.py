@@ -74,6 +74,9 @@ def load_library(path: str | None = None):
         lib.chol_probe_fma_peak.restype = ctypes.c_int
         lib.chol_probe_dmma_peak.argtypes = [i32, i64, vp, ctypes.POINTER(ctypes.c_double), vp]
         lib.chol_probe_dmma_peak.restype = ctypes.c_int
+        dp = ctypes.POINTER(ctypes.c_double)
+        lib.chol_probe_tc_update.argtypes = [i32, vp, i32, i32, dp, dp, dp, vp]
+        lib.chol_probe_tc_update.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -337,3 +340,18 @@ class _Cholesky(torch.autograd.Function):
 def cholesky(A: torch.Tensor, tile: int = 0):
     """Differentiable ``(L, status)``; ``A.grad`` gets the lower-triangle adjoint."""
     return _Cholesky.apply(A, tile)
+
+
+def probe_tc_update(L: torch.Tensor, k: int = 0, reps: int = 3, stream=None):
+    """Times the float64 tensor-core trailing update of step ``k`` on the
+    square float64 CUDA matrix ``L`` (modified: pass a scratch copy).
+    Returns ``(ms_per_launch, bf16_flops_per_s, fp64_equivalent_flops_per_s)``."""
+    _require(L, "L", torch.float64)
+    if L.dim() != 2 or L.shape[0] != L.shape[1]:
+        raise ValueError("L must be a square matrix")
+    ms, bf, fp = ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
+    rc = load_library().chol_probe_tc_update(int(L.shape[0]), L.data_ptr(), int(k), int(reps),
+                                             ctypes.byref(ms), ctypes.byref(bf), ctypes.byref(fp),
+                                             _stream_ptr(stream))
+    _check(rc)
+    return ms.value, bf.value, fp.value

@@ -57,16 +57,19 @@ constexpr int kThreads = 256;
 // callers cannot interleave their event records.
 // ---------------------------------------------------------------------------
 struct SideStream {
-    cudaStream_t s = nullptr;
-    cudaEvent_t look = nullptr;  // the caller's stream reached step k's lookahead column
+    cudaStream_t s = nullptr;    // the updates beside the chain (default priority)
+    cudaStream_t hi = nullptr;   // the chain itself (the device's highest priority)
+    cudaEvent_t look = nullptr;  // the chain reached step k's lookahead column
     cudaEvent_t rest = nullptr;  // the side stream finished step k's remaining columns
+    cudaEvent_t fork = nullptr;  // the caller's stream reached the forward / adjoint
+    cudaEvent_t done = nullptr;  // the chain finished
 };
 
 SideStream g_side[kMaxDevices];
 std::mutex g_side_lock[kMaxDevices];
 std::atomic<uint64_t> g_side_made{0};
 
-// The device's side stream (created on first use); false if there is none.
+// The device's side streams (created on first use); false if there are none.
 bool side_stream(int& dev, SideStream& out) {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
         cudaGetLastError();
@@ -74,9 +77,13 @@ bool side_stream(int& dev, SideStream& out) {
     }
     const cudaError_t e = once_per_device(g_side_made, [&]() -> cudaError_t {
         SideStream sd;
-        cudaError_t r = cudaStreamCreateWithFlags(&sd.s, cudaStreamNonBlocking);
-        if (r == cudaSuccess) r = cudaEventCreateWithFlags(&sd.look, cudaEventDisableTiming);
-        if (r == cudaSuccess) r = cudaEventCreateWithFlags(&sd.rest, cudaEventDisableTiming);
+        int least = 0, greatest = 0;
+        cudaError_t r = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+        if (r == cudaSuccess) r = cudaStreamCreateWithFlags(&sd.s, cudaStreamNonBlocking);
+        if (r == cudaSuccess)
+            r = cudaStreamCreateWithPriority(&sd.hi, cudaStreamNonBlocking, greatest);
+        for (cudaEvent_t* ev : {&sd.look, &sd.rest, &sd.fork, &sd.done})
+            if (r == cudaSuccess) r = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
         if (r == cudaSuccess) g_side[dev] = sd;
         return r;
     });
@@ -88,14 +95,41 @@ bool side_stream(int& dev, SideStream& out) {
     return true;
 }
 
-// On scope exit: the caller's stream waits for the side stream's last work.
+// The chain of a lookahead call runs on the high-priority stream, so that
+// when SMs free up the scheduler takes its (short, latency-bound) kernels
+// before the side stream's bulk updates; it starts after the caller's stream
+// has reached the call, and the caller's stream waits for the chain (which
+// itself waits for the side stream's last work) before the call ends.
 struct JoinSide {
-    cudaStream_t main;
+    cudaStream_t main;   // the caller's stream
+    cudaStream_t chain;  // where the chain runs: main, or the high-priority stream
     const SideStream* sd;
-    bool pending = false;
-    ~JoinSide() {
-        if (pending) cudaStreamWaitEvent(main, sd->rest, 0);
+    bool pending = false;  // side work the chain has not waited for yet
+    bool forked = false;   // chain != main
+    cudaError_t start(bool look) {
+        if (!look) return cudaSuccess;
+        cudaError_t e = cudaEventRecord(sd->fork, main);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(sd->hi, sd->fork, 0);
+        if (e == cudaSuccess) {
+            chain = sd->hi;
+            forked = true;
+        }
+        return e;
     }
+    cudaError_t finish() {
+        cudaError_t e = cudaSuccess;
+        if (pending) {
+            e = cudaStreamWaitEvent(chain, sd->rest, 0);
+            pending = false;
+        }
+        if (forked) {
+            if (e == cudaSuccess) e = cudaEventRecord(sd->done, chain);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(main, sd->done, 0);
+            forked = false;
+        }
+        return e;
+    }
+    ~JoinSide() { finish(); }
 };
 
 template <typename T> using real_t = typename chol_tile::detail::real_of<T>::type;
@@ -639,15 +673,17 @@ cudaError_t blocked_fwd(const T* A, T* L, int32_t* status, int64_t batch, int n,
     int dev = 0;
     bool look = false;
     if (oz && nt >= 3) {
-        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-        const bool idle = cudaStreamIsCapturing(stream, &cs) == cudaSuccess &&
-                          cs == cudaStreamCaptureStatusNone;
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        const bool idle = cudaStreamIsCapturing(stream, &cap) == cudaSuccess &&
+                          cap == cudaStreamCaptureStatusNone;
         cudaGetLastError();
         look = idle && side_stream(dev, sd);
     }
     std::unique_lock<std::mutex> side_lock;
     if (look) side_lock = std::unique_lock<std::mutex>(g_side_lock[dev]);
-    JoinSide join{stream, &sd};
+    JoinSide join{stream, stream, &sd};
+    CHOL_TRY(join.start(look));
+    const cudaStream_t cs = join.chain;  // the chain's stream
     for (int k = 0; k < nt; ++k) {
         const int k0 = k * tile;
         const int kb = std::min(tile, n - k0);
@@ -667,16 +703,16 @@ cudaError_t blocked_fwd(const T* A, T* L, int32_t* status, int64_t batch, int n,
                         inv = id;
                     }
                 }
-                CHOL_TRY(cluster_potrf_diag(L, status, batch, n, k0, kb, inv, bal, stream));
+                CHOL_TRY(cluster_potrf_diag(L, status, batch, n, k0, kb, inv, bal, cs));
                 on_cluster = true;
             }
         }
         if (on_cluster) {
         } else if (kb <= 32)
-            potrf_diag_kernel<T, 64><<<dim3(1, grid_y(batch)), 64, dsm, stream>>>(L, status, batch,
+            potrf_diag_kernel<T, 64><<<dim3(1, grid_y(batch)), 64, dsm, cs>>>(L, status, batch,
                                                                                  n, k0, kb);
         else
-            potrf_diag_kernel<T, kThreads><<<dim3(1, grid_y(batch)), kThreads, dsm, stream>>>(
+            potrf_diag_kernel<T, kThreads><<<dim3(1, grid_y(batch)), kThreads, dsm, cs>>>(
                 L, status, batch, n, k0, kb);
         CHOL_TRY(cudaGetLastError());
         if (k == nt - 1) break;
@@ -684,22 +720,22 @@ cudaError_t blocked_fwd(const T* A, T* L, int32_t* status, int64_t batch, int n,
             if (oz) {
                 // panel solve and trailing update on the tensor cores
                 double* Ld = reinterpret_cast<double*>(L);
-                CHOL_TRY(ozaki_panel_solve(Ld, work, status, batch, n, k, on_cluster, stream));
-                CHOL_TRY(ozaki_trailing_slice(Ld, work, status, batch, n, k, stream));
+                CHOL_TRY(ozaki_panel_solve(Ld, work, status, batch, n, k, on_cluster, cs));
+                CHOL_TRY(ozaki_trailing_slice(Ld, work, status, batch, n, k, cs));
                 if (!look) {
-                    CHOL_TRY(ozaki_trailing_gemm(Ld, work, status, batch, n, k, 0, stream));
+                    CHOL_TRY(ozaki_trailing_gemm(Ld, work, status, batch, n, k, 0, cs));
                     continue;
                 }
                 // block column k + 1 here (the last step's remaining columns,
                 // which include it, first); the columns right of it on the
                 // side stream, beside the next step's factor and panel solve
                 if (join.pending) {
-                    CHOL_TRY(cudaStreamWaitEvent(stream, sd.rest, 0));
+                    CHOL_TRY(cudaStreamWaitEvent(cs, sd.rest, 0));
                     join.pending = false;
                 }
-                CHOL_TRY(ozaki_trailing_gemm(Ld, work, status, batch, n, k, 1, stream));
+                CHOL_TRY(ozaki_trailing_gemm(Ld, work, status, batch, n, k, 1, cs));
                 if (nt - k - 1 >= 2) {
-                    CHOL_TRY(cudaEventRecord(sd.look, stream));
+                    CHOL_TRY(cudaEventRecord(sd.look, cs));
                     CHOL_TRY(cudaStreamWaitEvent(sd.s, sd.look, 0));
                     CHOL_TRY(ozaki_trailing_gemm(Ld, work, status, batch, n, k, 2, sd.s));
                     CHOL_TRY(cudaEventRecord(sd.rest, sd.s));
@@ -709,12 +745,12 @@ cudaError_t blocked_fwd(const T* A, T* L, int32_t* status, int64_t batch, int n,
             }
         }
         CHOL_TRY((launch_trsm<T, TRSM_FWD_PANEL>(L, L, status, batch, n, k0, kb, k0 + kb,
-                                                 n - k0 - kb, stream)));
+                                                 n - k0 - kb, cs)));
         const int m = nt - k - 1;
         GemmArgs<T> g{L, L, L, status, batch, n, tile, nt, k, 0, 0};
-        CHOL_TRY((launch_gemm<T, GEMM_FWD_TRAIL>(g, m * (m + 1) / 2, stream)));
+        CHOL_TRY((launch_gemm<T, GEMM_FWD_TRAIL>(g, m * (m + 1) / 2, cs)));
     }
-    return cudaSuccess;
+    return join.finish();
 }
 
 // Adjoint by the blocked reverse sweep of Murray (2016) over a left-looking
@@ -766,15 +802,17 @@ cudaError_t blocked_adj(const T* L, const T* Lbar, T* Abar, const int32_t* statu
     int dev = 0;
     bool look = false;
     if (oz && nt >= 3) {
-        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-        const bool idle = cudaStreamIsCapturing(stream, &cs) == cudaSuccess &&
-                          cs == cudaStreamCaptureStatusNone;
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        const bool idle = cudaStreamIsCapturing(stream, &cap) == cudaSuccess &&
+                          cap == cudaStreamCaptureStatusNone;
         cudaGetLastError();
         look = idle && side_stream(dev, sd);
     }
     std::unique_lock<std::mutex> side_lock;
     if (look) side_lock = std::unique_lock<std::mutex>(g_side_lock[dev]);
-    JoinSide join{stream, &sd};
+    JoinSide join{stream, stream, &sd};
+    CHOL_TRY(join.start(look));
+    const cudaStream_t cs = join.chain;  // the chain's stream
     for (int J = nt - 1; J >= 0; --J) {
         const int j0 = J * tile, kb = std::min(tile, n - j0), r0 = j0 + kb, nb = n - r0;
         if constexpr (std::is_same<T, double>::value) {
@@ -783,34 +821,34 @@ cudaError_t blocked_adj(const T* L, const T* Lbar, T* Abar, const int32_t* statu
                 // the side stream (below), after the update of column J - 1
                 const bool split_row = look && J >= 2;
                 if (nb > 0) {
-                    CHOL_TRY(ozaki_adj_solve(L, W, oz_work, status, batch, n, J, stream));
+                    CHOL_TRY(ozaki_adj_solve(L, W, oz_work, status, batch, n, J, cs));
                     CHOL_TRY(ozaki_adj_row(L, W, oz_work, status, batch, n, J, split_row ? 1 : 0,
-                                           stream));
+                                           cs));
                 }
                 if (ozaki_adj_lit_pays(batch)) {
                     // few matrices: the tile's adjoint as three parallel products
-                    CHOL_TRY(ozaki_adj_diag(L, W, oz_work, status, batch, n, J, stream));
+                    CHOL_TRY(ozaki_adj_diag(L, W, oz_work, status, batch, n, J, cs));
                 } else {
                     const size_t dsm = (size_t)kb * (kb + 1) * sizeof(T);
                     diag_rev_kernel<T, kThreads><<<dim3(1, grid_y(batch)), kThreads, dsm,
-                                                   stream>>>(L, W, status, batch, n, j0, kb);
+                                                   cs>>>(L, W, status, batch, n, j0, kb);
                     CHOL_TRY(cudaGetLastError());
                 }
                 // W_IK -= C_I L_JK (I > J) and W_JK -= (W_JJ + W_JJ^T) L_JK, K < J
                 if (J == 0) continue;
                 double* Wd = reinterpret_cast<double*>(W);
-                CHOL_TRY(ozaki_adj_upd_slice(Wd, oz_work, status, batch, n, J, stream));
+                CHOL_TRY(ozaki_adj_upd_slice(Wd, oz_work, status, batch, n, J, cs));
                 if (!look) {
-                    CHOL_TRY(ozaki_adj_upd_gemm(Wd, oz_work, status, batch, n, J, 0, stream));
+                    CHOL_TRY(ozaki_adj_upd_gemm(Wd, oz_work, status, batch, n, J, 0, cs));
                     continue;
                 }
                 if (join.pending) {
-                    CHOL_TRY(cudaStreamWaitEvent(stream, sd.rest, 0));
+                    CHOL_TRY(cudaStreamWaitEvent(cs, sd.rest, 0));
                     join.pending = false;
                 }
-                CHOL_TRY(ozaki_adj_upd_gemm(Wd, oz_work, status, batch, n, J, 1, stream));
+                CHOL_TRY(ozaki_adj_upd_gemm(Wd, oz_work, status, batch, n, J, 1, cs));
                 if (J >= 2) {
-                    CHOL_TRY(cudaEventRecord(sd.look, stream));
+                    CHOL_TRY(cudaEventRecord(sd.look, cs));
                     CHOL_TRY(cudaStreamWaitEvent(sd.s, sd.look, 0));
                     if (split_row && nb > 0)
                         CHOL_TRY(ozaki_adj_row(L, W, oz_work, status, batch, n, J, 2, sd.s));
@@ -822,33 +860,30 @@ cudaError_t blocked_adj(const T* L, const T* Lbar, T* Abar, const int32_t* statu
             }
         }
         if (nb > 0) {
-            CHOL_TRY((launch_trsm<T, TRSM_ADJ_M>(L, W, status, batch, n, j0, kb, r0, nb, stream)));
+            CHOL_TRY((launch_trsm<T, TRSM_ADJ_M>(L, W, status, batch, n, j0, kb, r0, nb, cs)));
             GemmArgs<T> g{W, L, W, status, batch, n, tile, nt, J, 0, 0};
             // enough blocks to fill the GPU twice over, splitting the long reduction
             const int64_t blocks = (int64_t)(J + 1) * subs * bmat;
             const int ks = (int)std::max<int64_t>(
                 1, std::min<int64_t>((2 * sms + blocks - 1) / blocks, (nb + 127) / 128));
-            CHOL_TRY((launch_gemm<T, GEMM_REV_ROW>(g, J + 1, stream, ks, nb)));
-            if (J > 0) CHOL_TRY((launch_gemm<T, GEMM_REV_UPD>(g, (nt - J - 1) * J, stream)));
+            CHOL_TRY((launch_gemm<T, GEMM_REV_ROW>(g, J + 1, cs, ks, nb)));
+            if (J > 0) CHOL_TRY((launch_gemm<T, GEMM_REV_UPD>(g, (nt - J - 1) * J, cs)));
         }
         const size_t dsm = (size_t)kb * (kb + 1) * sizeof(T);
         if (kb <= 32)
-            diag_rev_kernel<T, 64><<<dim3(1, grid_y(batch)), 64, dsm, stream>>>(L, W, status, batch,
+            diag_rev_kernel<T, 64><<<dim3(1, grid_y(batch)), 64, dsm, cs>>>(L, W, status, batch,
                                                                               n, j0, kb);
         else
-            diag_rev_kernel<T, kThreads><<<dim3(1, grid_y(batch)), kThreads, dsm, stream>>>(
+            diag_rev_kernel<T, kThreads><<<dim3(1, grid_y(batch)), kThreads, dsm, cs>>>(
                 L, W, status, batch, n, j0, kb);
         CHOL_TRY(cudaGetLastError());
         if (J > 0) {
             GemmArgs<T> g{W, L, W, status, batch, n, tile, nt, J, 0, 0};
-            CHOL_TRY((launch_gemm<T, GEMM_REV_SYM>(g, J, stream)));
+            CHOL_TRY((launch_gemm<T, GEMM_REV_SYM>(g, J, cs)));
         }
     }
-    // the side stream's last update lands before W is read below
-    if (join.pending) {
-        CHOL_TRY(cudaStreamWaitEvent(stream, sd.rest, 0));
-        join.pending = false;
-    }
+    // the chain and the side stream's last update land before W is read below
+    CHOL_TRY(join.finish());
     if (in_place) {
         if (status != nullptr)
             zero_lower_skipped_kernel<T><<<elementwise_blocks(total), kThreads, 0, stream>>>(

@@ -568,6 +568,23 @@ oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
             dst_r0 = job.out_r0;
             dst_c0 = p0 * kT;
         }
+        // The single-chunk updates (row per lane, below) read each lane's
+        // output row segment (cold rows of L or W) before the MMAs finish: an
+        // L2 prefetch of it here, which blocks no thread, then the loads into
+        // registers just before the wait for the accumulators, so the
+        // read-modify-write no longer waits on HBM after the MMAs.
+        constexpr bool kRowMode = !(MODE == OZ_REV_ROW || MODE == OZ_ASSIGN);
+        double rowv[kRowMode ? kN : 1];
+        if constexpr (kRowMode) {
+            const int row = job.out_r0 + tid;
+            if (row < g.n) {
+                const double* seg = out + (size_t)row * ld + job.out_c0;
+#pragma unroll
+                for (int l = 0; l < kN * 8 / 128; ++l)
+                    if (job.out_c0 + l * 16 < g.n)
+                        asm volatile("prefetch.global.L2 [%0];" ::"l"(seg + l * 16));
+            }
+        }
         for (int ch = job.ch_begin; ch < job.ch_end; ++ch, ++it) {
             const bool first = ch == job.ch_begin;
             size_t ablk, eaoff, bblk, eboff;
@@ -648,12 +665,24 @@ oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
                 ok = r < g.n && col < g.n && !(job.lower && col > r);
                 return out + (size_t)(r - dst_r0) * ld + (col - dst_c0);
             };
+            // (the MMA-issuing and copy-issuing lanes finish their loops first,
+            // so their warps do not split between those loops and these loads)
+            __syncwarp();
             if constexpr (kStaged) {
 #pragma unroll
                 for (int i = 0; i < kEC; ++i) {
                     bool okf;
                     const double* o = out_at(0, i, okf);
                     ov[i] = (need_old && okf) ? *o : 0.0;
+                }
+            } else {
+                const int row = job.out_r0 + tid;
+                const double* orow = out + (size_t)row * ld;
+#pragma unroll
+                for (int j = 0; j < kN; ++j) {
+                    const int col = job.out_c0 + j;
+                    rowv[j] =
+                        (row < g.n && col < g.n && !(job.lower && col > row)) ? orow[col] : 0.0;
                 }
             }
             const bool ok = __syncthreads_and(!failed) && mbar_wait(done, it & 1, max_polls);
@@ -714,13 +743,13 @@ oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
                 // next chunk's bulk copies into the same buffers (async proxy)
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             } else {
-                // out -= v 2^E, row per lane
+                // out = old - v 2^E, row per lane, the old values from rowv
                 const int32_t* ea = g.ea + b * g.ea_stride + eaoff;
                 const int32_t* eb = g.eb + b * g.eb_stride + eboff + job.h * kN;
                 const int er = ea[rl];
                 const int row = job.out_r0 + rl;
-                double* orow = out + (size_t)(row - dst_r0) * ld - dst_c0;
-#pragma unroll 1
+                double* orow = out + (size_t)row * ld;
+#pragma unroll
                 for (int cc = 0; cc < kN / 16; ++cc) {
                     uint32_t acc[kS][16];
 #pragma unroll
@@ -741,7 +770,7 @@ oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
                         if (er == kNonFinite || ec == kNonFinite)
                             orow[col] = __longlong_as_double(0x7ff8000000000000LL);  // NaN
                         else if (v != 0)
-                            orow[col] -= scale_int((long long)v, er + ec - 62);
+                            orow[col] = rowv[cc * 16 + j] - scale_int((long long)v, er + ec - 62);
                     }
                 }
             }

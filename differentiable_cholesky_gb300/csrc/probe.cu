@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include "chol_probe.h"
+#include "kernels.h"
 
 namespace {
 
@@ -173,4 +174,45 @@ extern "C" int chol_probe_dmma_peak(int32_t shape, int64_t iters, void* sink, do
         case CHOL_DMMA_M16N8K16: return run_dmma<3>(iters, sink, flops, s);
         default: return CHOL_EINVAL;
     }
+}
+
+// The dominant kernel of the float64 blocked path, timed alone: step k's
+// trailing update on the tensor cores (all lower tiles I >= J > k), with the
+// panel's rows sliced once before the timed launches.
+extern "C" int chol_probe_tc_update(int32_t n, void* L, int32_t k, int32_t reps, double* ms,
+                                    double* bf16_flops, double* fp64_equiv_flops, void* stream) {
+    if (n <= 128 || L == nullptr || ms == nullptr || bf16_flops == nullptr ||
+        fp64_equiv_flops == nullptr || reps <= 0)
+        return CHOL_EINVAL;
+    const int nt = (n + 127) / 128;
+    if (k < 0 || k >= nt - 1) return CHOL_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    double* Ld = static_cast<double*>(L);
+    void* work = nullptr;
+    if (cudaMallocAsync(&work, chol::ozaki_workspace_bytes(1, n), s) != cudaSuccess) {
+        cudaGetLastError();
+        return CHOL_ENOMEM;
+    }
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    cudaError_t e = cudaEventCreate(&e0);
+    if (e == cudaSuccess) e = cudaEventCreate(&e1);
+    if (e == cudaSuccess) e = chol::ozaki_trailing_slice(Ld, work, nullptr, 1, n, k, s);
+    if (e == cudaSuccess) e = cudaEventRecord(e0, s);
+    for (int r = 0; r < reps && e == cudaSuccess; ++r)
+        e = chol::ozaki_trailing_gemm(Ld, work, nullptr, 1, n, k, 0, s);
+    if (e == cudaSuccess) e = cudaEventRecord(e1, s);
+    if (e == cudaSuccess) e = cudaEventSynchronize(e1);
+    float t = 0.f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&t, e0, e1);
+    if (e0 != nullptr) cudaEventDestroy(e0);
+    if (e1 != nullptr) cudaEventDestroy(e1);
+    const cudaError_t ef = cudaFreeAsync(work, s);
+    if (e != cudaSuccess || ef != cudaSuccess) return CHOL_ECUDA;
+    const double m = nt - k - 1;
+    const double tiles = m * (m + 1) / 2;
+    const double per_tile = 2.0 * 128.0 * 128.0 * 128.0;
+    *ms = (double)t / reps;
+    *fp64_equiv_flops = tiles * per_tile / (*ms * 1e-3);
+    *bf16_flops = 28.0 * *fp64_equiv_flops;  // 28 digit products per element product
+    return CHOL_OK;
 }

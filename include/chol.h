@@ -258,7 +258,7 @@ CHOL_API const char* chol_strerror(int code);
 /* ABI version of this header: (major << 16) | minor. */
 CHOL_API int32_t chol_abi_version(void);
 
-#define CHOL_ABI_VERSION ((1 << 16) | 3)
+#define CHOL_ABI_VERSION ((1 << 16) | 4)
 
 #ifdef __cplusplus
 }

@@ -47,6 +47,24 @@ enum {
 CHOL_API int chol_probe_dmma_peak(int32_t shape, int64_t iters, void* sink, double* flops,
                                   void* stream);
 
+/*
+ * chol_probe_tc_update -- times the dominant kernel of the float64 blocked
+ * path, the trailing update on the bf16 tensor cores (exact digit-slice
+ * products), alone: for the float64 n x n row-major matrix L on the device
+ * (n > 128, 128-wide tiles) it slices the rows of panel k once, then launches
+ * `reps` times the update L_IJ -= L_Ik L_Jk^T of every lower tile I >= J > k,
+ * timed with CUDA events on `stream` (which it synchronises).  L's trailing
+ * tiles are modified: pass a scratch copy.  Writes the average time of one
+ * launch in ms, the rate of the bf16 digit products the tensor cores execute
+ * (28 products of 2 * 128^3 flops per tile) and the float64-equivalent rate
+ * (2 * 128^3 per tile), both in FLOP/s.  Takes a workspace with
+ * cudaMallocAsync on `stream`.  Returns CHOL_OK, CHOL_EINVAL (n <= 128, k not
+ * in [0, ceil(n/128) - 2], reps <= 0, null pointer), CHOL_ENOMEM or
+ * CHOL_ECUDA.
+ */
+CHOL_API int chol_probe_tc_update(int32_t n, void* L, int32_t k, int32_t reps, double* ms,
+                                  double* bf16_flops, double* fp64_equiv_flops, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -32,7 +32,7 @@ def test_library_exports_every_declared_symbol():
     lib = binding.load_library()
     for s in declared_symbols():
         assert hasattr(lib, s), f"{s} not exported"
-    assert lib.chol_abi_version() == (1 << 16) | 3
+    assert lib.chol_abi_version() == (1 << 16) | 4
 
 
 def test_strerror_covers_every_code():
@@ -70,6 +70,24 @@ def test_argument_checks_without_gpu():
     big = (ctypes.c_double * 64)()
     q = ctypes.addressof(big)
     assert lib.chol_fwd(1, 2, 1, q, q + 256, s, None) == CHOL_EINVAL
+
+
+def test_probe_argument_checks_without_gpu():
+    lib = binding.load_library()
+    d = ctypes.c_double()
+    p = ctypes.byref(d)
+    buf = (ctypes.c_double * 16)()
+    q = ctypes.addressof(buf)
+    lib.chol_probe_tc_update.argtypes = [ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32,
+                                         ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                                         ctypes.c_void_p, ctypes.c_void_p]
+    # n <= 128, k out of range, reps <= 0, null pointers: rejected before any GPU call
+    assert lib.chol_probe_tc_update(128, q, 0, 1, p, p, p, None) == CHOL_EINVAL
+    assert lib.chol_probe_tc_update(512, q, 3, 1, p, p, p, None) == CHOL_EINVAL
+    assert lib.chol_probe_tc_update(512, q, -1, 1, p, p, p, None) == CHOL_EINVAL
+    assert lib.chol_probe_tc_update(512, q, 0, 0, p, p, p, None) == CHOL_EINVAL
+    assert lib.chol_probe_tc_update(512, None, 0, 1, p, p, p, None) == CHOL_EINVAL
+    assert lib.chol_probe_tc_update(512, q, 0, 1, None, p, p, None) == CHOL_EINVAL
 
 
 def test_inplace_argument_checks_without_gpu():
