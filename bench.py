@@ -159,6 +159,11 @@ def launches_per_step(n: int, tile: int, batch: int = 1, float64: bool = False,
 # capture of that kernel (the summaries under profiles/).  Reported only while
 # the kernel source still hashes to what was captured; otherwise null.
 MEASURED_TRAFFIC = {
+    # the tensor-core trailing update of step 0 (profiles/oz_gemm_kernel_fwd_n4096.md,
+    # the full-size launch captured with the two DRAM counters alone: 1 pass)
+    "banded_8192": {"kernel": "tc_update", "bytes": (278.92 + 204.59) * 1e6,
+                    "source": "differentiable_cholesky_gb300/csrc/ozaki.cu",
+                    "code_sha256": "53cb91cafecbfa9b89e83f04283e9fde3206512f99eddf4750a3d5c07b05f8f3"},
     "batched_16": {"kernel": "adj", "bytes": (201.627904 + 23.920896) * 1e6,
                    "source": "differentiable_cholesky_gb300/csrc/small_kernels.cuh",
                    "code_sha256": "65783f7da4b7300d2208efe580890165b364e544a7082868691a0351e74e3502"},

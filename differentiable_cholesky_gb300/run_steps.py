@@ -31,12 +31,22 @@ def main():
     ap.add_argument("--warmup", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1)
     ap.add_argument("--fwd-only", action="store_true")
+    ap.add_argument("--tc-probe", type=int, default=None, metavar="K",
+                    help="instead: time the float64 tensor-core trailing update of step K "
+                         "once (chol_probe_tc_update) on an n x n Gram matrix")
     args = ap.parse_args()
 
     import torch
     from differentiable_cholesky_gb300 import binding
     from differentiable_cholesky_gb300 import workloads as W
 
+    if args.tc_probe is not None:
+        A = W.gram_spd(1, args.n, 0, 1.0, np.float64)[0]
+        At = torch.from_numpy(A).to(torch.device("cuda:0"))
+        ms, bf, fp = binding.probe_tc_update(At, k=args.tc_probe, reps=1)
+        print(f"tc update n={args.n} k={args.tc_probe}: {ms:.3f} ms, bf16 {bf / 1e12:.1f} TFLOP/s, "
+              f"float64-equivalent {fp / 1e12:.2f} TFLOP/s", flush=True)
+        return
     if args.workload:
         w = W.WORKLOADS[args.workload]()
         A, Lbar = w.A, w.adj_L

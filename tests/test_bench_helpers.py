@@ -53,6 +53,9 @@ def test_traffic_is_reported_only_for_the_captured_kernel_source():
     assert got is None or got == rec["bytes"]
     assert bench.measured_traffic("batched_16", "fwd" if rec["kernel"] == "adj" else "adj") is None
     assert bench.measured_traffic("banded_8192", "adj") is None
+    # the tensor-core update's record holds while ozaki.cu's code is the captured one
+    rec = bench.MEASURED_TRAFFIC["banded_8192"]
+    assert bench.measured_traffic("banded_8192", "tc_update") in (None, rec["bytes"])
 
 
 def test_reference_arm_prints_one_json_line():
