@@ -164,9 +164,9 @@ MEASURED_TRAFFIC = {
     "banded_8192": {"kernel": "tc_update", "bytes": (278.92 + 204.59) * 1e6,
                     "source": "differentiable_cholesky_gb300/csrc/ozaki.cu",
                     "code_sha256": "53cb91cafecbfa9b89e83f04283e9fde3206512f99eddf4750a3d5c07b05f8f3"},
-    "batched_16": {"kernel": "adj", "bytes": (201.627904 + 23.920896) * 1e6,
+    "batched_16": {"kernel": "adj", "bytes": (201.624320 + 24.680448) * 1e6,
                    "source": "differentiable_cholesky_gb300/csrc/small_kernels.cuh",
-                   "code_sha256": "65783f7da4b7300d2208efe580890165b364e544a7082868691a0351e74e3502"},
+                   "code_sha256": "4cab99b375b376b0c2a57aaea19c8dc55f9e22ad1b35cee7aa66e8af7dac280d"},
 }
 
 
