@@ -85,7 +85,7 @@ __device__ __forceinline__ int first_at_or_below(int rank, int lo) {
 }
 
 template <typename T, int C>
-__global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kClThreads, 1)
+__global__ void __launch_bounds__(kClThreads, 1)
 cl_potrf_kernel(T* __restrict__ L, int32_t* __restrict__ status, int64_t batch, int n, int k0,
                 int kb, T* __restrict__ Inv, int32_t* __restrict__ bal, int nt) {
     using Lay = ClLayout<C>;
@@ -300,23 +300,75 @@ cl_potrf_kernel(T* __restrict__ L, int32_t* __restrict__ status, int64_t batch, 
     cluster.sync();
 }
 
+// Launch with a cluster of C blocks (C = 16 is beyond the portable size of
+// 8: the kernel is allowed it, and it is used only where the device can
+// schedule such a cluster).
 template <typename T, int C>
 cudaError_t launch_cl_potrf(T* L, int32_t* status, int64_t batch, int n, int k0, int kb,
                             T* Inv, int32_t* bal, int nt, cudaStream_t stream) {
-    const size_t smem = cl_smem_bytes<T, C>(Inv != nullptr);
-    static std::atomic<uint64_t> smem_set{0};
-    cudaError_t e = allow_smem_once(cl_potrf_kernel<T, C>, cl_smem_bytes<T, C>(true), smem_set);
+    auto kern = cl_potrf_kernel<T, C>;
+    static std::atomic<uint64_t> attr_set{0};
+    cudaError_t e = once_per_device(attr_set, [&]() -> cudaError_t {
+        cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)cl_smem_bytes<T, C>(true));
+        if (r == cudaSuccess && C > 8)
+            r = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        return r;
+    });
     if (e != cudaSuccess) return e;
-    const unsigned gy = (unsigned)std::min<int64_t>(batch, 65535);
-    cl_potrf_kernel<T, C><<<dim3(C, gy), kClThreads, smem, stream>>>(L, status, batch, n, k0, kb,
-                                                                     Inv, bal, nt);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(C, (unsigned)std::min<int64_t>(batch, 65535));
+    cfg.blockDim = dim3(kClThreads);
+    cfg.dynamicSmemBytes = cl_smem_bytes<T, C>(Inv != nullptr);
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = C;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, L, status, batch, n, k0, kb, Inv, bal, nt);
+}
+
+// Whether a 16-block cluster of this kernel (with the inverse's shared
+// memory) fits on the current device; checked once per device.
+template <typename T>
+bool cluster16_fits() {
+    static PerDeviceInt fits;
+    return fits.get([] {
+        auto kern = cl_potrf_kernel<T, 16>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)cl_smem_bytes<T, 16>(true)) != cudaSuccess ||
+            cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+                cudaSuccess) {
+            cudaGetLastError();
+            return 1;  // 1: no (the cached value must be > 0)
+        }
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(16, 1);
+        cfg.blockDim = dim3(kClThreads);
+        cfg.dynamicSmemBytes = cl_smem_bytes<T, 16>(true);
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = 16;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            return 1;
+        }
+        return clusters >= 1 ? 2 : 1;  // 2: yes
+    }) == 2;
 }
 
 }  // namespace
 
 bool cluster_diag_pays(int64_t batch, int kb) {
-    // one cluster of 8 SMs per matrix while the clusters leave most SMs idle
+    // one cluster of 8 or 16 SMs per matrix while the clusters leave most SMs idle
     return kb > 32 && kb <= kTileMax && batch * 8 <= device_sm_count();
 }
 
@@ -325,6 +377,9 @@ cudaError_t cluster_potrf_diag(T* L, int32_t* status, int64_t batch, int n, int 
                                T* Inv, int32_t* bal, cudaStream_t stream) {
     if (kb <= 0 || kb > kTileMax) return cudaErrorInvalidValue;
     const int nt = (n + kTileMax - 1) / kTileMax;
+    // 16 SMs per matrix for one or a few matrices, where they fit
+    if (batch * 16 <= device_sm_count() && cluster16_fits<T>())
+        return launch_cl_potrf<T, 16>(L, status, batch, n, k0, kb, Inv, bal, nt, stream);
     return launch_cl_potrf<T, 8>(L, status, batch, n, k0, kb, Inv, bal, nt, stream);
 }
 

@@ -246,6 +246,24 @@ def test_cluster_diagonal_factor_matches_the_single_block_factor(n, tile, dtype)
     assert max_rel_err(G1, G40[-1:], lower=True) <= (1e-11 if dtype == np.float64 else 2e-5)
 
 
+def test_cluster_of_8_and_cluster_of_16_agree():
+    """One or a few matrices take a 16-SM cluster per diagonal tile (where the
+    device schedules one), up to SMs / 8 matrices an 8-SM cluster: the same
+    matrix factored in a batch of 1 and in a batch of 10 agrees to rounding,
+    with and without the tile's inverse (tile 128 float64: the tensor-core
+    panel solve uses it; tile 64 does not)."""
+    n = 300
+    for tile in (128, 64):
+        A1 = W.gram_spd(1, n, 93, 1.0, np.float64)
+        Lbar1 = W.tril_normal(1, n, 94, np.float64)
+        A10 = np.concatenate([W.gram_spd(9, n, 95, 1.0, np.float64), A1])
+        Lbar10 = np.concatenate([W.tril_normal(9, n, 96, np.float64), Lbar1])
+        L1, _, G1 = check(A1, Lbar1, np.float64, tile=tile)
+        L10, _, G10 = check(A10, Lbar10, np.float64, tile=tile)
+        assert max_rel_err(L1, L10[-1:]) <= 1e-13
+        assert max_rel_err(G1, G10[-1:], lower=True) <= 1e-11
+
+
 @pytest.mark.parametrize("tile", [64, 128])
 def test_cluster_diagonal_factor_status(tile):
     """Failing pivots inside the cluster factor: the first column whose pivot
