@@ -78,7 +78,7 @@ cudaError_t blocked_fwd(const T* A, T* L, int32_t* status, int64_t batch, int n,
 size_t blocked_fwd_workspace_bytes(bool real_double, int64_t batch, int n, int tile);
 
 // Diagonal-tile factor of the blocked forward on a cluster of 8 blocks
-// (8 SMs) per matrix: the tile L[k0 .. k0+kb, k0 .. k0+kb] (kb <= 128,
+// (8 SMs) per matrix, 16 for one or a few matrices where such a cluster fits: the tile L[k0 .. k0+kb, k0 .. k0+kb] (kb <= 128,
 // lower part) factored in place, status[b] = k0 + the failing column + 1.
 // With Inv (else null): also the tile's inverse into Inv[b] (128 x 128,
 // zeros above the diagonal and beyond kb) and, with bal, the balancing

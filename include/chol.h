@@ -100,7 +100,8 @@ enum {
  * diagonal factor; `stream` waits for it before the call's work ends, so the
  * call is ordered on `stream` like any other.  For batch * 8 <= SMs the
  * diagonal tiles (orders 33 .. 128, float and double) are factored by a
- * thread-block cluster of 8 SMs per matrix.
+ * thread-block cluster of 8 SMs per matrix (16 for batch * 16 <= SMs where
+ * the device schedules a 16-block cluster).
  */
 CHOL_API int chol_fwd(int64_t batch, int32_t n, int32_t dtype, const void* A, void* L,
              int32_t* status, void* stream);
