@@ -534,7 +534,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--e2e-steps", type=int, default=None,
-                    help="end-to-end steps (default: 20 for n <= 64, else 2)")
+                    help="end-to-end steps (default: 20 for n <= 64, else 6)")
     ap.add_argument("--e2e-chunks", type=int, default=2,
                     help="chunks of the batch in the end-to-end step (n <= 64)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -547,7 +547,7 @@ def main():
     if args.warmup is None:
         args.warmup = 20 if n <= 64 else 3
     if args.e2e_steps is None:
-        args.e2e_steps = 20 if n <= 64 else 2
+        args.e2e_steps = 20 if n <= 64 else 6
     args.warmup = max(args.warmup, 3)
 
     rank = int(os.environ.get("RANK", "0"))
