@@ -21,7 +21,7 @@
 //      arithmetic on the float64 bits.  The digits go to a workspace in the
 //      tensor cores' shared-memory tile layout (8 x 8 core matrices), so that
 //      one bulk copy moves a whole pipeline stage.
-//   2. oz_gemm_kernel (one CTA per 128 x 64 half of an output tile): per
+//   2. oz_gemm_kernel (one CTA per 128 x 32 quarter of an output tile): per
 //      128-long reduction chunk, for d = 0..6 the products of digit slices
 //      p + q = d are accumulated in one fp32 TMEM accumulator,
 //      acc_d = sum_{p+q=d} D_p(A) D_q(B)^T.  Every product is an integer of at
@@ -86,15 +86,28 @@ __device__ __forceinline__ int block_offset(int m, int k, int p) {
     return (k / kKC) * (kS * kSliceElems) + p * kSliceElems + core_offset(m, k % kKC);
 }
 
-// v * 2^E for an integer |v| <= 2^62: one int64 -> float64 conversion, then
-// the exponent moved by an integer add where the result stays normal (|v| in
-// [1, 2^62], so the new exponent lies in [E, E + 62]); ldexp otherwise.
+// v * 2^E for an integer |v| <= 2^62, rounded to the nearest float64 (ties
+// to even).  Where the result is a normal number it is assembled from v's
+// bits by integer instructions (leading-zero count, shift, round on the 11
+// bits below the 53 kept): an int64 -> float64 conversion would occupy the
+// FP64 pipe, the scarce one here, once per output entry.  Otherwise (a
+// result outside the normal range) the conversion and ldexp, which give the
+// same value wherever both apply.
 __device__ __forceinline__ double scale_int(long long v, int E) {
     if (v == 0) return 0.0;
-    const double vd = __ll2double_rn(v);
-    if (E >= -1022 && E <= 1023 - 62)
-        return __longlong_as_double(__double_as_longlong(vd) + ((long long)E << 52));
-    return ldexp(vd, E);
+    const unsigned long long sgn = (unsigned long long)v & 0x8000000000000000ull;
+    unsigned long long a = v < 0 ? 0ull - (unsigned long long)v : (unsigned long long)v;
+    const int lz = __clzll((long long)a);
+    const int ex = 63 - lz + E;  // exponent of v's leading bit, scaled
+    if (ex < -1022 || ex > 1022) return ldexp(__ll2double_rn(v), E);
+    a <<= lz;                                   // leading bit at bit 63
+    unsigned long long m = a >> 11;             // 53 bits, bit 52 set
+    const unsigned rem = (unsigned)a & 0x7ffu;  // the bits rounded off
+    m += (rem > 0x400u || (rem == 0x400u && (m & 1ull))) ? 1ull : 0ull;
+    // bit 52 of m (and a carry out of the rounding, m = 2^53) adds to the
+    // biased exponent ex + 1022, giving ex + 1023 (or ex + 1024, mantissa 0)
+    return __longlong_as_double(
+        (long long)(sgn | (((unsigned long long)(ex + 1022) << 52) + m)));
 }
 
 // Scale exponent of the 128-long vector a warp holds four values per lane:
@@ -323,17 +336,20 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46);
 }
 
-// Instruction descriptor of kind::f16: fp32 accumulator (bits 4-5 = 1), bf16
-// A and B (bits 7-9 and 10-12 = 1), both K-major, N >> 3 at bit 17, M >> 4 at
-// bit 24.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kN >> 3) << 17) |
-                            ((uint32_t)(kT >> 4) << 24);
+// Instruction descriptor of kind::f16 for an M = 128, N-wide product: fp32
+// accumulator (bits 4-5 = 1), bf16 A and B (bits 7-9 and 10-12 = 1), both
+// K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t mma_idesc(int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(kT >> 4) << 24);
+}
 
-__device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t acc) {
+__device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t acc) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-        "l"(a), "l"(b), "r"(kIdesc), "r"(acc)
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
 }
 
@@ -384,7 +400,7 @@ __device__ __forceinline__ void tri_index(int t, int& i, int& j) {
 
 
 // ---------------------------------------------------------------------------
-// The three contractions.  Per output half tile (128 rows x 64 columns) a CTA
+// The contractions.  Per output quarter tile (128 rows x 32 columns) a CTA
 // runs one or more 128-long reduction chunks, each with its own operand
 // blocks and scales.
 // ---------------------------------------------------------------------------
@@ -422,7 +438,7 @@ struct OzJob {
     int out_r0, out_c0;   // output half tile origin
     bool lower;           // diagonal tile: only entries with col <= row
     int ch_begin, ch_end; // reduction chunks of this CTA
-    int h;                // which 64-column half of the B block
+    int h;                // which 32-column quarter of the B block
     int split;            // which part of a split reduction (OZ_REV_ROW)
 };
 
@@ -620,19 +636,22 @@ oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
                     tc_fence_after();
                     const uint32_t sa = smem_u32(stages + s_ * kStageBytes);
                     const uint32_t sb = sa + kStageA;
+                    // The stage holds B's slices stacked (slice q in rows
+                    // 32q .. 32q + 31 of one K-major operand), so the product
+                    // of D_p(A) with slices 0 .. 6-p (N = 32 (7 - p)) puts
+                    // slice q's part in TMEM columns 32 (p + q) .., which is
+                    // accumulator p + q: 7 MMAs per 16-step instead of 28,
+                    // each reading its A slice from shared memory once.  The
+                    // first (p = 0) initialises all 7 accumulators.
 #pragma unroll
-                    for (int d = 0; d < kS; ++d) {
+                    for (int p = 0; p < kS; ++p) {
 #pragma unroll
-                        for (int p = 0; p <= d; ++p) {
-                            const int q = d - p;
-#pragma unroll
-                            for (int ks = 0; ks < kKC / 16; ++ks) {
-                                const uint64_t da =
-                                    smem_desc(sa + p * (kSliceElems * 2) + ks * 256, 128, kSbo);
-                                const uint64_t db =
-                                    smem_desc(sb + q * (kN * kKC * 2) + ks * 256, 128, kSbo);
-                                tc_mma(tmem + d * kN, da, db, (kc | p | ks) != 0);
-                            }
+                        for (int ks = 0; ks < kKC / 16; ++ks) {
+                            const uint64_t da =
+                                smem_desc(sa + p * (kSliceElems * 2) + ks * 256, 128, kSbo);
+                            const uint64_t db = smem_desc(sb + ks * 256, 128, kSbo);
+                            tc_mma(tmem + p * kN, da, db, mma_idesc((kS - p) * kN),
+                                   (kc | p | ks) != 0);
                         }
                     }
                     tc_commit(empty + s_);  // the stage may be refilled once these finish
