@@ -157,16 +157,18 @@ int adj_impl(int64_t batch, int32_t n, const void* L, const void* Lbar, void* Ab
         }
     }
     const bool in_place = !accumulate && Lbar == Abar;
-    tile = pick_tile(tile, n, batch, sizeof(T), std::is_same<T, double>::value && !in_place);
-    if (in_place)  // the sweep needs no workspace
-        return to_code(chol::blocked_adj<T>(l, lb, ab, status, batch, n, tile, nullptr, false,
-                                            nullptr, stream));
-    // float64 with 128-wide tiles also takes the tensor-core updates' operand
+    tile = pick_tile(tile, n, batch, sizeof(T), std::is_same<T, double>::value);
+    // float64 with 128-wide tiles takes the tensor-core updates' operand
     // slices, after the batch * n * n working matrices (256-byte aligned)
     const size_t oz_bytes = (std::is_same<T, double>::value && tile == 128)
                                 ? chol::ozaki_adj_workspace_bytes(batch, n)
                                 : 0;
-    const size_t wbytes = (bytes + 255) / 256 * 256;
+    // in place the sweep runs on the caller's buffer: no working matrices,
+    // and no workspace at all for the FMA-pipe updates
+    if (in_place && oz_bytes == 0)
+        return to_code(chol::blocked_adj<T>(l, lb, ab, status, batch, n, tile, nullptr, false,
+                                            nullptr, stream));
+    const size_t wbytes = in_place ? 0 : (bytes + 255) / 256 * 256;
     void* work = nullptr;
     if (cudaMallocAsync(&work, wbytes + oz_bytes, stream) != cudaSuccess) {
         cudaGetLastError();
@@ -174,7 +176,8 @@ int adj_impl(int64_t batch, int32_t n, const void* L, const void* Lbar, void* Ab
     }
     void* oz = oz_bytes > 0 ? static_cast<void*>(static_cast<char*>(work) + wbytes) : nullptr;
     const int rc = to_code(chol::blocked_adj<T>(l, lb, ab, status, batch, n, tile,
-                                                static_cast<T*>(work), accumulate, oz, stream));
+                                                in_place ? nullptr : static_cast<T*>(work),
+                                                accumulate, oz, stream));
     if (cudaFreeAsync(work, stream) != cudaSuccess) return CHOL_ECUDA;
     return rc;
 }

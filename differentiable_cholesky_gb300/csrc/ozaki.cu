@@ -68,6 +68,9 @@ constexpr int kTmemCols = 256;               // 7 accumulators x 32 columns, rou
 constexpr uint32_t kSbo = kKC / 8 * 128;     // bytes between 8-row core-matrix groups
 constexpr size_t kGemmSmem = 128 + (size_t)kStages * kStageBytes + 128;
 constexpr int32_t kNonFinite = INT_MIN;      // exponent sentinel of a non-finite vector
+constexpr int kOzThreads = 256;              // 8 warps: two per TMEM lane quadrant
+constexpr int kColHalves = kOzThreads / 128;  // column groups per lane quadrant
+constexpr int kWarpCols = kN / kColHalves;    // output columns per epilogue warp: 16
 constexpr int kEC = 8;                       // output columns per epilogue pass
 constexpr int kEpP = kEC + 1;                // pitch (doubles) of the epilogue's staged rows
 constexpr int kEpR = 32 / kEC;               // rows per warp-wide access of a pass
@@ -108,6 +111,21 @@ __device__ __forceinline__ double scale_int(long long v, int E) {
     // biased exponent ex + 1022, giving ex + 1023 (or ex + 1024, mantissa 0)
     return __longlong_as_double(
         (long long)(sgn | (((unsigned long long)(ex + 1022) << 52) + m)));
+}
+
+// v = sum_d acc_d 256^(6-d) from the 7 fp32 accumulators of one entry (exact
+// integers below 2^24 in magnitude), modulo 2^64, which is exact since
+// |v| <= 2^62: digits 3..6 by 64-bit multiply-adds of 32-bit values, digits
+// 0..2 in 32 bits (their sum is only needed modulo 2^32 once shifted by 32).
+template <int W>
+__device__ __forceinline__ long long combine_acc(const uint32_t (&acc)[kS][W], int j) {
+    int a[kS];
+#pragma unroll
+    for (int d = 0; d < kS; ++d) a[d] = __float2int_rn(__uint_as_float(acc[d][j]));
+    const long long lo = (long long)a[3] * (1 << 24) + (long long)a[4] * (1 << 16) +
+                         (long long)a[5] * (1 << 8) + (long long)a[6];
+    const unsigned hi = (unsigned)a[0] * 65536u + (unsigned)a[1] * 256u + (unsigned)a[2];
+    return (long long)((unsigned long long)lo + ((unsigned long long)hi << 32));
 }
 
 // Scale exponent of the 128-long vector a warp holds four values per lane:
@@ -367,17 +385,7 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// 16 consecutive fp32 columns of this warp's 32 TMEM lanes.
-__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&v)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-        "%14,%15}, [%16];"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
-          "=r"(v[14]), "=r"(v[15])
-        : "r"(taddr)
-        : "memory");
-}
+// 8 consecutive fp32 columns of this warp's 32 TMEM lanes.
 __device__ __forceinline__ void tc_ld8(uint32_t taddr, uint32_t (&v)[8]) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                  : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
@@ -532,10 +540,12 @@ __device__ __forceinline__ void oz_chunk(const OzArgs& g, int p0, int p1, int ch
 }
 
 // Warp 0 owns TMEM and (lane 0) issues the MMAs; warp 1 lane 0 issues the
-// bulk copies; all four warps run the epilogue (warp w reads TMEM lanes
-// 32w .. 32w + 31, i.e. output rows 32w .. of the tile).
+// bulk copies; all eight warps run the epilogue: warp w reads TMEM lanes
+// 32 (w % 4) .. + 31 (output rows 32 (w % 4) .. of the tile), columns
+// 16 (w / 4) .. + 15 of the CTA's 32, so that four warps per scheduler hide
+// the epilogue's latencies (two CTAs per SM, at most 128 registers a thread).
 template <int MODE>
-__global__ void __launch_bounds__(128, 2)
+__global__ void __launch_bounds__(kOzThreads, 2)
 oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     // full[kStages], empty[kStages], done
@@ -546,6 +556,10 @@ oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + 64);
     unsigned char* stages = smem_raw + 128;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3;                // TMEM lane quadrant
+    const int cw = (warp >> 2) * kWarpCols;   // first of this warp's output columns
+    const int rl = quad * 32 + lane;          // this thread's row of the tile
+    const uint32_t tlane = (uint32_t)(quad * 32) << 16;
 
     int p0 = 0, p1 = 0;
     const OzJob job = oz_job<MODE>(g, blockIdx.x, p0, p1);
@@ -590,16 +604,13 @@ oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
         // registers just before the wait for the accumulators, so the
         // read-modify-write no longer waits on HBM after the MMAs.
         constexpr bool kRowMode = !(MODE == OZ_REV_ROW || MODE == OZ_ASSIGN);
-        double rowv[kRowMode ? kN : 1];
+        double rowv[kRowMode ? kWarpCols : 1];
         if constexpr (kRowMode) {
-            const int row = job.out_r0 + tid;
-            if (row < g.n) {
-                const double* seg = out + (size_t)row * ld + job.out_c0;
-#pragma unroll
-                for (int l = 0; l < kN * 8 / 128; ++l)
-                    if (job.out_c0 + l * 16 < g.n)
-                        asm volatile("prefetch.global.L2 [%0];" ::"l"(seg + l * 16));
-            }
+            // one 128-byte line: 16 doubles from a multiple of 16 columns
+            const int row = job.out_r0 + rl;
+            if (row < g.n && job.out_c0 + cw < g.n)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(out + (size_t)row * ld +
+                                                              job.out_c0 + cw));
         }
         for (int ch = job.ch_begin; ch < job.ch_end; ++ch, ++it) {
             const bool first = ch == job.ch_begin;
@@ -674,13 +685,13 @@ oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
             //   accumulators are ready, the next while the current ones are
             //   combined.
             constexpr bool kStaged = MODE == OZ_REV_ROW || MODE == OZ_ASSIGN;
-            const int wrow0 = job.out_r0 + warp * 32;
+            const int wrow0 = job.out_r0 + quad * 32;
             const int ecol = lane % kEC;
             const bool need_old = MODE != OZ_ASSIGN && !(partial && first);
             double ov[kEC];
             auto out_at = [&](int cc, int i, bool& ok) -> double* {
                 const int r = wrow0 + kEpR * i + lane / kEC;
-                const int col = job.out_c0 + cc * kEC + ecol;
+                const int col = job.out_c0 + cw + cc * kEC + ecol;
                 ok = r < g.n && col < g.n && !(job.lower && col > r);
                 return out + (size_t)(r - dst_r0) * ld + (col - dst_c0);
             };
@@ -695,46 +706,39 @@ oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
                     ov[i] = (need_old && okf) ? *o : 0.0;
                 }
             } else {
-                const int row = job.out_r0 + tid;
+                const int row = job.out_r0 + rl;
                 const double* orow = out + (size_t)row * ld;
 #pragma unroll
-                for (int j = 0; j < kN; ++j) {
-                    const int col = job.out_c0 + j;
+                for (int j = 0; j < kWarpCols; ++j) {
+                    const int col = job.out_c0 + cw + j;
                     rowv[j] =
                         (row < g.n && col < g.n && !(job.lower && col > row)) ? orow[col] : 0.0;
                 }
             }
             const bool ok = __syncthreads_and(!failed) && mbar_wait(done, it & 1, max_polls);
             tc_fence_after();
-            const int rl = warp * 32 + lane;
             if (!__all_sync(0xffffffffu, ok)) {
                 if (tid == 0 && g.fail != nullptr) g.fail[b] = -1;  // reported, not hung
                 failed = true;
             } else if constexpr (kStaged) {
                 const int32_t* ea = g.ea + b * g.ea_stride + eaoff;
-                const int32_t* eb = g.eb + b * g.eb_stride + eboff + job.h * kN;
+                const int32_t* eb = g.eb + b * g.eb_stride + eboff + job.h * kN + cw;
                 const int er = ea[rl];
                 double* stg = reinterpret_cast<double*>(stages) + warp * (32 * kEpP);
 #pragma unroll 1
-                for (int cc = 0; cc < kN / kEC; ++cc) {
+                for (int cc = 0; cc < kWarpCols / kEC; ++cc) {
                     uint32_t acc[kS][kEC];
 #pragma unroll
                     for (int d = 0; d < kS; ++d)
-                        tc_ld8(tmem + ((uint32_t)(warp * 32) << 16) + d * kN + cc * kEC, acc[d]);
+                        tc_ld8(tmem + tlane + d * kN + cw + cc * kEC, acc[d]);
                     tc_wait_ld();
 #pragma unroll
                     for (int j = 0; j < kEC; ++j) {
                         const int ec = eb[cc * kEC + j];
-                        // sum_d acc_d 256^(6-d), modulo 2^64 (exact: |sum| <= 2^62)
-                        unsigned long long v = 0;
-#pragma unroll
-                        for (int d = 0; d < kS; ++d)
-                            v = v * 256ull + (unsigned long long)(long long)__float2int_rn(
-                                                 __uint_as_float(acc[d][j]));
                         stg[lane * kEpP + j] =
                             (er == kNonFinite || ec == kNonFinite)
                                 ? __longlong_as_double(0x7ff8000000000000LL)  // NaN
-                                : scale_int((long long)v, er + ec - 62);
+                                : scale_int(combine_acc(acc, j), er + ec - 62);
                     }
                     __syncwarp();
                     // the next pass's old values, in flight while these are
@@ -744,7 +748,7 @@ oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
                     for (int i = 0; i < kEC; ++i) {
                         bool okn = false;
                         const double* o = out_at(cc + 1, i, okn);
-                        nx[i] = (cc + 1 < kN / kEC && need_old && okn) ? *o : 0.0;
+                        nx[i] = (cc + 1 < kWarpCols / kEC && need_old && okn) ? *o : 0.0;
                     }
 #pragma unroll
                     for (int i = 0; i < kEC; ++i) {
@@ -764,32 +768,30 @@ oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
             } else {
                 // out = old - v 2^E, row per lane, the old values from rowv
                 const int32_t* ea = g.ea + b * g.ea_stride + eaoff;
-                const int32_t* eb = g.eb + b * g.eb_stride + eboff + job.h * kN;
+                const int32_t* eb = g.eb + b * g.eb_stride + eboff + job.h * kN + cw;
                 const int er = ea[rl];
                 const int row = job.out_r0 + rl;
                 double* orow = out + (size_t)row * ld;
 #pragma unroll
-                for (int cc = 0; cc < kN / 16; ++cc) {
-                    uint32_t acc[kS][16];
+                for (int cc = 0; cc < kWarpCols / kEC; ++cc) {
+                    // the column exponents first: their loads overlap the TMEM reads
+                    int ecv[kEC];
 #pragma unroll
-                    for (int d = 0; d < kS; ++d)
-                        tc_ld16(tmem + ((uint32_t)(warp * 32) << 16) + d * kN + cc * 16, acc[d]);
+                    for (int j = 0; j < kEC; ++j) ecv[j] = eb[cc * kEC + j];
+                    uint32_t acc[kS][kEC];
+#pragma unroll
+                    for (int d = 0; d < kS; ++d) tc_ld8(tmem + tlane + d * kN + cw + cc * kEC, acc[d]);
                     tc_wait_ld();
                     if (row >= g.n) continue;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int col = job.out_c0 + cc * 16 + j;
+                    for (int j = 0; j < kEC; ++j) {
+                        const int col = job.out_c0 + cw + cc * kEC + j;
                         if (col >= g.n || (job.lower && col > row)) continue;
-                        const int ec = eb[cc * 16 + j];
-                        unsigned long long v = 0;
-#pragma unroll
-                        for (int d = 0; d < kS; ++d)
-                            v = v * 256ull + (unsigned long long)(long long)__float2int_rn(
-                                                 __uint_as_float(acc[d][j]));
-                        if (er == kNonFinite || ec == kNonFinite)
+                        const long long v = combine_acc(acc, j);
+                        if (er == kNonFinite || ecv[j] == kNonFinite)
                             orow[col] = __longlong_as_double(0x7ff8000000000000LL);  // NaN
                         else if (v != 0)
-                            orow[col] = rowv[cc * 16 + j] - scale_int((long long)v, er + ec - 62);
+                            orow[col] = rowv[cc * kEC + j] - scale_int(v, er + ecv[j] - 62);
                     }
                 }
             }
@@ -829,7 +831,8 @@ cudaError_t launch_oz(const OzArgs& g, unsigned jobs, cudaStream_t stream) {
         return r;
     });
     if (e != cudaSuccess) return e;
-    oz_gemm_kernel<MODE><<<dim3(jobs, gy(g.batch)), 128, kGemmSmem, stream>>>(g, kMbarPolls);
+    oz_gemm_kernel<MODE><<<dim3(jobs, gy(g.batch)), kOzThreads, kGemmSmem, stream>>>(g,
+                                                                                  kMbarPolls);
     return cudaGetLastError();
 }
 

@@ -202,13 +202,16 @@ CHOL_API int chol_fwd_inplace(int64_t batch, int32_t n, int32_t dtype, void* A, 
  *                matrix with non-zero status gets zeros there.  The upper
  *                triangle is never written.
  *   status  in : as chol_adj (or NULL).  Must not overlap adj.
- *   tile    as chol_adj_ex.  No workspace is taken for any n: the blocked
- *           reverse sweep runs on `adj` itself (it never touches the upper
- *           triangle), so the call allocates nothing.
- * Results are bit-identical to chol_adj_ex into a zeroed adj_A, except for
- * float64 with 128-wide tiles and n > 128, where chol_adj_ex takes its
- * tensor-core updates and this call keeps the FMA-pipe ones (no workspace);
- * there the two agree to about 1e-12 relative.
+ *   tile    as chol_adj_ex.  The blocked reverse sweep runs on `adj` itself
+ *           (it never touches the upper triangle), so no working copy of
+ *           the matrices is taken: with the FMA-pipe updates the call
+ *           allocates nothing; float64 with 128-wide tiles (the default for
+ *           few large matrices) takes only the tensor-core updates' operand
+ *           slices and inverses that chol_adj takes beside its working
+ *           matrices (cudaMallocAsync/cudaFreeAsync on `stream`,
+ *           CHOL_ENOMEM on failure).
+ * Results are bit-identical to chol_adj_ex with the same tile into a zeroed
+ * adj_A (up to the sign of zeros).
  */
 CHOL_API int chol_adj_inplace(int64_t batch, int32_t n, int32_t dtype, const void* L, void* adj,
                               const int32_t* status, int32_t tile, void* stream);

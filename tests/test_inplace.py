@@ -10,8 +10,11 @@ from parity_util import TOL_ADJ, TOL_L, max_rel_err
 
 pytestmark = pytest.mark.gpu
 
+# (300 and 520 float64 at tile 128, the default for few such matrices, take
+# the tensor-core updates with the lookahead, in place as out of place)
 CASES = [(8, np.float32, 0), (16, np.float32, 0), (16, np.float64, 0), (20, np.float32, 0),
-         (64, np.float32, 0), (65, np.float64, 0), (130, np.float64, 32), (130, np.float32, 64)]
+         (64, np.float32, 0), (65, np.float64, 0), (130, np.float64, 32), (130, np.float32, 64),
+         (300, np.float64, 0), (520, np.float64, 128)]
 
 
 def _inputs(batch, n, dtype, seed):

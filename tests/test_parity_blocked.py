@@ -167,10 +167,10 @@ def test_tensor_core_update_wide_dynamic_range():
 
 @pytest.mark.parametrize("n", [200, 384])
 def test_tensor_core_adjoint_agrees_with_the_fp64_sweep(n):
-    """float64 with 128-wide tiles: chol_adj takes the adjoint's two large
-    updates on the tensor cores (digit slices), while chol_adj_inplace runs
-    the same reverse sweep on the FP64 pipe; both match the oracle and each
-    other."""
+    """float64 with 128-wide tiles: chol_adj (and chol_adj_inplace) take the
+    adjoint's two large updates on the tensor cores (digit slices), while
+    chol_adj_noalloc runs the same reverse sweep on the FP64 pipe; both match
+    the oracle and each other."""
     import torch
     from differentiable_cholesky_gb300 import binding
     A = W.gram_spd(3, n, 47 + n, 1.0, np.float64)
@@ -178,7 +178,12 @@ def test_tensor_core_adjoint_agrees_with_the_fp64_sweep(n):
     dev = torch.device("cuda:0")
     Lt, st = binding.chol_fwd(torch.from_numpy(A).to(dev), tile=128)
     G_tc = binding.chol_adj(Lt, torch.from_numpy(Lbar).to(dev), status=st, tile=128)
-    G_ip = binding.chol_adj_inplace(Lt, torch.from_numpy(Lbar).to(dev), status=st, tile=128)
+    G_ip = torch.zeros_like(Lt)
+    Lb = torch.from_numpy(Lbar).to(dev)
+    lib = binding.load_library()
+    assert lib.chol_adj_noalloc(3, n, 1, Lt.data_ptr(), Lb.data_ptr(), G_ip.data_ptr(),
+                                st.data_ptr(), 128,
+                                torch.cuda.current_stream().cuda_stream) == 0
     torch.cuda.synchronize()
     L_ref, _ = oracle.potrf(A)
     G_ref = oracle.potrf_adj(L_ref, Lbar)
