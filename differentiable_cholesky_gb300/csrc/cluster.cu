@@ -76,8 +76,29 @@ size_t cl_smem_bytes(bool with_inverse) {
 
 __device__ __forceinline__ int packed(int i, int j) { return i * (i + 1) / 2 + j; }
 
-__device__ __forceinline__ float rsqrt_t(float x) { return rsqrtf(x); }
-__device__ __forceinline__ double rsqrt_t(double x) { return rsqrt(x); }
+// 1 / sqrt(d) on the pivot chain.  float: rsqrtf.  double: a float seed
+// (d's leading 24 bits as a float, by integer arithmetic; then rsqrtf, about
+// 2^-22 relative error) and one step of Halley's iteration for the
+// reciprocal square root in FP64, y1 = y0 (1 + e/2 + 3 e^2/8) with
+// e = 1 - d y0^2, whose error is about (5/16) e^3 plus the rounding of its
+// five FP64 operations: the chain's FP64 instructions (a warp issues one per
+// 64 cycles here) are fewer than with rsqrt.  Pivots outside the float range,
+// and those that are not positive or not finite (the status decides about
+// them), take rsqrt.
+__device__ __forceinline__ float pivot_rsqrt(float d) { return rsqrtf(d); }
+__device__ __forceinline__ double pivot_rsqrt(double d) {
+    const long long bits = __double_as_longlong(d);
+    const int E = (int)((bits >> 52) & 0x7ff) - 1023;
+    if (bits <= 0 || E < -125 || E > 125) return rsqrt(d);
+    const float f = __int_as_float(((E + 127) << 23) | (int)((bits >> 29) & 0x7fffff));
+    const int fb = __float_as_int(rsqrtf(f));
+    const double y0 = __longlong_as_double(
+        ((long long)(((fb >> 23) & 0xff) - 127 + 1023) << 52) | ((long long)(fb & 0x7fffff) << 29));
+    const double h = d * y0;
+    const double e = fma(-h, y0, 1.0);
+    const double t = fma(0.375, e, 0.5);
+    return fma(y0, e * t, y0);
+}
 
 // Rows of the held set at or below row `lo`: t = first .. cnt - 1.
 template <int C>
@@ -99,6 +120,7 @@ cl_potrf_kernel(T* __restrict__ L, int32_t* __restrict__ status, int64_t batch, 
     T* colbuf = sm + Lay::col_off;
     T* rinv = sm + Lay::rinv_off;
     __shared__ int s_fail;
+    __shared__ T s_piv[kPW];
 
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = (int)cluster.block_rank();
@@ -134,40 +156,39 @@ cl_potrf_kernel(T* __restrict__ L, int32_t* __restrict__ status, int64_t batch, 
                 }
             }
             cluster.sync();
-            // B. the diagonal block (rows c0 .. c0 + 15 of pb), four warps: warp
-            // u holds columns u, u + 4, u + 8, u + 12 of row lane % 16
-            if (warp < 4) {
+            // B. the diagonal block (rows c0 .. c0 + 15 of pb), eight warps:
+            // warp u holds columns u (lanes 0-15) and u + 8 (lanes 16-31), row
+            // lane % 16, so that each column step costs every warp one FP64
+            // instruction (a warp issues one per 64 cycles here) and the next
+            // pivot's warp is never held up by updates of its other columns
+            {
                 const int r = lane & 15;
-                T a[4];
-#pragma unroll
-                for (int s = 0; s < 4; ++s) a[s] = pb[(c0 + r) * kPP + warp + 4 * s];
-#pragma unroll
+                const int col = warp + 8 * (lane >> 4);
+                T a = pb[(c0 + r) * kPP + col];
                 for (int j = 0; j < kPW; ++j) {
                     T* cb = colbuf + (j & 1) * kPW;
-                    if (warp == (j & 3)) {
-                        const T d = __shfl_sync(0xffffffffu, a[j >> 2], j);
-                        if (!(d > T(0)) && j < w && lane == 0) atomicMin(&s_fail, j);
-                        const T ri = rsqrt_t(d);
-                        T l = a[j >> 2] * ri;
-                        if (r == j) l = d * ri;
-                        a[j >> 2] = l;
-                        if (lane < 16) cb[r] = l;
-                        if (lane == 0) rinv[j] = j < w ? ri : T(0);
+                    if (warp == (j & 7)) {
+                        // (row j's own entry is d, so l_jj = d / sqrt(d) is the
+                        // same product; the pivot's sign is checked after the
+                        // loop, off the chain)
+                        const T d = __shfl_sync(0xffffffffu, a, 16 * (j >> 3) + j);
+                        const T ri = pivot_rsqrt(d);
+                        if ((lane >> 4) == (j >> 3)) {
+                            a *= ri;
+                            cb[r] = a;
+                        }
+                        if (lane == 0) {
+                            rinv[j] = j < w ? ri : T(0);
+                            s_piv[j] = d;
+                        }
                     }
-                    asm volatile("bar.sync 1, 128;" ::: "memory");
-                    const T lij = cb[r];
-                    // columns k > j of this warp, the nearest first (it is the
-                    // next pivot's column for one of the warps)
-#pragma unroll
-                    for (int s = 0; s < 4; ++s) {
-                        const int k = warp + 4 * s;
-                        if (k > j) a[s] = fma(-lij, cb[k], a[s]);
-                    }
+                    __syncthreads();
+                    if (col > j) a = fma(-cb[r], cb[col], a);
                 }
-                if (lane < 16) {
-#pragma unroll
-                    for (int s = 0; s < 4; ++s) pb[(c0 + r) * kPP + warp + 4 * s] = a[s];
-                }
+                pb[(c0 + r) * kPP + col] = a;
+                // the first pivot that is not > 0 (zero, negative, NaN); every
+                // pivot was written before the last column's barrier
+                if (warp == 0 && lane < w && !(s_piv[lane] > T(0))) atomicMin(&s_fail, lane);
             }
             __syncthreads();
             if (s_fail < w) {
