@@ -33,7 +33,8 @@ def main():
     ap.add_argument("--fwd-only", action="store_true")
     ap.add_argument("--tc-probe", type=int, default=None, metavar="K",
                     help="instead: time the float64 tensor-core trailing update of step K "
-                         "once (chol_probe_tc_update) on an n x n Gram matrix")
+                         "once (chol_probe_tc_update) on the factor of the workload's first "
+                         "matrix, or on an n x n Gram matrix")
     args = ap.parse_args()
 
     import torch
@@ -41,10 +42,18 @@ def main():
     from differentiable_cholesky_gb300 import workloads as W
 
     if args.tc_probe is not None:
-        A = W.gram_spd(1, args.n, 0, 1.0, np.float64)[0]
-        At = torch.from_numpy(A).to(torch.device("cuda:0"))
+        dev = torch.device("cuda:0")
+        if args.workload:
+            # as bench.py: on the factor of the workload's first matrix
+            w = W.WORKLOADS[args.workload]()
+            At, _ = binding.chol_fwd(torch.from_numpy(w.A[:1]).to(dev), tile=128)
+            At = At[0].clone()
+            n = w.n
+        else:
+            At = torch.from_numpy(W.gram_spd(1, args.n, 0, 1.0, np.float64)[0]).to(dev)
+            n = args.n
         ms, bf, fp = binding.probe_tc_update(At, k=args.tc_probe, reps=1)
-        print(f"tc update n={args.n} k={args.tc_probe}: {ms:.3f} ms, bf16 {bf / 1e12:.1f} TFLOP/s, "
+        print(f"tc update n={n} k={args.tc_probe}: {ms:.3f} ms, bf16 {bf / 1e12:.1f} TFLOP/s, "
               f"float64-equivalent {fp / 1e12:.2f} TFLOP/s", flush=True)
         return
     if args.workload:
