@@ -397,6 +397,18 @@ __device__ __forceinline__ void tc_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// 32-byte global accesses (four doubles; the address 32-byte aligned).
+__device__ __forceinline__ void ld_global_v4(const double* p, double (&v)[4]) {
+    asm volatile("ld.global.v4.f64 {%0, %1, %2, %3}, [%4];"
+                 : "=d"(v[0]), "=d"(v[1]), "=d"(v[2]), "=d"(v[3])
+                 : "l"(p));
+}
+__device__ __forceinline__ void st_global_v4(double* p, const double (&v)[4]) {
+    asm volatile("st.global.v4.f64 [%0], {%1, %2, %3, %4};" ::"l"(p), "d"(v[0]), "d"(v[1]),
+                 "d"(v[2]), "d"(v[3])
+                 : "memory");
+}
+
 // (i, j) of the t-th entry of a row-major enumeration of a lower triangle.
 __device__ __forceinline__ void tri_index(int t, int& i, int& j) {
     int r = (int)((sqrt(8.0 * t + 1.0) - 1.0) * 0.5);
@@ -685,6 +697,12 @@ oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
             //   accumulators are ready, the next while the current ones are
             //   combined.
             constexpr bool kStaged = MODE == OZ_REV_ROW || MODE == OZ_ASSIGN;
+            // Row per lane, a whole 16-column segment of an off-diagonal tile
+            // with 32-byte aligned rows: the old values and the results move
+            // four doubles at a time (each warp-wide access touches 32 rows'
+            // lines, so fewer accesses mean fewer L1 wavefronts).
+            const bool vec = !kStaged && !job.lower && job.out_c0 + cw + kWarpCols <= g.n &&
+                             ld % 4 == 0 && (reinterpret_cast<uintptr_t>(out) & 31) == 0;
             const int wrow0 = job.out_r0 + quad * 32;
             const int ecol = lane % kEC;
             const bool need_old = MODE != OZ_ASSIGN && !(partial && first);
@@ -704,6 +722,16 @@ oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
                     bool okf;
                     const double* o = out_at(0, i, okf);
                     ov[i] = (need_old && okf) ? *o : 0.0;
+                }
+            } else if (vec) {
+                const int row = job.out_r0 + rl;
+                const double* seg = out + (size_t)row * ld + job.out_c0 + cw;
+#pragma unroll
+                for (int q = 0; q < kWarpCols / 4; ++q) {
+                    double t[4] = {0.0, 0.0, 0.0, 0.0};
+                    if (row < g.n) ld_global_v4(seg + 4 * q, t);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) rowv[4 * q + e] = t[e];
                 }
             } else {
                 const int row = job.out_r0 + rl;
@@ -783,6 +811,29 @@ oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
                     for (int d = 0; d < kS; ++d) tc_ld8(tmem + tlane + d * kN + cw + cc * kEC, acc[d]);
                     tc_wait_ld();
                     if (row >= g.n) continue;
+                    if (vec) {
+                        double* seg = orow + job.out_c0 + cw + cc * kEC;
+#pragma unroll
+                        for (int q = 0; q < kEC / 4; ++q) {
+                            double nv[4];
+                            bool changed = false;
+#pragma unroll
+                            for (int h2 = 0; h2 < 4; ++h2) {
+                                const int j = 4 * q + h2;
+                                const long long v = combine_acc(acc, j);
+                                nv[h2] = rowv[cc * kEC + j];
+                                if (er == kNonFinite || ecv[j] == kNonFinite) {
+                                    nv[h2] = __longlong_as_double(0x7ff8000000000000LL);  // NaN
+                                    changed = true;
+                                } else if (v != 0) {
+                                    nv[h2] -= scale_int(v, er + ecv[j] - 62);
+                                    changed = true;
+                                }
+                            }
+                            if (changed) st_global_v4(seg + 4 * q, nv);
+                        }
+                        continue;
+                    }
 #pragma unroll
                     for (int j = 0; j < kEC; ++j) {
                         const int col = job.out_c0 + cw + cc * kEC + j;
