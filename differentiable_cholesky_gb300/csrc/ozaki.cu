@@ -693,9 +693,8 @@ oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
             //   go through the stage buffers in passes of kEC = 8 columns, so
             //   the output is written by whole 64-byte row segments; the old
             //   values are read 8 at a time (lane l on column l % 8 of row
-            //   l / 8 of each group of 4 rows), the first ones before the
-            //   accumulators are ready, the next while the current ones are
-            //   combined.
+            //   l / 8 of each group of 4 rows), all of them before the
+            //   accumulators are ready.
             constexpr bool kStaged = MODE == OZ_REV_ROW || MODE == OZ_ASSIGN;
             // Row per lane, a whole 16-column segment of an off-diagonal tile
             // with 32-byte aligned rows: the old values and the results move
@@ -706,7 +705,8 @@ oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
             const int wrow0 = job.out_r0 + quad * 32;
             const int ecol = lane % kEC;
             const bool need_old = MODE != OZ_ASSIGN && !(partial && first);
-            double ov[kEC];
+            constexpr int kPasses = kWarpCols / kEC;
+            double ov[kStaged ? kPasses : 1][kEC];
             auto out_at = [&](int cc, int i, bool& ok) -> double* {
                 const int r = wrow0 + kEpR * i + lane / kEC;
                 const int col = job.out_c0 + cw + cc * kEC + ecol;
@@ -717,12 +717,15 @@ oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
             // so their warps do not split between those loops and these loads)
             __syncwarp();
             if constexpr (kStaged) {
+                // every pass's old values, in flight while the MMAs finish
 #pragma unroll
-                for (int i = 0; i < kEC; ++i) {
-                    bool okf;
-                    const double* o = out_at(0, i, okf);
-                    ov[i] = (need_old && okf) ? *o : 0.0;
-                }
+                for (int cc = 0; cc < kPasses; ++cc)
+#pragma unroll
+                    for (int i = 0; i < kEC; ++i) {
+                        bool okf;
+                        const double* o = out_at(cc, i, okf);
+                        ov[cc][i] = (need_old && okf) ? *o : 0.0;
+                    }
             } else if (vec) {
                 const int row = job.out_r0 + rl;
                 const double* seg = out + (size_t)row * ld + job.out_c0 + cw;
@@ -753,40 +756,32 @@ oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
                 const int32_t* eb = g.eb + b * g.eb_stride + eboff + job.h * kN + cw;
                 const int er = ea[rl];
                 double* stg = reinterpret_cast<double*>(stages) + warp * (32 * kEpP);
-#pragma unroll 1
-                for (int cc = 0; cc < kWarpCols / kEC; ++cc) {
+#pragma unroll
+                for (int cc = 0; cc < kPasses; ++cc) {
+                    int ecv[kEC];
+#pragma unroll
+                    for (int j = 0; j < kEC; ++j) ecv[j] = eb[cc * kEC + j];
                     uint32_t acc[kS][kEC];
 #pragma unroll
                     for (int d = 0; d < kS; ++d)
                         tc_ld8(tmem + tlane + d * kN + cw + cc * kEC, acc[d]);
                     tc_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < kEC; ++j) {
-                        const int ec = eb[cc * kEC + j];
+                    for (int j = 0; j < kEC; ++j)
                         stg[lane * kEpP + j] =
-                            (er == kNonFinite || ec == kNonFinite)
+                            (er == kNonFinite || ecv[j] == kNonFinite)
                                 ? __longlong_as_double(0x7ff8000000000000LL)  // NaN
-                                : scale_int(combine_acc(acc, j), er + ec - 62);
-                    }
+                                : scale_int(combine_acc(acc, j), er + ecv[j] - 62);
                     __syncwarp();
-                    // the next pass's old values, in flight while these are
-                    // combined and stored
-                    double nx[kEC];
-#pragma unroll
-                    for (int i = 0; i < kEC; ++i) {
-                        bool okn = false;
-                        const double* o = out_at(cc + 1, i, okn);
-                        nx[i] = (cc + 1 < kWarpCols / kEC && need_old && okn) ? *o : 0.0;
-                    }
 #pragma unroll
                     for (int i = 0; i < kEC; ++i) {
                         bool oks;
                         double* o = out_at(cc, i, oks);
                         const double t = stg[(kEpR * i + lane / kEC) * kEpP + ecol];
                         if (oks)
-                            *o = MODE == OZ_ASSIGN ? t
-                                                   : (partial ? (first ? t : ov[i] + t) : ov[i] - t);
-                        ov[i] = nx[i];
+                            *o = MODE == OZ_ASSIGN
+                                     ? t
+                                     : (partial ? (first ? t : ov[cc][i] + t) : ov[cc][i] - t);
                     }
                     __syncwarp();
                 }
