@@ -624,8 +624,16 @@ oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(out + (size_t)row * ld +
                                                               job.out_c0 + cw));
         }
+        // staged modes: the running values of this thread's outputs across the
+        // reduction chunks of the job (the old value minus the chunks so far, or
+        // the partial sum), in registers: the output is read before the first
+        // chunk and written after the last one
+        constexpr bool kStagedMode = MODE == OZ_REV_ROW || MODE == OZ_ASSIGN;
+        constexpr int kPasses = kWarpCols / kEC;
+        double ov[kStagedMode ? kPasses : 1][kEC];
         for (int ch = job.ch_begin; ch < job.ch_end; ++ch, ++it) {
             const bool first = ch == job.ch_begin;
+            const bool last = ch == job.ch_end - 1;
             size_t ablk, eaoff, bblk, eboff;
             oz_chunk<MODE>(g, p0, p1, ch, ablk, eaoff, bblk, eboff);
             const bf16* blkA = g.a + b * g.a_stride + ablk;
@@ -691,10 +699,10 @@ oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
             // - the split row update (partial tiles, hot in L2 or written
             //   without a read) and the panel solves (written without a read)
             //   go through the stage buffers in passes of kEC = 8 columns, so
-            //   the output is written by whole 64-byte row segments; the old
-            //   values are read 8 at a time (lane l on column l % 8 of row
-            //   l / 8 of each group of 4 rows), all of them before the
-            //   accumulators are ready.
+            //   the output is written by whole 64-byte row segments, after the
+            //   job's last chunk; the old values are read 8 at a time (lane l
+            //   on column l % 8 of row l / 8 of each group of 4 rows), all of
+            //   them before the first chunk's accumulators are ready.
             constexpr bool kStaged = MODE == OZ_REV_ROW || MODE == OZ_ASSIGN;
             // Row per lane, a whole 16-column segment of an off-diagonal tile
             // with 32-byte aligned rows: the old values and the results move
@@ -704,9 +712,7 @@ oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
                              ld % 4 == 0 && (reinterpret_cast<uintptr_t>(out) & 31) == 0;
             const int wrow0 = job.out_r0 + quad * 32;
             const int ecol = lane % kEC;
-            const bool need_old = MODE != OZ_ASSIGN && !(partial && first);
-            constexpr int kPasses = kWarpCols / kEC;
-            double ov[kStaged ? kPasses : 1][kEC];
+            const bool need_old = MODE != OZ_ASSIGN && !partial;
             auto out_at = [&](int cc, int i, bool& ok) -> double* {
                 const int r = wrow0 + kEpR * i + lane / kEC;
                 const int col = job.out_c0 + cw + cc * kEC + ecol;
@@ -717,15 +723,18 @@ oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
             // so their warps do not split between those loops and these loads)
             __syncwarp();
             if constexpr (kStaged) {
-                // every pass's old values, in flight while the MMAs finish
+                // every pass's old values, in flight while the first chunk's
+                // MMAs finish
+                if (first) {
 #pragma unroll
-                for (int cc = 0; cc < kPasses; ++cc)
+                    for (int cc = 0; cc < kPasses; ++cc)
 #pragma unroll
-                    for (int i = 0; i < kEC; ++i) {
-                        bool okf;
-                        const double* o = out_at(cc, i, okf);
-                        ov[cc][i] = (need_old && okf) ? *o : 0.0;
-                    }
+                        for (int i = 0; i < kEC; ++i) {
+                            bool okf;
+                            const double* o = out_at(cc, i, okf);
+                            ov[cc][i] = (need_old && okf) ? *o : 0.0;
+                        }
+                }
             } else if (vec) {
                 const int row = job.out_r0 + rl;
                 const double* seg = out + (size_t)row * ld + job.out_c0 + cw;
@@ -778,10 +787,10 @@ oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
                         bool oks;
                         double* o = out_at(cc, i, oks);
                         const double t = stg[(kEpR * i + lane / kEC) * kEpP + ecol];
-                        if (oks)
-                            *o = MODE == OZ_ASSIGN
-                                     ? t
-                                     : (partial ? (first ? t : ov[cc][i] + t) : ov[cc][i] - t);
+                        ov[cc][i] = MODE == OZ_ASSIGN
+                                        ? t
+                                        : (partial ? (first ? t : ov[cc][i] + t) : ov[cc][i] - t);
+                        if (oks && last) *o = ov[cc][i];
                     }
                     __syncwarp();
                 }
