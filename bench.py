@@ -159,11 +159,12 @@ def launches_per_step(n: int, tile: int, batch: int = 1, float64: bool = False,
 # capture of that kernel (the summaries under profiles/).  Reported only while
 # the kernel source still hashes to what was captured; otherwise null.
 MEASURED_TRAFFIC = {
-    # the tensor-core trailing update of step 0 (profiles/oz_gemm_kernel_fwd_n4096.md,
-    # the full-size launch captured with the two DRAM counters alone: 1 pass)
-    "banded_8192": {"kernel": "tc_update", "bytes": (278.92 + 204.59) * 1e6,
+    # the tensor-core trailing update of step 0 on the workload's own factor
+    # (the launch this bench times; captured at full size with the two DRAM
+    # counters alone: 1 pass)
+    "banded_8192": {"kernel": "tc_update", "bytes": (279.01 + 3.00) * 1e6,
                     "source": "differentiable_cholesky_gb300/csrc/ozaki.cu",
-                    "code_sha256": "53cb91cafecbfa9b89e83f04283e9fde3206512f99eddf4750a3d5c07b05f8f3"},
+                    "code_sha256": "be95d5c04d6673ab1b0582071e46762337c3143d59a399fd3524d50d254170f8"},
     "batched_16": {"kernel": "adj", "bytes": (201.624320 + 24.680448) * 1e6,
                    "source": "differentiable_cholesky_gb300/csrc/small_kernels.cuh",
                    "code_sha256": "4cab99b375b376b0c2a57aaea19c8dc55f9e22ad1b35cee7aa66e8af7dac280d"},
