@@ -27,8 +27,9 @@
 //      acc_d = sum_{p+q=d} D_p(A) D_q(B)^T.  Every product is an integer of at
 //      most 2^14 and an accumulator sums at most 7 * 128 of them (< 2^24), so
 //      fp32 holds it exactly.  The epilogue combines v = sum_d acc_d
-//      256^(6-d) in int64 (exact: by Cauchy-Schwarz |v| <= 2^62) and applies
-//      out -= v 2^(e_r + e_c - 62) with one FP64 fused multiply-add per chunk.
+//      256^(6-d) in int64 (exact: by Cauchy-Schwarz |v| <= 2^62), forms the
+//      float64 v 2^(e_r + e_c - 62) from v's bits (one rounding) and applies
+//      out -= that with one FP64 subtraction per chunk.
 //
 // The result differs from an FP64 GEMM only by the dropped digit products
 // (p + q >= 7) and the truncation below 2^-55, both below 2^-53 of the
