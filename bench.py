@@ -119,10 +119,10 @@ def launches_per_step(n: int, tile: int, batch: int = 1, float64: bool = False,
     fwd = 1 + nt                              # copy, diagonal factors
     for k in range(nt - 1):
         if tc_fwd:
-            # inverse (unless the cluster factor made it), 2 slicings, assign;
-            # slicing, update (lookahead: column k + 1, then the rest while
-            # there is one)
-            fwd += (3 if cluster else 4) + 1 + ((1 + (1 if nt - k - 1 >= 2 else 0)) if look else 1)
+            # inverse (unless the cluster factor made it), one slicing of the
+            # panel and the inverse, assign; slicing, update (lookahead: column
+            # k + 1, then the rest while there is one)
+            fwd += (2 if cluster else 3) + 1 + ((1 + (1 if nt - k - 1 >= 2 else 0)) if look else 1)
         else:
             fwd += 2                          # panel solve, trailing update
     if not tc:

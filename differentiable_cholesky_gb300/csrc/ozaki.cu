@@ -201,9 +201,17 @@ struct Bal {
     int sign;
 };
 
+// x 2^s, exact: an integer add to the exponent field where x and the result
+// are normal numbers, ldexp otherwise (zeros, subnormals, non-finite values,
+// results out of the normal range).
 __device__ __forceinline__ double balance(double x, const Bal& bal, int64_t b, int r) {
     if (bal.sign == 0) return x;
-    return ldexp(x, bal.sign * bal.exp[b * bal.stride + bal.off + r]);
+    const int s = bal.sign * bal.exp[b * bal.stride + bal.off + r];
+    const long long bits = __double_as_longlong(x);
+    const int E = (int)((bits >> 52) & 0x7ff);
+    if (E != 0 && E != 0x7ff && E + s >= 1 && E + s <= 0x7fe)
+        return __longlong_as_double(bits + ((long long)s << 52));
+    return ldexp(x, s);
 }
 
 // ---------------------------------------------------------------------------
@@ -215,15 +223,34 @@ __device__ __forceinline__ double balance(double x, const Bal& bal, int64_t b, i
 // matrix S + S^T of the lower triangle of that diagonal block: the upper half
 // mirrors the lower one and the diagonal is doubled.  Rows >= n are zeros.
 // ---------------------------------------------------------------------------
+// One launch may slice two such row ranges (of two matrices): the warps
+// past the first range's rows take the second's.
+struct RowSlice {
+    const double* src;
+    bf16* dst;
+    int32_t* ex;
+    int n, row0, nrows, col0;
+    bool sym_first;
+    size_t dst_stride, ex_stride;
+    Bal bal;
+};
+
 __global__ void __launch_bounds__(256)
-slice_rows_kernel(const double* __restrict__ src, bf16* __restrict__ dst,
-                  int32_t* __restrict__ ex, const int32_t* __restrict__ status, int64_t batch,
-                  int n, int row0, int nrows, int col0, bool sym_first, size_t dst_stride,
-                  size_t ex_stride, Bal bal) {
+slice_rows_kernel(RowSlice s0, RowSlice s1, const int32_t* __restrict__ status, int64_t batch) {
     const int lane = threadIdx.x & 31;
-    const int rl = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
-    if (rl >= nrows) return;
-    const int row = row0 + rl;
+    int rl = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const bool second = rl >= s0.nrows;
+    if (second) rl -= s0.nrows;
+    const RowSlice sl = second ? s1 : s0;
+    if (rl >= sl.nrows) return;
+    const double* __restrict__ src = sl.src;
+    bf16* __restrict__ dst = sl.dst;
+    int32_t* __restrict__ ex = sl.ex;
+    const int n = sl.n, col0 = sl.col0;
+    const bool sym_first = sl.sym_first;
+    const size_t dst_stride = sl.dst_stride, ex_stride = sl.ex_stride;
+    const Bal bal = sl.bal;
+    const int row = sl.row0 + rl;
     for (int64_t b = blockIdx.y; b < batch; b += gridDim.y) {
         if (status != nullptr && status[b] != 0) continue;
         const double* S = src + (size_t)b * n * n;
@@ -894,14 +921,22 @@ cudaError_t launch_oz(const OzArgs& g, unsigned jobs, cudaStream_t stream) {
 
 constexpr size_t kColSmem = (size_t)kT * (kColW + 1) * sizeof(double);
 
+cudaError_t launch_slice_rows2(const RowSlice& s0, const RowSlice& s1, const int32_t* status,
+                               int64_t batch, cudaStream_t stream) {
+    const int64_t rows = (int64_t)std::max(s0.nrows, 0) + std::max(s1.nrows, 0);
+    if (rows <= 0) return cudaSuccess;
+    const unsigned blocks = (unsigned)((rows * 32 + 255) / 256);
+    slice_rows_kernel<<<dim3(blocks, gy(batch)), 256, 0, stream>>>(s0, s1, status, batch);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_slice_rows(const double* src, bf16* dst, int32_t* ex, const int32_t* status,
                               int64_t batch, int n, int row0, int nrows, int col0, bool sym,
                               size_t dst_stride, size_t ex_stride, Bal bal, cudaStream_t stream) {
     if (nrows <= 0) return cudaSuccess;
-    const unsigned blocks = (unsigned)((nrows * 32 + 255) / 256);
-    slice_rows_kernel<<<dim3(blocks, gy(batch)), 256, 0, stream>>>(
-        src, dst, ex, status, batch, n, row0, nrows, col0, sym, dst_stride, ex_stride, bal);
-    return cudaGetLastError();
+    const RowSlice s0{src, dst, ex, n, row0, nrows, col0, sym, dst_stride, ex_stride, bal};
+    const RowSlice s1{nullptr, nullptr, nullptr, 0, 0, 0, 0, false, 0, 0, Bal{nullptr, 0, 0, 0}};
+    return launch_slice_rows2(s0, s1, status, batch, stream);
 }
 
 cudaError_t launch_slice_cols(const double* src, bf16* dst, int32_t* ex, const int32_t* status,
@@ -1313,13 +1348,14 @@ cudaError_t ozaki_panel_solve(double* L, void* work, int32_t* status, int64_t ba
     if (e != cudaSuccess) return e;
     // L_Ik <- L_Ik G^-T: A = the panel's rows (reduction over the tile's
     // columns, divided by the balancing factors), B = rows of G^-1 (multiplied)
+    // (both in one launch: the panel's rows, then the inverse's)
     bf16* rs = w.rs[k & 1];
     int32_t* ers = w.ers[k & 1];
-    e = launch_slice_rows(L, rs, ers, status, batch, n, (k + 1) * kT, m * kT, k * kT, false,
-                          stride, estride, Bal{w.iv.bal, bstride, 0, -1}, stream);
-    if (e != cudaSuccess) return e;
-    e = launch_slice_rows(w.iv.inv, w.iv.sl, w.iv.ex, status, batch, kT, 0, kT, 0, false,
-                          kBlockElems, kT, Bal{w.iv.bal, bstride, k * kT, 1}, stream);
+    const RowSlice panel{L, rs, ers, n, (k + 1) * kT, m * kT, k * kT, false, stride, estride,
+                         Bal{w.iv.bal, bstride, 0, -1}};
+    const RowSlice ginv{w.iv.inv, w.iv.sl, w.iv.ex, kT, 0, kT, 0, false, kBlockElems, kT,
+                        Bal{w.iv.bal, bstride, k * kT, 1}};
+    e = launch_slice_rows2(panel, ginv, status, batch, stream);
     if (e != cudaSuccess) return e;
     OzArgs g{L, rs, ers, w.iv.sl, w.iv.ex, stride, estride, kBlockElems, kT, status, status,
              batch, n, nt, k, 1, nullptr};
