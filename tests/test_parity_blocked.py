@@ -281,3 +281,37 @@ def test_cluster_diagonal_factor_status(tile):
         Lbar = W.tril_normal(2, n, 72, np.float64)
         L, st, G = check(A, Lbar, np.float64, tile=tile)
         assert list(st) == [col + 1, 0]
+
+
+@pytest.mark.parametrize("n", [300, 520])
+def test_tensor_core_path_with_element_aligned_buffers(n):
+    """float64 buffers that start 8 bytes past a 32-byte boundary (the header
+    allows element-aligned pointers): the tensor-core updates' 32-byte row
+    accesses give way to element accesses, with the same results bit for bit."""
+    import torch
+    from differentiable_cholesky_gb300 import binding
+    dev = torch.device("cuda:0")
+    batch = 2
+    A = W.gram_spd(batch, n, 211 + n, 1.0, np.float64)
+    Lbar = W.tril_normal(batch, n, 212 + n, np.float64)
+    At, Lbt = torch.from_numpy(A).to(dev), torch.from_numpy(Lbar).to(dev)
+    L, st = binding.chol_fwd(At, tile=128)
+    G = binding.chol_adj(L, Lbt, status=st, tile=128)
+
+    def shifted(x=None):
+        buf = torch.zeros(batch * n * n + 1, dtype=torch.float64, device=dev)
+        v = buf[1:].view(batch, n, n)
+        assert v.data_ptr() % 32 == 8
+        if x is not None:
+            v.copy_(x)
+        return v
+    Au, Lbu, Lu, Gu = shifted(At), shifted(Lbt), shifted(), shifted()
+    stu = torch.empty(batch, dtype=torch.int32, device=dev)
+    binding.chol_fwd(Au, Lu, stu, tile=128)
+    binding.chol_adj(Lu, Lbu, Gu, status=stu, tile=128)
+    torch.cuda.synchronize()
+    assert torch.equal(st, stu)
+    assert torch.equal(L, Lu)
+    assert torch.equal(G, Gu)
+    L_ref, _ = oracle.potrf(A)
+    assert max_rel_err(Lu.cpu().numpy(), L_ref) <= 1e-12
