@@ -110,6 +110,7 @@ template <typename T, int C>
 __global__ void __launch_bounds__(kClThreads, 1)
 cl_potrf_kernel(T* __restrict__ L, int32_t* __restrict__ status, int64_t batch, int n, int k0,
                 int kb, T* __restrict__ Inv, int32_t* __restrict__ bal, int nt) {
+    pdl_wait();
     using Lay = ClLayout<C>;
     constexpr int AP = Lay::AP;
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -343,13 +344,16 @@ cudaError_t launch_cl_potrf(T* L, int32_t* status, int64_t batch, int n, int k0,
     cfg.blockDim = dim3(kClThreads);
     cfg.dynamicSmemBytes = cl_smem_bytes<T, C>(Inv != nullptr);
     cfg.stream = stream;
-    cudaLaunchAttribute at[1];
+    cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = C;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
+    // programmatic dependent launch (the kernel waits for its predecessor first)
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, L, status, batch, n, k0, kb, Inv, bal, nt);
 }
 

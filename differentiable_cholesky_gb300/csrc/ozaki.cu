@@ -237,6 +237,7 @@ struct RowSlice {
 
 __global__ void __launch_bounds__(256)
 slice_rows_kernel(RowSlice s0, RowSlice s1, const int32_t* __restrict__ status, int64_t batch) {
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     int rl = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const bool second = rl >= s0.nrows;
@@ -309,6 +310,7 @@ slice_cols_kernel(const double* __restrict__ src, bf16* __restrict__ dst,
                   int32_t* __restrict__ ex, const int32_t* __restrict__ status, int64_t batch,
                   int n, int c_begin, bool tri, int k_fixed, bool lower_only, size_t dst_stride,
                   size_t ex_stride, Bal bal) {
+    pdl_wait();
     extern __shared__ __align__(128) unsigned char smem_raw[];
     double* tile = reinterpret_cast<double*>(smem_raw);  // 128 x (kColW + 1)
     constexpr int P = kColW + 1;
@@ -587,6 +589,7 @@ __device__ __forceinline__ void oz_chunk(const OzArgs& g, int p0, int p1, int ch
 template <int MODE>
 __global__ void __launch_bounds__(kOzThreads, 2)
 oz_gemm_kernel(OzArgs g, uint32_t max_polls) {
+    pdl_wait();
     extern __shared__ __align__(128) unsigned char smem_raw[];
     // full[kStages], empty[kStages], done
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw);
@@ -914,9 +917,8 @@ cudaError_t launch_oz(const OzArgs& g, unsigned jobs, cudaStream_t stream) {
         return r;
     });
     if (e != cudaSuccess) return e;
-    oz_gemm_kernel<MODE><<<dim3(jobs, gy(g.batch)), kOzThreads, kGemmSmem, stream>>>(g,
-                                                                                  kMbarPolls);
-    return cudaGetLastError();
+    return launch_pdl(oz_gemm_kernel<MODE>, dim3(jobs, gy(g.batch)), dim3(kOzThreads), kGemmSmem,
+                      stream, g, (uint32_t)kMbarPolls);
 }
 
 constexpr size_t kColSmem = (size_t)kT * (kColW + 1) * sizeof(double);
@@ -926,8 +928,8 @@ cudaError_t launch_slice_rows2(const RowSlice& s0, const RowSlice& s1, const int
     const int64_t rows = (int64_t)std::max(s0.nrows, 0) + std::max(s1.nrows, 0);
     if (rows <= 0) return cudaSuccess;
     const unsigned blocks = (unsigned)((rows * 32 + 255) / 256);
-    slice_rows_kernel<<<dim3(blocks, gy(batch)), 256, 0, stream>>>(s0, s1, status, batch);
-    return cudaGetLastError();
+    return launch_pdl(slice_rows_kernel, dim3(blocks, gy(batch)), dim3(256), 0, stream, s0, s1,
+                      status, batch);
 }
 
 cudaError_t launch_slice_rows(const double* src, bf16* dst, int32_t* ex, const int32_t* status,
@@ -947,10 +949,9 @@ cudaError_t launch_slice_cols(const double* src, bf16* dst, int32_t* ex, const i
     static std::atomic<uint64_t> smem_set{0};
     cudaError_t e = allow_smem_once(slice_cols_kernel, kColSmem, smem_set);
     if (e != cudaSuccess) return e;
-    slice_cols_kernel<<<dim3(count * kColGroups, gy(batch)), kColThreads, kColSmem, stream>>>(
-        src, dst, ex, status, batch, n, c_begin, tri, k_fixed, lower_only, dst_stride, ex_stride,
-        bal);
-    return cudaGetLastError();
+    return launch_pdl(slice_cols_kernel, dim3(count * kColGroups, gy(batch)), dim3(kColThreads),
+                      kColSmem, stream, src, dst, ex, status, batch, n, c_begin, tri, k_fixed,
+                      lower_only, dst_stride, ex_stride, bal);
 }
 
 inline int tiles_of(int n) { return (n + kT - 1) / kT; }
@@ -962,6 +963,7 @@ __global__ void __launch_bounds__(256)
 split_reduce_kernel(double* __restrict__ W, const double* __restrict__ part,
                     const int32_t* __restrict__ status, int64_t batch, int n, int J, int splits,
                     int k_lo, int k_n) {
+    pdl_wait();
     const int64_t per = (int64_t)k_n * kT * kT;
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < batch * per;
          e += (int64_t)gridDim.x * blockDim.x) {
@@ -1249,6 +1251,7 @@ lit_diag_kernel(const double* __restrict__ L, double* __restrict__ W,
                 const double* __restrict__ X, size_t x_stride, double* __restrict__ S,
                 double* __restrict__ Tm, const int32_t* __restrict__ status, int64_t batch, int n,
                 int j0, int kb) {
+    pdl_wait();
     __shared__ double sA[kT * kLB], sB[kT * kLB], sC[kT * kLB], sD[kT * kLB];
     __shared__ double red[4][kLB * kLB];
     int ba, bb;
@@ -1483,9 +1486,8 @@ cudaError_t ozaki_adj_row(const double* L, double* W, void* work, const int32_t*
     const int64_t total = batch * (int64_t)k_n * kT * kT;
     const unsigned blocks = (unsigned)std::min<int64_t>((total + 255) / 256,
                                                         (int64_t)device_sm_count() * 16);
-    split_reduce_kernel<<<blocks, 256, 0, stream>>>(W, pbuf, status, batch, n, J, splits, k_lo,
-                                                    k_n);
-    return cudaGetLastError();
+    return launch_pdl(split_reduce_kernel, dim3(blocks), dim3(256), 0, stream, W, pbuf, status,
+                      batch, n, J, splits, k_lo, k_n);
 }
 
 cudaError_t ozaki_adj_upd_slice(double* W, void* work, const int32_t* status, int64_t batch,
@@ -1538,13 +1540,15 @@ cudaError_t ozaki_adj_diag(const double* L, double* W, void* work, const int32_t
     const size_t xs = cnt * kT * kT;
     double* S = w.lit;
     double* T = w.lit + (size_t)batch * kT * kT;
-    lit_diag_kernel<LIT_S><<<grid, kLitThreads, 0, stream>>>(L, W, X, xs, S, T, status, batch, n,
-                                                            j0, kb);
-    lit_diag_kernel<LIT_T><<<grid, kLitThreads, 0, stream>>>(L, W, X, xs, S, T, status, batch, n,
-                                                            j0, kb);
-    lit_diag_kernel<LIT_A><<<grid, kLitThreads, 0, stream>>>(L, W, X, xs, S, T, status, batch, n,
-                                                            j0, kb);
-    return cudaGetLastError();
+    cudaError_t e = launch_pdl(lit_diag_kernel<LIT_S>, grid, dim3(kLitThreads), 0, stream, L, W, X,
+                               xs, S, T, status, batch, n, j0, kb);
+    if (e == cudaSuccess)
+        e = launch_pdl(lit_diag_kernel<LIT_T>, grid, dim3(kLitThreads), 0, stream, L, W, X, xs, S,
+                       T, status, batch, n, j0, kb);
+    if (e == cudaSuccess)
+        e = launch_pdl(lit_diag_kernel<LIT_A>, grid, dim3(kLitThreads), 0, stream, L, W, X, xs, S,
+                       T, status, batch, n, j0, kb);
+    return e;
 }
 
 }  // namespace chol
