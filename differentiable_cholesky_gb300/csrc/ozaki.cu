@@ -979,8 +979,9 @@ split_reduce_kernel(double* __restrict__ W, const double* __restrict__ part,
     }
 }
 
-// Split of OZ_REV_ROW's reduction: enough CTAs for two per SM, the partial
-// tiles bounded by 2 * SMs per call.
+// Split of OZ_REV_ROW's reduction: about one split tile per SM (four
+// quarter-tile CTAs per SM, two waves at two CTAs per SM; half as many
+// measured slower), the partial tiles bounded by 2 * SMs per call.
 inline int row_splits(int64_t batch, int k_n, int chunks) {
     const int64_t tiles = batch * k_n;
     const int64_t want = (2 * (int64_t)device_sm_count() + 2 * tiles - 1) / (2 * tiles);
